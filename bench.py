@@ -1,0 +1,448 @@
+#!/usr/bin/env python
+"""Split-KV sparse-MLA decode benchmark: µs per call and HBM GB/s (fraction of the
+measured HBM peak) across s_q x num_splits, on synthetic data shaped like the
+FlashMLA PR #25 workload (h_q = 64, d_qk = 576, d_v = 512, topk = 128 + 512,
+one bf16 latent KV cache of 131072 rows, FP8 e4m3 output with a per-tensor scale).
+
+One "step" is one decode call: the split kernel plus the combine (or the
+direct-epilogue kernel when the plan picks one split), replayed as a CUDA graph
+with inputs resident in HBM; L2 is flushed (256 MiB write, untimed) before every
+timed call and each call is timed with CUDA events on its stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--s-q 96] [--impl ours|reference]
+
+Prints one JSON line. --impl reference times the fp64 CPU oracle on the same
+workload (a bounded sample per step) instead of the GPU library.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "split-KV sparse-MLA decode µs/call and HBM GB/s (% roofline) vs s_q x splits"
+N_KV = 131072
+TOPK = 640
+H_Q, D_QK, D_V = 64, 576, 512
+INV_SCALE = 64.0
+SWEEP_SQ = (1, 6, 16, 96, 384)
+SWEEP_S = (1, 2, 4, 8, 16)
+FLUSH_BYTES = 256 << 20
+
+
+def workload_name(s_q: int) -> str:
+    return (f"sparse-MLA decode, s_q={s_q}, h_q=64, d_qk=576 (512 latent + 64 RoPE), d_v=512, "
+            f"bf16 KV cache {N_KV} rows ~N(0,1), topk={TOPK} (128 most recent + 512 uniform), "
+            f"Q bf16 ~N(0,1), sm_scale 1/sqrt(576), no sink, FP8 e4m3 output (inv_scale {INV_SCALE:g})")
+
+
+def algorithmic_bytes(s_q: int, S: int, part: str = "call") -> int:
+    """Bytes the split method must move (gathered rows counted per token).
+
+    per token: Q 64*576*2 + idx topk*4 + rows topk*1152 (+ FP8 output 64*512 + LSE 64*4 when
+    the output is written); S > 1 adds the fp32 partial O + LSE, written by the split
+    kernel and read by the combine: S*(64*512*4 + 64*4) each way.
+    part: "call" (whole call), "split" (the split or direct kernel alone).
+    """
+    per_tok_in = H_Q * D_QK * 2 + TOPK * 4 + TOPK * D_QK * 2
+    out = H_Q * D_V * 1 + H_Q * 4
+    partial = S * (H_Q * D_V * 4 + H_Q * 4)
+    if S == 1:
+        return s_q * (per_tok_in + out)
+    if part == "split":
+        return s_q * (per_tok_in + partial)
+    return s_q * (per_tok_in + 2 * partial + out)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms in the background."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        t0, t1 = (self.marks[0], self.marks[1]) if len(self.marks) >= 2 else (0, 1e30)
+        rows = [l for (t, l) in self.lines if t0 - 0.05 <= t <= t1 + 0.05] or [l for _, l in self.lines]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- GPU arm --
+
+class Case:
+    """Device inputs, a plan, outputs and CUDA graphs for one (s_q, S) point."""
+
+    def __init__(self, b, torch, kv, inp, S):
+        self.b, self.torch = b, torch
+        dev = kv.device
+        self.s_q = inp.s_q
+        self.q = inp.q.to(dev)
+        self.idx = inp.idx.to(dev)
+        self.kv = kv
+        self.sm_scale = inp.sm_scale
+        self.plan = b.mla_decode_plan(self.s_q, TOPK, force_splits=S) if S else b.mla_decode_plan(self.s_q, TOPK)
+        self.S = self.plan.num_splits
+        self.ws = (torch.empty(self.plan.workspace_bytes, dtype=torch.uint8, device=dev)
+                   if self.plan.workspace_bytes else None)
+        self.out = torch.empty(self.s_q, H_Q, D_V, dtype=torch.uint8, device=dev)
+        self.lse = torch.empty(self.s_q, H_Q, dtype=torch.float32, device=dev)
+        self.stream = torch.cuda.Stream()
+        self.g_call = self._capture(self._call)
+        self.g_kernel = self._capture(self._kernel)
+
+    def _call(self):
+        self.b.mla_sparse_decode(self.plan, self.s_q, self.q, self.kv, N_KV, self.idx, self.sm_scale, None,
+                                 "e4m3", INV_SCALE, self.out, self.lse, None, self.ws, stream=self.stream)
+
+    def _kernel(self):
+        if self.S == 1:
+            self._call()
+        else:
+            self.b.mla_sparse_decode_split(self.plan, self.s_q, self.q, self.kv, N_KV, self.idx, self.sm_scale,
+                                           self.ws, stream=self.stream)
+
+    def _capture(self, fn):
+        torch = self.torch
+        with torch.cuda.stream(self.stream):
+            fn()                                  # eager once (warms the module, checks arguments)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            fn()
+        torch.cuda.synchronize()
+        return g
+
+    def time(self, graph, steps, warmup, flush):
+        """Per-call device time (µs) with L2 flushed before every call."""
+        torch = self.torch
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        with torch.cuda.stream(self.stream):
+            for _ in range(warmup):
+                flush.zero_()
+                graph.replay()
+            torch.cuda.synchronize()
+            for e0, e1 in ev:
+                flush.zero_()
+                e0.record(self.stream)
+                graph.replay()
+                e1.record(self.stream)
+        torch.cuda.synchronize()
+        return [1000.0 * e0.elapsed_time(e1) for e0, e1 in ev]
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import split_kv_sparse_gb300 as b
+    from split_kv_sparse_gb300 import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peak, peak_src = load_peaks()
+
+    # inputs: one KV cache shared by every s_q (generated once), Q / indices per s_q
+    base = wl.mla_inputs(1, N_KV, TOPK, seed=0)
+    kv = base.kv.to(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def inputs(s_q):
+        inp = wl.mla_inputs(s_q, N_KV, TOPK, seed=1000 + s_q) if s_q != 1 else base
+        return wl.MlaInputs(q=inp.q, kv=base.kv, idx=inp.idx, sink=None, sm_scale=inp.sm_scale)
+
+    inp_main = inputs(args.s_q)
+    case = Case(b, torch, kv, inp_main, 0)
+
+    props = torch.cuda.get_device_properties(local)
+    sampler = ClockSampler(getattr(props, "uuid", None) and f"GPU-{props.uuid}" or str(local))
+    sampler.start()
+    time.sleep(0.2)
+
+    # ---- headline: whole call, cold L2 ------------------------------------------------
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.mark()
+    t_wall0 = time.perf_counter()
+    call_us = case.time(case.g_call, args.steps, args.warmup, flush)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall0
+    sampler.mark()
+    kern_us = case.time(case.g_kernel, args.steps, max(3, args.warmup // 2), flush)
+    if world > 1:
+        dist.barrier()
+
+    mean_call = statistics.fmean(call_us)
+    mean_kern = statistics.fmean(kern_us)
+    if world > 1:
+        t = torch.tensor([mean_call, mean_kern], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        mean_call, mean_kern = float(t[0]), float(t[1])
+
+    kbytes = algorithmic_bytes(args.s_q, case.S, "split")
+    achieved = kbytes / (mean_kern * 1e-6) / 1e9
+
+    # ---- end to end through the C ABI with host buffers ---------------------------------
+    q_h = inp_main.q.pin_memory()
+    idx_h = inp_main.idx.pin_memory()
+    out_h = torch.empty(case.out.shape, dtype=case.out.dtype).pin_memory()
+    lse_h = torch.empty(case.lse.shape, dtype=case.lse.dtype).pin_memory()
+    e2e = []
+    with torch.cuda.stream(case.stream):
+        for i in range(args.warmup + min(args.steps, 500)):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(case.stream)
+            case.q.copy_(q_h, non_blocking=True)
+            case.idx.copy_(idx_h, non_blocking=True)
+            case._call()
+            out_h.copy_(case.out, non_blocking=True)
+            lse_h.copy_(case.lse, non_blocking=True)
+            e1.record(case.stream)
+            if i >= args.warmup:
+                e2e.append((e0, e1))
+    torch.cuda.synchronize()
+    e2e_us = statistics.fmean(1000.0 * a.elapsed_time(c) for a, c in e2e)
+    h2d = q_h.numel() * q_h.element_size() + idx_h.numel() * idx_h.element_size()
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+    # ---- sweep: s_q x splits (and the planner's choice) -------------------------------
+    sweep = []
+    if not args.no_sweep:
+        for s_q in SWEEP_SQ:
+            inp = inp_main if s_q == args.s_q else inputs(s_q)
+            auto = b.mla_decode_plan(s_q, TOPK).num_splits
+            for S in sorted(set(SWEEP_S) | {auto}):
+                c = Case(b, torch, kv, inp, S)
+                us = statistics.fmean(c.time(c.g_call, args.sweep_steps, 3, flush))
+                ks = statistics.fmean(c.time(c.g_kernel, args.sweep_steps, 3, flush))
+                cb = algorithmic_bytes(s_q, S, "call")
+                sweep.append({"s_q": s_q, "num_splits": S, "planner": S == auto, "us_per_call": round(us, 2),
+                              "split_kernel_us": round(ks, 2), "alg_bytes": cb,
+                              "gb_s": round(cb / (us * 1e-6) / 1e9, 1),
+                              "frac_of_peak": round(cb / (us * 1e-6) / 1e9 / peak, 4)})
+                del c
+        torch.cuda.synchronize()
+    sampler.stop()
+    clocks = sampler.summary()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.s_q, args.cpu_seconds)
+
+    st, site = b.mla_get_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st:#x} (wait site {site})")
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(mean_call, 3), "unit": "us/call", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_call / 1000.0, 6),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": workload_name(args.s_q), "s_q": args.s_q, "num_splits": case.S,
+                       "n_kv": N_KV, "topk": TOPK, "h_q": H_Q, "d_qk": D_QK, "d_v": D_V,
+                       "output": "e4m3", "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                       "l2": "flushed before every timed call (256 MiB write, untimed)",
+                       "timing": "CUDA graph replay of one decode call, CUDA events on its stream, mean of steps",
+                       "wall_s_timed_region": round(wall, 4)},
+            "roofline": {"bound": "hbm", "kernel": "mla_decode_kernel (split pass)" if case.S > 1
+                         else "mla_decode_kernel (direct epilogue)",
+                         "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": known_traffic(args.s_q, case.S),
+                         "alg_bytes_per_launch": kbytes, "kernel_us": round(mean_kern, 3),
+                         "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
+                         else "fallback 6.8 TB/s"},
+            "e2e": {"value": round(e2e_us, 3), "unit": "us/call", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h,
+                    "note": "H2D of Q and indices from pinned host memory + the call + D2H of FP8 O and LSE; "
+                            "the KV cache is resident decode state"},
+            "gpu_launches": args.steps * (2 if case.S > 1 else 1),
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+            "sweep": sweep,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def known_traffic(s_q, S):
+    """DRAM bytes per launch of the dominant kernel from an ncu capture of the current kernel
+    source (profiles/), or None when no capture matches it."""
+    import hashlib
+    src = os.path.join(ROOT, "split_kv_sparse_gb300", "csrc", "mla_decode.cu")
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    table = {}   # (source hash, s_q, S) -> dram bytes per launch
+    return table.get((h, s_q, S))
+
+
+# ---------------------------------------------------------------------- CPU baseline --
+
+def _cpu_worker(s_q: int, seconds: float, mode: str):
+    """Runs in a child process with a fixed BLAS thread count: times the fp64 oracle."""
+    import numpy as np
+
+    import oracle.mla as om
+    from split_kv_sparse_gb300 import workloads as wl
+
+    base = wl.mla_inputs(1, N_KV, TOPK, seed=0)
+    inp = wl.mla_inputs(s_q, N_KV, TOPK, seed=1000 + s_q) if s_q != 1 else base
+    q = inp.q.double().numpy()
+    kv = base.kv.double().numpy()
+    idx = inp.idx.numpy()
+    per_tok = []
+    t_start = time.perf_counter()
+    i = 0
+    while True:
+        t = i % s_q
+        t0 = time.perf_counter()
+        O, L = om.attention(q[t:t + 1], kv, idx[t:t + 1], inp.sm_scale, D_V)
+        from oracle import codecs
+        codecs.e4m3_encode(O * INV_SCALE)
+        per_tok.append(time.perf_counter() - t0)
+        i += 1
+        if time.perf_counter() - t_start > seconds and i >= min(s_q, 4):
+            break
+    print(json.dumps({"per_token_s": per_tok, "tokens": i}))
+
+
+def cpu_baseline(s_q: int, seconds: float, steps=None):
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = str(cores)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    p = subprocess.run([sys.executable, os.path.abspath(__file__), "--_cpu-worker", "--s-q", str(s_q),
+                        "--cpu-seconds", str(seconds)], stdout=subprocess.PIPE, stderr=subprocess.PIPE,
+                       text=True, env=env, cwd=ROOT)
+    if p.returncode != 0:
+        return {"value": None, "unit": "us/call", "cores": cores, "kind": "oracle",
+                "sample": f"failed: {p.stderr[-300:]}"}
+    d = json.loads(p.stdout.strip().splitlines()[-1])
+    per_tok = statistics.fmean(d["per_token_s"])
+    return {"value": round(per_tok * s_q * 1e6, 1), "unit": "us/call", "cores": cores, "kind": "oracle",
+            "sample": f"{d['tokens']} single-token oracle calls (fp64 numpy, BLAS threads = {cores}) of the "
+                      f"s_q={s_q} workload, ~{seconds:g} s; per-call value = mean per-token time x {s_q}",
+            "per_token_s": per_tok}
+
+
+def run_reference(args):
+    """The fp64 oracle as the reference arm, on this process's host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    # each step is a bounded sample: one token of the workload, scaled to the call
+    seconds = max(5.0, min(60.0, 0.05 * (args.steps + args.warmup)))
+    cb = cpu_baseline(args.s_q, seconds)
+    v = cb["value"]
+    line = {"metric": METRIC, "value": v, "unit": "us/call", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": (v / 1000.0) if v else None,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": workload_name(args.s_q), "s_q": args.s_q, "n_kv": N_KV, "topk": TOPK,
+                       "h_q": H_Q, "d_qk": D_QK, "d_v": D_V, "output": "e4m3"},
+            "cpu_baseline": cb,
+            "e2e": {"value": v, "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--s-q", type=int, default=96)
+    ap.add_argument("--sweep-steps", type=int, default=50)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--_cpu-worker", action="store_true", help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args._cpu_worker:
+        _cpu_worker(args.s_q, args.cpu_seconds, "call")
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

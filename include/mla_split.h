@@ -1,0 +1,275 @@
+/*
+ * mla_split.h -- C ABI of the GB300 (sm_103a) split-KV sparse-MLA decode library.
+ *
+ * Scope (every call below cites the passage that defines its operation):
+ *
+ *   FlashMLA PR #25 (vllm-project/FlashMLA), "Purpose" and "What changes":
+ *     decode tokens with h_q = 64 heads attend over a top-k set of rows of one
+ *     shared latent KV cache; the job space is (query token, KV split); each
+ *     job stores an fp32 partial O normalised by its own l_i plus a log2-space
+ *     LSE, and a combine kernel folds the splits, owns the attention sink and
+ *     performs the final cast. Without partial buffers the kernel runs the
+ *     unsplit path with a direct (fused) epilogue.
+ *   "The Split-K Dispatch" (magik.net), "The Reasoning Behind the Design":
+ *     the split count is a deterministic function of the batch so the scratch
+ *     size and the branch are fixed per CUDA graph; the combine takes the
+ *     global max of the per-split maxima and weights splits by exp2(local - global).
+ *   cuDNN-frontend PR #768, SM120 FP8 commit: KV ranges cut into near-equal
+ *     chunks with the remainder to the leading splits; a chunk past the end is
+ *     empty and yields O = 0 / LSE = -inf; the combine owns the amax; the host
+ *     requires an LSE under a split and sizes O/LSE as partial workspaces.
+ *
+ * Conventions for every entry point:
+ *   - Every function returns an int status (MLA_OK = 0). Nothing throws.
+ *     mla_status_string() maps a status to text. Argument errors are detected
+ *     on the host before any launch and leave device memory untouched.
+ *   - Pointers named q, kv, idx, workspace, out, lse_out, amax_out, sink are
+ *     DEVICE pointers owned by the caller; the library never frees or keeps
+ *     them and allocates nothing on any call below.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream). All device work is asynchronous on that stream; no call
+ *     synchronises except mla_get_status().
+ *   - The calls are capturable into a CUDA graph: no allocation, no host
+ *     synchronisation and no data-dependent host branch (the split count comes
+ *     from the plan, fixed per s_q_max).
+ *   - The calling thread's current CUDA device is the device used.
+ */
+#ifndef MLA_SPLIT_H_
+#define MLA_SPLIT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define MLA_OK                0
+#define MLA_ERR_INVALID_ARG   1   /* null / misaligned pointer, bad size, s_q > plan.s_q_max ... */
+#define MLA_ERR_UNSUPPORTED   2   /* shape outside what the kernels implement (e.g. h_q != 64)  */
+#define MLA_ERR_WORKSPACE     3   /* workspace missing or smaller than the plan requires       */
+#define MLA_ERR_CUDA          4   /* a CUDA runtime/driver call failed (launch, attribute ...) */
+#define MLA_ERR_NO_DEVICE     5   /* no usable sm_100-family device is current                 */
+
+/* Bits of the device status word (see mla_get_status). */
+#define MLA_STATUS_TIMEOUT    0x1u  /* a bounded wait inside a kernel ran out; that CTA aborted */
+#define MLA_STATUS_BAD_SHAPE  0x2u  /* a dense job held more than 64 query rows (s_q_b * h_q/h_kv);
+                                       it wrote nothing */
+
+/* Output element types of the final cast (FlashMLA PR #25, "What changes":
+ * the FP8 cast moves into the combine; the fp32 pass-through exists for parity). */
+#define MLA_OUT_F32   0
+#define MLA_OUT_BF16  1
+#define MLA_OUT_E4M3  2   /* code = e4m3_satfinite_rn(O * out_inv_scale); one per-tensor scale */
+
+/* Largest split count any plan may use. */
+#define MLA_MAX_SPLITS 64
+
+/* ======================================================================= *
+ *  Sparse MLA decode                                                       *
+ * ======================================================================= */
+
+/* A plan: every size and offset the split and combine calls need, computed once
+ * per s_q bucket on the host ("The Split-K Dispatch", "CUDA Graph Safety").
+ * Workspace layout (one caller-owned device buffer, 256-byte aligned):
+ *   [0, o_acc_bytes)                       fp32 O partials, split-major
+ *                                          [num_splits][s_q][h_q][d_v]
+ *   [lse_acc_offset, + lse_acc_bytes)      fp32 log2 LSE partials
+ *                                          [num_splits][s_q][h_q]
+ * where s_q is the s_q of the call (<= s_q_max). For num_splits == 1 no
+ * workspace is needed (workspace_bytes == 0) and the direct path runs. */
+typedef struct {
+  int32_t s_q_max;      /* largest number of decode tokens per call               */
+  int32_t h_q;          /* query heads; 64                                         */
+  int32_t d_qk;         /* 576 = 512 latent + 64 RoPE dims                         */
+  int32_t d_v;          /* 512 = the first 512 dims of each row                    */
+  int32_t topk;         /* top-k entries per token (row stride of idx)             */
+  int32_t block_rows;   /* 64: top-k entries per KV block, the unit of a split     */
+  int32_t num_blocks;   /* ceil(topk / block_rows)                                 */
+  int32_t num_splits;   /* S; may exceed num_blocks (those splits are empty)       */
+  int32_t num_sms;      /* SM count the split choice was made for                  */
+  int32_t reserved;
+  uint64_t o_acc_bytes;     /* num_splits * s_q_max * h_q * d_v * 4                */
+  uint64_t lse_acc_offset;  /* o_acc_bytes rounded up to 256                       */
+  uint64_t lse_acc_bytes;   /* num_splits * s_q_max * h_q * 4                      */
+  uint64_t workspace_bytes; /* 0 when num_splits == 1                              */
+} mla_plan_t;
+
+/* Choose the split count and size the workspace ("The Split-K Dispatch",
+ * "Adaptive NSPLIT"; FlashMLA PR #25, "Measured": partial bytes
+ * num_splits * s_q * h_q * d_v * 4).
+ *   num_sms      0 = query the current device.
+ *   max_splits   0 = MLA_MAX_SPLITS; caps the automatic choice.
+ *   force_splits 0 = automatic; > 0 uses exactly that many splits (<= MLA_MAX_SPLITS),
+ *                even above num_blocks (the extra splits are empty).
+ * Automatic rule: among split counts S with s_q_max * S <= num_sms (at least 1),
+ * take the smallest S that reaches the fewest blocks per split, ceil(num_blocks / S).
+ * Errors: MLA_ERR_UNSUPPORTED unless h_q == 64, d_qk == 576, d_v == 512;
+ *         MLA_ERR_INVALID_ARG for s_q_max < 1, topk < 1, out == NULL, or bad split counts. */
+MLA_API int mla_decode_plan(int s_q_max, int h_q, int d_qk, int d_v, int topk,
+                    int num_sms, int max_splits, int force_splits, mla_plan_t* out);
+
+/* Split pass: one CTA per (token t, split s) job; the job walks the top-k
+ * entries of its own block range (FlashMLA PR #25, "What changes"), gathers the
+ * rows idx[t, r] of kv, and writes
+ *     O_acc[s][t][h][:] = sum_r exp(s_r) V_r / sum_r exp(s_r)       (fp32)
+ *     LSE_acc[s][t][h]  = log2 sum_r exp(s_r)                       (fp32)
+ * with s_r = sm_scale * <q[t,h,:], kv[idx[t,r], :]> in natural-log units; an
+ * empty split (no blocks, or no valid index) writes O = 0 and LSE = -inf
+ * (cuDNN-frontend PR #768, SM120 FP8 commit). No sink is applied here.
+ *   q    bf16 [s_q][h_q][576], contiguous, 16-byte aligned.
+ *   kv   bf16 [n_kv][576], contiguous rows, 16-byte aligned; 1 <= n_kv < 2^31.
+ *   idx  int32 [s_q][topk]; an entry outside [0, n_kv) (e.g. -1 padding) is masked.
+ *   workspace >= plan->workspace_bytes, 256-byte aligned (layout in mla_plan_t).
+ * Requires plan->num_splits > 1 (MLA_ERR_INVALID_ARG otherwise: use
+ * mla_sparse_decode_direct) and 1 <= s_q <= plan->s_q_max. */
+MLA_API int mla_sparse_decode_split(const mla_plan_t* plan, int s_q,
+                            const void* q, const void* kv, int64_t n_kv,
+                            const int32_t* idx, float sm_scale,
+                            void* workspace, void* stream);
+
+/* Combine: for every (t, h), with M = max_s LSE_acc[s][t][h],
+ *     w_s = 2^(LSE_acc[s] - M)               (0 for an empty split)
+ *     O   = sum_s w_s O_acc[s] / (sum_s w_s + 2^(sink_h * log2(e) - M))
+ *     LSE = M + log2 sum_s w_s               (the sink is NOT included)
+ * then casts O to out_dtype ("The Split-K Dispatch", "The LSE Combine Strategy";
+ * FlashMLA PR #25, "What changes": the combine owns the sink and the cast). A
+ * (t, h) whose splits are all empty gives O = 0, LSE = -inf.
+ *   sink      fp32 [h_q] natural-log logits, or NULL for no sink.
+ *   out       [s_q][h_q][d_v] of out_dtype (fp32 / bf16 / e4m3 bytes), 16-byte aligned.
+ *   out_inv_scale  multiplies O before the e4m3 cast (ignored otherwise).
+ *   lse_out   fp32 [s_q][h_q] or NULL.
+ *   amax_out  fp32 scalar or NULL: overwritten with max |O| of the recombined,
+ *             pre-cast O (cuDNN-frontend PR #768: the combine owns the amax). */
+MLA_API int mla_split_combine(const mla_plan_t* plan, int s_q, const void* workspace,
+                      const float* sink, int out_dtype, float out_inv_scale,
+                      void* out, float* lse_out, float* amax_out, void* stream);
+
+/* Unsplit path with the fused epilogue (FlashMLA PR #25, "What changes":
+ * "Unsplit behaviour is unchanged"): one CTA per token over all top-k entries,
+ * sink and cast applied in the epilogue; the same O / LSE / amax definitions as
+ * mla_split_combine. Needs no plan and no workspace. Arguments as above;
+ * topk >= 1, s_q >= 1. */
+MLA_API int mla_sparse_decode_direct(int s_q, int topk, const void* q, const void* kv, int64_t n_kv,
+                             const int32_t* idx, float sm_scale, const float* sink,
+                             int out_dtype, float out_inv_scale,
+                             void* out, float* lse_out, float* amax_out, void* stream);
+
+/* One call for the whole decode step: the direct path when plan->num_splits == 1,
+ * otherwise mla_sparse_decode_split followed by mla_split_combine on the same stream. */
+MLA_API int mla_sparse_decode(const mla_plan_t* plan, int s_q,
+                      const void* q, const void* kv, int64_t n_kv,
+                      const int32_t* idx, float sm_scale, const float* sink,
+                      int out_dtype, float out_inv_scale,
+                      void* out, float* lse_out, float* amax_out,
+                      void* workspace, void* stream);
+
+/* ======================================================================= *
+ *  Dense FP8 GQA split-KV SDPA decode (cuDNN-frontend PR #768 form)        *
+ * ======================================================================= */
+
+/* Workspace layout as for MLA with rows = total_q * h_q and d = head dim:
+ *   [0, o_acc_bytes)                    fp32 [num_splits][total_q][h_q][d]
+ *   [lse_acc_offset, + lse_acc_bytes)   fp32 [num_splits][total_q][h_q]          */
+typedef struct {
+  int32_t batch;          /* sequences                                           */
+  int32_t h_q;            /* query heads (32)                                     */
+  int32_t h_kv;           /* KV heads (8); h_q % h_kv == 0, group <= 16           */
+  int32_t d;              /* head dim; 128                                        */
+  int32_t max_q_per_seq;  /* new tokens per sequence, <= 64 / (h_q / h_kv)        */
+  int32_t total_q_max;    /* bound on sum of new tokens over the batch            */
+  int32_t max_kv;         /* bound on keys per sequence                           */
+  int32_t key_tile;       /* 128: keys per tile, the unit of a split              */
+  int32_t num_splits;
+  int32_t num_sms;
+  uint64_t o_acc_bytes;
+  uint64_t lse_acc_offset;
+  uint64_t lse_acc_bytes;
+  uint64_t workspace_bytes;
+} sdpa_plan_t;
+
+/* Split count for the dense path: S with batch * h_kv * S <= num_sms (at least 1),
+ * smallest S reaching the fewest tiles per split for a sequence of max_kv keys;
+ * force_splits > 0 overrides. Errors as for mla_decode_plan (d must be 128). */
+MLA_API int sdpa_fp8_decode_plan(int batch, int h_q, int h_kv, int d, int max_q_per_seq,
+                         int total_q_max, int max_kv, int num_sms, int max_splits,
+                         int force_splits, sdpa_plan_t* out);
+
+/* Split pass over jobs (sequence b, KV head g, split s). Sequence b has
+ * s_q_b = cu_seqlens_q[b+1] - cu_seqlens_q[b] new tokens and kv_b keys
+ * (cu_seqlens_kv); query i sits at position kv_b - s_q_b + i and sees keys
+ * 0..that position (bottom-right causal); query head j reads KV head j / (h_q/h_kv).
+ * The key range [0, kv_b) is cut into num_splits near-equal runs of 128-key
+ * tiles, remainder to the leading splits; an empty run writes O = 0 / LSE = -inf
+ * (cuDNN-frontend PR #768, SM120 FP8 commit). Values are code * descale.
+ *   q  e4m3 codes [total_q][h_q][d]; k, v e4m3 codes [total_kv][h_kv][d] (16-byte aligned).
+ *   total_q, total_kv  row counts of q and k/v (= cu_seqlens_q[batch], cu_seqlens_kv[batch]);
+ *      the kernels never read outside them.
+ *   cu_seqlens_q, cu_seqlens_kv  int32 [batch + 1] device arrays, starting at 0, with
+ *      s_q_b * (h_q / h_kv) <= 64 for every sequence (a sequence beyond that is not
+ *      computed and sets MLA_STATUS_BAD_SHAPE).
+ *   descale_q/k/v  fp32 device scalars (NULL = 1.0).
+ * Requires plan->num_splits > 1 and total_q <= plan->total_q_max. */
+MLA_API int sdpa_fp8_decode_split(const sdpa_plan_t* plan, int total_q, int64_t total_kv,
+                          const void* q, const void* k, const void* v,
+                          const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                          const float* descale_q, const float* descale_k, const float* descale_v,
+                          float sm_scale, void* workspace, void* stream);
+
+/* Combine for the dense path: the mla_split_combine fold with no sink; writes O
+ * (bf16 by default), the log2 LSE and, if amax_out != NULL, max |O| of the
+ * recombined O (cuDNN-frontend PR #768: the in-kernel amax stands down under a split). */
+MLA_API int sdpa_split_combine(const sdpa_plan_t* plan, int total_q, const void* workspace,
+                       int out_dtype, float out_inv_scale,
+                       void* out, float* lse_out, float* amax_out, void* stream);
+
+/* Unsplit dense path with the direct epilogue (bf16/fp32/e4m3 O, LSE, amax). */
+MLA_API int sdpa_fp8_decode_direct(int batch, int h_q, int h_kv, int d, int total_q, int64_t total_kv,
+                           const void* q, const void* k, const void* v,
+                           const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                           const float* descale_q, const float* descale_k, const float* descale_v,
+                           float sm_scale, int out_dtype, float out_inv_scale,
+                           void* out, float* lse_out, float* amax_out, void* stream);
+
+/* One call: direct when plan->num_splits == 1, else split + combine. */
+MLA_API int sdpa_fp8_decode(const sdpa_plan_t* plan, int total_q, int64_t total_kv,
+                    const void* q, const void* k, const void* v,
+                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                    const float* descale_q, const float* descale_k, const float* descale_v,
+                    float sm_scale, int out_dtype, float out_inv_scale,
+                    void* out, float* lse_out, float* amax_out,
+                    void* workspace, void* stream);
+
+/* ======================================================================= *
+ *  Status and diagnostics                                                  *
+ * ======================================================================= */
+
+/* Synchronises the current device, then reads and clears its status word
+ * (MLA_STATUS_* bits set by kernels whose bounded waits ran out). *site_out,
+ * if not NULL, receives the code of the first wait that ran out (0 = none). */
+MLA_API int mla_get_status(uint32_t* status_out, uint32_t* site_out);
+
+/* Launches a one-CTA kernel that waits on an mbarrier nothing ever arrives on,
+ * with the given limit in nanoseconds; the wait gives up, sets
+ * MLA_STATUS_TIMEOUT and the kernel returns normally. Exercises the abort path
+ * of the bounded waits without hanging or faulting the GPU. */
+MLA_API int mla_selftest_wait_timeout(uint64_t limit_ns, void* stream);
+
+/* Text for a status code. */
+MLA_API const char* mla_status_string(int status);
+
+/* ABI version of this header (bumped on any signature or layout change). */
+MLA_API int mla_abi_version(void);
+#define MLA_ABI_VERSION 1
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_SPLIT_H_ */

@@ -1,0 +1,540 @@
+// extern "C" entry points of include/mla_split.h: planning, argument checks,
+// TMA descriptor encoding and kernel launches. No entry point allocates device
+// memory; the only device state is the per-device status word below.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.h"
+#include "mla_split.h"
+
+namespace {
+
+using skv::kMlaBlockRows;
+using skv::kMlaDqk;
+using skv::kMlaDv;
+using skv::kMlaHeads;
+
+// [0] = MLA_STATUS_* bits, [1] = code of the first wait that ran out.
+__device__ uint32_t g_status[2];
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  uint32_t* status = nullptr;
+  int num_sms = 0;
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+bool g_encode_tried = false;
+
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return MLA_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& d = g_devices[dev];
+  if (!d.ready) {
+    int major = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return MLA_ERR_NO_DEVICE;
+    }
+    if (major != 10) return MLA_ERR_NO_DEVICE;   // the kernels are built for the sm_100 family (sm_103a)
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) {
+      cudaGetLastError();
+      return MLA_ERR_CUDA;
+    }
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return MLA_ERR_CUDA;
+    }
+    d.status = static_cast<uint32_t*>(p);
+    d.ready = true;
+  }
+  *out = &d;
+  return MLA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_encode_tried) {
+    g_encode_tried = true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    } else {
+      cudaGetLastError();
+    }
+  }
+  return g_encode;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+uint64_t round_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+
+int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+              uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  auto enc = encoder();
+  if (enc == nullptr) return MLA_ERR_CUDA;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int encode_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, const uint64_t dims_in[3],
+              const uint64_t strides_in[2], const uint32_t box_in[3]) {
+  auto enc = encoder();
+  if (enc == nullptr) return MLA_ERR_CUDA;
+  cuuint64_t dims[3] = {dims_in[0], dims_in[1], dims_in[2]};
+  cuuint64_t strides[2] = {strides_in[0], strides_in[1]};
+  cuuint32_t box[3] = {box_in[0], box_in[1], box_in[2]};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MLA_OK;
+  cudaGetLastError();
+  return MLA_ERR_CUDA;
+}
+
+bool valid_out_dtype(int t) { return t == MLA_OUT_F32 || t == MLA_OUT_BF16 || t == MLA_OUT_E4M3; }
+
+// Shared argument checks of the MLA decode calls.
+int check_mla_inputs(int s_q, int topk, const void* q, const void* kv, int64_t n_kv, const int32_t* idx,
+                     float sm_scale) {
+  if (s_q < 1 || topk < 1) return MLA_ERR_INVALID_ARG;
+  if (q == nullptr || kv == nullptr || idx == nullptr) return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(idx, 4)) return MLA_ERR_INVALID_ARG;
+  if (n_kv < 1 || n_kv > 0x7FFFFFFFll) return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale)) return MLA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(s_q) * kMlaHeads > 0x7FFFFFFFll) return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
+
+int mla_tensor_maps(int s_q, const void* q, const void* kv, int64_t n_kv, CUtensorMap* tq, CUtensorMap* tkv) {
+  int st = encode_2d(tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, kMlaDqk,
+                     static_cast<uint64_t>(s_q) * kMlaHeads, kMlaDqk * 2, 64, 64);
+  if (st != MLA_OK) return st;
+  return encode_2d(tkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kv, kMlaDqk, static_cast<uint64_t>(n_kv),
+                   kMlaDqk * 2, 64, 1);
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_abi_version(void) { return MLA_ABI_VERSION; }
+
+const char* mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported shape";
+    case MLA_ERR_WORKSPACE: return "workspace missing or too small";
+    case MLA_ERR_CUDA: return "CUDA call failed";
+    case MLA_ERR_NO_DEVICE: return "no usable sm_100-family device";
+    default: return "unknown status";
+  }
+}
+
+int mla_decode_plan(int s_q_max, int h_q, int d_qk, int d_v, int topk, int num_sms, int max_splits,
+                    int force_splits, mla_plan_t* out) {
+  if (out == nullptr) return MLA_ERR_INVALID_ARG;
+  std::memset(out, 0, sizeof(*out));
+  if (h_q != kMlaHeads || d_qk != kMlaDqk || d_v != kMlaDv) return MLA_ERR_UNSUPPORTED;
+  if (s_q_max < 1 || topk < 1 || num_sms < 0) return MLA_ERR_INVALID_ARG;
+  if (max_splits < 0 || max_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID_ARG;
+  if (force_splits < 0 || force_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID_ARG;
+  if (num_sms == 0) {
+    DeviceState* d = nullptr;
+    const int st = device_state(&d);
+    if (st != MLA_OK) return st;
+    num_sms = d->num_sms;
+  }
+  const int nblk = (topk + kMlaBlockRows - 1) / kMlaBlockRows;
+  int S = force_splits;
+  if (S == 0) {
+    const int cap = max_splits > 0 ? max_splits : MLA_MAX_SPLITS;
+    int smax = num_sms / s_q_max;
+    if (smax > cap) smax = cap;
+    if (smax > nblk) smax = nblk;
+    if (smax < 1) smax = 1;
+    const int best = (nblk + smax - 1) / smax;   // fewest blocks any split must walk
+    S = smax;
+    for (int c = 1; c <= smax; ++c)
+      if ((nblk + c - 1) / c == best) {
+        S = c;
+        break;
+      }
+  }
+  if (static_cast<int64_t>(s_q_max) * S > 0x7FFFFFFFll) return MLA_ERR_INVALID_ARG;
+  out->s_q_max = s_q_max;
+  out->h_q = h_q;
+  out->d_qk = d_qk;
+  out->d_v = d_v;
+  out->topk = topk;
+  out->block_rows = kMlaBlockRows;
+  out->num_blocks = nblk;
+  out->num_splits = S;
+  out->num_sms = num_sms;
+  if (S > 1) {
+    out->o_acc_bytes = static_cast<uint64_t>(S) * s_q_max * h_q * d_v * 4ull;
+    out->lse_acc_offset = round_up(out->o_acc_bytes, 256);
+    out->lse_acc_bytes = static_cast<uint64_t>(S) * s_q_max * h_q * 4ull;
+    out->workspace_bytes = round_up(out->lse_acc_offset + out->lse_acc_bytes, 256);
+  }
+  return MLA_OK;
+}
+
+int mla_sparse_decode_split(const mla_plan_t* plan, int s_q, const void* q, const void* kv, int64_t n_kv,
+                            const int32_t* idx, float sm_scale, void* workspace, void* stream) {
+  if (plan == nullptr || plan->num_splits < 2 || plan->num_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID_ARG;
+  if (plan->h_q != kMlaHeads || plan->d_qk != kMlaDqk || plan->d_v != kMlaDv) return MLA_ERR_UNSUPPORTED;
+  if (s_q > plan->s_q_max) return MLA_ERR_INVALID_ARG;
+  int st = check_mla_inputs(s_q, plan->topk, q, kv, n_kv, idx, sm_scale);
+  if (st != MLA_OK) return st;
+  if (workspace == nullptr || !aligned(workspace, 256) || plan->workspace_bytes == 0) return MLA_ERR_WORKSPACE;
+  DeviceState* dev = nullptr;
+  if ((st = device_state(&dev)) != MLA_OK) return st;
+  CUtensorMap tq, tkv;
+  if ((st = mla_tensor_maps(s_q, q, kv, n_kv, &tq, &tkv)) != MLA_OK) return st;
+  skv::MlaArgs a{};
+  a.idx = idx;
+  a.s_q = s_q;
+  a.topk = plan->topk;
+  a.n_kv = static_cast<int>(n_kv);
+  a.num_splits = plan->num_splits;
+  a.num_blocks = plan->num_blocks;
+  a.scale_log2 = sm_scale * 1.4426950408889634f;
+  a.o_acc = static_cast<float*>(workspace);
+  a.lse_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan->lse_acc_offset);
+  a.status = dev->status;
+  a.wait_limit_ns = kWaitLimitNs;
+  return cuda_status(skv::launch_mla_decode(tq, tkv, a, false, static_cast<cudaStream_t>(stream)));
+}
+
+int mla_split_combine(const mla_plan_t* plan, int s_q, const void* workspace, const float* sink, int out_dtype,
+                      float out_inv_scale, void* out, float* lse_out, float* amax_out, void* stream) {
+  if (plan == nullptr || plan->num_splits < 2 || plan->num_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID_ARG;
+  if (plan->h_q != kMlaHeads || plan->d_v != kMlaDv) return MLA_ERR_UNSUPPORTED;
+  if (s_q < 1 || s_q > plan->s_q_max || out == nullptr || !aligned(out, 16)) return MLA_ERR_INVALID_ARG;
+  if (!valid_out_dtype(out_dtype)) return MLA_ERR_INVALID_ARG;
+  if (out_dtype == MLA_OUT_E4M3 && !std::isfinite(out_inv_scale)) return MLA_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned(workspace, 256) || plan->workspace_bytes == 0) return MLA_ERR_WORKSPACE;
+  DeviceState* dev = nullptr;
+  const int st = device_state(&dev);
+  if (st != MLA_OK) return st;
+  skv::CombineArgs c{};
+  c.o_acc = static_cast<const float*>(workspace);
+  c.lse_acc = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + plan->lse_acc_offset);
+  c.num_splits = plan->num_splits;
+  c.rows = s_q * kMlaHeads;
+  c.heads = kMlaHeads;
+  c.d = kMlaDv;
+  c.sink = sink;
+  c.out = out;
+  c.out_dtype = out_dtype;
+  c.inv_scale = out_inv_scale;
+  c.lse_out = lse_out;
+  c.amax = amax_out;
+  return cuda_status(skv::launch_combine(c, static_cast<cudaStream_t>(stream)));
+}
+
+int mla_sparse_decode_direct(int s_q, int topk, const void* q, const void* kv, int64_t n_kv, const int32_t* idx,
+                             float sm_scale, const float* sink, int out_dtype, float out_inv_scale, void* out,
+                             float* lse_out, float* amax_out, void* stream) {
+  int st = check_mla_inputs(s_q, topk, q, kv, n_kv, idx, sm_scale);
+  if (st != MLA_OK) return st;
+  if (out == nullptr || !aligned(out, 16) || !valid_out_dtype(out_dtype)) return MLA_ERR_INVALID_ARG;
+  if (out_dtype == MLA_OUT_E4M3 && !std::isfinite(out_inv_scale)) return MLA_ERR_INVALID_ARG;
+  DeviceState* dev = nullptr;
+  if ((st = device_state(&dev)) != MLA_OK) return st;
+  CUtensorMap tq, tkv;
+  if ((st = mla_tensor_maps(s_q, q, kv, n_kv, &tq, &tkv)) != MLA_OK) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (amax_out != nullptr) {
+    if ((st = cuda_status(cudaMemsetAsync(amax_out, 0, sizeof(float), cs))) != MLA_OK) return st;
+  }
+  skv::MlaArgs a{};
+  a.idx = idx;
+  a.s_q = s_q;
+  a.topk = topk;
+  a.n_kv = static_cast<int>(n_kv);
+  a.num_splits = 1;
+  a.num_blocks = (topk + kMlaBlockRows - 1) / kMlaBlockRows;
+  a.scale_log2 = sm_scale * 1.4426950408889634f;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.inv_scale = out_inv_scale;
+  a.lse_out = lse_out;
+  a.sink = sink;
+  a.amax = amax_out;
+  a.status = dev->status;
+  a.wait_limit_ns = kWaitLimitNs;
+  return cuda_status(skv::launch_mla_decode(tq, tkv, a, true, cs));
+}
+
+int mla_sparse_decode(const mla_plan_t* plan, int s_q, const void* q, const void* kv, int64_t n_kv,
+                      const int32_t* idx, float sm_scale, const float* sink, int out_dtype, float out_inv_scale,
+                      void* out, float* lse_out, float* amax_out, void* workspace, void* stream) {
+  if (plan == nullptr) return MLA_ERR_INVALID_ARG;
+  if (plan->num_splits == 1) {
+    if (s_q > plan->s_q_max) return MLA_ERR_INVALID_ARG;
+    return mla_sparse_decode_direct(s_q, plan->topk, q, kv, n_kv, idx, sm_scale, sink, out_dtype, out_inv_scale,
+                                    out, lse_out, amax_out, stream);
+  }
+  // validate the combine's own arguments before launching anything
+  if (out == nullptr || !aligned(out, 16) || !valid_out_dtype(out_dtype)) return MLA_ERR_INVALID_ARG;
+  if (out_dtype == MLA_OUT_E4M3 && !std::isfinite(out_inv_scale)) return MLA_ERR_INVALID_ARG;
+  const int st = mla_sparse_decode_split(plan, s_q, q, kv, n_kv, idx, sm_scale, workspace, stream);
+  if (st != MLA_OK) return st;
+  return mla_split_combine(plan, s_q, workspace, sink, out_dtype, out_inv_scale, out, lse_out, amax_out, stream);
+}
+
+// ---------------------------------------------------------------- dense -----
+
+int sdpa_fp8_decode_plan(int batch, int h_q, int h_kv, int d, int max_q_per_seq, int total_q_max, int max_kv,
+                         int num_sms, int max_splits, int force_splits, sdpa_plan_t* out) {
+  if (out == nullptr) return MLA_ERR_INVALID_ARG;
+  std::memset(out, 0, sizeof(*out));
+  if (d != 128) return MLA_ERR_UNSUPPORTED;
+  if (batch < 1 || h_q < 1 || h_kv < 1 || h_q % h_kv != 0) return MLA_ERR_INVALID_ARG;
+  const int group = h_q / h_kv;
+  if (group > 64 || max_q_per_seq < 1 || group * max_q_per_seq > 64) return MLA_ERR_UNSUPPORTED;
+  if (total_q_max < 1 || max_kv < 1 || num_sms < 0) return MLA_ERR_INVALID_ARG;
+  if (max_splits < 0 || max_splits > MLA_MAX_SPLITS || force_splits < 0 || force_splits > MLA_MAX_SPLITS)
+    return MLA_ERR_INVALID_ARG;
+  if (num_sms == 0) {
+    DeviceState* dv = nullptr;
+    const int st = device_state(&dv);
+    if (st != MLA_OK) return st;
+    num_sms = dv->num_sms;
+  }
+  const int ntiles = (max_kv + 127) / 128;
+  int S = force_splits;
+  if (S == 0) {
+    const int cap = max_splits > 0 ? max_splits : MLA_MAX_SPLITS;
+    int smax = num_sms / (batch * h_kv);
+    if (smax > cap) smax = cap;
+    if (smax > ntiles) smax = ntiles;
+    if (smax < 1) smax = 1;
+    const int best = (ntiles + smax - 1) / smax;
+    S = smax;
+    for (int c = 1; c <= smax; ++c)
+      if ((ntiles + c - 1) / c == best) {
+        S = c;
+        break;
+      }
+  }
+  out->batch = batch;
+  out->h_q = h_q;
+  out->h_kv = h_kv;
+  out->d = d;
+  out->max_q_per_seq = max_q_per_seq;
+  out->total_q_max = total_q_max;
+  out->max_kv = max_kv;
+  out->key_tile = 128;
+  out->num_splits = S;
+  out->num_sms = num_sms;
+  if (S > 1) {
+    out->o_acc_bytes = static_cast<uint64_t>(S) * total_q_max * h_q * d * 4ull;
+    out->lse_acc_offset = round_up(out->o_acc_bytes, 256);
+    out->lse_acc_bytes = static_cast<uint64_t>(S) * total_q_max * h_q * 4ull;
+    out->workspace_bytes = round_up(out->lse_acc_offset + out->lse_acc_bytes, 256);
+  }
+  return MLA_OK;
+}
+
+namespace {
+int sdpa_launch(int batch, int h_q, int h_kv, int total_q, int64_t total_kv, int num_splits, const void* q,
+                const void* k, const void* v, const int32_t* cu_q, const int32_t* cu_kv, const float* dq,
+                const float* dk, const float* dv, float sm_scale, float* o_acc, float* lse_acc, void* out,
+                int out_dtype, float inv_scale, float* lse_out, float* amax, bool direct, void* stream) {
+  if (batch < 1 || h_kv < 1 || h_q < h_kv || h_q % h_kv != 0) return MLA_ERR_INVALID_ARG;
+  const int group = h_q / h_kv;
+  if (64 % group != 0) return MLA_ERR_UNSUPPORTED;
+  if (q == nullptr || k == nullptr || v == nullptr || cu_q == nullptr || cu_kv == nullptr)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(cu_q, 4) || !aligned(cu_kv, 4))
+    return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale) || total_q < 1 || total_kv < 1 || total_kv > 0x7FFFFFFFll) return MLA_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(batch) * h_kv * num_splits > 0x7FFFFFFFll) return MLA_ERR_INVALID_ARG;
+  DeviceState* dev = nullptr;
+  int st = device_state(&dev);
+  if (st != MLA_OK) return st;
+  CUtensorMap tq, tk, tv;
+  {
+    const uint64_t dims[3] = {128, static_cast<uint64_t>(h_q), static_cast<uint64_t>(total_q)};
+    const uint64_t strides[2] = {128, static_cast<uint64_t>(h_q) * 128};
+    const uint32_t box[3] = {128, static_cast<uint32_t>(group), static_cast<uint32_t>(64 / group)};
+    if ((st = encode_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, dims, strides, box)) != MLA_OK) return st;
+  }
+  {
+    const uint64_t dims[3] = {128, static_cast<uint64_t>(h_kv), static_cast<uint64_t>(total_kv)};
+    const uint64_t strides[2] = {128, static_cast<uint64_t>(h_kv) * 128};
+    const uint32_t box[3] = {128, 1, 128};
+    if ((st = encode_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, k, dims, strides, box)) != MLA_OK) return st;
+    if ((st = encode_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, v, dims, strides, box)) != MLA_OK) return st;
+  }
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (direct && amax != nullptr) {
+    if ((st = cuda_status(cudaMemsetAsync(amax, 0, sizeof(float), cs))) != MLA_OK) return st;
+  }
+  skv::SdpaArgs a{};
+  a.q = static_cast<const uint8_t*>(q);
+  a.cu_q = cu_q;
+  a.cu_kv = cu_kv;
+  a.descale_q = dq;
+  a.descale_k = dk;
+  a.descale_v = dv;
+  a.batch = batch;
+  a.h_q = h_q;
+  a.h_kv = h_kv;
+  a.total_q = total_q;
+  a.num_splits = num_splits;
+  a.scale_log2 = sm_scale * 1.4426950408889634f;
+  a.o_acc = o_acc;
+  a.lse_acc = lse_acc;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.inv_scale = inv_scale;
+  a.lse_out = lse_out;
+  a.amax = amax;
+  a.status = dev->status;
+  a.wait_limit_ns = kWaitLimitNs;
+  return cuda_status(skv::launch_sdpa_decode(tq, tk, tv, a, direct, cs));
+}
+}  // namespace
+
+int sdpa_fp8_decode_split(const sdpa_plan_t* plan, int total_q, int64_t total_kv, const void* q, const void* k,
+                          const void* v, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                          const float* descale_q, const float* descale_k, const float* descale_v, float sm_scale,
+                          void* workspace, void* stream) {
+  if (plan == nullptr || plan->num_splits < 2 || plan->num_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID_ARG;
+  if (plan->d != 128) return MLA_ERR_UNSUPPORTED;
+  if (total_q < 1 || total_q > plan->total_q_max) return MLA_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned(workspace, 256) || plan->workspace_bytes == 0) return MLA_ERR_WORKSPACE;
+  return sdpa_launch(plan->batch, plan->h_q, plan->h_kv, total_q, total_kv, plan->num_splits, q, k, v,
+                     cu_seqlens_q, cu_seqlens_kv, descale_q, descale_k, descale_v, sm_scale,
+                     static_cast<float*>(workspace),
+                     reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan->lse_acc_offset), nullptr, 0,
+                     1.f, nullptr, nullptr, false, stream);
+}
+
+int sdpa_split_combine(const sdpa_plan_t* plan, int total_q, const void* workspace, int out_dtype,
+                       float out_inv_scale, void* out, float* lse_out, float* amax_out, void* stream) {
+  if (plan == nullptr || plan->num_splits < 2 || plan->num_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID_ARG;
+  if (plan->d != 128) return MLA_ERR_UNSUPPORTED;
+  if (total_q < 1 || total_q > plan->total_q_max || out == nullptr || !aligned(out, 16)) return MLA_ERR_INVALID_ARG;
+  if (!valid_out_dtype(out_dtype)) return MLA_ERR_INVALID_ARG;
+  if (out_dtype == MLA_OUT_E4M3 && !std::isfinite(out_inv_scale)) return MLA_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned(workspace, 256) || plan->workspace_bytes == 0) return MLA_ERR_WORKSPACE;
+  DeviceState* dev = nullptr;
+  const int st = device_state(&dev);
+  if (st != MLA_OK) return st;
+  skv::CombineArgs c{};
+  c.o_acc = static_cast<const float*>(workspace);
+  c.lse_acc = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + plan->lse_acc_offset);
+  c.num_splits = plan->num_splits;
+  c.rows = total_q * plan->h_q;
+  c.heads = plan->h_q;
+  c.d = 128;
+  c.sink = nullptr;
+  c.out = out;
+  c.out_dtype = out_dtype;
+  c.inv_scale = out_inv_scale;
+  c.lse_out = lse_out;
+  c.amax = amax_out;
+  return cuda_status(skv::launch_combine(c, static_cast<cudaStream_t>(stream)));
+}
+
+int sdpa_fp8_decode_direct(int batch, int h_q, int h_kv, int d, int total_q, int64_t total_kv, const void* q,
+                           const void* k, const void* v, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                           const float* descale_q, const float* descale_k, const float* descale_v, float sm_scale,
+                           int out_dtype, float out_inv_scale, void* out, float* lse_out, float* amax_out,
+                           void* stream) {
+  if (d != 128) return MLA_ERR_UNSUPPORTED;
+  if (out == nullptr || !aligned(out, 16) || !valid_out_dtype(out_dtype)) return MLA_ERR_INVALID_ARG;
+  if (out_dtype == MLA_OUT_E4M3 && !std::isfinite(out_inv_scale)) return MLA_ERR_INVALID_ARG;
+  return sdpa_launch(batch, h_q, h_kv, total_q, total_kv, 1, q, k, v, cu_seqlens_q, cu_seqlens_kv, descale_q,
+                     descale_k, descale_v, sm_scale, nullptr, nullptr, out, out_dtype, out_inv_scale, lse_out,
+                     amax_out, true, stream);
+}
+
+int sdpa_fp8_decode(const sdpa_plan_t* plan, int total_q, int64_t total_kv, const void* q, const void* k,
+                    const void* v, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                    const float* descale_q, const float* descale_k, const float* descale_v, float sm_scale,
+                    int out_dtype, float out_inv_scale, void* out, float* lse_out, float* amax_out,
+                    void* workspace, void* stream) {
+  if (plan == nullptr) return MLA_ERR_INVALID_ARG;
+  if (total_q > plan->total_q_max) return MLA_ERR_INVALID_ARG;
+  if (plan->num_splits == 1)
+    return sdpa_fp8_decode_direct(plan->batch, plan->h_q, plan->h_kv, plan->d, total_q, total_kv, q, k, v,
+                                  cu_seqlens_q, cu_seqlens_kv, descale_q, descale_k, descale_v, sm_scale, out_dtype,
+                                  out_inv_scale, out, lse_out, amax_out, stream);
+  if (out == nullptr || !aligned(out, 16) || !valid_out_dtype(out_dtype)) return MLA_ERR_INVALID_ARG;
+  if (out_dtype == MLA_OUT_E4M3 && !std::isfinite(out_inv_scale)) return MLA_ERR_INVALID_ARG;
+  const int st = sdpa_fp8_decode_split(plan, total_q, total_kv, q, k, v, cu_seqlens_q, cu_seqlens_kv, descale_q,
+                                       descale_k, descale_v, sm_scale, workspace, stream);
+  if (st != MLA_OK) return st;
+  return sdpa_split_combine(plan, total_q, workspace, out_dtype, out_inv_scale, out, lse_out, amax_out, stream);
+}
+
+// ---------------------------------------------------------------- status ----
+
+int mla_get_status(uint32_t* status_out, uint32_t* site_out) {
+  DeviceState* dev = nullptr;
+  const int st = device_state(&dev);
+  if (st != MLA_OK) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  uint32_t h[2] = {0, 0};
+  if (cudaMemcpy(h, dev->status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  const uint32_t zero[2] = {0, 0};
+  if (cudaMemcpy(dev->status, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  if (status_out != nullptr) *status_out = h[0];
+  if (site_out != nullptr) *site_out = h[1];
+  return MLA_OK;
+}
+
+int mla_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
+  DeviceState* dev = nullptr;
+  const int st = device_state(&dev);
+  if (st != MLA_OK) return st;
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return MLA_ERR_INVALID_ARG;
+  return cuda_status(skv::launch_wait_selftest(dev->status, limit_ns, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

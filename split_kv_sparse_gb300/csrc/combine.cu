@@ -1,0 +1,141 @@
+// Log-sum-exp combine of split-KV partials ("The Split-K Dispatch", "The LSE
+// Combine Strategy"; FlashMLA PR #25, "What changes": the combine owns the
+// attention sink and the final cast; cuDNN-frontend PR #768: it also owns the
+// amax of the recombined output).
+//
+// One warp per output row (token, head): the lanes read the row's split LSEs,
+// take M = max_s LSE_s and w_s = 2^(LSE_s - M), then stream the d-wide fp32
+// partials of the splits with w_s > 0 (empty splits are never read) as float4
+// loads, four splits in flight at a time.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "kernels.h"
+
+namespace skv {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32) combine_kernel(const CombineArgs a) {
+  constexpr int V = D / 128;   // float4 per lane
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kWarps + warp;
+  if (row >= a.rows) return;   // whole warp leaves together
+  const int S = a.num_splits;
+  const size_t rows = static_cast<size_t>(a.rows);
+
+  const float l0 = lane < S ? a.lse_acc[static_cast<size_t>(lane) * rows + row] : -INFINITY;
+  const float l1 = lane + 32 < S ? a.lse_acc[static_cast<size_t>(lane + 32) * rows + row] : -INFINITY;
+  const float M = warp_max(fmaxf(l0, l1));
+  const bool empty = (M == -INFINITY);
+  const float w0 = (l0 == -INFINITY) ? 0.f : exp2f(l0 - M);
+  const float w1 = (l1 == -INFINITY) ? 0.f : exp2f(l1 - M);
+  const float wsum = warp_sum(w0 + w1);
+
+  float4 acc[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (!empty) {
+#pragma unroll 1
+    for (int s0 = 0; s0 < S; s0 += 4) {
+      float ws[4];
+      float4 x[4][V];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int s = s0 + u;
+        const float w = (s < S) ? __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31) : 0.f;
+        ws[u] = w;
+        const float4* src = reinterpret_cast<const float4*>(a.o_acc + (static_cast<size_t>(s) * rows + row) * D);
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+          x[u][v] = (w != 0.f) ? __ldcs(src + lane + 32 * v) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+          acc[v].x = fmaf(ws[u], x[u][v].x, acc[v].x);
+          acc[v].y = fmaf(ws[u], x[u][v].y, acc[v].y);
+          acc[v].z = fmaf(ws[u], x[u][v].z, acc[v].z);
+          acc[v].w = fmaf(ws[u], x[u][v].w, acc[v].w);
+        }
+    }
+  }
+  float inv = 0.f;
+  if (!empty) {
+    float den = wsum;
+    if (a.sink != nullptr) den += exp2f(a.sink[row % a.heads] * kLog2e - M);
+    inv = 1.f / den;
+  }
+  float amax_l = 0.f;
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    acc[v].x *= inv;
+    acc[v].y *= inv;
+    acc[v].z *= inv;
+    acc[v].w *= inv;
+    amax_l = fmaxf(amax_l, fmaxf(fmaxf(fabsf(acc[v].x), fabsf(acc[v].y)),
+                                 fmaxf(fabsf(acc[v].z), fabsf(acc[v].w))));
+  }
+  const size_t base = static_cast<size_t>(row) * D;
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    const int e = 4 * (lane + 32 * v);
+    if (a.out_dtype == 0) {
+      reinterpret_cast<float4*>(static_cast<float*>(a.out) + base)[lane + 32 * v] = acc[v];
+    } else if (a.out_dtype == 1) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc[v].x, acc[v].y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc[v].z, acc[v].w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + base + e) = pk;
+    } else {
+      const float2 lo = make_float2(acc[v].x * a.inv_scale, acc[v].y * a.inv_scale);
+      const float2 hi = make_float2(acc[v].z * a.inv_scale, acc[v].w * a.inv_scale);
+      const uint32_t c01 = __nv_cvt_float2_to_fp8x2(lo, __NV_SATFINITE, __NV_E4M3);
+      const uint32_t c23 = __nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, __NV_E4M3);
+      *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.out) + base + e) = (c01 & 0xFFFFu) | (c23 << 16);
+    }
+  }
+  if (lane == 0 && a.lse_out != nullptr) a.lse_out[row] = empty ? -INFINITY : M + log2f(wsum);
+  if (a.amax != nullptr) {
+    amax_l = warp_max(amax_l);
+    if (lane == 0) atomicMax(reinterpret_cast<int*>(a.amax), __float_as_int(amax_l));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
+  if (a.amax != nullptr) {
+    const cudaError_t e = cudaMemsetAsync(a.amax, 0, sizeof(float), stream);
+    if (e != cudaSuccess) return e;
+  }
+  const dim3 grid((a.rows + kWarps - 1) / kWarps);
+  if (a.d == 512) {
+    combine_kernel<512><<<grid, kWarps * 32, 0, stream>>>(a);
+  } else if (a.d == 128) {
+    combine_kernel<128><<<grid, kWarps * 32, 0, stream>>>(a);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace skv

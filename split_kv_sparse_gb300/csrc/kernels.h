@@ -1,0 +1,93 @@
+// Host-side launch interface between the C ABI (abi.cu) and the kernel
+// translation units. Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace skv {
+
+constexpr int kMlaHeads = 64;
+constexpr int kMlaDqk = 576;
+constexpr int kMlaDv = 512;
+constexpr int kMlaBlockRows = 64;   // top-k entries per block (split unit and pipeline step)
+
+// Per-launch arguments of the sparse-MLA decode kernel (split or direct epilogue).
+struct MlaArgs {
+  const int32_t* idx;   // [s_q][topk]
+  int s_q;
+  int topk;
+  int n_kv;
+  int num_splits;       // 1 for the direct path
+  int num_blocks;       // ceil(topk / 64)
+  float scale_log2;     // sm_scale * log2(e)
+  // split path: partial workspace
+  float* o_acc;         // [S][s_q][64][512]
+  float* lse_acc;       // [S][s_q][64]
+  // direct path: final output
+  void* out;            // [s_q][64][512] of out_dtype
+  int out_dtype;
+  float inv_scale;
+  float* lse_out;       // [s_q][64] or null
+  const float* sink;    // [64] or null
+  float* amax;          // scalar or null (zeroed by the launcher)
+  uint32_t* status;     // device status words [2]
+  uint64_t wait_limit_ns;
+};
+
+// Dynamic shared memory the MLA decode kernel needs.
+int mla_decode_smem_bytes();
+
+// tm_q: Q viewed as 2-D [s_q*64 rows][576] bf16, box 64x64, 128B swizzle.
+// tm_kv: KV viewed as 2-D [n_kv rows][576] bf16, box 64x1 (gather4), 128B swizzle.
+cudaError_t launch_mla_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
+                              const MlaArgs& a, bool direct, cudaStream_t stream);
+
+// Log-sum-exp combine over `rows` output rows of width d (512 or 128).
+struct CombineArgs {
+  const float* o_acc;   // [S][rows][d]
+  const float* lse_acc; // [S][rows]
+  int num_splits;
+  int rows;             // tokens * heads
+  int heads;            // head index = row % heads (for the sink)
+  int d;
+  const float* sink;    // [heads] or null
+  void* out;
+  int out_dtype;
+  float inv_scale;
+  float* lse_out;       // [rows] or null
+  float* amax;          // scalar or null (zeroed by the launcher)
+};
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
+
+// Bounded-wait self test: one CTA waits on a barrier nobody arrives on.
+cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
+
+// Dense FP8 split-KV SDPA decode.
+struct SdpaArgs {
+  const uint8_t* q;             // [total_q][h_q][128] e4m3
+  const int32_t* cu_q;          // [batch+1]
+  const int32_t* cu_kv;         // [batch+1]
+  const float* descale_q;       // device scalars or null
+  const float* descale_k;
+  const float* descale_v;
+  int batch, h_q, h_kv, total_q, num_splits;
+  float scale_log2;
+  float* o_acc;                 // split path [S][total_q][h_q][128]
+  float* lse_acc;               // [S][total_q][h_q]
+  void* out;                    // direct path [total_q][h_q][128]
+  int out_dtype;
+  float inv_scale;
+  float* lse_out;
+  float* amax;
+  uint32_t* status;
+  uint64_t wait_limit_ns;
+};
+int sdpa_decode_smem_bytes();
+// tm_q: Q viewed as 3-D [total_q][h_q][128] e4m3, box {128 d, group heads, 64/group tokens}.
+// tm_k / tm_v: K and V viewed as 3-D [total_kv][h_kv][128] e4m3, box {128 d, 1 head, 128 keys}.
+cudaError_t launch_sdpa_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                               const SdpaArgs& a, bool direct, cudaStream_t stream);
+
+}  // namespace skv

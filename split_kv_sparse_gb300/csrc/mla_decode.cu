@@ -1,0 +1,539 @@
+// Split-KV sparse-MLA decode kernel for sm_103a (tcgen05 + TMA gather).
+//
+// What one CTA computes (FlashMLA PR #25, "What changes"): the job
+// (query token t, KV split s) walks the top-k entries [row0, row1) of its own
+// block range, gathers those rows of the shared latent KV cache, and produces
+// for each of the 64 heads either
+//   split path:  O_acc = sum_r e^{s_r} V_r / sum_r e^{s_r} (fp32) and the log2 LSE,
+//   direct path: the same O with the attention sink folded into the
+//                denominator, cast to fp32 / bf16 / e4m3, plus LSE and amax.
+//
+// Layout of the work (one CTA per job, 192 threads):
+//   warp 0     TMA: Q once (9 tiles of 64 heads x 64 dims), then per step 64
+//              gathered rows as 16 x 9 tile::gather4 loads (4 rows x 128 B each)
+//              into a ring of two 64-row halves; invalid indices become an
+//              out-of-range row, which TMA fills with zeros.
+//   warp 1     tcgen05 issue (one thread):
+//                S^T[128 window rows x 64 heads] = K_window . Q^T  (M=128, N=64, K=576)
+//                O^T[512 x 64] += V_half^T . P^T  (4 x (M=128, N=64, K=64))
+//              V is read straight out of the gathered rows as an MN-major
+//              operand; K and Q are K-major; all tiles use the 128-byte swizzle.
+//   warps 2-5  softmax on the rows of the new half (TMEM lanes 64h..64h+63),
+//              online max with a lazy rescale of O^T in TMEM, P^T (bf16) into
+//              the free RoPE column chunk of the half, then the epilogue.
+// The 128-row window is the two halves together: each step computes S^T for
+// both halves and keeps the 64 new rows, which lets every MMA use the M=128
+// data path with one TMEM lane per row.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "softmax_util.cuh"
+
+namespace skv {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kChunks = 9;                          // 576 dims = 9 column chunks of 64 (128 B)
+constexpr int kSlotBytes = 16384;                   // one column chunk of the 128-row window
+constexpr int kHalfBytes = 8192;                    // the 64-row half of a slot
+constexpr int kQChunkBytes = 8192;                  // 64 heads x 128 B
+constexpr int kRingBytes = kChunks * kSlotBytes;    // 147456
+constexpr int kQBytes = kChunks * kQChunkBytes;     // 73728
+constexpr int kStepTx = kChunks * kHalfBytes;       // bytes landing per step (64 rows x 1152 B)
+
+constexpr int kOffRing = 0;
+constexpr int kOffQ = kOffRing + kRingBytes;
+constexpr int kOffBars = kOffQ + kQBytes;
+constexpr int kOffMisc = kOffBars + 128;            // [0] tmem base, [1] abort flag, [4..] warp flags
+constexpr int kOffMuse = kOffMisc + 128;            // float[64] reference max per head (log2 units)
+constexpr int kOffAlpha = kOffMuse + 256;           // float[64] rescale factor of a rescale step
+constexpr int kOffMnew = kOffAlpha + 256;           // float[64]
+constexpr int kOffTmax = kOffMnew + 256;            // float[4][64] per-warp tile maxima
+constexpr int kOffLred = kOffTmax + 1024;           // float[4][64] per-warp row sums
+constexpr int kOffInv = kOffLred + 1024;            // float[64] 1 / denominator
+constexpr int kSmemUsed = kOffInv + 256;
+constexpr int kSmemBytes = kSmemUsed + 1024;        // slack to align the base to 1024 B
+
+enum {
+  B_QFULL = 0, B_FULL0, B_FULL1, B_EMPTY0, B_EMPTY1, B_SFULL0, B_SFULL1,
+  B_PFULL0, B_PFULL1, B_PVDONE, B_DRAIN, kNumBars
+};
+static_assert(kNumBars * 8 <= 128, "barrier area");
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS = 256;                    // S^T buffers at columns 256 and 320
+constexpr float kRescaleThreshold = 8.0f;           // p = 2^(x - m_ref) <= 256 between rescales
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Wait sites reported in the status word when a bounded wait runs out.
+enum : uint32_t {
+  W_PROD_EMPTY = 1, W_MMA_Q, W_MMA_P, W_MMA_FULL, W_SM_S, W_SM_PV_RESCALE, W_SM_PV_EPI,
+  W_DRAIN_MMA, W_DRAIN_TMA
+};
+
+template <bool kDirect>
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_kv, const MlaArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- job decode: one place, shared by every role --------------------------
+  const int t = blockIdx.x / a.num_splits;
+  const int s = blockIdx.x - t * a.num_splits;
+  const int base = a.num_blocks / a.num_splits;
+  const int rem = a.num_blocks - base * a.num_splits;
+  const int blk0 = s * base + min(s, rem);
+  const int nblk = base + (s < rem ? 1 : 0);
+  const int row0 = min(blk0 * kMlaBlockRows, a.topk);
+  const int row1 = min((blk0 + nblk) * kMlaBlockRows, a.topk);
+  const int nsteps = (row1 - row0 + kMlaBlockRows - 1) / kMlaBlockRows;
+  const size_t out_row = kDirect ? static_cast<size_t>(t) * kMlaHeads
+                                 : (static_cast<size_t>(s) * a.s_q + t) * kMlaHeads;
+
+  if (nsteps == 0) {
+    // A split with no block of its own: O = 0, LSE = -inf (only the split path
+    // can have one; the direct path always has topk >= 1 entries).
+    float4* o = reinterpret_cast<float4*>(a.o_acc + out_row * kMlaDv);
+    for (int i = threadIdx.x; i < kMlaHeads * kMlaDv / 4; i += kThreads)
+      o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (threadIdx.x < kMlaHeads) a.lse_acc[out_row + threadIdx.x] = -INFINITY;
+    return;
+  }
+
+  auto bar = [&](int i) -> uint32_t { return sbase + kOffBars + 8 * i; };
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  volatile int* flags = reinterpret_cast<volatile int*>(misc + 4);   // [2][4] step flags, [8..11] final
+  float* m_use = reinterpret_cast<float*>(smem + kOffMuse);
+  float* alpha = reinterpret_cast<float*>(smem + kOffAlpha);
+  float* m_new = reinterpret_cast<float*>(smem + kOffMnew);
+  float* tmax = reinterpret_cast<float*>(smem + kOffTmax);
+  float* lred = reinterpret_cast<float*>(smem + kOffLred);
+  float* inv_s = reinterpret_cast<float*>(smem + kOffInv);
+  const WaitCtx wc{a.wait_limit_ns, a.status, abort_flag};
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(B_QFULL), 1);
+    mbar_init(bar(B_FULL0), 1);
+    mbar_init(bar(B_FULL1), 1);
+    mbar_init(bar(B_EMPTY0), 1);
+    mbar_init(bar(B_EMPTY1), 1);
+    mbar_init(bar(B_SFULL0), 1);
+    mbar_init(bar(B_SFULL1), 1);
+    mbar_init(bar(B_PFULL0), 4);
+    mbar_init(bar(B_PFULL1), 4);
+    mbar_init(bar(B_PVDONE), 1);
+    mbar_init(bar(B_DRAIN), 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (threadIdx.x >= 64 && threadIdx.x < 128) m_use[threadIdx.x - 64] = -INFINITY;
+  if (warp == 1) {
+    tmem_alloc(smem_u32(misc), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+
+  if (warp == 0) {
+    // ======================================================= TMA producer ===
+    const int32_t* idx_t = a.idx + static_cast<size_t>(t) * a.topk;
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_kv);
+      mbar_arrive_expect_tx(bar(B_QFULL), kQBytes);
+#pragma unroll 1
+      for (int c = 0; c < kChunks; ++c)
+        tma_load_2d(sbase + kOffQ + c * kQChunkBytes, &tm_q, 64 * c, kMlaHeads * t, bar(B_QFULL));
+    }
+    // lane g < 16 owns rows 4g..4g+3 of each step
+    auto load_rows = [&](int k, int (&y)[4]) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = row0 + kMlaBlockRows * k + 4 * lane + i;
+        int v = -1;
+        if (lane < 16 && r < row1) {
+          v = __ldg(idx_t + r);
+          if (v < 0 || v >= a.n_kv) v = -1;
+        }
+        y[i] = v;
+      }
+    };
+    int cur[4];
+    load_rows(0, cur);
+    int last_issued[2] = {-1, -1};
+    bool ok = true;
+#pragma unroll 1
+    for (int k = 0; k < nsteps; ++k) {
+      const int h = k & 1;
+      int nxt[4] = {-1, -1, -1, -1};
+      if (k + 1 < nsteps) load_rows(k + 1, nxt);       // in flight while we wait for the slot
+      if (k >= 2) {
+        int w = 1;
+        if (lane == 0) w = wait_bounded(bar(B_EMPTY0 + h), ((k >> 1) - 1) & 1, wc, W_PROD_EMPTY);
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (!w) {
+          ok = false;
+          break;
+        }
+      }
+      if (lane == 0) mbar_arrive_expect_tx(bar(B_FULL0 + h), kStepTx);
+      __syncwarp();
+      if (lane < 16) {
+        const uint32_t dst = sbase + kOffRing + h * kHalfBytes + lane * 512;
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c)
+          tma_gather4(dst + c * kSlotBytes, &tm_kv, 64 * c, cur[0], cur[1], cur[2], cur[3],
+                      bar(B_FULL0 + h));
+      }
+      last_issued[h] = k;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
+    }
+    if (!ok && lane == 0) {
+      // leave no load in flight into this CTA's shared memory
+      for (int h = 0; h < 2; ++h)
+        if (last_issued[h] >= 0 &&
+            !wait_drain(bar(B_FULL0 + h), (last_issued[h] >> 1) & 1, a.wait_limit_ns))
+          atomicCAS(&a.status[1], 0u, W_DRAIN_TMA);
+    }
+  } else if (warp == 1) {
+    // ========================================================= MMA issuer ===
+    if (lane == 0) {
+      constexpr uint32_t kIdescQK = idesc_make(128, 64, 1, false, false);
+      constexpr uint32_t kIdescPV = idesc_make(128, 64, 1, true, false);
+      const uint32_t ring = sbase + kOffRing;
+      const uint32_t qs = sbase + kOffQ;
+      auto issue_qk = [&](int k) {
+        const uint32_t d = tmem + kTmemS + 64 * (k & 1);
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f16(d, sdesc_sw128(ring + c * kSlotBytes + kk * 32, 16, 1024),
+                    sdesc_sw128(qs + c * kQChunkBytes + kk * 32, 16, 1024), kIdescQK,
+                    (c | kk) != 0);
+      };
+      auto issue_pv = [&](int k) {
+        const int h = k & 1;
+        const uint32_t pt = ring + 8 * kSlotBytes + h * kHalfBytes;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f16(tmem + 64 * j,
+                    sdesc_sw128(ring + 2 * j * kSlotBytes + h * kHalfBytes + kk * 2048, kSlotBytes,
+                                1024),
+                    sdesc_sw128(pt + kk * 32, 16, 1024), kIdescPV, (k > 0 || kk > 0));
+      };
+      bool ok = wait_bounded(bar(B_QFULL), 0, wc, W_MMA_Q);
+#pragma unroll 1
+      for (int k = 0; ok && k < nsteps; ++k) {
+        if (k >= 1) {
+          ok = wait_bounded(bar(B_PFULL0 + ((k - 1) & 1)), ((k - 1) >> 1) & 1, wc, W_MMA_P);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(k - 1);
+          mma_commit(bar(B_EMPTY0 + ((k - 1) & 1)));
+          mma_commit(bar(B_PVDONE));
+        }
+        ok = wait_bounded(bar(B_FULL0 + (k & 1)), (k >> 1) & 1, wc, W_MMA_FULL);
+        if (!ok) break;
+        tc_fence_after();
+        issue_qk(k);
+        mma_commit(bar(B_SFULL0 + (k & 1)));
+      }
+      if (ok) {
+        const int k = nsteps - 1;
+        ok = wait_bounded(bar(B_PFULL0 + (k & 1)), (k >> 1) & 1, wc, W_MMA_P);
+        if (ok) {
+          tc_fence_after();
+          issue_pv(k);
+          mma_commit(bar(B_EMPTY0 + (k & 1)));
+          mma_commit(bar(B_PVDONE));
+        }
+      }
+      if (!ok) {
+        // no MMA may still be reading shared memory or writing TMEM when the CTA exits
+        mma_commit(bar(B_DRAIN));
+        if (!wait_drain(bar(B_DRAIN), 0, a.wait_limit_ns)) atomicCAS(&a.status[1], 0u, W_DRAIN_MMA);
+      }
+    }
+  } else {
+    // ============================================== softmax + epilogue ====
+    const int sp = warp & 3;               // TMEM sub-partition (lanes 32sp..32sp+31)
+    const int wi = warp - 2;               // 0..3
+    const int tid = threadIdx.x - 64;      // 0..127
+    const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
+    const int32_t* idx_t = a.idx + static_cast<size_t>(t) * a.topk;
+    uint8_t* const ring_p = smem + kOffRing;
+    // Running softmax denominators of heads 2*lane and 2*lane+1 over this warp's
+    // rows: lsum* from the fp32 p (gives the LSE), rsum* from the bf16-rounded p
+    // that the PV MMA actually multiplies (normalises O, so a dominant row comes
+    // out exact instead of carrying its own rounding error).
+    float lsum0 = 0.f, lsum1 = 0.f, rsum0 = 0.f, rsum1 = 0.f;
+    int bad = 0;   // a bounded wait of this warp ran out
+
+#pragma unroll 1
+    for (int k = 0; k < nsteps; ++k) {
+      const int h = k & 1;
+      const bool active = (sp >> 1) == h;  // this warp's lanes hold the new half's rows
+      const int rloc = (sp & 1) * 32 + lane;
+      const int r = row0 + kMlaBlockRows * k + rloc;
+      int myidx = -1;
+      if (active && r < row1) myidx = __ldg(idx_t + r);
+      const bool valid = active && r < row1 && myidx >= 0 && myidx < a.n_kv;
+
+      int w = 1;
+      if (lane == 0) w = wait_bounded(bar(B_SFULL0 + h), (k >> 1) & 1, wc, W_SM_S);
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (!w) bad = 1;
+      tc_fence_after();
+
+      float x[64];
+      if (active && w) {
+        uint32_t raw[64];
+        tmem_ld_32x32b_x64(tmem + lane_base + kTmemS + 64 * h, raw);
+        tmem_wait_ld_x64(raw);
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          x[i] = valid ? __uint_as_float(raw[i]) * a.scale_log2 : -INFINITY;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) x[i] = -INFINITY;
+      }
+
+      // Lazy rescale: only when some score exceeds its head's reference max by
+      // more than the threshold (always on the first valid row of a head).
+      bool need = false;
+      if (valid) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) need |= x[i] > m_use[i] + kRescaleThreshold;
+      }
+      const unsigned vote = __ballot_sync(0xffffffffu, need);
+      if (lane == 0) flags[(k & 1) * 4 + wi] = (vote != 0u ? 1 : 0) | (bad ? 2 : 0);
+      named_bar_sync(1, 128);
+      const int f = flags[(k & 1) * 4 + 0] | flags[(k & 1) * 4 + 1] | flags[(k & 1) * 4 + 2] |
+                    flags[(k & 1) * 4 + 3];
+      if (f & 2) {
+        bad = 1;
+        break;   // every softmax warp sees the same flags and leaves together
+      }
+      if (f & 1) {
+        float mx0, mx1;
+        warp_transpose_reduce<true>(x, lane, mx0, mx1);
+        tmax[wi * 64 + 2 * lane] = mx0;
+        tmax[wi * 64 + 2 * lane + 1] = mx1;
+        named_bar_sync(1, 128);
+        if (tid < 64) {
+          const float tm = fmaxf(fmaxf(tmax[tid], tmax[64 + tid]), fmaxf(tmax[128 + tid], tmax[192 + tid]));
+          const float mo = m_use[tid];
+          const float mn = fmaxf(mo, tm);
+          alpha[tid] = (mn == -INFINITY) ? 1.f : ex2_approx(mo - mn);
+          m_new[tid] = mn;
+        }
+        named_bar_sync(1, 128);
+        lsum0 *= alpha[2 * lane];
+        lsum1 *= alpha[2 * lane + 1];
+        rsum0 *= alpha[2 * lane];
+        rsum1 *= alpha[2 * lane + 1];
+        if (k >= 1) {
+          // O^T holds PV of steps < k: wait for the last one, then scale every head column
+          int wp = 1;
+          if (lane == 0) wp = wait_bounded(bar(B_PVDONE), (k - 1) & 1, wc, W_SM_PV_RESCALE);
+          wp = __shfl_sync(0xffffffffu, wp, 0);
+          tc_fence_after();
+          if (wp) {
+#pragma unroll 1
+            for (int j = 0; j < 8; ++j) {   // 4 O^T chunks x 2 halves of 32 head columns
+              uint32_t o[32];
+              const int c0 = 32 * (j & 1);
+              tmem_ld_32x32b_x32(tmem + lane_base + 64 * (j >> 1) + c0, o);
+              tmem_wait_ld_x32(o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha[c0 + i]);
+              tmem_st_32x32b_x32(tmem + lane_base + 64 * (j >> 1) + c0, o);
+            }
+            tmem_wait_st();
+          } else {
+            bad = 1;
+          }
+        }
+        if (tid < 64) m_use[tid] = m_new[tid];
+        named_bar_sync(1, 128);
+      }
+
+      if (active) {
+        // p = 2^(x - m_ref) into P^T (bf16, K-major, 128-byte swizzle) in the
+        // RoPE chunk of this half, which the QK of this step no longer needs.
+        uint8_t* pt = ring_p + 8 * kSlotBytes + h * kHalfBytes;
+        const int rchunk = rloc >> 3;
+        const int rbyte = (rloc & 7) * 2;
+        float pr[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const float p = (x[i] == -INFINITY) ? 0.f : ex2_approx(x[i] - m_use[i]);
+          x[i] = p;
+          const __nv_bfloat16 pb = __float2bfloat16_rn(p);
+          pr[i] = __bfloat162float(pb);
+          const int off = (i >> 3) * 1024 + (i & 7) * 128 + ((rchunk ^ (i & 7)) << 4) + rbyte;
+          *reinterpret_cast<__nv_bfloat16*>(pt + off) = pb;
+        }
+        fence_proxy_async_smem();
+        float s0, s1;
+        warp_transpose_reduce<false>(x, lane, s0, s1);
+        lsum0 += s0;
+        lsum1 += s1;
+        warp_transpose_reduce<false>(pr, lane, s0, s1);
+        rsum0 += s0;
+        rsum1 += s1;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_PFULL0 + h));
+    }
+
+    // ---- epilogue ---------------------------------------------------------
+    lred[wi * 64 + 2 * lane] = lsum0;
+    lred[wi * 64 + 2 * lane + 1] = lsum1;
+    tmax[wi * 64 + 2 * lane] = rsum0;       // the tile-max scratch is free here
+    tmax[wi * 64 + 2 * lane + 1] = rsum1;
+    if (lane == 0) flags[8 + wi] = bad;
+    named_bar_sync(1, 128);
+    const bool any_bad = flags[8] | flags[9] | flags[10] | flags[11];
+    if (tid < 64) {
+      const float l = (lred[tid] + lred[64 + tid]) + (lred[128 + tid] + lred[192 + tid]);
+      const float lr = (tmax[tid] + tmax[64 + tid]) + (tmax[128 + tid] + tmax[192 + tid]);
+      const float mu = m_use[tid];
+      float lse = -INFINITY, inv = 0.f;
+      if (l > 0.f) {
+        lse = mu + log2f(l);
+        float den = lr;
+        if (kDirect && a.sink != nullptr) den += exp2f(a.sink[tid] * kLog2e - mu);
+        inv = 1.f / den;
+      }
+      inv_s[tid] = inv;
+      if (kDirect) {
+        if (a.lse_out != nullptr) a.lse_out[out_row + tid] = lse;
+      } else {
+        a.lse_acc[out_row + tid] = lse;
+      }
+    }
+    named_bar_sync(1, 128);
+    if (!any_bad) {
+      int wp = 1;
+      if (lane == 0) wp = wait_bounded(bar(B_PVDONE), (nsteps - 1) & 1, wc, W_SM_PV_EPI);
+      wp = __shfl_sync(0xffffffffu, wp, 0);
+      tc_fence_after();
+      if (wp) {
+        float amax_l = 0.f;
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+          uint32_t o[64];
+          tmem_ld_32x32b_x64(tmem + lane_base + 64 * j, o);
+          tmem_wait_ld_x64(o);
+          const int d = 128 * j + 32 * sp + lane;
+          if (!kDirect) {
+            float* dst = a.o_acc + out_row * kMlaDv + d;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) dst[c * kMlaDv] = __uint_as_float(o[c]) * inv_s[c];
+          } else if (a.out_dtype == 0) {
+            float* dst = static_cast<float*>(a.out) + out_row * kMlaDv + d;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+              const float v = __uint_as_float(o[c]) * inv_s[c];
+              amax_l = fmaxf(amax_l, fabsf(v));
+              dst[c * kMlaDv] = v;
+            }
+          } else if (a.out_dtype == 1) {
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + out_row * kMlaDv + d;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+              const float v = __uint_as_float(o[c]) * inv_s[c];
+              amax_l = fmaxf(amax_l, fabsf(v));
+              dst[c * kMlaDv] = __float2bfloat16_rn(v);
+            }
+          } else {
+            uint8_t* dst = static_cast<uint8_t*>(a.out) + out_row * kMlaDv + d;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+              const float v = __uint_as_float(o[c]) * inv_s[c];
+              amax_l = fmaxf(amax_l, fabsf(v));
+              dst[c * kMlaDv] = static_cast<uint8_t>(
+                  __nv_cvt_float_to_fp8(v * a.inv_scale, __NV_SATFINITE, __NV_E4M3));
+            }
+          }
+        }
+        if (kDirect && a.amax != nullptr) {
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) amax_l = fmaxf(amax_l, __shfl_xor_sync(0xffffffffu, amax_l, o));
+          if (lane == 0) atomicMax(reinterpret_cast<int*>(a.amax), __float_as_int(amax_l));
+        }
+      }
+    }
+  }
+
+  // ---- teardown: every role reaches this point, TMEM is freed by its owner --
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+int mla_decode_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_mla_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const MlaArgs& a,
+                              bool direct, cudaStream_t stream) {
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  const dim3 grid(static_cast<unsigned>(a.s_q) * static_cast<unsigned>(a.num_splits));
+  cudaError_t e;
+  if (direct) {
+    e = cudaFuncSetAttribute(mla_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
+    if (e != cudaSuccess) return e;
+    mla_decode_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_kv, a);
+  } else {
+    e = cudaFuncSetAttribute(mla_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
+    if (e != cudaSuccess) return e;
+    mla_decode_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_kv, a);
+  }
+  return cudaGetLastError();
+}
+
+// ---- bounded-wait self test ---------------------------------------------------
+
+__global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t b;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&b), 1);
+    abort_flag = 0;
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const WaitCtx wc{limit_ns, status, &abort_flag};
+    (void)wait_bounded(smem_u32(&b), 0, wc, 0x5E1F);   // nothing ever arrives
+  }
+}
+
+cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace skv

@@ -1,0 +1,491 @@
+// Dense split-KV FP8 SDPA decode for sm_103a (the form of cuDNN-frontend PR #768,
+// SM120 FP8 commit): per-tensor scaled e4m3 Q/K/V, GQA, bottom-right causal
+// mask, the KV range of each sequence cut into near-equal runs of 128-key
+// tiles with the remainder to the leading splits, fp32 partial O + log2 LSE
+// into split-major slots (or, unsplit, a direct bf16/fp32/e4m3 epilogue that
+// also computes the amax).
+//
+// One CTA per job (sequence b, KV head g, split s), 320 threads:
+//   warp 0     TMA: the job's Q rows once (the group's h_q/h_kv heads of up to
+//              64/group tokens = 64 rows x 128 B), then per tile K and V
+//              (128 keys x 128 B each, e4m3) into a 3-stage ring.
+//   warp 1     tcgen05 issue:  S^T[128 keys x 64 rows] = K . Q^T   (kind::f8f6f4, K=128)
+//                              O^T[128 d x 64 rows] += V^T . P^T   (kind::f16, f16 operands)
+//   warps 2-5  softmax over keys (TMEM lane = key), lazy rescale of O^T,
+//              P^T in f16, then the epilogue.
+//   warps 6-9  convert each V tile from e4m3 to f16 (exact) into the
+//              MN-major 128-byte-swizzled layout the PV MMA reads.
+// The QK product of e4m3 codes is exact in fp32; descales multiply the scores
+// (dq*dk*sm_scale) and the output (dv).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "softmax_util.cuh"
+
+namespace skv {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kD = 128;
+constexpr int kTile = 128;                 // keys per tile (split unit)
+constexpr int kRows = 64;                  // query rows per job (tokens x group heads)
+constexpr int kStages = 3;
+constexpr int kKVTileBytes = kTile * kD;   // 16384 (e4m3)
+constexpr int kStageBytes = 2 * kKVTileBytes;
+constexpr int kV16Bytes = kTile * kD * 2;  // 32768
+constexpr int kPBytes = kRows * kTile * 2; // 16384
+constexpr int kQBytes = kRows * kD;        // 8192
+
+constexpr int kOffStage = 0;
+constexpr int kOffV16 = kOffStage + kStages * kStageBytes;   // 98304
+constexpr int kOffP = kOffV16 + 2 * kV16Bytes;               // 163840
+constexpr int kOffQ = kOffP + 2 * kPBytes;                   // 196608
+constexpr int kOffBars = kOffQ + kQBytes;                    // 204800
+constexpr int kOffMisc = kOffBars + 256;
+constexpr int kOffMuse = kOffMisc + 128;
+constexpr int kOffAlpha = kOffMuse + 256;
+constexpr int kOffMnew = kOffAlpha + 256;
+constexpr int kOffTmax = kOffMnew + 256;
+constexpr int kOffLred = kOffTmax + 1024;
+constexpr int kOffInv = kOffLred + 1024;
+constexpr int kOffLim = kOffInv + 256;                       // int[64] last visible key per row
+constexpr int kSmemUsed = kOffLim + 256;
+constexpr int kSmemBytes = kSmemUsed + 1024;
+
+enum {
+  B_QFULL = 0, B_SFULL_STAGE0, B_SFULL_STAGE1, B_SFULL_STAGE2, B_SEMPTY0, B_SEMPTY1, B_SEMPTY2,
+  B_SREADY0, B_SREADY1, B_PFULL0, B_PFULL1, B_V16FULL0, B_V16FULL1, B_V16EMPTY0, B_V16EMPTY1,
+  B_FINAL, B_DRAIN, kNumBars
+};
+static_assert(kNumBars * 8 <= 256, "barrier area");
+
+constexpr uint32_t kTmemCols = 256;        // O^T at [0, 64), S^T buffers at 64 and 128
+constexpr uint32_t kTmemS = 64;
+constexpr float kRescaleThreshold = 8.0f;
+
+enum : uint32_t {
+  W_PROD = 101, W_MMA_Q, W_MMA_P, W_MMA_V, W_MMA_FULL, W_SM_S, W_SM_FINAL, W_CV_FULL, W_CV_EMPTY,
+  W_DRAIN_MMA2, W_DRAIN_TMA2
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    sdpa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const SdpaArgs a, const int direct) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- job decode (shared by every role) ------------------------------------
+  const int S = a.num_splits;
+  const int s = blockIdx.x % S;
+  const int bg = blockIdx.x / S;
+  const int g = bg % a.h_kv;
+  const int b = bg / a.h_kv;
+  const int group = a.h_q / a.h_kv;
+  const int q0 = a.cu_q[b];
+  const int sq = a.cu_q[b + 1] - q0;
+  const int k0 = a.cu_kv[b];
+  const int kvlen = a.cu_kv[b + 1] - k0;
+  const int R = sq * group;                              // valid rows, <= 64
+  const int ntiles_all = (kvlen + kTile - 1) / kTile;
+  const int base = ntiles_all / S, rem = ntiles_all - base * S;
+  const int tile0 = s * base + min(s, rem);
+  const int nt = base + (s < rem ? 1 : 0);
+  const int key_end = min((tile0 + nt) * kTile, kvlen);  // exclusive, sequence-relative
+  const float dq = a.descale_q ? *a.descale_q : 1.f;
+  const float dk = a.descale_k ? *a.descale_k : 1.f;
+  const float dv = a.descale_v ? *a.descale_v : 1.f;
+  // output row of (row rho): token q0 + rho / group, head g*group + rho % group
+  auto out_index = [&](int rho) -> size_t {
+    const size_t tok = static_cast<size_t>(q0 + rho / group);
+    const size_t head = static_cast<size_t>(g * group + rho % group);
+    return direct ? tok * a.h_q + head : (static_cast<size_t>(s) * a.total_q + tok) * a.h_q + head;
+  };
+
+  if (R > kRows) {   // more query rows than one job holds: refuse, report, write nothing
+    if (threadIdx.x == 0) atomicOr(&a.status[0], 2u);
+    return;
+  }
+  if (nt == 0 || R <= 0) {
+    // nothing to attend in this split: O = 0, LSE = -inf for the job's rows
+    for (int i = threadIdx.x; i < R * kD; i += kThreads) {
+      const size_t oi = out_index(i / kD) * kD + (i % kD);
+      if (!direct) a.o_acc[oi] = 0.f;
+      else if (a.out_dtype == 0) static_cast<float*>(a.out)[oi] = 0.f;
+      else if (a.out_dtype == 1) static_cast<__nv_bfloat16*>(a.out)[oi] = __float2bfloat16_rn(0.f);
+      else static_cast<uint8_t*>(a.out)[oi] = 0;
+    }
+    for (int i = threadIdx.x; i < R; i += kThreads) {
+      if (!direct) a.lse_acc[out_index(i)] = -INFINITY;
+      else if (a.lse_out != nullptr) a.lse_out[out_index(i)] = -INFINITY;
+    }
+    return;
+  }
+
+  auto bar = [&](int i) -> uint32_t { return sbase + kOffBars + 8 * i; };
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  volatile int* flags = reinterpret_cast<volatile int*>(misc + 4);
+  float* m_use = reinterpret_cast<float*>(smem + kOffMuse);
+  float* alpha = reinterpret_cast<float*>(smem + kOffAlpha);
+  float* m_new = reinterpret_cast<float*>(smem + kOffMnew);
+  float* tmax = reinterpret_cast<float*>(smem + kOffTmax);
+  float* lred = reinterpret_cast<float*>(smem + kOffLred);
+  float* inv_s = reinterpret_cast<float*>(smem + kOffInv);
+  int* lim = reinterpret_cast<int*>(smem + kOffLim);
+  const WaitCtx wc{a.wait_limit_ns, a.status, abort_flag};
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(B_QFULL), 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(bar(B_SFULL_STAGE0 + i), 1);
+      mbar_init(bar(B_SEMPTY0 + i), 5);            // QK commit + 4 converter warps
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_SREADY0 + i), 1);
+      mbar_init(bar(B_PFULL0 + i), 4);
+      mbar_init(bar(B_V16FULL0 + i), 4);
+      mbar_init(bar(B_V16EMPTY0 + i), 1);
+    }
+    mbar_init(bar(B_FINAL), 1);
+    mbar_init(bar(B_DRAIN), 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (threadIdx.x >= 64 && threadIdx.x < 128) {
+    const int rho = threadIdx.x - 64;
+    m_use[rho] = -INFINITY;
+    // last key (sequence-relative) row rho may see inside this split: bottom-right causal
+    const int pos = kvlen - sq + rho / group;
+    lim[rho] = rho < R ? min(key_end - 1, pos) : -1;
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(misc), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+
+  if (warp == 0) {
+    // ======================================================= TMA producer ===
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(bar(B_QFULL), kQBytes);
+      tma_load_3d(sbase + kOffQ, &tm_q, 0, g * group, q0, bar(B_QFULL));
+      int last[kStages] = {-1, -1, -1};
+      bool ok = true;
+#pragma unroll 1
+      for (int t = 0; t < nt; ++t) {
+        const int st = t % kStages;
+        if (t >= kStages && !wait_bounded(bar(B_SEMPTY0 + st), ((t / kStages) - 1) & 1, wc, W_PROD)) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = sbase + kOffStage + st * kStageBytes;
+        mbar_arrive_expect_tx(bar(B_SFULL_STAGE0 + st), kStageBytes);
+        const int key = k0 + (tile0 + t) * kTile;
+        tma_load_3d(dst, &tm_k, 0, g, key, bar(B_SFULL_STAGE0 + st));
+        tma_load_3d(dst + kKVTileBytes, &tm_v, 0, g, key, bar(B_SFULL_STAGE0 + st));
+        last[st] = t;
+      }
+      if (!ok)
+        for (int st = 0; st < kStages; ++st)
+          if (last[st] >= 0 && !wait_drain(bar(B_SFULL_STAGE0 + st), (last[st] / kStages) & 1, a.wait_limit_ns))
+            atomicCAS(&a.status[1], 0u, W_DRAIN_TMA2);
+    }
+  } else if (warp == 1) {
+    // ========================================================= MMA issuer ===
+    if (lane == 0) {
+      constexpr uint32_t kIdescQK = idesc_make(128, 64, 0, false, false);   // e4m3 x e4m3
+      constexpr uint32_t kIdescPV = idesc_make(128, 64, 0, true, false);    // f16, A MN-major
+      auto issue_qk = [&](int t) {
+        const uint32_t kt = sbase + kOffStage + (t % kStages) * kStageBytes;
+        const uint32_t d = tmem + kTmemS + 64 * (t & 1);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f8(d, sdesc_sw128(kt + kk * 32, 16, 1024), sdesc_sw128(sbase + kOffQ + kk * 32, 16, 1024),
+                 kIdescQK, kk != 0);
+      };
+      auto issue_pv = [&](int t) {
+        const uint32_t v16 = sbase + kOffV16 + (t & 1) * kV16Bytes;
+        const uint32_t pt = sbase + kOffP + (t & 1) * kPBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_f16(tmem, sdesc_sw128(v16 + kk * 2048, 16384, 1024),
+                  sdesc_sw128(pt + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), kIdescPV, (t > 0 || kk > 0));
+      };
+      bool ok = wait_bounded(bar(B_QFULL), 0, wc, W_MMA_Q);
+#pragma unroll 1
+      for (int t = 0; ok && t < nt; ++t) {
+        if (t >= 1) {
+          const int u = t - 1;
+          ok = wait_bounded(bar(B_PFULL0 + (u & 1)), (u >> 1) & 1, wc, W_MMA_P) &&
+               wait_bounded(bar(B_V16FULL0 + (u & 1)), (u >> 1) & 1, wc, W_MMA_V);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(u);
+          mma_commit(bar(B_V16EMPTY0 + (u & 1)));
+        }
+        ok = wait_bounded(bar(B_SFULL_STAGE0 + t % kStages), (t / kStages) & 1, wc, W_MMA_FULL);
+        if (!ok) break;
+        tc_fence_after();
+        issue_qk(t);
+        mma_commit(bar(B_SREADY0 + (t & 1)));
+        mma_commit(bar(B_SEMPTY0 + t % kStages));
+      }
+      if (ok) {
+        const int u = nt - 1;
+        ok = wait_bounded(bar(B_PFULL0 + (u & 1)), (u >> 1) & 1, wc, W_MMA_P) &&
+             wait_bounded(bar(B_V16FULL0 + (u & 1)), (u >> 1) & 1, wc, W_MMA_V);
+        if (ok) {
+          tc_fence_after();
+          issue_pv(u);
+          mma_commit(bar(B_V16EMPTY0 + (u & 1)));
+          mma_commit(bar(B_FINAL));
+        }
+      }
+      if (!ok) {
+        mma_commit(bar(B_DRAIN));
+        if (!wait_drain(bar(B_DRAIN), 0, a.wait_limit_ns)) atomicCAS(&a.status[1], 0u, W_DRAIN_MMA2);
+      }
+    }
+  } else if (warp >= 6) {
+    // ==================================================== V e4m3 -> f16 ===
+    const int key = threadIdx.x - 192;      // 0..127: one key row per thread
+    const int r8 = key & 7;
+#pragma unroll 1
+    for (int t = 0; t < nt; ++t) {
+      const int st = t % kStages;
+      int w = 1;
+      if (lane == 0) {
+        w = wait_bounded(bar(B_SFULL_STAGE0 + st), (t / kStages) & 1, wc, W_CV_FULL);
+        if (w && t >= 2) w = wait_bounded(bar(B_V16EMPTY0 + (t & 1)), ((t - 2) >> 1) & 1, wc, W_CV_EMPTY);
+      }
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (!w) break;   // the abort flag is set; the other roles stop on their own waits
+      const uint8_t* vrow = smem + kOffStage + st * kStageBytes + kKVTileBytes + (key >> 3) * 1024 + r8 * 128;
+      uint8_t* v16 = smem + kOffV16 + (t & 1) * kV16Bytes + (key >> 3) * 1024 + r8 * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {              // 16 e4m3 values (d = 16c .. 16c+15) per chunk
+        const uint4 raw = *reinterpret_cast<const uint4*>(vrow + ((c ^ r8) << 4));
+        const uint32_t wds[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t h[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wds[j] & 0xFFFFu), __NV_E4M3);
+          const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wds[j] >> 16), __NV_E4M3);
+          h[2 * j] = static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16);
+          h[2 * j + 1] = static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16);
+        }
+        // d = 16c .. 16c+7 -> MN atom (16c)/64, 16-B chunk ((16c)%64)/8; then +8
+        const int d0 = 16 * c;
+        const int a0 = d0 >> 6, c0 = (d0 & 63) >> 3;
+        *reinterpret_cast<uint4*>(v16 + a0 * 16384 + ((c0 ^ r8) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(v16 + a0 * 16384 + (((c0 + 1) ^ r8) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(B_V16FULL0 + (t & 1)));
+        mbar_arrive(bar(B_SEMPTY0 + st));
+      }
+    }
+  } else {
+    // ============================================== softmax + epilogue ====
+    const int sp = warp & 3;
+    const int wi = warp - 2;
+    const int tid = threadIdx.x - 64;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
+    const float sc = dq * dk * a.scale_log2;
+    float lsum0 = 0.f, lsum1 = 0.f, rsum0 = 0.f, rsum1 = 0.f;
+    int bad = 0;
+#pragma unroll 1
+    for (int t = 0; t < nt; ++t) {
+      const int keyrel = (tile0 + t) * kTile + 32 * sp + lane;   // this thread's key, sequence-relative
+      int w = 1;
+      if (lane == 0) w = wait_bounded(bar(B_SREADY0 + (t & 1)), (t >> 1) & 1, wc, W_SM_S);
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (!w) bad = 1;
+      tc_fence_after();
+      float x[64];
+      if (w) {
+        uint32_t raw[64];
+        tmem_ld_32x32b_x64(tmem + lane_base + kTmemS + 64 * (t & 1), raw);
+        tmem_wait_ld_x64(raw);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) x[i] = keyrel <= lim[i] ? __uint_as_float(raw[i]) * sc : -INFINITY;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) x[i] = -INFINITY;
+      }
+      bool need = false;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) need |= x[i] > m_use[i] + kRescaleThreshold;
+      const unsigned vote = __ballot_sync(0xffffffffu, need);
+      if (lane == 0) flags[(t & 1) * 4 + wi] = (vote != 0u ? 1 : 0) | (bad ? 2 : 0);
+      named_bar_sync(1, 128);
+      const int f = flags[(t & 1) * 4 + 0] | flags[(t & 1) * 4 + 1] | flags[(t & 1) * 4 + 2] |
+                    flags[(t & 1) * 4 + 3];
+      if (f & 2) {
+        bad = 1;
+        break;
+      }
+      if (f & 1) {
+        float mx0, mx1;
+        warp_transpose_reduce<true>(x, lane, mx0, mx1);
+        tmax[wi * 64 + 2 * lane] = mx0;
+        tmax[wi * 64 + 2 * lane + 1] = mx1;
+        named_bar_sync(1, 128);
+        if (tid < 64) {
+          const float tm = fmaxf(fmaxf(tmax[tid], tmax[64 + tid]), fmaxf(tmax[128 + tid], tmax[192 + tid]));
+          const float mo = m_use[tid];
+          const float mn = fmaxf(mo, tm);
+          alpha[tid] = (mn == -INFINITY) ? 1.f : ex2_approx(mo - mn);
+          m_new[tid] = mn;
+        }
+        named_bar_sync(1, 128);
+        lsum0 *= alpha[2 * lane];
+        lsum1 *= alpha[2 * lane + 1];
+        rsum0 *= alpha[2 * lane];
+        rsum1 *= alpha[2 * lane + 1];
+        if (t >= 1) {
+          // S^T(t) ready implies every earlier PV has completed: O^T is final up to tile t-1
+#pragma unroll 1
+          for (int j = 0; j < 2; ++j) {
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(tmem + lane_base + 32 * j, o);
+            tmem_wait_ld_x32(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha[32 * j + i]);
+            tmem_st_32x32b_x32(tmem + lane_base + 32 * j, o);
+          }
+          tmem_wait_st();
+        }
+        if (tid < 64) m_use[tid] = m_new[tid];
+        named_bar_sync(1, 128);
+      }
+      // P^T (f16, K-major over keys, two 64-key swizzle atoms) for this tile
+      uint8_t* pt = smem + kOffP + (t & 1) * kPBytes;
+      const int key = 32 * sp + lane;
+      const int kb = key >> 6, kc = (key & 63) >> 3, kbyte = (key & 7) * 2;
+      float pr[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const float p = (x[i] == -INFINITY) ? 0.f : ex2_approx(x[i] - m_use[i]);
+        x[i] = p;
+        const __half ph = __float2half_rn(p);
+        pr[i] = __half2float(ph);
+        const int off = kb * 8192 + (i >> 3) * 1024 + (i & 7) * 128 + ((kc ^ (i & 7)) << 4) + kbyte;
+        *reinterpret_cast<__half*>(pt + off) = ph;
+      }
+      fence_proxy_async_smem();
+      float s0, s1;
+      warp_transpose_reduce<false>(x, lane, s0, s1);
+      lsum0 += s0;
+      lsum1 += s1;
+      warp_transpose_reduce<false>(pr, lane, s0, s1);
+      rsum0 += s0;
+      rsum1 += s1;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_PFULL0 + (t & 1)));
+    }
+
+    // ---- epilogue ---------------------------------------------------------
+    lred[wi * 64 + 2 * lane] = lsum0;
+    lred[wi * 64 + 2 * lane + 1] = lsum1;
+    tmax[wi * 64 + 2 * lane] = rsum0;
+    tmax[wi * 64 + 2 * lane + 1] = rsum1;
+    if (lane == 0) flags[8 + wi] = bad;
+    named_bar_sync(1, 128);
+    const bool any_bad = flags[8] | flags[9] | flags[10] | flags[11];
+    if (tid < 64) {
+      const float l = (lred[tid] + lred[64 + tid]) + (lred[128 + tid] + lred[192 + tid]);
+      const float lr = (tmax[tid] + tmax[64 + tid]) + (tmax[128 + tid] + tmax[192 + tid]);
+      float lse = -INFINITY, inv = 0.f;
+      if (l > 0.f) {
+        lse = m_use[tid] + log2f(l);
+        inv = dv / lr;
+      }
+      inv_s[tid] = inv;
+      if (tid < R) {
+        if (direct) {
+          if (a.lse_out != nullptr) a.lse_out[out_index(tid)] = lse;
+        } else {
+          a.lse_acc[out_index(tid)] = lse;
+        }
+      }
+    }
+    named_bar_sync(1, 128);
+    if (!any_bad) {
+      int w = 1;
+      if (lane == 0) w = wait_bounded(bar(B_FINAL), 0, wc, W_SM_FINAL);
+      w = __shfl_sync(0xffffffffu, w, 0);
+      tc_fence_after();
+      if (w) {
+        uint32_t o[64];
+        tmem_ld_32x32b_x64(tmem + lane_base, o);
+        tmem_wait_ld_x64(o);
+        const int d = 32 * sp + lane;
+        float amax_l = 0.f;
+#pragma unroll
+        for (int rho = 0; rho < kRows; ++rho) {
+          if (rho >= R) continue;
+          const float v = __uint_as_float(o[rho]) * inv_s[rho];
+          const size_t oi = out_index(rho) * kD + d;
+          if (!direct) {
+            a.o_acc[oi] = v;
+          } else {
+            amax_l = fmaxf(amax_l, fabsf(v));
+            if (a.out_dtype == 0) {
+              static_cast<float*>(a.out)[oi] = v;
+            } else if (a.out_dtype == 1) {
+              static_cast<__nv_bfloat16*>(a.out)[oi] = __float2bfloat16_rn(v);
+            } else {
+              static_cast<uint8_t*>(a.out)[oi] =
+                  static_cast<uint8_t>(__nv_cvt_float_to_fp8(v * a.inv_scale, __NV_SATFINITE, __NV_E4M3));
+            }
+          }
+        }
+        if (direct && a.amax != nullptr) {
+#pragma unroll
+          for (int o2 = 16; o2 > 0; o2 >>= 1) amax_l = fmaxf(amax_l, __shfl_xor_sync(0xffffffffu, amax_l, o2));
+          if (lane == 0) atomicMax(reinterpret_cast<int*>(a.amax), __float_as_int(amax_l));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+int sdpa_decode_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_sdpa_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                               const SdpaArgs& a, bool direct, cudaStream_t stream) {
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(sdpa_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(static_cast<unsigned>(a.batch) * a.h_kv * a.num_splits);
+  sdpa_decode_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, a, direct ? 1 : 0);
+  return cudaGetLastError();
+}
+
+}  // namespace skv

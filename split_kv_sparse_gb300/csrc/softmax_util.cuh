@@ -1,0 +1,82 @@
+// Device helpers shared by the decode kernels: the approximate exp2 used for
+// softmax numerators, a drain wait for in-flight copies, and the transposed
+// warp butterfly that reduces 64 per-lane values over the 32 lanes of a warp.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace skv {
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Waits without looking at the abort flag (used to drain in-flight copies on abort).
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+// Transposed butterfly over a warp: each lane holds x[j] for 64 heads j; on
+// return lane l holds the reduction over all 32 lanes for heads 2l and 2l+1.
+template <bool kMax>
+__device__ __forceinline__ void warp_transpose_reduce(const float (&x)[64], int lane, float& r0,
+                                                      float& r1) {
+  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+  float a[32];
+  {
+    const bool up = lane & 16;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float send = up ? x[i] : x[i + 32];
+      const float keep = up ? x[i + 32] : x[i];
+      a[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+    }
+  }
+  float b[16];
+  {
+    const bool up = lane & 8;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float send = up ? a[i] : a[i + 16];
+      const float keep = up ? a[i + 16] : a[i];
+      b[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+    }
+  }
+  float c[8];
+  {
+    const bool up = lane & 4;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float send = up ? b[i] : b[i + 8];
+      const float keep = up ? b[i + 8] : b[i];
+      c[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+    }
+  }
+  float d[4];
+  {
+    const bool up = lane & 2;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float send = up ? c[i] : c[i + 4];
+      const float keep = up ? c[i + 4] : c[i];
+      d[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+    }
+  }
+  {
+    const bool up = lane & 1;
+    const float send0 = up ? d[0] : d[2];
+    const float keep0 = up ? d[2] : d[0];
+    const float send1 = up ? d[1] : d[3];
+    const float keep1 = up ? d[3] : d[1];
+    r0 = op(keep0, __shfl_xor_sync(0xffffffffu, send0, 1));
+    r1 = op(keep1, __shfl_xor_sync(0xffffffffu, send1, 1));
+  }
+}
+
+}  // namespace skv

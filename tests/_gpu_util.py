@@ -1,0 +1,119 @@
+"""Shared helpers of the GPU parity tests: run the C-ABI path, compare with the oracle.
+
+Tolerances (stated once, used by every parity test):
+  * O in fp32 output mode: for every (token, head) row,
+        ||O_gpu - O_ref||_2 / ||O_ref||_2 <= 2e-3;
+    a row whose reference is exactly 0 must be exactly 0 on the GPU.
+  * LSE (log2): |LSE_gpu - LSE_ref| <= 1e-5; -inf must match exactly.
+  * bf16 / e4m3 output ("compared after the same cast"): every GPU value must be
+    a value that the same cast gives for some input within the fp32 tolerance
+    of the reference, i.e. lie between cast(O_ref - delta) and cast(O_ref + delta)
+    with delta = 2e-3 * rms(O_ref row) (+ the cast's own rounding, which the
+    interval already includes).
+  * amax: |amax_gpu - max|O_ref|| <= 2e-3 * max|O_ref|.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle.mla as om
+from oracle import codecs
+from split_kv_sparse_gb300 import binding as b
+
+O_RTOL = 2e-3
+LSE_ATOL = 1e-5
+
+TORCH_OUT = {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.uint8}
+
+
+def check_status():
+    st, site = b.mla_get_status()
+    assert st == 0, f"device status {st:#x}, first timed-out wait site {site}"
+
+
+def run_mla(inp, S: int, out_dtype: str = "f32", inv_scale: float = 1.0, with_amax: bool = False,
+            keep_workspace: bool = False):
+    """Whole decode step through mla_sparse_decode (direct path when S == 1)."""
+    dev = torch.device("cuda")
+    q, kv, idx = inp.q.to(dev), inp.kv.to(dev), inp.idx.to(dev)
+    sink = inp.sink.to(dev) if inp.sink is not None else None
+    plan = b.mla_decode_plan(inp.s_q, inp.topk, force_splits=S)
+    ws = torch.empty(max(plan.workspace_bytes, 1), dtype=torch.uint8, device=dev) if plan.workspace_bytes else None
+    out = torch.empty(inp.s_q, 64, 512, dtype=TORCH_OUT[out_dtype], device=dev)
+    lse = torch.empty(inp.s_q, 64, dtype=torch.float32, device=dev)
+    amax = torch.empty(1, dtype=torch.float32, device=dev) if with_amax else None
+    b.mla_sparse_decode(plan, inp.s_q, q, kv, inp.n_kv, idx, inp.sm_scale, sink, out_dtype, inv_scale, out,
+                        lse, amax, ws)
+    torch.cuda.synchronize()
+    check_status()
+    res = {"out": out.cpu(), "lse": lse.cpu().double().numpy(), "plan": plan}
+    if with_amax:
+        res["amax"] = float(amax.cpu()[0])
+    if keep_workspace and ws is not None:
+        res["o_acc"], res["lse_acc"] = workspace_views(plan, inp.s_q, ws)
+    return res
+
+
+def workspace_views(plan, s_q, ws):
+    S = plan.num_splits
+    o = ws[: S * s_q * 64 * 512 * 4].view(torch.float32).view(S, s_q, 64, 512)
+    off = plan.lse_acc_offset
+    l = ws[off: off + S * s_q * 64 * 4].view(torch.float32).view(S, s_q, 64)
+    return o.cpu().double().numpy(), l.cpu().double().numpy()
+
+
+def oracle_mla(inp):
+    return om.attention(inp.q, inp.kv, inp.idx, inp.sm_scale, 512, sink=inp.sink)
+
+
+def assert_o_close(O_gpu, O_ref, rtol=O_RTOL, what="O"):
+    O_gpu = np.asarray(O_gpu, dtype=np.float64).reshape(-1, O_ref.shape[-1])
+    O_ref = np.asarray(O_ref, dtype=np.float64).reshape(-1, O_ref.shape[-1])
+    assert np.all(np.isfinite(O_gpu)), f"{what}: non-finite values"
+    nref = np.linalg.norm(O_ref, axis=1)
+    err = np.linalg.norm(O_gpu - O_ref, axis=1)
+    zero = nref == 0
+    assert np.all(O_gpu[zero] == 0), f"{what}: rows with a zero reference are not zero"
+    rel = err[~zero] / nref[~zero]
+    worst = float(rel.max()) if rel.size else 0.0
+    assert worst <= rtol, f"{what}: worst row relative error {worst:.3e} > {rtol:.1e}"
+    return worst
+
+
+def assert_lse_close(L_gpu, L_ref, atol=LSE_ATOL, what="LSE"):
+    L_gpu = np.asarray(L_gpu, dtype=np.float64)
+    L_ref = np.asarray(L_ref, dtype=np.float64)
+    ninf = np.isneginf(L_ref)
+    assert np.array_equal(np.isneginf(L_gpu), ninf), f"{what}: -inf pattern differs"
+    if (~ninf).any():
+        worst = float(np.max(np.abs(L_gpu[~ninf] - L_ref[~ninf])))
+        assert worst <= atol, f"{what}: worst abs error {worst:.3e} > {atol:.1e}"
+        return worst
+    return 0.0
+
+
+def _row_delta(O_ref, rtol):
+    rms = np.sqrt(np.mean(np.square(O_ref), axis=-1, keepdims=True))
+    return rtol * rms
+
+
+def assert_cast_close(gpu_out: torch.Tensor, O_ref: np.ndarray, out_dtype: str, inv_scale: float = 1.0,
+                      rtol: float = O_RTOL):
+    """Every GPU code lies between cast(O_ref - delta) and cast(O_ref + delta)."""
+    delta = _row_delta(O_ref, rtol)
+    if out_dtype == "bf16":
+        g = gpu_out.float().double().numpy()
+        lo = codecs.bf16_round(O_ref - delta)
+        hi = codecs.bf16_round(O_ref + delta)
+        ref_codes_equal = g == codecs.bf16_round(O_ref)
+    elif out_dtype == "e4m3":
+        g = codecs.e4m3_decode(gpu_out.numpy())
+        lo = codecs.e4m3_round((O_ref - delta) * inv_scale)
+        hi = codecs.e4m3_round((O_ref + delta) * inv_scale)
+        ref_codes_equal = gpu_out.numpy() == codecs.e4m3_encode(O_ref * inv_scale)
+    else:
+        raise ValueError(out_dtype)
+    ok = (g >= lo) & (g <= hi)
+    assert ok.all(), f"{out_dtype}: {int((~ok).sum())} values outside the cast interval"
+    return float(ref_codes_equal.mean())

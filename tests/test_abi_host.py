@@ -1,0 +1,178 @@
+"""Host-side tests of the C ABI (no GPU needed).
+
+* libsplitkv.so builds for sm_103a, loads without a GPU, and exports every
+  function include/mla_split.h declares;
+* the planner: workspace formula against the sizes printed in FlashMLA PR #25
+  ("Measured"), determinism (a pure function of its arguments, so a CUDA graph
+  bucket sees one split count), the automatic rule, forcing, and error codes;
+* argument checks that run before any device work return their codes.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle.mla as om
+from split_kv_sparse_gb300 import binding as b
+from split_kv_sparse_gb300 import build as bld
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    if not os.path.exists(b.LIB_PATH):
+        bld.build()
+    return b.lib()
+
+
+def _declared_functions():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            names += re.findall(r"^MLA_API\s+[\w\s\*]+?\b(\w+)\(", src, flags=re.M)
+    return names
+
+
+def test_library_exports_every_declared_function():
+    declared = _declared_functions()
+    assert len(declared) >= 14
+    assert sorted(declared) == sorted(b.EXPORTS)
+    L = ctypes.CDLL(b.LIB_PATH)
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_abi_version_matches_header():
+    src = open(os.path.join(ROOT, "include", "mla_split.h")).read()
+    v = int(re.search(r"#define MLA_ABI_VERSION (\d+)", src).group(1))
+    assert b.mla_abi_version() == v
+
+
+def test_status_strings():
+    for code in range(6):
+        assert b.status_string(code) != "unknown status"
+    assert b.status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("S,s_q", [(8, 1), (8, 16)])
+def test_workspace_matches_page(S, s_q):
+    p = b.mla_decode_plan(s_q, 640, num_sms=152, force_splits=S)
+    assert p.o_acc_bytes == om.workspace_bytes(S, s_q) == S * s_q * 64 * 512 * 4
+    assert p.lse_acc_offset % 256 == 0 and p.lse_acc_offset >= p.o_acc_bytes
+    assert p.lse_acc_bytes == S * s_q * 64 * 4
+    assert p.workspace_bytes >= p.lse_acc_offset + p.lse_acc_bytes and p.workspace_bytes % 256 == 0
+
+
+def test_plan_is_deterministic_and_follows_rule():
+    for sms in [148, 152, 160, 188]:
+        for s_q in [1, 2, 4, 6, 8, 16, 32, 96, 384]:
+            for topk in [64, 128, 640, 2048]:
+                p1 = b.mla_decode_plan(s_q, topk, num_sms=sms)
+                p2 = b.mla_decode_plan(s_q, topk, num_sms=sms)
+                assert bytes(p1) == bytes(p2)
+                nblk = -(-topk // 64)
+                S = p1.num_splits
+                assert 1 <= S <= nblk
+                assert s_q * S <= max(sms, s_q)
+                smax = max(1, min(sms // s_q, nblk, 64))
+                best = -(-nblk // smax)
+                assert -(-nblk // S) == best
+                assert all(-(-nblk // c) > best for c in range(1, S))
+                assert (p1.workspace_bytes == 0) == (S == 1)
+
+
+def test_plan_examples():
+    assert b.mla_decode_plan(1, 640, num_sms=152).num_splits == 10
+    assert b.mla_decode_plan(16, 640, num_sms=152).num_splits == 5
+    assert b.mla_decode_plan(96, 640, num_sms=152).num_splits == 1
+    assert b.mla_decode_plan(1, 640, num_sms=152, max_splits=4).num_splits == 4
+    p = b.mla_decode_plan(4, 64, num_sms=152, force_splits=16)   # more splits than blocks
+    assert p.num_splits == 16 and p.num_blocks == 1
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(h_q=32), 2), (dict(d_qk=512), 2), (dict(d_v=576), 2),
+    (dict(force_splits=65), 1), (dict(max_splits=-1), 1), (dict(num_sms=-1), 1),
+])
+def test_plan_errors(kw, code):
+    with pytest.raises(b.SplitKVError) as e:
+        b.mla_decode_plan(1, 640, **({"num_sms": 152} | kw))
+    assert e.value.status == code
+
+
+def test_plan_rejects_bad_sizes():
+    for s_q, topk in [(0, 640), (1, 0), (-3, 640)]:
+        with pytest.raises(b.SplitKVError) as e:
+            b.mla_decode_plan(s_q, topk, num_sms=152)
+        assert e.value.status == 1
+
+
+def test_split_call_argument_checks_before_device_work():
+    plan = b.mla_decode_plan(4, 640, num_sms=152, force_splits=4)
+    fake = 1 << 20   # never dereferenced: every case below fails its host check first
+    cases = [
+        dict(s_q=5),                      # s_q > s_q_max
+        dict(s_q=0),
+        dict(q=None), dict(kv=None), dict(idx=None),
+        dict(q=fake + 8),                 # q not 16-byte aligned
+        dict(n_kv=0),
+        dict(sm_scale=float("nan")),
+    ]
+    for c in cases:
+        args = dict(s_q=2, q=fake, kv=fake, n_kv=100, idx=fake, sm_scale=0.1, workspace=fake) | c
+        with pytest.raises(b.SplitKVError) as e:
+            b.mla_sparse_decode_split(plan, args["s_q"], args["q"], args["kv"], args["n_kv"], args["idx"],
+                                      args["sm_scale"], args["workspace"], stream=0)
+        assert e.value.status == 1, c
+    with pytest.raises(b.SplitKVError) as e:   # workspace missing
+        b.mla_sparse_decode_split(plan, 2, fake, fake, 100, fake, 0.1, None, stream=0)
+    assert e.value.status == 3
+    plan1 = b.mla_decode_plan(4, 640, num_sms=152, force_splits=1)
+    with pytest.raises(b.SplitKVError) as e:   # the split call needs S > 1
+        b.mla_sparse_decode_split(plan1, 2, fake, fake, 100, fake, 0.1, fake, stream=0)
+    assert e.value.status == 1
+
+
+def test_combine_argument_checks():
+    plan = b.mla_decode_plan(4, 640, num_sms=152, force_splits=4)
+    fake = 1 << 20
+    with pytest.raises(b.SplitKVError) as e:
+        b.mla_split_combine(plan, 2, fake, None, 7, 1.0, fake, stream=0)      # bad dtype
+    assert e.value.status == 1
+    with pytest.raises(b.SplitKVError) as e:
+        b.mla_split_combine(plan, 2, fake, None, "e4m3", float("inf"), fake, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(b.SplitKVError) as e:
+        b.mla_split_combine(plan, 2, fake + 64, None, "f32", 1.0, fake, stream=0)   # workspace alignment
+    assert e.value.status == 3
+
+
+def test_no_device_is_reported_not_crashed():
+    """Without a GPU, a call that passes its host checks reports MLA_ERR_NO_DEVICE."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    plan = b.mla_decode_plan(2, 640, num_sms=152, force_splits=2)
+    fake = 1 << 20
+    with pytest.raises(b.SplitKVError) as e:
+        b.mla_sparse_decode_split(plan, 2, fake, fake, 100, fake, 0.1, fake, stream=0)
+    assert e.value.status == 5
+
+
+def test_dense_plan():
+    p = b.sdpa_fp8_decode_plan(8, 32, 8, 128, 16, 128, 16384, num_sms=152)
+    assert p.num_splits >= 1 and 8 * 8 * p.num_splits <= 152
+    assert p.o_acc_bytes == (p.num_splits * 128 * 32 * 128 * 4 if p.num_splits > 1 else 0)
+    with pytest.raises(b.SplitKVError) as e:
+        b.sdpa_fp8_decode_plan(8, 32, 8, 64, 16, 128, 16384, num_sms=152)
+    assert e.value.status == 2
+    with pytest.raises(b.SplitKVError) as e:   # 4 heads per group x 17 tokens > 64 rows per job
+        b.sdpa_fp8_decode_plan(8, 32, 8, 128, 17, 128, 16384, num_sms=152)
+    assert e.value.status == 2
+
+
+def test_build_targets_sm103a_only():
+    assert bld.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1,0 +1,248 @@
+"""GPU parity of the sparse-MLA split-KV decode path against the fp64 oracle.
+
+Every call goes through the C ABI (libsplitkv.so) via the ctypes binding.
+Cases follow the pages' workloads (FlashMLA PR #25: h_q = 64, topk 128+512;
+its test matrix s_q {1, 6, 16} x splits {2, 4, 8} x sink {off, on}, a
+degenerate case with more splits than KV blocks, and the unsplit FP8 output),
+plus ragged top-k, padding, out-of-range indices, the lazy-rescale path, graph
+capture and the bounded-wait abort path. Tolerances: see _gpu_util.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.mla as om
+from _gpu_util import (assert_cast_close, assert_lse_close, assert_o_close, check_status, oracle_mla,
+                       run_mla, workspace_views)
+from split_kv_sparse_gb300 import binding as b
+from split_kv_sparse_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    assert torch.cuda.is_available(), "the -m gpu tests need a CUDA GPU"
+    b.lib()            # fails loudly if the library is missing
+    check_status()
+
+
+# ---- small config: s_q = 1, 4096 rows, 640 distinct uniform indices, S in {1, 4} ----------
+
+@pytest.mark.parametrize("S", [1, 4])
+def test_small_config(S):
+    inp = wl.mla_inputs(1, 4096, 640, seed=0, index_mode="uniform")
+    O, L = oracle_mla(inp)
+    r = run_mla(inp, S)
+    assert_o_close(r["out"].numpy(), O)
+    assert_lse_close(r["lse"], L)
+
+
+# ---- the page's test matrix on a 32768-row cache ---------------------------------------
+
+@pytest.mark.parametrize("s_q", [1, 6, 16])
+@pytest.mark.parametrize("with_sink", [False, True])
+@pytest.mark.parametrize("v_mean", [0.0, 1.0])
+def test_matrix(s_q, with_sink, v_mean):
+    inp = wl.mla_inputs(s_q, 32768, 640, seed=10 + s_q, v_mean=v_mean, with_sink=with_sink)
+    O, L = oracle_mla(inp)
+    for S in (2, 4, 8):
+        r = run_mla(inp, S)
+        assert_o_close(r["out"].numpy(), O, what=f"O S={S}")
+        assert_lse_close(r["lse"], L, what=f"LSE S={S}")
+
+
+@pytest.mark.parametrize("S", [2, 3, 8, 10, 16])
+def test_split_partials_match_oracle(S):
+    """Each split's fp32 partial O and log2 LSE in the workspace, against the oracle's partials."""
+    inp = wl.mla_inputs(3, 32768, 640, seed=21)
+    O_s, L_s = om.split_partials(inp.q, inp.kv, inp.idx, inp.sm_scale, S)
+    r = run_mla(inp, S, keep_workspace=True)
+    for s in range(S):
+        assert_o_close(r["o_acc"][s], O_s[s], what=f"partial O split {s}")
+        assert_lse_close(r["lse_acc"][s], L_s[s], what=f"partial LSE split {s}")
+
+
+def test_degenerate_more_splits_than_blocks():
+    """s_q = 4, topk = 64 with per-token valid counts in [1, 64] (rest -1), 16 splits over 1 block."""
+    inp = wl.mla_inputs(4, 32768, 64, seed=3, index_mode="padded", with_sink=True)
+    O, L = oracle_mla(inp)
+    r = run_mla(inp, 16, keep_workspace=True)
+    assert np.all(r["o_acc"][1:] == 0) and np.all(np.isneginf(r["lse_acc"][1:]))
+    O_s, L_s = om.split_partials(inp.q, inp.kv, inp.idx, inp.sm_scale, 16)
+    assert_o_close(r["o_acc"][0], O_s[0])
+    assert_lse_close(r["lse_acc"][0], L_s[0])
+    assert_o_close(r["out"].numpy(), O)
+    assert_lse_close(r["lse"], L)
+
+
+@pytest.mark.parametrize("topk,s_q,S", [(1, 2, 1), (10, 3, 1), (63, 2, 2), (65, 2, 2), (200, 5, 3),
+                                         (200, 5, 1), (1000, 2, 7), (2048, 1, 16), (129, 1, 1)])
+def test_ragged_topk(topk, s_q, S):
+    inp = wl.mla_inputs(s_q, 4096, topk, seed=topk, index_mode="uniform", with_sink=(topk % 2 == 0))
+    O, L = oracle_mla(inp)
+    r = run_mla(inp, S)
+    assert_o_close(r["out"].numpy(), O)
+    assert_lse_close(r["lse"], L)
+
+
+def test_padding_out_of_range_duplicates_and_empty_token():
+    inp = wl.mla_inputs(4, 4096, 256, seed=5, index_mode="uniform", with_sink=True)
+    idx = inp.idx.clone()
+    idx[0, :] = -1                         # nothing to attend: O = 0, LSE = -inf even with a sink
+    idx[1, 10:50] = 4096 + 13              # past the end of the cache: masked
+    idx[1, 50:60] = -7                     # any negative index is masked
+    idx[2, 1::2] = idx[2, 0::2]            # duplicates count twice
+    idx[3, 64:] = -1                       # only the first block is valid
+    inp.idx = idx
+    O, L = oracle_mla(inp)
+    for S in (1, 2, 4):
+        r = run_mla(inp, S)
+        assert np.all(r["out"].numpy()[0] == 0) and np.all(np.isneginf(r["lse"][0]))
+        assert_o_close(r["out"].numpy(), O)
+        assert_lse_close(r["lse"], L)
+
+
+def _rising_scores(s_q, topk, seed, step_natural=0.13, descending=False):
+    """Scores that rise along the top-k order by ~8.3 natural units per 64 rows, so
+    the running max moves past the lazy-rescale threshold at every block."""
+    rng = np.random.default_rng(seed)
+    n_kv = 4096
+    u = np.zeros(576, np.float32)
+    u[0] = 1.0
+    kv = (0.05 * rng.standard_normal((n_kv, 576))).astype(np.float32)
+    idx = rng.permutation(n_kv)[: s_q * topk].reshape(s_q, topk).astype(np.int32)   # disjoint per token
+    a = step_natural * np.arange(topk, dtype=np.float32)
+    if descending:
+        a = a[::-1].copy()
+    for t in range(s_q):
+        kv[idx[t], 0] = a
+    q = np.zeros((s_q, 64, 576), np.float32)
+    q[:, :, 0] = 24.0 * (1.0 + np.arange(64) / 64.0)[None, :]
+    q += (0.05 * rng.standard_normal(q.shape)).astype(np.float32)
+    return wl.MlaInputs(q=torch.from_numpy(q).bfloat16(), kv=torch.from_numpy(kv).bfloat16(),
+                        idx=torch.from_numpy(idx), sink=None, sm_scale=1.0 / 24.0)
+
+
+@pytest.mark.parametrize("descending", [False, True])
+@pytest.mark.parametrize("S", [1, 2, 5])
+def test_lazy_rescale_path(descending, S):
+    inp = _rising_scores(2, 640, seed=7, descending=descending)
+    O, L = oracle_mla(inp)
+    r = run_mla(inp, S)
+    assert_o_close(r["out"].numpy(), O)
+    assert_lse_close(r["lse"], L)
+
+
+@pytest.mark.parametrize("out_dtype", ["bf16", "e4m3"])
+@pytest.mark.parametrize("S", [1, 4])
+@pytest.mark.parametrize("v_mean", [0.0, 1.0])
+def test_output_casts_and_amax(out_dtype, S, v_mean):
+    inp = wl.mla_inputs(6, 32768, 640, seed=31, v_mean=v_mean, with_sink=True)
+    O, L = oracle_mla(inp)
+    inv_scale = 64.0 if out_dtype == "e4m3" else 1.0
+    r = run_mla(inp, S, out_dtype=out_dtype, inv_scale=inv_scale, with_amax=True)
+    same = assert_cast_close(r["out"], O, out_dtype, inv_scale)
+    if v_mean == 1.0:
+        # FlashMLA PR #25, "Test plan": 99.6% identical FP8 codes with non-cancelling values
+        assert same >= 0.99, f"only {same:.4f} of the codes equal the oracle's"
+    assert_lse_close(r["lse"], L)
+    amax_ref = float(np.max(np.abs(O)))
+    assert abs(r["amax"] - amax_ref) <= 2e-3 * amax_ref
+
+
+def test_split_equals_direct_closely():
+    """The split + combine path and the direct path agree with each other (LSE to 1e-5)."""
+    inp = wl.mla_inputs(16, 32768, 640, seed=44, with_sink=True)
+    r1 = run_mla(inp, 1)
+    for S in (2, 5, 10):
+        rs = run_mla(inp, S)
+        assert_o_close(rs["out"].numpy(), r1["out"].double().numpy())
+        assert_lse_close(rs["lse"], r1["lse"])
+
+
+def test_cuda_graph_capture_and_replay():
+    inp = wl.mla_inputs(6, 32768, 640, seed=9, with_sink=True)
+    dev = torch.device("cuda")
+    q, kv, idx, sink = inp.q.to(dev), inp.kv.to(dev), inp.idx.to(dev), inp.sink.to(dev)
+    plan = b.mla_decode_plan(16, 640)          # one plan for the whole s_q <= 16 bucket
+    assert plan.num_splits > 1
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty(6, 64, 512, dtype=torch.uint8, device=dev)
+    lse = torch.empty(6, 64, dtype=torch.float32, device=dev)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        b.mla_sparse_decode(plan, 6, q, kv, inp.n_kv, idx, inp.sm_scale, sink, "e4m3", 64.0, out, lse, None, ws,
+                            stream=s)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    eager_lse = lse.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        b.mla_sparse_decode(plan, 6, q, kv, inp.n_kv, idx, inp.sm_scale, sink, "e4m3", 64.0, out, lse, None, ws,
+                            stream=s)
+    out.zero_()
+    lse.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    check_status()
+    assert torch.equal(out, eager)
+    assert torch.equal(lse, eager_lse)
+
+
+def test_bounded_wait_gives_up_and_context_survives():
+    check_status()
+    b.mla_selftest_wait_timeout(2_000_000)     # 2 ms on a barrier nothing arrives on
+    st, site = b.mla_get_status()
+    assert st & b.MLA_STATUS_TIMEOUT and site == 0x5E1F
+    assert b.mla_get_status() == (0, 0)        # read-and-clear
+    # the context is still usable
+    inp = wl.mla_inputs(1, 4096, 128, seed=1, index_mode="uniform")
+    O, L = oracle_mla(inp)
+    r = run_mla(inp, 2)
+    assert_o_close(r["out"].numpy(), O)
+
+
+def test_host_errors_on_gpu():
+    inp = wl.mla_inputs(2, 4096, 640, seed=2, index_mode="uniform")
+    dev = torch.device("cuda")
+    q, kv, idx = inp.q.to(dev), inp.kv.to(dev), inp.idx.to(dev)
+    plan = b.mla_decode_plan(2, 640, force_splits=4)
+    small = torch.empty(64, dtype=torch.uint8, device=dev)
+    out = torch.empty(2, 64, 512, device=dev)
+    with pytest.raises(b.SplitKVError) as e:
+        b.mla_sparse_decode(plan, 3, q, kv, inp.n_kv, idx, inp.sm_scale, None, "f32", 1.0, out, None, None, small)
+    assert e.value.status == 1
+    with pytest.raises(b.SplitKVError) as e:
+        b.mla_sparse_decode(plan, 2, q[:, :, 1:], kv, inp.n_kv, idx, inp.sm_scale, None, "f32", 1.0, out, None,
+                            None, small)
+    assert e.value.status == 1                 # q not 16-byte aligned
+    check_status()
+
+
+# ---- full-size workload, in the bench's launch configuration, sampled tokens ----------
+
+@pytest.mark.parametrize("s_q", [96, 384])
+def test_full_size_sampled(s_q):
+    inp = wl.mla_inputs(s_q, 131072, 640, seed=0)
+    r = run_mla(inp, b.mla_decode_plan(s_q, 640).num_splits, out_dtype="e4m3", inv_scale=64.0)
+    rng = np.random.default_rng(s_q)
+    ts = np.sort(rng.choice(s_q, 6, replace=False))
+    sub = wl.MlaInputs(q=inp.q[ts], kv=inp.kv, idx=inp.idx[ts], sink=None, sm_scale=inp.sm_scale)
+    O, L = oracle_mla(sub)
+    assert_cast_close(r["out"][ts], O, "e4m3", 64.0)
+    assert_lse_close(r["lse"][ts], L)
+
+
+def test_full_size_forced_splits_sampled():
+    inp = wl.mla_inputs(16, 131072, 640, seed=4, with_sink=True)
+    ts = np.array([0, 7, 15])
+    sub = wl.MlaInputs(q=inp.q[ts], kv=inp.kv, idx=inp.idx[ts], sink=inp.sink, sm_scale=inp.sm_scale)
+    O, L = oracle_mla(sub)
+    for S in (1, 2, 4, 8, 16):
+        r = run_mla(inp, S)
+        assert_o_close(r["out"].numpy()[ts], O)
+        assert_lse_close(r["lse"][ts], L)
