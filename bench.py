@@ -243,12 +243,7 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
 
-    mean_call = statistics.fmean(call_us)
-    mean_kern = statistics.fmean(kern_us)
-    if world > 1:
-        t = torch.tensor([mean_call, mean_kern], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        mean_call, mean_kern = float(t[0]), float(t[1])
+    mean_call, mean_kern = max_over_ranks([statistics.fmean(call_us), statistics.fmean(kern_us)], dev)
 
     kbytes = algorithmic_bytes(args.s_q, case.S, "split")
     achieved = kbytes / (mean_kern * 1e-6) / 1e9
@@ -336,6 +331,18 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def max_over_ranks(values, device=None):
+    """Element-wise max of per-rank values across the process group (identity on one
+    process): each rank runs an independent replica and the slowest one sets the number."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
 
 
 def known_traffic(s_q, S):

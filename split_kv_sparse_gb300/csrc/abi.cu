@@ -236,8 +236,15 @@ int mla_sparse_decode_split(const mla_plan_t* plan, int s_q, const void* q, cons
   return cuda_status(skv::launch_mla_decode(tq, tkv, a, false, static_cast<cudaStream_t>(stream)));
 }
 
-int mla_split_combine(const mla_plan_t* plan, int s_q, const void* workspace, const float* sink, int out_dtype,
-                      float out_inv_scale, void* out, float* lse_out, float* amax_out, void* stream) {
+}  // extern "C"
+
+namespace {
+// The combine launch shared by the public call (which clears amax itself) and
+// the one-shot call (which clears amax before the split pass, so the combine can
+// follow the split kernel as a programmatic dependent launch).
+int mla_combine_impl(const mla_plan_t* plan, int s_q, const void* workspace, const float* sink, int out_dtype,
+                     float out_inv_scale, void* out, float* lse_out, float* amax_out, bool zero_amax,
+                     void* stream) {
   if (plan == nullptr || plan->num_splits < 2 || plan->num_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID_ARG;
   if (plan->h_q != kMlaHeads || plan->d_v != kMlaDv) return MLA_ERR_UNSUPPORTED;
   if (s_q < 1 || s_q > plan->s_q_max || out == nullptr || !aligned(out, 16)) return MLA_ERR_INVALID_ARG;
@@ -260,7 +267,16 @@ int mla_split_combine(const mla_plan_t* plan, int s_q, const void* workspace, co
   c.inv_scale = out_inv_scale;
   c.lse_out = lse_out;
   c.amax = amax_out;
-  return cuda_status(skv::launch_combine(c, static_cast<cudaStream_t>(stream)));
+  return cuda_status(skv::launch_combine(c, zero_amax, /*pdl=*/true, static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+extern "C" {
+
+int mla_split_combine(const mla_plan_t* plan, int s_q, const void* workspace, const float* sink, int out_dtype,
+                      float out_inv_scale, void* out, float* lse_out, float* amax_out, void* stream) {
+  return mla_combine_impl(plan, s_q, workspace, sink, out_dtype, out_inv_scale, out, lse_out, amax_out, true,
+                          stream);
 }
 
 int mla_sparse_decode_direct(int s_q, int topk, const void* q, const void* kv, int64_t n_kv, const int32_t* idx,
@@ -309,9 +325,15 @@ int mla_sparse_decode(const mla_plan_t* plan, int s_q, const void* q, const void
   // validate the combine's own arguments before launching anything
   if (out == nullptr || !aligned(out, 16) || !valid_out_dtype(out_dtype)) return MLA_ERR_INVALID_ARG;
   if (out_dtype == MLA_OUT_E4M3 && !std::isfinite(out_inv_scale)) return MLA_ERR_INVALID_ARG;
+  if (amax_out != nullptr &&
+      cudaMemsetAsync(amax_out, 0, sizeof(float), static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
   const int st = mla_sparse_decode_split(plan, s_q, q, kv, n_kv, idx, sm_scale, workspace, stream);
   if (st != MLA_OK) return st;
-  return mla_split_combine(plan, s_q, workspace, sink, out_dtype, out_inv_scale, out, lse_out, amax_out, stream);
+  return mla_combine_impl(plan, s_q, workspace, sink, out_dtype, out_inv_scale, out, lse_out, amax_out, false,
+                          stream);
 }
 
 // ---------------------------------------------------------------- dense -----
@@ -428,25 +450,9 @@ int sdpa_launch(int batch, int h_q, int h_kv, int total_q, int64_t total_kv, int
   a.wait_limit_ns = kWaitLimitNs;
   return cuda_status(skv::launch_sdpa_decode(tq, tk, tv, a, direct, cs));
 }
-}  // namespace
-
-int sdpa_fp8_decode_split(const sdpa_plan_t* plan, int total_q, int64_t total_kv, const void* q, const void* k,
-                          const void* v, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
-                          const float* descale_q, const float* descale_k, const float* descale_v, float sm_scale,
-                          void* workspace, void* stream) {
-  if (plan == nullptr || plan->num_splits < 2 || plan->num_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID_ARG;
-  if (plan->d != 128) return MLA_ERR_UNSUPPORTED;
-  if (total_q < 1 || total_q > plan->total_q_max) return MLA_ERR_INVALID_ARG;
-  if (workspace == nullptr || !aligned(workspace, 256) || plan->workspace_bytes == 0) return MLA_ERR_WORKSPACE;
-  return sdpa_launch(plan->batch, plan->h_q, plan->h_kv, total_q, total_kv, plan->num_splits, q, k, v,
-                     cu_seqlens_q, cu_seqlens_kv, descale_q, descale_k, descale_v, sm_scale,
-                     static_cast<float*>(workspace),
-                     reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan->lse_acc_offset), nullptr, 0,
-                     1.f, nullptr, nullptr, false, stream);
-}
-
-int sdpa_split_combine(const sdpa_plan_t* plan, int total_q, const void* workspace, int out_dtype,
-                       float out_inv_scale, void* out, float* lse_out, float* amax_out, void* stream) {
+int sdpa_combine_impl(const sdpa_plan_t* plan, int total_q, const void* workspace, int out_dtype,
+                      float out_inv_scale, void* out, float* lse_out, float* amax_out, bool zero_amax,
+                      void* stream) {
   if (plan == nullptr || plan->num_splits < 2 || plan->num_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID_ARG;
   if (plan->d != 128) return MLA_ERR_UNSUPPORTED;
   if (total_q < 1 || total_q > plan->total_q_max || out == nullptr || !aligned(out, 16)) return MLA_ERR_INVALID_ARG;
@@ -469,7 +475,29 @@ int sdpa_split_combine(const sdpa_plan_t* plan, int total_q, const void* workspa
   c.inv_scale = out_inv_scale;
   c.lse_out = lse_out;
   c.amax = amax_out;
-  return cuda_status(skv::launch_combine(c, static_cast<cudaStream_t>(stream)));
+  return cuda_status(skv::launch_combine(c, zero_amax, /*pdl=*/true, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+int sdpa_fp8_decode_split(const sdpa_plan_t* plan, int total_q, int64_t total_kv, const void* q, const void* k,
+                          const void* v, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                          const float* descale_q, const float* descale_k, const float* descale_v, float sm_scale,
+                          void* workspace, void* stream) {
+  if (plan == nullptr || plan->num_splits < 2 || plan->num_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID_ARG;
+  if (plan->d != 128) return MLA_ERR_UNSUPPORTED;
+  if (total_q < 1 || total_q > plan->total_q_max) return MLA_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned(workspace, 256) || plan->workspace_bytes == 0) return MLA_ERR_WORKSPACE;
+  return sdpa_launch(plan->batch, plan->h_q, plan->h_kv, total_q, total_kv, plan->num_splits, q, k, v,
+                     cu_seqlens_q, cu_seqlens_kv, descale_q, descale_k, descale_v, sm_scale,
+                     static_cast<float*>(workspace),
+                     reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan->lse_acc_offset), nullptr, 0,
+                     1.f, nullptr, nullptr, false, stream);
+}
+
+int sdpa_split_combine(const sdpa_plan_t* plan, int total_q, const void* workspace, int out_dtype,
+                       float out_inv_scale, void* out, float* lse_out, float* amax_out, void* stream) {
+  return sdpa_combine_impl(plan, total_q, workspace, out_dtype, out_inv_scale, out, lse_out, amax_out, true, stream);
 }
 
 int sdpa_fp8_decode_direct(int batch, int h_q, int h_kv, int d, int total_q, int64_t total_kv, const void* q,
@@ -498,10 +526,16 @@ int sdpa_fp8_decode(const sdpa_plan_t* plan, int total_q, int64_t total_kv, cons
                                   out_inv_scale, out, lse_out, amax_out, stream);
   if (out == nullptr || !aligned(out, 16) || !valid_out_dtype(out_dtype)) return MLA_ERR_INVALID_ARG;
   if (out_dtype == MLA_OUT_E4M3 && !std::isfinite(out_inv_scale)) return MLA_ERR_INVALID_ARG;
+  if (amax_out != nullptr &&
+      cudaMemsetAsync(amax_out, 0, sizeof(float), static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
   const int st = sdpa_fp8_decode_split(plan, total_q, total_kv, q, k, v, cu_seqlens_q, cu_seqlens_kv, descale_q,
                                        descale_k, descale_v, sm_scale, workspace, stream);
   if (st != MLA_OK) return st;
-  return sdpa_split_combine(plan, total_q, workspace, out_dtype, out_inv_scale, out, lse_out, amax_out, stream);
+  return sdpa_combine_impl(plan, total_q, workspace, out_dtype, out_inv_scale, out, lse_out, amax_out, false,
+                           stream);
 }
 
 // ---------------------------------------------------------------- status ----

@@ -11,6 +11,7 @@
 #include <cuda_fp8.h>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace skv {
 namespace {
@@ -35,6 +36,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const CombineArgs 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * kWarps + warp;
+  grid_dependency_wait();      // the split pass has finished writing the partials
   if (row >= a.rows) return;   // whole warp leaves together
   const int S = a.num_splits;
   const size_t rows = static_cast<size_t>(a.rows);
@@ -122,20 +124,24 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const CombineArgs 
 
 }  // namespace
 
-cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
-  if (a.amax != nullptr) {
+cudaError_t launch_combine(const CombineArgs& a, bool zero_amax, bool pdl, cudaStream_t stream) {
+  if (zero_amax && a.amax != nullptr) {
     const cudaError_t e = cudaMemsetAsync(a.amax, 0, sizeof(float), stream);
     if (e != cudaSuccess) return e;
   }
-  const dim3 grid((a.rows + kWarps - 1) / kWarps);
-  if (a.d == 512) {
-    combine_kernel<512><<<grid, kWarps * 32, 0, stream>>>(a);
-  } else if (a.d == 128) {
-    combine_kernel<128><<<grid, kWarps * 32, 0, stream>>>(a);
-  } else {
-    return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.rows + kWarps - 1) / kWarps);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (a.d == 512) return cudaLaunchKernelEx(&cfg, combine_kernel<512>, a);
+  if (a.d == 128) return cudaLaunchKernelEx(&cfg, combine_kernel<128>, a);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace skv

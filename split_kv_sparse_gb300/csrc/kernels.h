@@ -57,9 +57,11 @@ struct CombineArgs {
   int out_dtype;
   float inv_scale;
   float* lse_out;       // [rows] or null
-  float* amax;          // scalar or null (zeroed by the launcher)
+  float* amax;          // scalar or null
 };
-cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
+// zero_amax: clear *amax first (a memset on the stream); pdl: launch as a
+// programmatic dependent of the preceding kernel on the stream.
+cudaError_t launch_combine(const CombineArgs& a, bool zero_amax, bool pdl, cudaStream_t stream);
 
 // Bounded-wait self test: one CTA waits on a barrier nobody arrives on.
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);

@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (nsteps == 0) {
     // A split with no block of its own: O = 0, LSE = -inf (only the split path
     // can have one; the direct path always has topk >= 1 entries).
+    grid_launch_dependents();
     float4* o = reinterpret_cast<float4*>(a.o_acc + out_row * kMlaDv);
     for (int i = threadIdx.x; i < kMlaHeads * kMlaDv / 4; i += kThreads)
       o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -143,6 +144,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
+  // The combine (a programmatic dependent) may begin launching now; it waits
+  // for this whole grid to finish before it reads any partial.
+  grid_launch_dependents();
 
   if (warp == 0) {
     // ======================================================= TMA producer ===

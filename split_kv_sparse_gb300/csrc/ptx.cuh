@@ -95,6 +95,19 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// ------------------------------------------- programmatic dependent launch --
+
+// Lets the next kernel in the stream (launched with programmatic serialisation)
+// start its launch now; it still waits in grid_dependency_wait() for this grid.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Blocks until the preceding grid has completed and its memory is visible
+// (returns at once when the kernel was not launched as a dependent).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------- TMA --
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {

@@ -109,11 +109,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (R > kRows) {   // more query rows than one job holds: refuse, report, write nothing
+    grid_launch_dependents();
     if (threadIdx.x == 0) atomicOr(&a.status[0], 2u);
     return;
   }
   if (nt == 0 || R <= 0) {
     // nothing to attend in this split: O = 0, LSE = -inf for the job's rows
+    grid_launch_dependents();
     for (int i = threadIdx.x; i < R * kD; i += kThreads) {
       const size_t oi = out_index(i / kD) * kD + (i % kD);
       if (!direct) a.o_acc[oi] = 0.f;
@@ -173,6 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
+  grid_launch_dependents();   // the combine may start launching; it waits for this grid
 
   if (warp == 0) {
     // ======================================================= TMA producer ===

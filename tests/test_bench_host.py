@@ -1,0 +1,49 @@
+"""Host-side pieces of bench.py: the byte model and the multi-rank aggregation.
+
+bench.py runs one independent replica per GPU under torchrun (the sparse path
+shards by token with no exchange); the only cross-rank step is the max of the
+timed values, checked here with two gloo ranks on CPU.
+"""
+import os
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def test_algorithmic_bytes_model():
+    per_tok = 64 * 576 * 2 + 640 * 4 + 640 * 1152
+    assert bench.algorithmic_bytes(1, 1) == per_tok + 64 * 512 + 256
+    assert bench.algorithmic_bytes(1, 8, "split") == per_tok + 8 * (131072 + 256)
+    assert bench.algorithmic_bytes(1, 8, "call") == per_tok + 2 * 8 * (131072 + 256) + 64 * 512 + 256
+    assert bench.algorithmic_bytes(96, 1) == 96 * (per_tok + 32768 + 256)
+
+
+def test_single_process_max_is_identity():
+    assert bench.max_over_ranks([1.5, 2.0]) == [1.5, 2.0]
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    vals = [10.0 + rank, 5.0 - rank]
+    out = bench.max_over_ranks(vals)
+    q.put((rank, out))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_max():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + os.getpid() % 1000
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res[0] == res[1] == [11.0, 5.0]
