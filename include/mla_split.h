@@ -32,7 +32,10 @@
  *   - The calls are capturable into a CUDA graph: no allocation, no host
  *     synchronisation and no data-dependent host branch (the split count comes
  *     from the plan, fixed per s_q_max).
- *   - The calling thread's current CUDA device is the device used.
+ *   - The calling thread's current CUDA device is the device used. The first call
+ *     that touches a device (any call below except the planners with num_sms > 0)
+ *     sets that device up once (kernel attributes, status word); make that first
+ *     call before capturing a stream into a CUDA graph.
  */
 #ifndef MLA_SPLIT_H_
 #define MLA_SPLIT_H_
@@ -62,6 +65,8 @@ extern "C" {
 #define MLA_STATUS_TIMEOUT    0x1u  /* a bounded wait inside a kernel ran out; that CTA aborted */
 #define MLA_STATUS_BAD_SHAPE  0x2u  /* a dense job held more than 64 query rows (s_q_b * h_q/h_kv);
                                        it wrote nothing */
+#define MLA_STATUS_BAD_ALIGN  0x4u  /* the dynamic shared memory base was not 1024-byte aligned;
+                                       the sparse kernel wrote nothing */
 
 /* Output element types of the final cast (FlashMLA PR #25, "What changes":
  * the FP8 cast moves into the combine; the fp32 pass-through exists for parity). */

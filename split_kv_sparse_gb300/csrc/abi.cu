@@ -58,6 +58,10 @@ int device_state(DeviceState** out) {
       cudaGetLastError();
       return MLA_ERR_CUDA;
     }
+    if (skv::prepare_mla_kernels() != cudaSuccess || skv::prepare_sdpa_kernels() != cudaSuccess) {
+      cudaGetLastError();
+      return MLA_ERR_CUDA;
+    }
     d.status = static_cast<uint32_t*>(p);
     d.ready = true;
   }

@@ -38,6 +38,10 @@ struct MlaArgs {
 
 // Dynamic shared memory the MLA decode kernel needs.
 int mla_decode_smem_bytes();
+// One-time per-device set-up (shared-memory opt-in of the kernels); called by the
+// ABI the first time it sees a device, outside any stream capture.
+cudaError_t prepare_mla_kernels();
+cudaError_t prepare_sdpa_kernels();
 
 // tm_q: Q viewed as 2-D [s_q*64 rows][576] bf16, box 64x64, 128B swizzle.
 // tm_kv: KV viewed as 2-D [n_kv rows][576] bf16, box 64x1 (gather4), 128B swizzle.

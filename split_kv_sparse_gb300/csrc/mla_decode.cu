@@ -15,15 +15,24 @@
 //              out-of-range row, which TMA fills with zeros.
 //   warp 1     tcgen05 issue (one thread):
 //                S^T[128 window rows x 64 heads] = K_window . Q^T  (M=128, N=64, K=576)
-//                O^T[512 x 64] += V_half^T . P^T  (4 x (M=128, N=64, K=64))
+//                O^T[512 x 64] += V_half^T . (P_hi + P_lo)^T       (8 x (M=128, N=64, K=64))
+//                L[. x 64]     += 1 . (P_hi + P_lo)^T              (row sums, 2 x (M=128, N=64, K=64))
 //              V is read straight out of the gathered rows as an MN-major
 //              operand; K and Q are K-major; all tiles use the 128-byte swizzle.
+//              QK of the next step is issued as soon as its rows have landed,
+//              so it overlaps the softmax of the current step.
 //   warps 2-5  softmax on the rows of the new half (TMEM lanes 64h..64h+63),
-//              online max with a lazy rescale of O^T in TMEM, P^T (bf16) into
-//              the free RoPE column chunk of the half, then the epilogue.
+//              online max with a lazy rescale of O^T in TMEM, then the epilogue.
 // The 128-row window is the two halves together: each step computes S^T for
 // both halves and keeps the 64 new rows, which lets every MMA use the M=128
 // data path with one TMEM lane per row.
+//
+// Precision: p = 2^(x - m_ref) is stored as P_hi = bf16(p) and
+// P_lo = bf16(p - P_hi); the PV product uses both, so P enters O with ~2^-16
+// relative error instead of the 2^-8 of a single bf16. O is normalised by the
+// sum of the same P_hi + P_lo (formed by the tensor core against a 128-byte
+// all-ones operand read at zero stride); the fp32 sum of p that gives the LSE
+// stays in per-thread partials, reduced once at the end.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -43,18 +52,19 @@ constexpr int kRingBytes = kChunks * kSlotBytes;    // 147456
 constexpr int kQBytes = kChunks * kQChunkBytes;     // 73728
 constexpr int kStepTx = kChunks * kHalfBytes;       // bytes landing per step (64 rows x 1152 B)
 
+// Shared memory map. The dynamic shared memory base is 1024-byte aligned (the
+// kernel checks it and refuses to run otherwise), so no slack is reserved.
 constexpr int kOffRing = 0;
-constexpr int kOffQ = kOffRing + kRingBytes;
-constexpr int kOffBars = kOffQ + kQBytes;
+constexpr int kOffQ = kOffRing + kRingBytes;        // 147456
+constexpr int kOffPlo = kOffQ + kQBytes;            // 221184: P_lo^T, 64 heads x 64 rows bf16
+constexpr int kOffBars = kOffPlo + kHalfBytes;      // 229376
 constexpr int kOffMisc = kOffBars + 128;            // [0] tmem base, [1] abort flag, [4..] warp flags
 constexpr int kOffMuse = kOffMisc + 128;            // float[64] reference max per head (log2 units)
-constexpr int kOffAlpha = kOffMuse + 256;           // float[64] rescale factor of a rescale step
-constexpr int kOffMnew = kOffAlpha + 256;           // float[64]
-constexpr int kOffTmax = kOffMnew + 256;            // float[4][64] per-warp tile maxima
-constexpr int kOffLred = kOffTmax + 1024;           // float[4][64] per-warp row sums
-constexpr int kOffInv = kOffLred + 1024;            // float[64] 1 / denominator
-constexpr int kSmemUsed = kOffInv + 256;
-constexpr int kSmemBytes = kSmemUsed + 1024;        // slack to align the base to 1024 B
+constexpr int kOffAlpha = kOffMuse + 256;           // float[64] rescale factors; 1/denominator at the end
+constexpr int kOffTmax = kOffAlpha + 256;           // float[4][64] tile maxima; row sums at the end
+constexpr int kOffOnes = kOffTmax + 1024;           // 8 x 8 bf16 ones: the A operand of the row-sum MMA
+constexpr int kOffRsum = kOffOnes + 128;            // float[64] sums of P_hi + P_lo
+constexpr int kSmemBytes = kOffRsum + 256;          // 231552
 
 enum {
   B_QFULL = 0, B_FULL0, B_FULL1, B_EMPTY0, B_EMPTY1, B_SFULL0, B_SFULL1,
@@ -64,22 +74,20 @@ static_assert(kNumBars * 8 <= 128, "barrier area");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 256;                    // S^T buffers at columns 256 and 320
+constexpr uint32_t kTmemL = 384;                    // row sums of P (every lane the same)
 constexpr float kRescaleThreshold = 8.0f;           // p = 2^(x - m_ref) <= 256 between rescales
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Wait sites reported in the status word when a bounded wait runs out.
 enum : uint32_t {
-  W_PROD_EMPTY = 1, W_MMA_Q, W_MMA_P, W_MMA_FULL, W_SM_S, W_SM_PV_RESCALE, W_SM_PV_EPI,
-  W_DRAIN_MMA, W_DRAIN_TMA
+  W_PROD_EMPTY = 1, W_MMA_Q, W_MMA_STALL, W_SM_S, W_SM_PV, W_SM_PV_EPI, W_DRAIN_MMA, W_DRAIN_TMA
 };
 
 template <bool kDirect>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_kv, const MlaArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -107,6 +115,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x < kMlaHeads) a.lse_acc[out_row + threadIdx.x] = -INFINITY;
     return;
   }
+  if ((sbase & 1023u) != 0) {
+    // the swizzled tiles need a 1024-byte aligned base; report and do nothing
+    grid_launch_dependents();
+    if (threadIdx.x == 0) atomicOr(&a.status[0], 4u);
+    return;
+  }
 
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBars + 8 * i; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kOffMisc);
@@ -114,10 +128,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* flags = reinterpret_cast<volatile int*>(misc + 4);   // [2][4] step flags, [8..11] final
   float* m_use = reinterpret_cast<float*>(smem + kOffMuse);
   float* alpha = reinterpret_cast<float*>(smem + kOffAlpha);
-  float* m_new = reinterpret_cast<float*>(smem + kOffMnew);
+  float* inv_s = alpha;                                               // epilogue reuse
   float* tmax = reinterpret_cast<float*>(smem + kOffTmax);
-  float* lred = reinterpret_cast<float*>(smem + kOffLred);
-  float* inv_s = reinterpret_cast<float*>(smem + kOffInv);
+  float* lred = tmax;                                                 // epilogue reuse
+  float* rsum_s = reinterpret_cast<float*>(smem + kOffRsum);
   const WaitCtx wc{a.wait_limit_ns, a.status, abort_flag};
 
   if (threadIdx.x == 0) {
@@ -136,6 +150,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init_fence();
   }
   if (threadIdx.x >= 64 && threadIdx.x < 128) m_use[threadIdx.x - 64] = -INFINITY;
+  if (threadIdx.x >= 128 && threadIdx.x < 136) {
+    // bf16 1.0 = 0x3F80; read by the tensor core (async proxy) after the fence
+    reinterpret_cast<uint4*>(smem + kOffOnes)[threadIdx.x - 128] =
+        make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_proxy_async_smem();
+  }
   if (warp == 1) {
     tmem_alloc(smem_u32(misc), kTmemCols);
     tmem_relinquish();
@@ -213,10 +233,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ========================================================= MMA issuer ===
     if (lane == 0) {
-      constexpr uint32_t kIdescQK = idesc_make(128, 64, 1, false, false);
-      constexpr uint32_t kIdescPV = idesc_make(128, 64, 1, true, false);
+      constexpr uint32_t kIdescKK = idesc_make(128, 64, 1, false, false);   // A, B K-major
+      constexpr uint32_t kIdescPV = idesc_make(128, 64, 1, true, false);    // A MN-major (V^T)
       const uint32_t ring = sbase + kOffRing;
       const uint32_t qs = sbase + kOffQ;
+      const uint64_t ones_desc = sdesc_noswizzle(sbase + kOffOnes, 0, 0);   // one 8x8 core matrix, zero strides
       auto issue_qk = [&](int k) {
         const uint32_t d = tmem + kTmemS + 64 * (k & 1);
 #pragma unroll
@@ -224,46 +245,66 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_f16(d, sdesc_sw128(ring + c * kSlotBytes + kk * 32, 16, 1024),
-                    sdesc_sw128(qs + c * kQChunkBytes + kk * 32, 16, 1024), kIdescQK,
+                    sdesc_sw128(qs + c * kQChunkBytes + kk * 32, 16, 1024), kIdescKK,
                     (c | kk) != 0);
       };
       auto issue_pv = [&](int k) {
         const int h = k & 1;
-        const uint32_t pt = ring + 8 * kSlotBytes + h * kHalfBytes;
+        const uint32_t p_hi = ring + 8 * kSlotBytes + h * kHalfBytes;
+        const uint32_t p_lo = sbase + kOffPlo;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int part = 0; part < 2; ++part) {
+          const uint32_t pt = part ? p_lo : p_hi;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16(tmem + 64 * j,
+                      sdesc_sw128(ring + 2 * j * kSlotBytes + h * kHalfBytes + kk * 2048, kSlotBytes, 1024),
+                      sdesc_sw128(pt + kk * 32, 16, 1024), kIdescPV, (k > 0 || part > 0 || kk > 0));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_f16(tmem + 64 * j,
-                    sdesc_sw128(ring + 2 * j * kSlotBytes + h * kHalfBytes + kk * 2048, kSlotBytes,
-                                1024),
-                    sdesc_sw128(pt + kk * 32, 16, 1024), kIdescPV, (k > 0 || kk > 0));
+            mma_f16(tmem + kTmemL, ones_desc, sdesc_sw128(pt + kk * 32, 16, 1024), kIdescKK,
+                    (k > 0 || part > 0 || kk > 0));
+        }
       };
       bool ok = wait_bounded(bar(B_QFULL), 0, wc, W_MMA_Q);
-#pragma unroll 1
-      for (int k = 0; ok && k < nsteps; ++k) {
-        if (k >= 1) {
-          ok = wait_bounded(bar(B_PFULL0 + ((k - 1) & 1)), ((k - 1) >> 1) & 1, wc, W_MMA_P);
-          if (!ok) break;
+      // Issue QK(k) as soon as its rows have landed and its S^T buffer is free
+      // (softmax(k-2) is done, i.e. PV(k-2) was issued), and PV(k) as soon as
+      // softmax(k) has written P. One thread; tcgen05 runs them in issue order.
+      int nqk = 0, npv = 0;
+      uint64_t t_idle = 0;
+      while (ok && npv < nsteps) {
+        bool progress = false;
+        if (nqk < nsteps && nqk <= npv + 1 && mbar_try_wait(bar(B_FULL0 + (nqk & 1)), (nqk >> 1) & 1)) {
           tc_fence_after();
-          issue_pv(k - 1);
-          mma_commit(bar(B_EMPTY0 + ((k - 1) & 1)));
-          mma_commit(bar(B_PVDONE));
+          issue_qk(nqk);
+          mma_commit(bar(B_SFULL0 + (nqk & 1)));
+          ++nqk;
+          progress = true;
         }
-        ok = wait_bounded(bar(B_FULL0 + (k & 1)), (k >> 1) & 1, wc, W_MMA_FULL);
-        if (!ok) break;
-        tc_fence_after();
-        issue_qk(k);
-        mma_commit(bar(B_SFULL0 + (k & 1)));
-      }
-      if (ok) {
-        const int k = nsteps - 1;
-        ok = wait_bounded(bar(B_PFULL0 + (k & 1)), (k >> 1) & 1, wc, W_MMA_P);
-        if (ok) {
+        if (npv < nqk && mbar_try_wait(bar(B_PFULL0 + (npv & 1)), (npv >> 1) & 1)) {
           tc_fence_after();
-          issue_pv(k);
-          mma_commit(bar(B_EMPTY0 + (k & 1)));
+          issue_pv(npv);
+          mma_commit(bar(B_EMPTY0 + (npv & 1)));
           mma_commit(bar(B_PVDONE));
+          ++npv;
+          progress = true;
+        }
+        if (progress) {
+          t_idle = 0;
+        } else {
+          const uint64_t now = globaltimer_ns();
+          if (*abort_flag) {
+            ok = false;
+          } else if (t_idle == 0) {
+            t_idle = now;
+          } else if (now - t_idle > a.wait_limit_ns) {
+            *abort_flag = 1;
+            atomicOr(&a.status[0], 1u);
+            atomicCAS(&a.status[1], 0u, W_MMA_STALL);
+            ok = false;
+          }
         }
       }
       if (!ok) {
@@ -279,12 +320,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x - 64;      // 0..127
     const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
     const int32_t* idx_t = a.idx + static_cast<size_t>(t) * a.topk;
-    uint8_t* const ring_p = smem + kOffRing;
-    // Running softmax denominators of heads 2*lane and 2*lane+1 over this warp's
-    // rows: lsum* from the fp32 p (gives the LSE), rsum* from the bf16-rounded p
-    // that the PV MMA actually multiplies (normalises O, so a dominant row comes
-    // out exact instead of carrying its own rounding error).
-    float lsum0 = 0.f, lsum1 = 0.f, rsum0 = 0.f, rsum1 = 0.f;
+    // fp32 softmax denominators per head over the rows this thread has held
+    // (gives the LSE); reduced over threads once, in the epilogue.
+    float lpart[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) lpart[i] = 0.f;
     int bad = 0;   // a bounded wait of this warp ran out
 
 #pragma unroll 1
@@ -332,6 +372,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         bad = 1;
         break;   // every softmax warp sees the same flags and leaves together
       }
+
+      // PV(k-1) must be complete before O^T is rescaled and before P_lo (one
+      // buffer for all steps) is overwritten.
+      if (k >= 1) {
+        int wp = 1;
+        if (lane == 0) wp = wait_bounded(bar(B_PVDONE), (k - 1) & 1, wc, W_SM_PV);
+        wp = __shfl_sync(0xffffffffu, wp, 0);
+        if (!wp) bad = 1;
+        tc_fence_after();
+      }
+
       if (f & 1) {
         float mx0, mx1;
         warp_transpose_reduce<true>(x, lane, mx0, mx1);
@@ -343,63 +394,47 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float mo = m_use[tid];
           const float mn = fmaxf(mo, tm);
           alpha[tid] = (mn == -INFINITY) ? 1.f : ex2_approx(mo - mn);
-          m_new[tid] = mn;
+          m_use[tid] = mn;   // nobody else reads m_use until the barrier below
         }
         named_bar_sync(1, 128);
-        lsum0 *= alpha[2 * lane];
-        lsum1 *= alpha[2 * lane + 1];
-        rsum0 *= alpha[2 * lane];
-        rsum1 *= alpha[2 * lane + 1];
-        if (k >= 1) {
-          // O^T holds PV of steps < k: wait for the last one, then scale every head column
-          int wp = 1;
-          if (lane == 0) wp = wait_bounded(bar(B_PVDONE), (k - 1) & 1, wc, W_SM_PV_RESCALE);
-          wp = __shfl_sync(0xffffffffu, wp, 0);
-          tc_fence_after();
-          if (wp) {
-#pragma unroll 1
-            for (int j = 0; j < 8; ++j) {   // 4 O^T chunks x 2 halves of 32 head columns
-              uint32_t o[32];
-              const int c0 = 32 * (j & 1);
-              tmem_ld_32x32b_x32(tmem + lane_base + 64 * (j >> 1) + c0, o);
-              tmem_wait_ld_x32(o);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha[c0 + i]);
-              tmem_st_32x32b_x32(tmem + lane_base + 64 * (j >> 1) + c0, o);
-            }
-            tmem_wait_st();
-          } else {
-            bad = 1;
+        for (int i = 0; i < 64; ++i) lpart[i] *= alpha[i];
+        if (k >= 1 && !bad) {
+          // O^T and the row sums hold PV of steps < k: scale every head column
+#pragma unroll 1
+          for (int j = 0; j < 10; ++j) {   // 4 O^T chunks + the row sums, 2 x 32 head columns each
+            uint32_t o[32];
+            const int c0 = 32 * (j & 1);
+            const uint32_t col = (j < 8 ? 64 * (j >> 1) : kTmemL) + c0;
+            tmem_ld_32x32b_x32(tmem + lane_base + col, o);
+            tmem_wait_ld_x32(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha[c0 + i]);
+            tmem_st_32x32b_x32(tmem + lane_base + col, o);
           }
+          tmem_wait_st();
         }
-        if (tid < 64) m_use[tid] = m_new[tid];
-        named_bar_sync(1, 128);
       }
 
       if (active) {
-        // p = 2^(x - m_ref) into P^T (bf16, K-major, 128-byte swizzle) in the
-        // RoPE chunk of this half, which the QK of this step no longer needs.
-        uint8_t* pt = ring_p + 8 * kSlotBytes + h * kHalfBytes;
+        // p = 2^(x - m_ref) as P_hi (bf16, into the RoPE chunk of this half, which
+        // the QK of this step no longer needs) and P_lo = bf16(p - P_hi); both
+        // K-major with the 128-byte swizzle.
+        uint8_t* pt_hi = smem + kOffRing + 8 * kSlotBytes + h * kHalfBytes;
+        uint8_t* pt_lo = smem + kOffPlo;
         const int rchunk = rloc >> 3;
         const int rbyte = (rloc & 7) * 2;
-        float pr[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
           const float p = (x[i] == -INFINITY) ? 0.f : ex2_approx(x[i] - m_use[i]);
-          x[i] = p;
-          const __nv_bfloat16 pb = __float2bfloat16_rn(p);
-          pr[i] = __bfloat162float(pb);
+          lpart[i] += p;
+          const __nv_bfloat16 hi = __float2bfloat16_rn(p);
+          const __nv_bfloat16 lo = __float2bfloat16_rn(p - __bfloat162float(hi));
           const int off = (i >> 3) * 1024 + (i & 7) * 128 + ((rchunk ^ (i & 7)) << 4) + rbyte;
-          *reinterpret_cast<__nv_bfloat16*>(pt + off) = pb;
+          *reinterpret_cast<__nv_bfloat16*>(pt_hi + off) = hi;
+          *reinterpret_cast<__nv_bfloat16*>(pt_lo + off) = lo;
         }
         fence_proxy_async_smem();
-        float s0, s1;
-        warp_transpose_reduce<false>(x, lane, s0, s1);
-        lsum0 += s0;
-        lsum1 += s1;
-        warp_transpose_reduce<false>(pr, lane, s0, s1);
-        rsum0 += s0;
-        rsum1 += s1;
       }
       tc_fence_before();
       __syncwarp();
@@ -407,16 +442,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---- epilogue ---------------------------------------------------------
-    lred[wi * 64 + 2 * lane] = lsum0;
-    lred[wi * 64 + 2 * lane + 1] = lsum1;
-    tmax[wi * 64 + 2 * lane] = rsum0;       // the tile-max scratch is free here
-    tmax[wi * 64 + 2 * lane + 1] = rsum1;
+    {
+      float ls0, ls1;
+      warp_transpose_reduce<false>(lpart, lane, ls0, ls1);
+      lred[wi * 64 + 2 * lane] = ls0;
+      lred[wi * 64 + 2 * lane + 1] = ls1;
+    }
     if (lane == 0) flags[8 + wi] = bad;
     named_bar_sync(1, 128);
     const bool any_bad = flags[8] | flags[9] | flags[10] | flags[11];
+    int wp = 0;
+    if (!any_bad) {
+      if (lane == 0) wp = wait_bounded(bar(B_PVDONE), (nsteps - 1) & 1, wc, W_SM_PV_EPI);
+      wp = __shfl_sync(0xffffffffu, wp, 0);
+      tc_fence_after();
+      if (wp && wi == 0) {
+        // every TMEM lane of the row-sum block holds the same 64 sums; lane c%32 keeps column c
+        uint32_t r[64];
+        tmem_ld_32x32b_x64(tmem + lane_base + kTmemL, r);
+        tmem_wait_ld_x64(r);
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if ((c & 31) == lane) rsum_s[c] = __uint_as_float(r[c]);
+      }
+    }
+    named_bar_sync(1, 128);
     if (tid < 64) {
       const float l = (lred[tid] + lred[64 + tid]) + (lred[128 + tid] + lred[192 + tid]);
-      const float lr = (tmax[tid] + tmax[64 + tid]) + (tmax[128 + tid] + tmax[192 + tid]);
+      const float lr = rsum_s[tid];
       const float mu = m_use[tid];
       float lse = -INFINITY, inv = 0.f;
       if (l > 0.f) {
@@ -433,55 +486,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     named_bar_sync(1, 128);
-    if (!any_bad) {
-      int wp = 1;
-      if (lane == 0) wp = wait_bounded(bar(B_PVDONE), (nsteps - 1) & 1, wc, W_SM_PV_EPI);
-      wp = __shfl_sync(0xffffffffu, wp, 0);
-      tc_fence_after();
-      if (wp) {
-        float amax_l = 0.f;
+    if (!any_bad && wp) {
+      float amax_l = 0.f;
 #pragma unroll 1
-        for (int j = 0; j < 4; ++j) {
-          uint32_t o[64];
-          tmem_ld_32x32b_x64(tmem + lane_base + 64 * j, o);
-          tmem_wait_ld_x64(o);
-          const int d = 128 * j + 32 * sp + lane;
-          if (!kDirect) {
-            float* dst = a.o_acc + out_row * kMlaDv + d;
+      for (int j = 0; j < 4; ++j) {
+        uint32_t o[64];
+        tmem_ld_32x32b_x64(tmem + lane_base + 64 * j, o);
+        tmem_wait_ld_x64(o);
+        const int d = 128 * j + 32 * sp + lane;
+        if (!kDirect) {
+          float* dst = a.o_acc + out_row * kMlaDv + d;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) dst[c * kMlaDv] = __uint_as_float(o[c]) * inv_s[c];
-          } else if (a.out_dtype == 0) {
-            float* dst = static_cast<float*>(a.out) + out_row * kMlaDv + d;
+          for (int c = 0; c < 64; ++c) dst[c * kMlaDv] = __uint_as_float(o[c]) * inv_s[c];
+        } else if (a.out_dtype == 0) {
+          float* dst = static_cast<float*>(a.out) + out_row * kMlaDv + d;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-              const float v = __uint_as_float(o[c]) * inv_s[c];
-              amax_l = fmaxf(amax_l, fabsf(v));
-              dst[c * kMlaDv] = v;
-            }
-          } else if (a.out_dtype == 1) {
-            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + out_row * kMlaDv + d;
+          for (int c = 0; c < 64; ++c) {
+            const float v = __uint_as_float(o[c]) * inv_s[c];
+            amax_l = fmaxf(amax_l, fabsf(v));
+            dst[c * kMlaDv] = v;
+          }
+        } else if (a.out_dtype == 1) {
+          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + out_row * kMlaDv + d;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-              const float v = __uint_as_float(o[c]) * inv_s[c];
-              amax_l = fmaxf(amax_l, fabsf(v));
-              dst[c * kMlaDv] = __float2bfloat16_rn(v);
-            }
-          } else {
-            uint8_t* dst = static_cast<uint8_t*>(a.out) + out_row * kMlaDv + d;
+          for (int c = 0; c < 64; ++c) {
+            const float v = __uint_as_float(o[c]) * inv_s[c];
+            amax_l = fmaxf(amax_l, fabsf(v));
+            dst[c * kMlaDv] = __float2bfloat16_rn(v);
+          }
+        } else {
+          uint8_t* dst = static_cast<uint8_t*>(a.out) + out_row * kMlaDv + d;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-              const float v = __uint_as_float(o[c]) * inv_s[c];
-              amax_l = fmaxf(amax_l, fabsf(v));
-              dst[c * kMlaDv] = static_cast<uint8_t>(
-                  __nv_cvt_float_to_fp8(v * a.inv_scale, __NV_SATFINITE, __NV_E4M3));
-            }
+          for (int c = 0; c < 64; ++c) {
+            const float v = __uint_as_float(o[c]) * inv_s[c];
+            amax_l = fmaxf(amax_l, fabsf(v));
+            dst[c * kMlaDv] = static_cast<uint8_t>(
+                __nv_cvt_float_to_fp8(v * a.inv_scale, __NV_SATFINITE, __NV_E4M3));
           }
         }
-        if (kDirect && a.amax != nullptr) {
+      }
+      if (kDirect && a.amax != nullptr) {
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) amax_l = fmaxf(amax_l, __shfl_xor_sync(0xffffffffu, amax_l, o));
-          if (lane == 0) atomicMax(reinterpret_cast<int*>(a.amax), __float_as_int(amax_l));
-        }
+        for (int o = 16; o > 0; o >>= 1) amax_l = fmaxf(amax_l, __shfl_xor_sync(0xffffffffu, amax_l, o));
+        if (lane == 0) atomicMax(reinterpret_cast<int*>(a.amax), __float_as_int(amax_l));
       }
     }
   }
@@ -499,22 +546,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int mla_decode_smem_bytes() { return kSmemBytes; }
 
+cudaError_t prepare_mla_kernels() {
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(mla_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+}
+
 cudaError_t launch_mla_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const MlaArgs& a,
                               bool direct, cudaStream_t stream) {
-  static_assert(kSmemBytes <= 232448, "shared memory budget");
   const dim3 grid(static_cast<unsigned>(a.s_q) * static_cast<unsigned>(a.num_splits));
-  cudaError_t e;
-  if (direct) {
-    e = cudaFuncSetAttribute(mla_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
-    if (e != cudaSuccess) return e;
+  if (direct)
     mla_decode_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_kv, a);
-  } else {
-    e = cudaFuncSetAttribute(mla_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
-    if (e != cudaSuccess) return e;
+  else
     mla_decode_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_kv, a);
-  }
   return cudaGetLastError();
 }
 

@@ -219,6 +219,17 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Descriptor of an operand without swizzling (8-row x 16-byte core matrices):
+// lbo = byte stride between core matrices along K, sbo = along M/N.
+__device__ __forceinline__ uint64_t sdesc_noswizzle(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
 // Instruction descriptor: fp32 accumulator, A/B element format `fmt`
 // (kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4: 0 = e4m3), operand majorness,
 // M and N. Bits: [4,6) D format (1 = f32), [7,10) A fmt, [10,13) B fmt,

@@ -481,11 +481,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int sdpa_decode_smem_bytes() { return kSmemBytes; }
 
+cudaError_t prepare_sdpa_kernels() {
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  return cudaFuncSetAttribute(sdpa_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+}
+
 cudaError_t launch_sdpa_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                const SdpaArgs& a, bool direct, cudaStream_t stream) {
-  static_assert(kSmemBytes <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(sdpa_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(a.batch) * a.h_kv * a.num_splits);
   sdpa_decode_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, a, direct ? 1 : 0);
   return cudaGetLastError();
