@@ -138,12 +138,9 @@ int check_mla_inputs(int s_q, int topk, const void* q, const void* kv, int64_t n
   return MLA_OK;
 }
 
-int mla_tensor_maps(int s_q, const void* q, const void* kv, int64_t n_kv, CUtensorMap* tq, CUtensorMap* tkv) {
-  int st = encode_2d(tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, kMlaDqk,
-                     static_cast<uint64_t>(s_q) * kMlaHeads, kMlaDqk * 2, 64, 64);
-  if (st != MLA_OK) return st;
-  return encode_2d(tkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kv, kMlaDqk, static_cast<uint64_t>(n_kv),
-                   kMlaDqk * 2, 64, 1);
+int mla_q_tensor_map(int s_q, const void* q, CUtensorMap* tq) {
+  return encode_2d(tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, kMlaDqk, static_cast<uint64_t>(s_q) * kMlaHeads,
+                   kMlaDqk * 2, 64, 64);
 }
 
 }  // namespace
@@ -223,9 +220,10 @@ int mla_sparse_decode_split(const mla_plan_t* plan, int s_q, const void* q, cons
   if (workspace == nullptr || !aligned(workspace, 256) || plan->workspace_bytes == 0) return MLA_ERR_WORKSPACE;
   DeviceState* dev = nullptr;
   if ((st = device_state(&dev)) != MLA_OK) return st;
-  CUtensorMap tq, tkv;
-  if ((st = mla_tensor_maps(s_q, q, kv, n_kv, &tq, &tkv)) != MLA_OK) return st;
+  CUtensorMap tq;
+  if ((st = mla_q_tensor_map(s_q, q, &tq)) != MLA_OK) return st;
   skv::MlaArgs a{};
+  a.kv = static_cast<const uint8_t*>(kv);
   a.idx = idx;
   a.s_q = s_q;
   a.topk = plan->topk;
@@ -237,7 +235,7 @@ int mla_sparse_decode_split(const mla_plan_t* plan, int s_q, const void* q, cons
   a.lse_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan->lse_acc_offset);
   a.status = dev->status;
   a.wait_limit_ns = kWaitLimitNs;
-  return cuda_status(skv::launch_mla_decode(tq, tkv, a, false, static_cast<cudaStream_t>(stream)));
+  return cuda_status(skv::launch_mla_decode(tq, a, false, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"
@@ -292,13 +290,14 @@ int mla_sparse_decode_direct(int s_q, int topk, const void* q, const void* kv, i
   if (out_dtype == MLA_OUT_E4M3 && !std::isfinite(out_inv_scale)) return MLA_ERR_INVALID_ARG;
   DeviceState* dev = nullptr;
   if ((st = device_state(&dev)) != MLA_OK) return st;
-  CUtensorMap tq, tkv;
-  if ((st = mla_tensor_maps(s_q, q, kv, n_kv, &tq, &tkv)) != MLA_OK) return st;
+  CUtensorMap tq;
+  if ((st = mla_q_tensor_map(s_q, q, &tq)) != MLA_OK) return st;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (amax_out != nullptr) {
     if ((st = cuda_status(cudaMemsetAsync(amax_out, 0, sizeof(float), cs))) != MLA_OK) return st;
   }
   skv::MlaArgs a{};
+  a.kv = static_cast<const uint8_t*>(kv);
   a.idx = idx;
   a.s_q = s_q;
   a.topk = topk;
@@ -314,7 +313,7 @@ int mla_sparse_decode_direct(int s_q, int topk, const void* q, const void* kv, i
   a.amax = amax_out;
   a.status = dev->status;
   a.wait_limit_ns = kWaitLimitNs;
-  return cuda_status(skv::launch_mla_decode(tq, tkv, a, true, cs));
+  return cuda_status(skv::launch_mla_decode(tq, a, true, cs));
 }
 
 int mla_sparse_decode(const mla_plan_t* plan, int s_q, const void* q, const void* kv, int64_t n_kv,

@@ -15,6 +15,7 @@ constexpr int kMlaBlockRows = 64;   // top-k entries per block (split unit and p
 
 // Per-launch arguments of the sparse-MLA decode kernel (split or direct epilogue).
 struct MlaArgs {
+  const uint8_t* kv;    // [n_kv][576] bf16 rows of 1152 B
   const int32_t* idx;   // [s_q][topk]
   int s_q;
   int topk;
@@ -44,9 +45,7 @@ cudaError_t prepare_mla_kernels();
 cudaError_t prepare_sdpa_kernels();
 
 // tm_q: Q viewed as 2-D [s_q*64 rows][576] bf16, box 64x64, 128B swizzle.
-// tm_kv: KV viewed as 2-D [n_kv rows][576] bf16, box 64x1 (gather4), 128B swizzle.
-cudaError_t launch_mla_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
-                              const MlaArgs& a, bool direct, cudaStream_t stream);
+cudaError_t launch_mla_decode(const CUtensorMap& tm_q, const MlaArgs& a, bool direct, cudaStream_t stream);
 
 // Log-sum-exp combine over `rows` output rows of width d (512 or 128).
 struct CombineArgs {

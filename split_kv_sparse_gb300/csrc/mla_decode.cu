@@ -8,12 +8,15 @@
 //   direct path: the same O with the attention sink folded into the
 //                denominator, cast to fp32 / bf16 / e4m3, plus LSE and amax.
 //
-// Layout of the work (one CTA per job, 192 threads):
-//   warp 0     TMA: Q once (9 tiles of 64 heads x 64 dims), then per step 64
-//              gathered rows as 16 x 9 tile::gather4 loads (4 rows x 128 B each)
-//              into a ring of two 64-row halves; invalid indices become an
-//              out-of-range row, which TMA fills with zeros.
-//   warp 1     tcgen05 issue (one thread):
+// Layout of the work (one CTA per job, 256 threads):
+//   warps 0-2  loads: Q once by TMA (9 tiles of 64 heads x 64 dims); per step
+//              the 64 gathered rows as 4608 16-byte cp.async copies (each row
+//              is 72 contiguous 16-byte pieces; a warp instruction covers 512
+//              contiguous bytes of a row), written in the 128-byte-swizzled
+//              layout into one half of a ring of two 64-row halves; an invalid
+//              index copies zeros and reads nothing. Completion is tracked per
+//              thread by cp.async.mbarrier.arrive.
+//   warp 3     tcgen05 issue (one thread):
 //                S^T[128 window rows x 64 heads] = K_window . Q^T  (M=128, N=64, K=576)
 //                O^T[512 x 64] += V_half^T . (P_hi + P_lo)^T       (8 x (M=128, N=64, K=64))
 //                L[. x 64]     += 1 . (P_hi + P_lo)^T              (row sums, 2 x (M=128, N=64, K=64))
@@ -21,7 +24,7 @@
 //              operand; K and Q are K-major; all tiles use the 128-byte swizzle.
 //              QK of the next step is issued as soon as its rows have landed,
 //              so it overlaps the softmax of the current step.
-//   warps 2-5  softmax on the rows of the new half (TMEM lanes 64h..64h+63),
+//   warps 4-7  softmax on the rows of the new half (TMEM lanes 64h..64h+63),
 //              online max with a lazy rescale of O^T in TMEM, then the epilogue.
 // The 128-row window is the two halves together: each step computes S^T for
 // both halves and keeps the 64 new rows, which lets every MMA use the M=128
@@ -43,14 +46,16 @@
 namespace skv {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 256;
+constexpr int kProducers = 96;                      // warps 0-2
+constexpr int kPiecesPerRow = 72;                   // 1152 B / 16 B
+constexpr int kPiecesPerThread = kMlaBlockRows * kPiecesPerRow / kProducers;   // 48
 constexpr int kChunks = 9;                          // 576 dims = 9 column chunks of 64 (128 B)
 constexpr int kSlotBytes = 16384;                   // one column chunk of the 128-row window
 constexpr int kHalfBytes = 8192;                    // the 64-row half of a slot
 constexpr int kQChunkBytes = 8192;                  // 64 heads x 128 B
 constexpr int kRingBytes = kChunks * kSlotBytes;    // 147456
 constexpr int kQBytes = kChunks * kQChunkBytes;     // 73728
-constexpr int kStepTx = kChunks * kHalfBytes;       // bytes landing per step (64 rows x 1152 B)
 
 // Shared memory map. The dynamic shared memory base is 1024-byte aligned (the
 // kernel checks it and refuses to run otherwise), so no slack is reserved.
@@ -64,7 +69,8 @@ constexpr int kOffAlpha = kOffMuse + 256;           // float[64] rescale factors
 constexpr int kOffTmax = kOffAlpha + 256;           // float[4][64] tile maxima; row sums at the end
 constexpr int kOffOnes = kOffTmax + 1024;           // 8 x 8 bf16 ones: the A operand of the row-sum MMA
 constexpr int kOffRsum = kOffOnes + 128;            // float[64] sums of P_hi + P_lo
-constexpr int kSmemBytes = kOffRsum + 256;          // 231552
+constexpr int kOffIdx = kOffRsum + 256;             // int[2][64] row indices of the step, per half
+constexpr int kSmemBytes = kOffIdx + 512;           // 232064
 
 enum {
   B_QFULL = 0, B_FULL0, B_FULL1, B_EMPTY0, B_EMPTY1, B_SFULL0, B_SFULL1,
@@ -80,13 +86,12 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // Wait sites reported in the status word when a bounded wait runs out.
 enum : uint32_t {
-  W_PROD_EMPTY = 1, W_MMA_Q, W_MMA_STALL, W_SM_S, W_SM_PV, W_SM_PV_EPI, W_DRAIN_MMA, W_DRAIN_TMA
+  W_PROD_EMPTY = 1, W_MMA_Q, W_MMA_STALL, W_SM_S, W_SM_PV, W_SM_PV_EPI, W_DRAIN_MMA
 };
 
 template <bool kDirect>
 __global__ void __launch_bounds__(kThreads, 1)
-    mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
-                      const __grid_constant__ CUtensorMap tm_kv, const MlaArgs a) {
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const MlaArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
@@ -136,8 +141,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
-    mbar_init(bar(B_FULL0), 1);
-    mbar_init(bar(B_FULL1), 1);
+    mbar_init(bar(B_FULL0), kProducers);   // one cp.async completion arrival per producer thread
+    mbar_init(bar(B_FULL1), kProducers);
     mbar_init(bar(B_EMPTY0), 1);
     mbar_init(bar(B_EMPTY1), 1);
     mbar_init(bar(B_SFULL0), 1);
@@ -149,14 +154,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     mbar_init_fence();
   }
-  if (threadIdx.x >= 64 && threadIdx.x < 128) m_use[threadIdx.x - 64] = -INFINITY;
-  if (threadIdx.x >= 128 && threadIdx.x < 136) {
+  if (threadIdx.x >= 128 && threadIdx.x < 192) m_use[threadIdx.x - 128] = -INFINITY;
+  if (threadIdx.x < 8) {
     // bf16 1.0 = 0x3F80; read by the tensor core (async proxy) after the fence
-    reinterpret_cast<uint4*>(smem + kOffOnes)[threadIdx.x - 128] =
+    reinterpret_cast<uint4*>(smem + kOffOnes)[threadIdx.x] =
         make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
     fence_proxy_async_smem();
   }
-  if (warp == 1) {
+  if (warp == 3) {
     tmem_alloc(smem_u32(misc), kTmemCols);
     tmem_relinquish();
   }
@@ -168,69 +173,54 @@ __global__ void __launch_bounds__(kThreads, 1)
   // for this whole grid to finish before it reads any partial.
   grid_launch_dependents();
 
-  if (warp == 0) {
-    // ======================================================= TMA producer ===
+  if (warp < 3) {
+    // ========================================================== loaders ===
+    const int ptid = threadIdx.x;          // 0..95
     const int32_t* idx_t = a.idx + static_cast<size_t>(t) * a.topk;
-    if (lane == 0) {
+    int* idx_s = reinterpret_cast<int*>(smem + kOffIdx);
+    volatile int* go = reinterpret_cast<volatile int*>(misc + 2);   // [2]: by step parity
+    if (ptid == 0) {
       tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_kv);
       mbar_arrive_expect_tx(bar(B_QFULL), kQBytes);
 #pragma unroll 1
       for (int c = 0; c < kChunks; ++c)
         tma_load_2d(sbase + kOffQ + c * kQChunkBytes, &tm_q, 64 * c, kMlaHeads * t, bar(B_QFULL));
     }
-    // lane g < 16 owns rows 4g..4g+3 of each step
-    auto load_rows = [&](int k, int (&y)[4]) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = row0 + kMlaBlockRows * k + 4 * lane + i;
-        int v = -1;
-        if (lane < 16 && r < row1) {
-          v = __ldg(idx_t + r);
-          if (v < 0 || v >= a.n_kv) v = -1;
-        }
-        y[i] = v;
+    // thread ptid < 64 fetches the row index of row ptid of a step
+    auto fetch = [&](int k) -> int {
+      const int r = row0 + kMlaBlockRows * k + ptid;
+      int v = -1;
+      if (ptid < kMlaBlockRows && r < row1) {
+        v = __ldg(idx_t + r);
+        if (v < 0 || v >= a.n_kv) v = -1;
       }
+      return v;
     };
-    int cur[4];
-    load_rows(0, cur);
-    int last_issued[2] = {-1, -1};
-    bool ok = true;
+    int cur = fetch(0);
 #pragma unroll 1
     for (int k = 0; k < nsteps; ++k) {
       const int h = k & 1;
-      int nxt[4] = {-1, -1, -1, -1};
-      if (k + 1 < nsteps) load_rows(k + 1, nxt);       // in flight while we wait for the slot
-      if (k >= 2) {
-        int w = 1;
-        if (lane == 0) w = wait_bounded(bar(B_EMPTY0 + h), ((k >> 1) - 1) & 1, wc, W_PROD_EMPTY);
-        w = __shfl_sync(0xffffffffu, w, 0);
-        if (!w) {
-          ok = false;
-          break;
-        }
+      const int nxt = (k + 1 < nsteps) ? fetch(k + 1) : -1;   // in flight during the wait below
+      if (ptid < kMlaBlockRows) idx_s[h * kMlaBlockRows + ptid] = cur;
+      if (ptid == 0) go[h] = (k < 2) ? 1 : wait_bounded(bar(B_EMPTY0 + h), ((k >> 1) - 1) & 1, wc, W_PROD_EMPTY);
+      named_bar_sync(2, kProducers);     // the half is free and its row indices are visible
+      if (!go[h]) break;                 // every loader sees the same flag
+      const uint32_t half_base = sbase + kOffRing + h * kHalfBytes;
+#pragma unroll 8
+      for (int i = 0; i < kPiecesPerThread; ++i) {
+        const int u = ptid + kProducers * i;
+        const int row = u / kPiecesPerRow;
+        const int seg = u - row * kPiecesPerRow;
+        const int ix = idx_s[h * kMlaBlockRows + row];
+        const uint32_t dst = half_base + (seg >> 3) * kSlotBytes + row * 128 + (((seg & 7) ^ (row & 7)) << 4);
+        const uint8_t* src = a.kv + static_cast<size_t>(ix < 0 ? 0 : ix) * (kMlaDqk * 2) + seg * 16;
+        cp_async_16(dst, src, ix < 0 ? 0u : 16u);
       }
-      if (lane == 0) mbar_arrive_expect_tx(bar(B_FULL0 + h), kStepTx);
-      __syncwarp();
-      if (lane < 16) {
-        const uint32_t dst = sbase + kOffRing + h * kHalfBytes + lane * 512;
-#pragma unroll
-        for (int c = 0; c < kChunks; ++c)
-          tma_gather4(dst + c * kSlotBytes, &tm_kv, 64 * c, cur[0], cur[1], cur[2], cur[3],
-                      bar(B_FULL0 + h));
-      }
-      last_issued[h] = k;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
+      cp_async_arrive_noinc(bar(B_FULL0 + h));
+      cur = nxt;
     }
-    if (!ok && lane == 0) {
-      // leave no load in flight into this CTA's shared memory
-      for (int h = 0; h < 2; ++h)
-        if (last_issued[h] >= 0 &&
-            !wait_drain(bar(B_FULL0 + h), (last_issued[h] >> 1) & 1, a.wait_limit_ns))
-          atomicCAS(&a.status[1], 0u, W_DRAIN_TMA);
-    }
-  } else if (warp == 1) {
+    cp_async_wait_all();   // nothing of this thread is still landing when the CTA exits
+  } else if (warp == 3) {
     // ========================================================= MMA issuer ===
     if (lane == 0) {
       constexpr uint32_t kIdescKK = idesc_make(128, 64, 1, false, false);   // A, B K-major
@@ -277,6 +267,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok && npv < nsteps) {
         bool progress = false;
         if (nqk < nsteps && nqk <= npv + 1 && mbar_try_wait(bar(B_FULL0 + (nqk & 1)), (nqk >> 1) & 1)) {
+          // the rows were written by other threads' cp.async (generic proxy); make
+          // them visible to the tensor core's reads (async proxy)
+          fence_proxy_async_smem();
           tc_fence_after();
           issue_qk(nqk);
           mma_commit(bar(B_SFULL0 + (nqk & 1)));
@@ -316,8 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ============================================== softmax + epilogue ====
     const int sp = warp & 3;               // TMEM sub-partition (lanes 32sp..32sp+31)
-    const int wi = warp - 2;               // 0..3
-    const int tid = threadIdx.x - 64;      // 0..127
+    const int wi = warp - 4;               // 0..3
+    const int tid = threadIdx.x - 128;     // 0..127
     const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
     const int32_t* idx_t = a.idx + static_cast<size_t>(t) * a.topk;
     // fp32 softmax denominators per head over the rows this thread has held
@@ -536,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- teardown: every role reaches this point, TMEM is freed by its owner --
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 3) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -554,13 +547,12 @@ cudaError_t prepare_mla_kernels() {
   return cudaFuncSetAttribute(mla_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
 }
 
-cudaError_t launch_mla_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const MlaArgs& a,
-                              bool direct, cudaStream_t stream) {
+cudaError_t launch_mla_decode(const CUtensorMap& tm_q, const MlaArgs& a, bool direct, cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>(a.s_q) * static_cast<unsigned>(a.num_splits));
   if (direct)
-    mla_decode_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_kv, a);
+    mla_decode_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tm_q, a);
   else
-    mla_decode_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_kv, a);
+    mla_decode_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tm_q, a);
   return cudaGetLastError();
 }
 

@@ -132,15 +132,21 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, int x
       : "memory");
 }
 
-// Four rows (y0..y3) of one box-wide column strip starting at x; a row index
-// outside the tensor is filled with zeros (no memory traffic for that row).
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* map, int x, int y0, int y1,
-                                            int y2, int y3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
-      : "memory");
+// ----------------------------------------------------------------- cp.async --
+
+// 16-byte global -> shared copy through L2 (L1 bypassed); src_bytes = 0 writes
+// 16 zero bytes and reads nothing.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+// Arrives on `bar` once every cp.async this thread issued so far has landed
+// (the barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05 --
