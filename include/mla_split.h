@@ -267,6 +267,41 @@ MLA_API int mla_get_status(uint32_t* status_out, uint32_t* site_out);
  * of the bounded waits without hanging or faulting the GPU. */
 MLA_API int mla_selftest_wait_timeout(uint64_t limit_ns, void* stream);
 
+/* ======================================================================= *
+ *  Decode without allocation                                               *
+ * ======================================================================= */
+
+/* Size of the library-owned scratch array used by mla_sparse_decode_noalloc. */
+#define MLA_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* The whole decode step (as mla_sparse_decode) for callers that cannot call
+ * cudaMalloc: for example a plugin whose host hands it only its input and output
+ * buffers and owns all device memory through a fixed memory plan, or code on a
+ * path where an allocation could block on device synchronisation. The fp32
+ * partial workspace of the split pass is a 16 MiB array inside the library's own
+ * device image (MLA_NOALLOC_SCRATCH_BYTES); every GPU that loads the library
+ * holds that array until the process exits. The caller still passes q, kv, idx,
+ * sink and the outputs, as for mla_sparse_decode; the plan is made internally
+ * for this s_q (num_splits: 0 = the automatic choice, > 0 forces that many).
+ * This entry point has no counterpart in the pages: it is a packaging of the
+ * same split + combine for that kind of caller.
+ *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ *   - A call whose workspace would exceed MLA_NOALLOC_SCRATCH_BYTES
+ *     (num_splits * s_q * 64 * (512 + 1) * 4 bytes, rounded up) returns
+ *     MLA_ERR_WORKSPACE and launches nothing; use fewer splits or
+ *     mla_sparse_decode with a caller workspace.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; the split pass overwrites every slot it needs before the combine
+ *     reads it, so no clearing is needed. Calls that overlap on the GPU (on
+ *     different streams, or from several threads) race on the array: order them.
+ *   - The first call on a device resolves the array's device address for that
+ *     device (cudaGetSymbolAddress); make that first call before capturing a
+ *     stream into a CUDA graph. */
+MLA_API int mla_sparse_decode_noalloc(int s_q, int topk, const void* q, const void* kv, int64_t n_kv,
+                                      const int32_t* idx, float sm_scale, const float* sink,
+                                      int num_splits, int out_dtype, float out_inv_scale,
+                                      void* out, float* lse_out, float* amax_out, void* stream);
+
 /* Text for a status code. */
 MLA_API const char* mla_status_string(int status);
 

@@ -28,7 +28,7 @@ EXPORTS = [
     "mla_decode_plan", "mla_sparse_decode_split", "mla_split_combine", "mla_sparse_decode_direct",
     "mla_sparse_decode", "sdpa_fp8_decode_plan", "sdpa_fp8_decode_split", "sdpa_split_combine",
     "sdpa_fp8_decode_direct", "sdpa_fp8_decode", "mla_get_status", "mla_selftest_wait_timeout",
-    "mla_status_string", "mla_abi_version",
+    "mla_status_string", "mla_abi_version", "mla_sparse_decode_noalloc",
 ]
 
 
@@ -80,6 +80,7 @@ _SIGS = {
     "mla_selftest_wait_timeout": [_U64, _P],
     "mla_status_string": [_I],
     "mla_abi_version": [],
+    "mla_sparse_decode_noalloc": [_I, _I, _P, _P, _I64, _P, _F, _P, _I, _I, _F, _P, _P, _P, _P],
 }
 
 
@@ -211,6 +212,15 @@ def sdpa_fp8_decode(plan: SdpaPlan, total_q: int, total_kv: int, q, k, v, cu_seq
                                  _dtype(out_dtype), out_inv_scale, _ptr(out), _ptr(lse_out), _ptr(amax_out),
                                  _ptr(workspace), _stream(stream)),
            "sdpa_fp8_decode")
+
+
+def mla_sparse_decode_noalloc(s_q: int, topk: int, q, kv, n_kv: int, idx, sm_scale: float, sink, num_splits: int,
+                              out_dtype, out_inv_scale: float, out, lse_out=None, amax_out=None, stream=None):
+    """Decode step whose split workspace is the library's own scratch array (no allocation)."""
+    _check(lib().mla_sparse_decode_noalloc(s_q, topk, _ptr(q), _ptr(kv), n_kv, _ptr(idx), sm_scale, _ptr(sink),
+                                           num_splits, _dtype(out_dtype), out_inv_scale, _ptr(out), _ptr(lse_out),
+                                           _ptr(amax_out), _stream(stream)),
+           "mla_sparse_decode_noalloc")
 
 
 # ------------------------------------------------------------------- status --

@@ -575,3 +575,62 @@ int mla_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------- no-allocation entry --
+//
+// A decode call for callers that cannot allocate device memory: the partial
+// workspace of the split pass lives in this file-scope array instead of a
+// caller buffer. The array is part of the library's device image, so every GPU
+// that loads the library holds MLA_NOALLOC_SCRATCH_BYTES of it until the
+// process exits.
+namespace {
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MLA_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};   // device address of g_noalloc_scratch, per device
+
+// Resolves the array's device address for the current device (once per device,
+// with that device current). In host code the symbol itself is only a stand-in,
+// never a device address, so it must not be handed to a kernel.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return MLA_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return MLA_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_sparse_decode_noalloc(int s_q, int topk, const void* q, const void* kv, int64_t n_kv, const int32_t* idx,
+                              float sm_scale, const float* sink, int num_splits, int out_dtype, float out_inv_scale,
+                              void* out, float* lse_out, float* amax_out, void* stream) {
+  if (num_splits < 0 || num_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID_ARG;
+  mla_plan_t plan;
+  int st = mla_decode_plan(s_q, kMlaHeads, kMlaDqk, kMlaDv, topk, 0, 0, num_splits, &plan);
+  if (st != MLA_OK) return st;
+  if (plan.workspace_bytes > MLA_NOALLOC_SCRATCH_BYTES) return MLA_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if (plan.workspace_bytes > 0 && (st = noalloc_scratch(&scratch)) != MLA_OK) return st;
+  // Same split + combine (or direct) launches as mla_sparse_decode; the split
+  // pass writes every partial slot it owns before the combine reads it, so
+  // nothing in the scratch array needs to start at zero.
+  return mla_sparse_decode(&plan, s_q, q, kv, n_kv, idx, sm_scale, sink, out_dtype, out_inv_scale, out, lse_out,
+                           amax_out, scratch, stream);
+}
+
+}  // extern "C"
