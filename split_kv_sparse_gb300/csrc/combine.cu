@@ -3,10 +3,11 @@
 // attention sink and the final cast; cuDNN-frontend PR #768: it also owns the
 // amax of the recombined output).
 //
-// One warp per output row (token, head): the lanes read the row's split LSEs,
-// take M = max_s LSE_s and w_s = 2^(LSE_s - M), then stream the d-wide fp32
-// partials of the splits with w_s > 0 (empty splits are never read) as float4
-// loads, four splits in flight at a time.
+// One warp per (output row, 128-wide column slice), so even one decode token
+// (64 rows x 4 slices of the 512-wide O) spreads over 32 CTAs: the lanes read
+// the row's split LSEs, take M = max_s LSE_s and w_s = 2^(LSE_s - M), then
+// stream their slice of the fp32 partials of the splits with w_s > 0 (empty
+// splits are never read) as float4 loads, four splits in flight at a time.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -32,10 +33,13 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 template <int D>
 __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const CombineArgs a) {
-  constexpr int V = D / 128;   // float4 per lane
+  constexpr int kSlices = D / 128;   // 128 floats = one float4 per lane
+  constexpr int V = 1;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kWarps + warp;
+  const int item = blockIdx.x * kWarps + warp;
+  const int row = item / kSlices;
+  const int slice = item - row * kSlices;
   grid_dependency_wait();      // the split pass has finished writing the partials
   if (row >= a.rows) return;   // whole warp leaves together
   const int S = a.num_splits;
@@ -62,7 +66,8 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const CombineArgs 
         const int s = s0 + u;
         const float w = (s < S) ? __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31) : 0.f;
         ws[u] = w;
-        const float4* src = reinterpret_cast<const float4*>(a.o_acc + (static_cast<size_t>(s) * rows + row) * D);
+        const float4* src =
+            reinterpret_cast<const float4*>(a.o_acc + (static_cast<size_t>(s) * rows + row) * D + slice * 128);
 #pragma unroll
         for (int v = 0; v < V; ++v)
           x[u][v] = (w != 0.f) ? __ldcs(src + lane + 32 * v) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -94,7 +99,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const CombineArgs 
     amax_l = fmaxf(amax_l, fmaxf(fmaxf(fabsf(acc[v].x), fabsf(acc[v].y)),
                                  fmaxf(fabsf(acc[v].z), fabsf(acc[v].w))));
   }
-  const size_t base = static_cast<size_t>(row) * D;
+  const size_t base = static_cast<size_t>(row) * D + slice * 128;
 #pragma unroll
   for (int v = 0; v < V; ++v) {
     const int e = 4 * (lane + 32 * v);
@@ -115,7 +120,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const CombineArgs 
       *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.out) + base + e) = (c01 & 0xFFFFu) | (c23 << 16);
     }
   }
-  if (lane == 0 && a.lse_out != nullptr) a.lse_out[row] = empty ? -INFINITY : M + log2f(wsum);
+  if (slice == 0 && lane == 0 && a.lse_out != nullptr) a.lse_out[row] = empty ? -INFINITY : M + log2f(wsum);
   if (a.amax != nullptr) {
     amax_l = warp_max(amax_l);
     if (lane == 0) atomicMax(reinterpret_cast<int*>(a.amax), __float_as_int(amax_l));
@@ -130,7 +135,8 @@ cudaError_t launch_combine(const CombineArgs& a, bool zero_amax, bool pdl, cudaS
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.rows + kWarps - 1) / kWarps);
+  const int items = a.rows * (a.d / 128);
+  cfg.gridDim = dim3((items + kWarps - 1) / kWarps);
   cfg.blockDim = dim3(kWarps * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

@@ -19,7 +19,6 @@
 //   warp 3     tcgen05 issue (one thread):
 //                S^T[128 window rows x 64 heads] = K_window . Q^T  (M=128, N=64, K=576)
 //                O^T[512 x 64] += V_half^T . (P_hi + P_lo)^T       (8 x (M=128, N=64, K=64))
-//                L[. x 64]     += 1 . (P_hi + P_lo)^T              (row sums, 2 x (M=128, N=64, K=64))
 //              V is read straight out of the gathered rows as an MN-major
 //              operand; K and Q are K-major; all tiles use the 128-byte swizzle.
 //              QK of the next step is issued as soon as its rows have landed,
@@ -32,10 +31,9 @@
 //
 // Precision: p = 2^(x - m_ref) is stored as P_hi = bf16(p) and
 // P_lo = bf16(p - P_hi); the PV product uses both, so P enters O with ~2^-16
-// relative error instead of the 2^-8 of a single bf16. O is normalised by the
-// sum of the same P_hi + P_lo (formed by the tensor core against a 128-byte
-// all-ones operand read at zero stride); the fp32 sum of p that gives the LSE
-// stays in per-thread partials, reduced once at the end.
+// relative error instead of the 2^-8 of a single bf16. The fp32 sum of p (the
+// softmax denominator, and the LSE) stays in per-thread partials, reduced once
+// at the end; it matches the P the product used to the same ~2^-16.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -67,10 +65,8 @@ constexpr int kOffMisc = kOffBars + 128;            // [0] tmem base, [1] abort 
 constexpr int kOffMuse = kOffMisc + 128;            // float[64] reference max per head (log2 units)
 constexpr int kOffAlpha = kOffMuse + 256;           // float[64] rescale factors; 1/denominator at the end
 constexpr int kOffTmax = kOffAlpha + 256;           // float[4][64] tile maxima; row sums at the end
-constexpr int kOffOnes = kOffTmax + 1024;           // 8 x 8 bf16 ones: the A operand of the row-sum MMA
-constexpr int kOffRsum = kOffOnes + 128;            // float[64] sums of P_hi + P_lo
-constexpr int kOffIdx = kOffRsum + 256;             // int[2][64] row indices of the step, per half
-constexpr int kSmemBytes = kOffIdx + 512;           // 232064
+constexpr int kOffIdx = kOffTmax + 1024;            // int[2][64] row indices of the step, per half
+constexpr int kSmemBytes = kOffIdx + 512;           // 231680
 
 enum {
   B_QFULL = 0, B_FULL0, B_FULL1, B_EMPTY0, B_EMPTY1, B_SFULL0, B_SFULL1,
@@ -80,7 +76,6 @@ static_assert(kNumBars * 8 <= 128, "barrier area");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 256;                    // S^T buffers at columns 256 and 320
-constexpr uint32_t kTmemL = 384;                    // row sums of P (every lane the same)
 constexpr float kRescaleThreshold = 8.0f;           // p = 2^(x - m_ref) <= 256 between rescales
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -136,7 +131,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* inv_s = alpha;                                               // epilogue reuse
   float* tmax = reinterpret_cast<float*>(smem + kOffTmax);
   float* lred = tmax;                                                 // epilogue reuse
-  float* rsum_s = reinterpret_cast<float*>(smem + kOffRsum);
   const WaitCtx wc{a.wait_limit_ns, a.status, abort_flag};
 
   if (threadIdx.x == 0) {
@@ -155,12 +149,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init_fence();
   }
   if (threadIdx.x >= 128 && threadIdx.x < 192) m_use[threadIdx.x - 128] = -INFINITY;
-  if (threadIdx.x < 8) {
-    // bf16 1.0 = 0x3F80; read by the tensor core (async proxy) after the fence
-    reinterpret_cast<uint4*>(smem + kOffOnes)[threadIdx.x] =
-        make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-    fence_proxy_async_smem();
-  }
   if (warp == 3) {
     tmem_alloc(smem_u32(misc), kTmemCols);
     tmem_relinquish();
@@ -227,7 +215,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdescPV = idesc_make(128, 64, 1, true, false);    // A MN-major (V^T)
       const uint32_t ring = sbase + kOffRing;
       const uint32_t qs = sbase + kOffQ;
-      const uint64_t ones_desc = sdesc_noswizzle(sbase + kOffOnes, 0, 0);   // one 8x8 core matrix, zero strides
       auto issue_qk = [&](int k) {
         const uint32_t d = tmem + kTmemS + 64 * (k & 1);
 #pragma unroll
@@ -252,10 +239,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_f16(tmem + 64 * j,
                       sdesc_sw128(ring + 2 * j * kSlotBytes + h * kHalfBytes + kk * 2048, kSlotBytes, 1024),
                       sdesc_sw128(pt + kk * 32, 16, 1024), kIdescPV, (k > 0 || part > 0 || kk > 0));
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f16(tmem + kTmemL, ones_desc, sdesc_sw128(pt + kk * 32, 16, 1024), kIdescKK,
-                    (k > 0 || part > 0 || kk > 0));
         }
       };
       bool ok = wait_bounded(bar(B_QFULL), 0, wc, W_MMA_Q);
@@ -393,12 +376,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 64; ++i) lpart[i] *= alpha[i];
         if (k >= 1 && !bad) {
-          // O^T and the row sums hold PV of steps < k: scale every head column
+          // O^T holds PV of steps < k: scale every head column
 #pragma unroll 1
-          for (int j = 0; j < 10; ++j) {   // 4 O^T chunks + the row sums, 2 x 32 head columns each
+          for (int j = 0; j < 8; ++j) {   // 4 O^T chunks x 2 halves of 32 head columns
             uint32_t o[32];
             const int c0 = 32 * (j & 1);
-            const uint32_t col = (j < 8 ? 64 * (j >> 1) : kTmemL) + c0;
+            const uint32_t col = 64 * (j >> 1) + c0;
             tmem_ld_32x32b_x32(tmem + lane_base + col, o);
             tmem_wait_ld_x32(o);
 #pragma unroll
@@ -444,30 +427,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) flags[8 + wi] = bad;
     named_bar_sync(1, 128);
     const bool any_bad = flags[8] | flags[9] | flags[10] | flags[11];
-    int wp = 0;
-    if (!any_bad) {
-      if (lane == 0) wp = wait_bounded(bar(B_PVDONE), (nsteps - 1) & 1, wc, W_SM_PV_EPI);
-      wp = __shfl_sync(0xffffffffu, wp, 0);
-      tc_fence_after();
-      if (wp && wi == 0) {
-        // every TMEM lane of the row-sum block holds the same 64 sums; lane c%32 keeps column c
-        uint32_t r[64];
-        tmem_ld_32x32b_x64(tmem + lane_base + kTmemL, r);
-        tmem_wait_ld_x64(r);
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if ((c & 31) == lane) rsum_s[c] = __uint_as_float(r[c]);
-      }
-    }
-    named_bar_sync(1, 128);
     if (tid < 64) {
       const float l = (lred[tid] + lred[64 + tid]) + (lred[128 + tid] + lred[192 + tid]);
-      const float lr = rsum_s[tid];
       const float mu = m_use[tid];
       float lse = -INFINITY, inv = 0.f;
       if (l > 0.f) {
         lse = mu + log2f(l);
-        float den = lr;
+        float den = l;
         if (kDirect && a.sink != nullptr) den += exp2f(a.sink[tid] * kLog2e - mu);
         inv = 1.f / den;
       }
@@ -479,6 +445,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     named_bar_sync(1, 128);
+    int wp = 0;
+    if (!any_bad) {
+      if (lane == 0) wp = wait_bounded(bar(B_PVDONE), (nsteps - 1) & 1, wc, W_SM_PV_EPI);
+      wp = __shfl_sync(0xffffffffu, wp, 0);
+      tc_fence_after();
+    }
     if (!any_bad && wp) {
       float amax_l = 0.f;
 #pragma unroll 1
