@@ -29,11 +29,11 @@
 // both halves and keeps the 64 new rows, which lets every MMA use the M=128
 // data path with one TMEM lane per row.
 //
-// Precision: p = 2^(x - m_ref) is stored as P_hi = bf16(p) and
-// P_lo = bf16(p - P_hi); the PV product uses both, so P enters O with ~2^-16
+// Precision: p = 2^(x - m_ref) is stored as P_hi = p truncated to bf16 and
+// P_lo = bf16(p - P_hi); the PV product uses both, so P enters O with ~2^-15
 // relative error instead of the 2^-8 of a single bf16. The fp32 sum of p (the
 // softmax denominator, and the LSE) stays in per-thread partials, reduced once
-// at the end; it matches the P the product used to the same ~2^-16.
+// at the end; it matches the P the product used to the same ~2^-15.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -133,6 +133,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* lred = tmax;                                                 // epilogue reuse
   const WaitCtx wc{a.wait_limit_ns, a.status, abort_flag};
 
+  // The loaders' first row indices: fetched before the set-up barrier so the
+  // global-memory latency overlaps TMEM allocation and barrier initialisation.
+  int first_idx = -1;
+  if (threadIdx.x < kMlaBlockRows && row0 + static_cast<int>(threadIdx.x) < row1) {
+    first_idx = __ldg(a.idx + static_cast<size_t>(t) * a.topk + row0 + threadIdx.x);
+    if (first_idx < 0 || first_idx >= a.n_kv) first_idx = -1;
+  }
+
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
     mbar_init(bar(B_FULL0), kProducers);   // one cp.async completion arrival per producer thread
@@ -184,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return v;
     };
-    int cur = fetch(0);
+    int cur = first_idx;
 #pragma unroll 1
     for (int k = 0; k < nsteps; ++k) {
       const int h = k & 1;
@@ -194,12 +202,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(2, kProducers);     // the half is free and its row indices are visible
       if (!go[h]) break;                 // every loader sees the same flag
       const uint32_t half_base = sbase + kOffRing + h * kHalfBytes;
-#pragma unroll 8
+      // all index reads first: a read after a cp.async (which writes shared
+      // memory) would have to wait for it
+      int ixr[kPiecesPerThread];
+#pragma unroll
+      for (int i = 0; i < kPiecesPerThread; ++i) ixr[i] = idx_s[h * kMlaBlockRows + (ptid + kProducers * i) / kPiecesPerRow];
+#pragma unroll
       for (int i = 0; i < kPiecesPerThread; ++i) {
         const int u = ptid + kProducers * i;
         const int row = u / kPiecesPerRow;
         const int seg = u - row * kPiecesPerRow;
-        const int ix = idx_s[h * kMlaBlockRows + row];
+        const int ix = ixr[i];
         const uint32_t dst = half_base + (seg >> 3) * kSlotBytes + row * 128 + (((seg & 7) ^ (row & 7)) << 4);
         const uint8_t* src = a.kv + static_cast<size_t>(ix < 0 ? 0 : ix) * (kMlaDqk * 2) + seg * 16;
         cp_async_16(dst, src, ix < 0 ? 0u : 16u);
@@ -215,15 +228,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdescPV = idesc_make(128, 64, 1, true, false);    // A MN-major (V^T)
       const uint32_t ring = sbase + kOffRing;
       const uint32_t qs = sbase + kOffQ;
-      auto issue_qk = [&](int k) {
+      // one 64-dim column chunk of QK(k): 4 MMAs
+      auto issue_qk_chunk = [&](int k, int c) {
         const uint32_t d = tmem + kTmemS + 64 * (k & 1);
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f16(d, sdesc_sw128(ring + c * kSlotBytes + kk * 32, 16, 1024),
-                    sdesc_sw128(qs + c * kQChunkBytes + kk * 32, 16, 1024), kIdescKK,
-                    (c | kk) != 0);
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f16(d, sdesc_sw128(ring + c * kSlotBytes + kk * 32, 16, 1024),
+                  sdesc_sw128(qs + c * kQChunkBytes + kk * 32, 16, 1024), kIdescKK, (c | kk) != 0);
       };
       auto issue_pv = [&](int k) {
         const int h = k & 1;
@@ -242,29 +253,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       bool ok = wait_bounded(bar(B_QFULL), 0, wc, W_MMA_Q);
-      // Issue QK(k) as soon as its rows have landed and its S^T buffer is free
-      // (softmax(k-2) is done, i.e. PV(k-2) was issued), and PV(k) as soon as
-      // softmax(k) has written P. One thread; tcgen05 runs them in issue order.
-      int nqk = 0, npv = 0;
+      // PV(k) is issued as soon as softmax(k) has written P: its completion
+      // frees the half for the loads of step k+2, the loop's critical chain.
+      // QK(k) is issued once its rows have landed and its S^T buffer is free
+      // (softmax(k-2) is done, i.e. PV(k-2) was issued), one 64-dim chunk at a
+      // time so a ready PV never waits behind a whole QK (the issuing thread
+      // stalls on the tensor pipe's queue). tcgen05 runs them in issue order.
+      int nqk = 0, qk_c = 0, npv = 0;
       uint64_t t_idle = 0;
       while (ok && npv < nsteps) {
         bool progress = false;
-        if (nqk < nsteps && nqk <= npv + 1 && mbar_try_wait(bar(B_FULL0 + (nqk & 1)), (nqk >> 1) & 1)) {
-          // the rows were written by other threads' cp.async (generic proxy); make
-          // them visible to the tensor core's reads (async proxy)
-          fence_proxy_async_smem();
-          tc_fence_after();
-          issue_qk(nqk);
-          mma_commit(bar(B_SFULL0 + (nqk & 1)));
-          ++nqk;
-          progress = true;
-        }
         if (npv < nqk && mbar_try_wait(bar(B_PFULL0 + (npv & 1)), (npv >> 1) & 1)) {
           tc_fence_after();
           issue_pv(npv);
           mma_commit(bar(B_EMPTY0 + (npv & 1)));
           mma_commit(bar(B_PVDONE));
           ++npv;
+          progress = true;
+        } else if (nqk < nsteps && nqk <= npv + 1 &&
+                   (qk_c > 0 || mbar_try_wait(bar(B_FULL0 + (nqk & 1)), (nqk >> 1) & 1))) {
+          if (qk_c == 0) {
+            // the rows were written by other threads' cp.async (generic proxy);
+            // make them visible to the tensor core's reads (async proxy)
+            fence_proxy_async_smem();
+            tc_fence_after();
+          }
+          issue_qk_chunk(nqk, qk_c);
+          if (++qk_c == kChunks) {
+            mma_commit(bar(B_SFULL0 + (nqk & 1)));
+            ++nqk;
+            qk_c = 0;
+          }
           progress = true;
         }
         if (progress) {
@@ -380,12 +399,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
           for (int j = 0; j < 8; ++j) {   // 4 O^T chunks x 2 halves of 32 head columns
             uint32_t o[32];
+            float al[32];
             const int c0 = 32 * (j & 1);
             const uint32_t col = 64 * (j >> 1) + c0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) al[i] = alpha[c0 + i];
             tmem_ld_32x32b_x32(tmem + lane_base + col, o);
             tmem_wait_ld_x32(o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha[c0 + i]);
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * al[i]);
             tmem_st_32x32b_x32(tmem + lane_base + col, o);
           }
           tmem_wait_st();
@@ -400,15 +422,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* pt_lo = smem + kOffPlo;
         const int rchunk = rloc >> 3;
         const int rbyte = (rloc & 7) * 2;
+        // every read of m_use happens before the first store below, so the
+        // compiler need not reload it after each (possibly aliasing) store
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
-          const float p = (x[i] == -INFINITY) ? 0.f : ex2_approx(x[i] - m_use[i]);
-          lpart[i] += p;
-          const __nv_bfloat16 hi = __float2bfloat16_rn(p);
-          const __nv_bfloat16 lo = __float2bfloat16_rn(p - __bfloat162float(hi));
-          const int off = (i >> 3) * 1024 + (i & 7) * 128 + ((rchunk ^ (i & 7)) << 4) + rbyte;
-          *reinterpret_cast<__nv_bfloat16*>(pt_hi + off) = hi;
-          *reinterpret_cast<__nv_bfloat16*>(pt_lo + off) = lo;
+          x[i] = (x[i] == -INFINITY) ? 0.f : ex2_approx(x[i] - m_use[i]);
+          lpart[i] += x[i];
+        }
+        // P_hi = p with its mantissa cut to bf16 (exact bit truncation, no
+        // conversion); P_lo = bf16(p - P_hi), two heads per packed conversion.
+        // |P_lo| < 2^-7 p, so P_hi + P_lo matches p to 2^-15.
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+          const uint32_t b0 = __float_as_uint(x[i]) & 0xFFFF0000u;
+          const uint32_t b1 = __float_as_uint(x[i + 1]) & 0xFFFF0000u;
+          const __nv_bfloat162 lo2 =
+              __floats2bfloat162_rn(x[i] - __uint_as_float(b0), x[i + 1] - __uint_as_float(b1));
+          const uint32_t lo = *reinterpret_cast<const uint32_t*>(&lo2);
+          const int off0 = (i >> 3) * 1024 + (i & 7) * 128 + ((rchunk ^ (i & 7)) << 4) + rbyte;
+          const int off1 = ((i + 1) >> 3) * 1024 + ((i + 1) & 7) * 128 + ((rchunk ^ ((i + 1) & 7)) << 4) + rbyte;
+          *reinterpret_cast<uint16_t*>(pt_hi + off0) = static_cast<uint16_t>(b0 >> 16);
+          *reinterpret_cast<uint16_t*>(pt_hi + off1) = static_cast<uint16_t>(b1 >> 16);
+          *reinterpret_cast<uint16_t*>(pt_lo + off0) = static_cast<uint16_t>(lo & 0xFFFFu);
+          *reinterpret_cast<uint16_t*>(pt_lo + off1) = static_cast<uint16_t>(lo >> 16);
         }
         fence_proxy_async_smem();
       }
@@ -452,43 +488,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
     }
     if (!any_bad && wp) {
+      // Stage the [64 heads][512] output tile in the ring (free now: every load
+      // has landed and every MMA has completed), then copy it to global memory
+      // with one bulk copy; a job's output rows are contiguous there.
       float amax_l = 0.f;
+      float inv[64];   // in registers: no shared-memory reload between the stores
+#pragma unroll
+      for (int c = 0; c < 64; ++c) inv[c] = inv_s[c];
+      const int esize = (!kDirect || a.out_dtype == 0) ? 4 : (a.out_dtype == 1 ? 2 : 1);
+      uint8_t* stage = smem + kOffRing;
 #pragma unroll 1
       for (int j = 0; j < 4; ++j) {
         uint32_t o[64];
         tmem_ld_32x32b_x64(tmem + lane_base + 64 * j, o);
         tmem_wait_ld_x64(o);
         const int d = 128 * j + 32 * sp + lane;
-        if (!kDirect) {
-          float* dst = a.o_acc + out_row * kMlaDv + d;
-#pragma unroll
-          for (int c = 0; c < 64; ++c) dst[c * kMlaDv] = __uint_as_float(o[c]) * inv_s[c];
-        } else if (a.out_dtype == 0) {
-          float* dst = static_cast<float*>(a.out) + out_row * kMlaDv + d;
+        if (esize == 4) {
+          float* st = reinterpret_cast<float*>(stage) + d;
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
-            const float v = __uint_as_float(o[c]) * inv_s[c];
+            const float v = __uint_as_float(o[c]) * inv[c];
             amax_l = fmaxf(amax_l, fabsf(v));
-            dst[c * kMlaDv] = v;
+            st[c * kMlaDv] = v;
           }
-        } else if (a.out_dtype == 1) {
-          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + out_row * kMlaDv + d;
+        } else if (esize == 2) {
+          __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stage) + d;
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
-            const float v = __uint_as_float(o[c]) * inv_s[c];
+            const float v = __uint_as_float(o[c]) * inv[c];
             amax_l = fmaxf(amax_l, fabsf(v));
-            dst[c * kMlaDv] = __float2bfloat16_rn(v);
+            st[c * kMlaDv] = __float2bfloat16_rn(v);
           }
         } else {
-          uint8_t* dst = static_cast<uint8_t*>(a.out) + out_row * kMlaDv + d;
+          uint8_t* st = stage + d;
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
-            const float v = __uint_as_float(o[c]) * inv_s[c];
+            const float v = __uint_as_float(o[c]) * inv[c];
             amax_l = fmaxf(amax_l, fabsf(v));
-            dst[c * kMlaDv] = static_cast<uint8_t>(
-                __nv_cvt_float_to_fp8(v * a.inv_scale, __NV_SATFINITE, __NV_E4M3));
+            st[c * kMlaDv] =
+                static_cast<uint8_t>(__nv_cvt_float_to_fp8(v * a.inv_scale, __NV_SATFINITE, __NV_E4M3));
           }
         }
+      }
+      fence_proxy_async_smem();          // the bulk copy reads the tile through the async proxy
+      named_bar_sync(1, 128);
+      if (tid == 0) {
+        uint8_t* gdst = kDirect ? static_cast<uint8_t*>(a.out) + out_row * kMlaDv * esize
+                                : reinterpret_cast<uint8_t*>(a.o_acc + out_row * kMlaDv);
+        bulk_store(gdst, sbase + kOffRing, kMlaHeads * kMlaDv * esize);
+        bulk_commit_and_wait_all();
       }
       if (kDirect && a.amax != nullptr) {
 #pragma unroll

@@ -132,6 +132,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, int x
       : "memory");
 }
 
+// Bulk shared -> global copy (async proxy), bytes a multiple of 16, both addresses
+// 16-byte aligned; tracked by the issuing thread's bulk groups.
+__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_and_wait_all() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- cp.async --
 
 // 16-byte global -> shared copy through L2 (L1 bypassed); src_bytes = 0 writes

@@ -5,7 +5,7 @@
 // into split-major slots (or, unsplit, a direct bf16/fp32/e4m3 epilogue that
 // also computes the amax).
 //
-// One CTA per job (sequence b, KV head g, split s), 320 threads:
+// One CTA per job (sequence b, KV head g, split s), 256 threads:
 //   warp 0     TMA: the job's Q rows once (the group's h_q/h_kv heads of up to
 //              64/group tokens = 64 rows x 128 B), then per tile K and V
 //              (128 keys x 128 B each, e4m3) into a 3-stage ring.
@@ -13,7 +13,7 @@
 //                              O^T[128 d x 64 rows] += V^T . P^T   (kind::f16, f16 operands)
 //   warps 2-5  softmax over keys (TMEM lane = key), lazy rescale of O^T,
 //              P^T in f16, then the epilogue.
-//   warps 6-9  convert each V tile from e4m3 to f16 (exact) into the
+//   warps 6-7  convert each V tile from e4m3 to f16 (exact) into the
 //              MN-major 128-byte-swizzled layout the PV MMA reads.
 // The QK product of e4m3 codes is exact in fp32; descales multiply the scores
 // (dq*dk*sm_scale) and the output (dv).
@@ -28,7 +28,7 @@
 namespace skv {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 256;
 constexpr int kD = 128;
 constexpr int kTile = 128;                 // keys per tile (split unit)
 constexpr int kRows = 64;                  // query rows per job (tokens x group heads)
@@ -147,12 +147,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_QFULL), 1);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar(B_SFULL_STAGE0 + i), 1);
-      mbar_init(bar(B_SEMPTY0 + i), 5);            // QK commit + 4 converter warps
+      mbar_init(bar(B_SEMPTY0 + i), 3);            // QK commit + 2 converter warps
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_SREADY0 + i), 1);
       mbar_init(bar(B_PFULL0 + i), 4);
-      mbar_init(bar(B_V16FULL0 + i), 4);
+      mbar_init(bar(B_V16FULL0 + i), 2);
       mbar_init(bar(B_V16EMPTY0 + i), 1);
     }
     mbar_init(bar(B_FINAL), 1);
@@ -264,8 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 6) {
     // ==================================================== V e4m3 -> f16 ===
-    const int key = threadIdx.x - 192;      // 0..127: one key row per thread
-    const int r8 = key & 7;
+    const int ct = threadIdx.x - 192;       // 0..63: key rows ct and ct + 64 of each tile
 #pragma unroll 1
     for (int t = 0; t < nt; ++t) {
       const int st = t % kStages;
@@ -276,25 +275,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       w = __shfl_sync(0xffffffffu, w, 0);
       if (!w) break;   // the abort flag is set; the other roles stop on their own waits
-      const uint8_t* vrow = smem + kOffStage + st * kStageBytes + kKVTileBytes + (key >> 3) * 1024 + r8 * 128;
-      uint8_t* v16 = smem + kOffV16 + (t & 1) * kV16Bytes + (key >> 3) * 1024 + r8 * 128;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {              // 16 e4m3 values (d = 16c .. 16c+15) per chunk
-        const uint4 raw = *reinterpret_cast<const uint4*>(vrow + ((c ^ r8) << 4));
-        const uint32_t wds[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t h[8];
+      for (int rr = 0; rr < 2; ++rr) {
+        const int key = ct + 64 * rr;
+        const int r8 = key & 7;
+        const uint8_t* vrow = smem + kOffStage + st * kStageBytes + kKVTileBytes + (key >> 3) * 1024 + r8 * 128;
+        uint8_t* v16 = smem + kOffV16 + (t & 1) * kV16Bytes + (key >> 3) * 1024 + r8 * 128;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wds[j] & 0xFFFFu), __NV_E4M3);
-          const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wds[j] >> 16), __NV_E4M3);
-          h[2 * j] = static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16);
-          h[2 * j + 1] = static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16);
+        for (int c = 0; c < 8; ++c) {            // 16 e4m3 values (d = 16c .. 16c+15) per chunk
+          const uint4 raw = *reinterpret_cast<const uint4*>(vrow + ((c ^ r8) << 4));
+          const uint32_t wds[4] = {raw.x, raw.y, raw.z, raw.w};
+          uint32_t h[8];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wds[j] & 0xFFFFu), __NV_E4M3);
+            const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wds[j] >> 16), __NV_E4M3);
+            h[2 * j] = static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16);
+            h[2 * j + 1] = static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16);
+          }
+          // d = 16c .. 16c+7 -> MN atom (16c)/64, 16-B chunk ((16c)%64)/8; then +8
+          const int d0 = 16 * c;
+          const int a0 = d0 >> 6, c0 = (d0 & 63) >> 3;
+          *reinterpret_cast<uint4*>(v16 + a0 * 16384 + ((c0 ^ r8) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+          *reinterpret_cast<uint4*>(v16 + a0 * 16384 + (((c0 + 1) ^ r8) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
         }
-        // d = 16c .. 16c+7 -> MN atom (16c)/64, 16-B chunk ((16c)%64)/8; then +8
-        const int d0 = 16 * c;
-        const int a0 = d0 >> 6, c0 = (d0 & 63) >> 3;
-        *reinterpret_cast<uint4*>(v16 + a0 * 16384 + ((c0 ^ r8) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(v16 + a0 * 16384 + (((c0 + 1) ^ r8) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -310,7 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x - 64;
     const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
     const float sc = dq * dk * a.scale_log2;
-    float lsum0 = 0.f, lsum1 = 0.f, rsum0 = 0.f, rsum1 = 0.f;
+    // fp32 softmax denominators per row over the keys this thread has held;
+    // reduced over threads once, in the epilogue (P in f16 matches p to 2^-12)
+    float lpart[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) lpart[i] = 0.f;
     int bad = 0;
 #pragma unroll 1
     for (int t = 0; t < nt; ++t) {
@@ -357,10 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_new[tid] = mn;
         }
         named_bar_sync(1, 128);
-        lsum0 *= alpha[2 * lane];
-        lsum1 *= alpha[2 * lane + 1];
-        rsum0 *= alpha[2 * lane];
-        rsum1 *= alpha[2 * lane + 1];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) lpart[i] *= alpha[i];
         if (t >= 1) {
           // S^T(t) ready implies every earlier PV has completed: O^T is final up to tile t-1
 #pragma unroll 1
@@ -381,44 +387,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* pt = smem + kOffP + (t & 1) * kPBytes;
       const int key = 32 * sp + lane;
       const int kb = key >> 6, kc = (key & 63) >> 3, kbyte = (key & 7) * 2;
-      float pr[64];
+      // all reads of m_use before the first store (stores could alias it)
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        const float p = (x[i] == -INFINITY) ? 0.f : ex2_approx(x[i] - m_use[i]);
-        x[i] = p;
-        const __half ph = __float2half_rn(p);
-        pr[i] = __half2float(ph);
-        const int off = kb * 8192 + (i >> 3) * 1024 + (i & 7) * 128 + ((kc ^ (i & 7)) << 4) + kbyte;
-        *reinterpret_cast<__half*>(pt + off) = ph;
+        x[i] = (x[i] == -INFINITY) ? 0.f : ex2_approx(x[i] - m_use[i]);
+        lpart[i] += x[i];
+      }
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) {
+        const __half2 ph = __floats2half2_rn(x[i], x[i + 1]);
+        const int off0 = kb * 8192 + (i >> 3) * 1024 + (i & 7) * 128 + ((kc ^ (i & 7)) << 4) + kbyte;
+        const int off1 = kb * 8192 + ((i + 1) >> 3) * 1024 + ((i + 1) & 7) * 128 + ((kc ^ ((i + 1) & 7)) << 4) + kbyte;
+        *reinterpret_cast<__half*>(pt + off0) = __low2half(ph);
+        *reinterpret_cast<__half*>(pt + off1) = __high2half(ph);
       }
       fence_proxy_async_smem();
-      float s0, s1;
-      warp_transpose_reduce<false>(x, lane, s0, s1);
-      lsum0 += s0;
-      lsum1 += s1;
-      warp_transpose_reduce<false>(pr, lane, s0, s1);
-      rsum0 += s0;
-      rsum1 += s1;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PFULL0 + (t & 1)));
     }
 
     // ---- epilogue ---------------------------------------------------------
-    lred[wi * 64 + 2 * lane] = lsum0;
-    lred[wi * 64 + 2 * lane + 1] = lsum1;
-    tmax[wi * 64 + 2 * lane] = rsum0;
-    tmax[wi * 64 + 2 * lane + 1] = rsum1;
+    {
+      float ls0, ls1;
+      warp_transpose_reduce<false>(lpart, lane, ls0, ls1);
+      lred[wi * 64 + 2 * lane] = ls0;
+      lred[wi * 64 + 2 * lane + 1] = ls1;
+    }
     if (lane == 0) flags[8 + wi] = bad;
     named_bar_sync(1, 128);
     const bool any_bad = flags[8] | flags[9] | flags[10] | flags[11];
     if (tid < 64) {
       const float l = (lred[tid] + lred[64 + tid]) + (lred[128 + tid] + lred[192 + tid]);
-      const float lr = (tmax[tid] + tmax[64 + tid]) + (tmax[128 + tid] + tmax[192 + tid]);
       float lse = -INFINITY, inv = 0.f;
       if (l > 0.f) {
         lse = m_use[tid] + log2f(l);
-        inv = dv / lr;
+        inv = dv / l;
       }
       inv_s[tid] = inv;
       if (tid < R) {
@@ -441,10 +445,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld_x64(o);
         const int d = 32 * sp + lane;
         float amax_l = 0.f;
+        float inv[kRows];   // in registers: no shared-memory reload between the global stores
+#pragma unroll
+        for (int rho = 0; rho < kRows; ++rho) inv[rho] = inv_s[rho];
 #pragma unroll
         for (int rho = 0; rho < kRows; ++rho) {
           if (rho >= R) continue;
-          const float v = __uint_as_float(o[rho]) * inv_s[rho];
+          const float v = __uint_as_float(o[rho]) * inv[rho];
           const size_t oi = out_index(rho) * kD + d;
           if (!direct) {
             a.o_acc[oi] = v;
