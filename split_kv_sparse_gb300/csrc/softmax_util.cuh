@@ -1,6 +1,7 @@
 // Device helpers shared by the decode kernels: the approximate exp2 used for
 // softmax numerators, a drain wait for in-flight copies, and the transposed
-// warp butterfly that reduces 64 per-lane values over the 32 lanes of a warp.
+// warp butterflies that reduce per-lane head vectors over the lanes of a warp
+// (64 heads over 32 lanes) or of a half-warp (32 heads over 16 lanes).
 #pragma once
 
 #include "ptx.cuh"
@@ -45,6 +46,55 @@ __device__ __forceinline__ void warp_transpose_reduce(const float (&x)[64], int 
     for (int i = 0; i < 16; ++i) {
       const float send = up ? a[i] : a[i + 16];
       const float keep = up ? a[i + 16] : a[i];
+      b[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+    }
+  }
+  float c[8];
+  {
+    const bool up = lane & 4;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float send = up ? b[i] : b[i + 8];
+      const float keep = up ? b[i + 8] : b[i];
+      c[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+    }
+  }
+  float d[4];
+  {
+    const bool up = lane & 2;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float send = up ? c[i] : c[i + 4];
+      const float keep = up ? c[i + 4] : c[i];
+      d[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+    }
+  }
+  {
+    const bool up = lane & 1;
+    const float send0 = up ? d[0] : d[2];
+    const float keep0 = up ? d[2] : d[0];
+    const float send1 = up ? d[1] : d[3];
+    const float keep1 = up ? d[3] : d[1];
+    r0 = op(keep0, __shfl_xor_sync(0xffffffffu, send0, 1));
+    r1 = op(keep1, __shfl_xor_sync(0xffffffffu, send1, 1));
+  }
+}
+
+
+// The same over each half of a warp: each lane holds x[j] for 32 heads j; on
+// return lane l holds the reduction over the 16 lanes of its half-warp for heads
+// 2(l mod 16) and 2(l mod 16)+1. The two halves never exchange values.
+template <bool kMax>
+__device__ __forceinline__ void halfwarp_transpose_reduce(const float (&x)[32], int lane, float& r0,
+                                                          float& r1) {
+  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+  float b[16];
+  {
+    const bool up = lane & 8;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float send = up ? x[i] : x[i + 16];
+      const float keep = up ? x[i + 16] : x[i];
       b[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
     }
   }
