@@ -63,6 +63,38 @@ def algorithmic_bytes(s_q: int, S: int, part: str = "call") -> int:
     return s_q * (per_tok_in + 2 * partial + out)
 
 
+def balanced_schedule(s_q: int, nb: int, num_sms: int):
+    """The balanced one-shot schedule of mla_sparse_decode, restated on the host:
+    the s_q * nb 64-row blocks cut into P near-equal contiguous ranges (one CTA
+    each, P the fewest reaching ceil(s_q * nb / num_sms) blocks per CTA).
+    Returns (P, blocks per CTA, tokens cut by a range boundary, pieces of those)."""
+    U = s_q * nb
+    per = -(-U // num_sms)
+    P = -(-U // per)
+    base, rem = divmod(U, P)
+    big = rem * (base + 1)
+    cta = lambda u: u // (base + 1) if u < big else rem + (u - big) // base
+    cut = pieces = 0
+    for t in range(s_q):
+        pa, pb = cta(t * nb), cta((t + 1) * nb - 1)
+        if pa != pb:
+            cut += 1
+            pieces += pb - pa + 1
+    return P, per, cut, pieces
+
+
+def balanced_bytes(s_q: int, num_sms: int) -> int:
+    """Algorithmic bytes of the balanced schedule: every token's Q, indices,
+    gathered rows and FP8 output + LSE; a token cut into n pieces adds n - 1 fp32
+    partials (O + LSE), each written by its piece and read by the piece that
+    merges them."""
+    per_tok_in = H_Q * D_QK * 2 + TOPK * 4 + TOPK * D_QK * 2
+    out = H_Q * D_V * 1 + H_Q * 4
+    partial = H_Q * D_V * 4 + H_Q * 4
+    _, _, cut, pieces = balanced_schedule(s_q, -(-TOPK // 64), num_sms)
+    return s_q * (per_tok_in + out) + 2 * (pieces - cut) * partial
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -148,8 +180,17 @@ class Case:
         self.sm_scale = inp.sm_scale
         self.plan = b.mla_decode_plan(self.s_q, TOPK, force_splits=S) if S else b.mla_decode_plan(self.s_q, TOPK)
         self.S = self.plan.num_splits
+        # the automatic plan's one-shot call runs the balanced schedule (one kernel)
+        # when the planner enabled it and this s_q leaves >= 2 blocks per CTA
+        per = -(-(self.s_q * self.plan.num_blocks) // max(self.plan.num_sms, 1))
+        self.balanced = self.plan.balanced_ctas > 0 and per >= 2
+        if self.balanced:
+            self.P, self.per, self.cut, self.pieces = balanced_schedule(self.s_q, self.plan.num_blocks,
+                                                                        self.plan.num_sms)
         self.ws = (torch.empty(self.plan.workspace_bytes, dtype=torch.uint8, device=dev)
                    if self.plan.workspace_bytes else None)
+        if self.ws is not None:
+            b.mla_workspace_init(self.plan, self.ws)
         self.out = torch.empty(self.s_q, H_Q, D_V, dtype=torch.uint8, device=dev)
         self.lse = torch.empty(self.s_q, H_Q, dtype=torch.float32, device=dev)
         self.stream = torch.cuda.Stream()
@@ -161,11 +202,21 @@ class Case:
                                  "e4m3", INV_SCALE, self.out, self.lse, None, self.ws, stream=self.stream)
 
     def _kernel(self):
-        if self.S == 1:
+        if self.balanced or self.S == 1:
             self._call()
         else:
             self.b.mla_sparse_decode_split(self.plan, self.s_q, self.q, self.kv, N_KV, self.idx, self.sm_scale,
                                            self.ws, stream=self.stream)
+
+    def launches(self) -> int:
+        """Kernels one call launches (the balanced call also clears its counters)."""
+        return 1 if (self.balanced or self.S == 1) else 2
+
+    def schedule(self) -> str:
+        if self.balanced:
+            return (f"balanced: {self.P} CTAs x <= {self.per} blocks of 64 rows; "
+                    f"{self.cut} of {self.s_q} tokens cut into {self.pieces} pieces, merged in-kernel")
+        return f"uniform: {self.S} split(s) per token, {self.s_q * self.S} CTAs"
 
     def _capture(self, fn):
         torch = self.torch
@@ -245,7 +296,8 @@ def run_gpu(args):
 
     mean_call, mean_kern = max_over_ranks([statistics.fmean(call_us), statistics.fmean(kern_us)], dev)
 
-    kbytes = algorithmic_bytes(args.s_q, case.S, "split")
+    kbytes = (balanced_bytes(args.s_q, case.plan.num_sms) if case.balanced
+              else algorithmic_bytes(args.s_q, case.S, "split"))
     achieved = kbytes / (mean_kern * 1e-6) / 1e9
 
     # ---- end to end through the C ABI with host buffers ---------------------------------
@@ -277,13 +329,15 @@ def run_gpu(args):
     if not args.no_sweep:
         for s_q in SWEEP_SQ:
             inp = inp_main if s_q == args.s_q else inputs(s_q)
-            auto = b.mla_decode_plan(s_q, TOPK).num_splits
-            for S in sorted(set(SWEEP_S) | {auto}):
+            # forced (token, split) grids, then the planner's choice (S = 0: the
+            # balanced schedule of the one-shot call)
+            for S in list(SWEEP_S) + [0]:
                 c = Case(b, torch, kv, inp, S)
                 us = statistics.fmean(c.time(c.g_call, args.sweep_steps, 3, flush))
                 ks = statistics.fmean(c.time(c.g_kernel, args.sweep_steps, 3, flush))
-                cb = algorithmic_bytes(s_q, S, "call")
-                sweep.append({"s_q": s_q, "num_splits": S, "planner": S == auto, "us_per_call": round(us, 2),
+                cb = balanced_bytes(s_q, c.plan.num_sms) if c.balanced else algorithmic_bytes(s_q, S, "call")
+                sweep.append({"s_q": s_q, "num_splits": S if S else "planner", "planner": S == 0,
+                              "schedule": c.schedule(), "us_per_call": round(us, 2),
                               "split_kernel_us": round(ks, 2), "alg_bytes": cb,
                               "gb_s": round(cb / (us * 1e-6) / 1e9, 1),
                               "frac_of_peak": round(cb / (us * 1e-6) / 1e9 / peak, 4)})
@@ -306,16 +360,18 @@ def run_gpu(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_call / 1000.0, 6),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": workload_name(args.s_q), "s_q": args.s_q, "num_splits": case.S,
+            "config": {"workload": workload_name(args.s_q), "s_q": args.s_q, "schedule": case.schedule(),
                        "n_kv": N_KV, "topk": TOPK, "h_q": H_Q, "d_qk": D_QK, "d_v": D_V,
                        "output": "e4m3", "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                        "l2": "flushed before every timed call (256 MiB write, untimed)",
                        "timing": "CUDA graph replay of one decode call, CUDA events on its stream, mean of steps",
                        "wall_s_timed_region": round(wall, 4)},
-            "roofline": {"bound": "hbm", "kernel": "mla_decode_kernel (split pass)" if case.S > 1
-                         else "mla_decode_kernel (direct epilogue)",
+            "roofline": {"bound": "hbm", "kernel": ("mla_decode_kernel (balanced, in-kernel merge)" if case.balanced
+                                                    else "mla_decode_kernel (split pass)" if case.S > 1
+                                                    else "mla_decode_kernel (direct epilogue)"),
                          "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": known_traffic(args.s_q, case.S),
+                         "frac": round(achieved / peak, 4),
+                         "traffic": known_traffic(args.s_q, "balanced" if case.balanced else case.S),
                          "alg_bytes_per_launch": kbytes, "kernel_us": round(mean_kern, 3),
                          "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
                          else "fallback 6.8 TB/s"},
@@ -323,7 +379,7 @@ def run_gpu(args):
                     "d2h_bytes_per_step": d2h,
                     "note": "H2D of Q and indices from pinned host memory + the call + D2H of FP8 O and LSE; "
                             "the KV cache is resident decode state"},
-            "gpu_launches": args.steps * (2 if case.S > 1 else 1),
+            "gpu_launches": args.steps * case.launches(),
             "clocks": clocks,
             "cpu_baseline": cpu,
             "sweep": sweep,

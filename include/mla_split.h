@@ -100,12 +100,33 @@ typedef struct {
   int32_t num_blocks;   /* ceil(topk / block_rows)                                 */
   int32_t num_splits;   /* S; may exceed num_blocks (those splits are empty)       */
   int32_t num_sms;      /* SM count the split choice was made for                  */
-  int32_t reserved;
+  int32_t balanced_ctas; /* > 0: mla_sparse_decode runs the balanced schedule with at
+                            most this many CTAs (see below); 0: the (token, split) jobs */
   uint64_t o_acc_bytes;     /* num_splits * s_q_max * h_q * d_v * 4                */
   uint64_t lse_acc_offset;  /* o_acc_bytes rounded up to 256                       */
   uint64_t lse_acc_bytes;   /* num_splits * s_q_max * h_q * 4                      */
-  uint64_t workspace_bytes; /* 0 when num_splits == 1                              */
+  uint64_t workspace_bytes; /* what every call on this plan needs; 0 when num_splits == 1
+                               and balanced_ctas == 0                              */
 } mla_plan_t;
+
+/* Balanced schedule of the one-shot call (plan->balanced_ctas > 0). FlashMLA PR #25
+ * ("Measured") shows the (token, split) grid losing at s_q >= 96, where s_q * S
+ * jobs do not spread evenly over the SMs. Here the s_q * num_blocks 64-row blocks
+ * of all tokens, token-major, are cut into P contiguous near-equal ranges, one per
+ * CTA, with P the fewest CTAs that reach the smallest per-CTA block count on
+ * num_sms SMs: per = ceil(s_q * num_blocks / num_sms), P = ceil(s_q * num_blocks / per).
+ * A token inside one range is finished by that CTA (sink, cast, LSE, amax). The
+ * pieces of a token cut by range boundaries are partials with the split
+ * definition; the piece that ends last folds the others in by the combine's rule
+ * and writes the token's final rows, so the call is one kernel. Workspace of this
+ * schedule, with C = balanced_ctas: fp32 O partials [2*C][h_q][d_v] (in the
+ * kernel's own element order) and fp32 LSE partials [2*C][h_q] from offset 0
+ * (the LSE part 256-byte aligned), and uint32 per-token counters [s_q_max]
+ * followed by ready flags [2*C] in the last round_up((s_q_max + 2*C) * 4, 256)
+ * bytes of plan->workspace_bytes. Those counters and flags must be zero before
+ * the first call: run mla_workspace_init once on a new workspace (each call
+ * leaves them at zero again), and once more after a call that set
+ * MLA_STATUS_TIMEOUT. */
 
 /* Choose the split count and size the workspace ("The Split-K Dispatch",
  * "Adaptive NSPLIT"; FlashMLA PR #25, "Measured": partial bytes
@@ -116,10 +137,27 @@ typedef struct {
  *                even above num_blocks (the extra splits are empty).
  * Automatic rule: among split counts S with s_q_max * S <= num_sms (at least 1),
  * take the smallest S that reaches the fewest blocks per split, ceil(num_blocks / S).
+ * With force_splits == 0 the plan also enables the balanced schedule for the
+ * one-shot call when it beats that grid at s_q_max: with per = ceil(s_q_max *
+ * num_blocks / num_sms), when 2 <= per < ceil(s_q_max * S / num_sms) *
+ * ceil(num_blocks / S) (the most blocks any SM walks under the grid) and
+ * ceil(num_blocks / per) + 1 <= 32. It then sets balanced_ctas = min(num_sms,
+ * s_q_max * num_blocks) and sizes the workspace for both schedules: the larger
+ * of the two partial areas plus the balanced counters at the end. With
+ * force_splits > 0 the one-shot call runs the (token, split) jobs.
  * Errors: MLA_ERR_UNSUPPORTED unless h_q == 64, d_qk == 576, d_v == 512;
  *         MLA_ERR_INVALID_ARG for s_q_max < 1, topk < 1, out == NULL, or bad split counts. */
 MLA_API int mla_decode_plan(int s_q_max, int h_q, int d_qk, int d_v, int topk,
                     int num_sms, int max_splits, int force_splits, mla_plan_t* out);
+
+/* Zeroes all plan->workspace_bytes of `workspace` on `stream`. Needed once on a
+ * new workspace before the first mla_sparse_decode call of a plan with
+ * balanced_ctas > 0 (its counters must start at zero), and after a call that
+ * timed out; harmless otherwise. Returns MLA_OK at once when the plan needs no
+ * workspace; MLA_ERR_WORKSPACE for a NULL or not 256-byte aligned workspace;
+ * MLA_ERR_INVALID_ARG for plan == NULL; MLA_ERR_CUDA when the clear cannot be
+ * queued. */
+MLA_API int mla_workspace_init(const mla_plan_t* plan, void* workspace, void* stream);
 
 /* Split pass: one CTA per (token t, split s) job; the job walks the top-k
  * entries of its own block range (FlashMLA PR #25, "What changes"), gathers the
@@ -167,8 +205,11 @@ MLA_API int mla_sparse_decode_direct(int s_q, int topk, const void* q, const voi
                              int out_dtype, float out_inv_scale,
                              void* out, float* lse_out, float* amax_out, void* stream);
 
-/* One call for the whole decode step: the direct path when plan->num_splits == 1,
- * otherwise mla_sparse_decode_split followed by mla_split_combine on the same stream. */
+/* One call for the whole decode step. With plan->balanced_ctas > 0: the balanced
+ * schedule (described above mla_decode_plan) unless this call's s_q leaves fewer
+ * than 2 blocks per CTA (per rule above with s_q for s_q_max). Otherwise the direct path when
+ * plan->num_splits == 1, else mla_sparse_decode_split followed by
+ * mla_split_combine on the same stream. Same O / LSE / amax definitions either way. */
 MLA_API int mla_sparse_decode(const mla_plan_t* plan, int s_q,
                       const void* q, const void* kv, int64_t n_kv,
                       const int32_t* idx, float sm_scale, const float* sink,

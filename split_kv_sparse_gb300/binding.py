@@ -28,7 +28,7 @@ EXPORTS = [
     "mla_decode_plan", "mla_sparse_decode_split", "mla_split_combine", "mla_sparse_decode_direct",
     "mla_sparse_decode", "sdpa_fp8_decode_plan", "sdpa_fp8_decode_split", "sdpa_split_combine",
     "sdpa_fp8_decode_direct", "sdpa_fp8_decode", "mla_get_status", "mla_selftest_wait_timeout",
-    "mla_status_string", "mla_abi_version", "mla_sparse_decode_noalloc",
+    "mla_status_string", "mla_abi_version", "mla_sparse_decode_noalloc", "mla_workspace_init",
 ]
 
 
@@ -42,7 +42,7 @@ class MlaPlan(ctypes.Structure):
     _fields_ = [("s_q_max", ctypes.c_int32), ("h_q", ctypes.c_int32), ("d_qk", ctypes.c_int32),
                 ("d_v", ctypes.c_int32), ("topk", ctypes.c_int32), ("block_rows", ctypes.c_int32),
                 ("num_blocks", ctypes.c_int32), ("num_splits", ctypes.c_int32), ("num_sms", ctypes.c_int32),
-                ("reserved", ctypes.c_int32), ("o_acc_bytes", ctypes.c_uint64),
+                ("balanced_ctas", ctypes.c_int32), ("o_acc_bytes", ctypes.c_uint64),
                 ("lse_acc_offset", ctypes.c_uint64), ("lse_acc_bytes", ctypes.c_uint64),
                 ("workspace_bytes", ctypes.c_uint64)]
 
@@ -81,6 +81,7 @@ _SIGS = {
     "mla_status_string": [_I],
     "mla_abi_version": [],
     "mla_sparse_decode_noalloc": [_I, _I, _P, _P, _I64, _P, _F, _P, _I, _I, _F, _P, _P, _P, _P],
+    "mla_workspace_init": [ctypes.POINTER(MlaPlan), _P, _P],
 }
 
 
@@ -137,6 +138,10 @@ def mla_decode_plan(s_q_max: int, topk: int, *, h_q: int = 64, d_qk: int = 576, 
     _check(lib().mla_decode_plan(s_q_max, h_q, d_qk, d_v, topk, num_sms, max_splits, force_splits,
                                  ctypes.byref(plan)), "mla_decode_plan")
     return plan
+
+
+def mla_workspace_init(plan: MlaPlan, workspace, stream=None):
+    _check(lib().mla_workspace_init(ctypes.byref(plan), _ptr(workspace), _stream(stream)), "mla_workspace_init")
 
 
 def mla_sparse_decode_split(plan: MlaPlan, s_q: int, q, kv, n_kv: int, idx, sm_scale: float, workspace,

@@ -3,6 +3,7 @@
 // memory; the only device state is the per-device status word below.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -89,6 +90,38 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 uint64_t round_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+
+// Workspace of the balanced schedule for at most `ctas` CTAs and `s_q_max` tokens:
+//   fp32 O partials [2 * ctas][64][512] at 0, fp32 LSE partials [2 * ctas][64]
+//   after them; its uint32 per-token piece counters [s_q_max] and per-slot ready
+//   flags [2 * ctas] sit at the end of the plan's workspace (past what the
+//   uniform schedule uses too) and must start at zero (mla_workspace_init); each
+//   call leaves them at zero again.
+struct BalancedLayout {
+  uint64_t lse_off, partial_bytes, flag_bytes;
+};
+// Blocks per CTA of the balanced schedule for s_q tokens (0 when it does not
+// apply: fewer than 2 blocks per CTA, i.e. every block its own piece, or more
+// pieces per cut token than the merge's table holds).
+int64_t balanced_per(int64_t s_q, int nb, int num_sms) {
+  const int64_t U = s_q * nb;
+  const int64_t per = (U + num_sms - 1) / num_sms;
+  if (per < 2 || (nb + per - 1) / per + 1 > 32) return 0;
+  return per;
+}
+// Blocks the busiest SM walks under the uniform (token, split) grid.
+int64_t uniform_makespan(int64_t s_q, int nb, int S, int num_sms) {
+  return (s_q * S + num_sms - 1) / num_sms * ((nb + S - 1) / S);
+}
+
+BalancedLayout balanced_layout(int ctas, int s_q_max) {
+  BalancedLayout L;
+  const uint64_t slots = 2ull * static_cast<uint64_t>(ctas);
+  L.lse_off = round_up(slots * kMlaHeads * kMlaDv * 4ull, 256);
+  L.partial_bytes = round_up(L.lse_off + slots * kMlaHeads * 4ull, 256);
+  L.flag_bytes = round_up((static_cast<uint64_t>(s_q_max) + slots) * 4ull, 256);
+  return L;
+}
 
 int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
@@ -207,6 +240,14 @@ int mla_decode_plan(int s_q_max, int h_q, int d_qk, int d_v, int topk, int num_s
     out->lse_acc_bytes = static_cast<uint64_t>(S) * s_q_max * h_q * 4ull;
     out->workspace_bytes = round_up(out->lse_acc_offset + out->lse_acc_bytes, 256);
   }
+  const int64_t per = balanced_per(s_q_max, nblk, num_sms);
+  if (force_splits == 0 && per > 0 && per < uniform_makespan(s_q_max, nblk, S, num_sms)) {
+    // the one-shot call spreads all tokens' blocks over at most num_sms CTAs
+    const int64_t units = static_cast<int64_t>(s_q_max) * nblk;
+    out->balanced_ctas = static_cast<int32_t>(std::min<int64_t>(units, num_sms));
+    const BalancedLayout L = balanced_layout(out->balanced_ctas, s_q_max);
+    out->workspace_bytes = std::max(out->workspace_bytes, L.partial_bytes) + L.flag_bytes;
+  }
   return MLA_OK;
 }
 
@@ -230,12 +271,14 @@ int mla_sparse_decode_split(const mla_plan_t* plan, int s_q, const void* q, cons
   a.n_kv = static_cast<int>(n_kv);
   a.num_splits = plan->num_splits;
   a.num_blocks = plan->num_blocks;
+  a.sched = 0;
+  a.direct_whole = 0;
   a.scale_log2 = sm_scale * 1.4426950408889634f;
   a.o_acc = static_cast<float*>(workspace);
   a.lse_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan->lse_acc_offset);
   a.status = dev->status;
   a.wait_limit_ns = kWaitLimitNs;
-  return cuda_status(skv::launch_mla_decode(tq, a, false, static_cast<cudaStream_t>(stream)));
+  return cuda_status(skv::launch_mla_decode(tq, a, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"
@@ -271,9 +314,78 @@ int mla_combine_impl(const mla_plan_t* plan, int s_q, const void* workspace, con
   c.amax = amax_out;
   return cuda_status(skv::launch_combine(c, zero_amax, /*pdl=*/true, static_cast<cudaStream_t>(stream)));
 }
+
+// The one-shot call on the balanced schedule: every SM walks (nearly) the same
+// number of 64-row blocks whatever s_q is. One kernel: whole tokens are finished
+// by the CTA that holds them, a cut token by the CTA whose piece ends last.
+int mla_decode_balanced(const mla_plan_t* plan, int s_q, const void* q, const void* kv, int64_t n_kv,
+                        const int32_t* idx, float sm_scale, const float* sink, int out_dtype, float out_inv_scale,
+                        void* out, float* lse_out, float* amax_out, void* workspace, void* stream) {
+  if (plan->h_q != kMlaHeads || plan->d_qk != kMlaDqk || plan->d_v != kMlaDv) return MLA_ERR_UNSUPPORTED;
+  if (s_q > plan->s_q_max || plan->num_sms < 1 || plan->num_blocks < 1) return MLA_ERR_INVALID_ARG;
+  int st = check_mla_inputs(s_q, plan->topk, q, kv, n_kv, idx, sm_scale);
+  if (st != MLA_OK) return st;
+  if (out == nullptr || !aligned(out, 16) || !valid_out_dtype(out_dtype)) return MLA_ERR_INVALID_ARG;
+  if (out_dtype == MLA_OUT_E4M3 && !std::isfinite(out_inv_scale)) return MLA_ERR_INVALID_ARG;
+  const BalancedLayout L = balanced_layout(plan->balanced_ctas, plan->s_q_max);
+  if (workspace == nullptr || !aligned(workspace, 256) || plan->workspace_bytes < L.partial_bytes + L.flag_bytes)
+    return MLA_ERR_WORKSPACE;
+  // CTAs: the fewest that reach the smallest per-CTA block count on num_sms SMs
+  const int nb = plan->num_blocks;
+  const int64_t U = static_cast<int64_t>(s_q) * nb;
+  if (U > 0x7FFFFFFFll) return MLA_ERR_INVALID_ARG;
+  const int64_t per = (U + plan->num_sms - 1) / plan->num_sms;
+  const int P = static_cast<int>((U + per - 1) / per);
+  if (P > plan->balanced_ctas) return MLA_ERR_WORKSPACE;
+  DeviceState* dev = nullptr;
+  if ((st = device_state(&dev)) != MLA_OK) return st;
+  CUtensorMap tq;
+  if ((st = mla_q_tensor_map(s_q, q, &tq)) != MLA_OK) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* flags = reinterpret_cast<uint32_t*>(ws + plan->workspace_bytes - L.flag_bytes);
+  if (amax_out != nullptr) {
+    if ((st = cuda_status(cudaMemsetAsync(amax_out, 0, sizeof(float), cs))) != MLA_OK) return st;
+  }
+  skv::MlaArgs a{};
+  a.kv = static_cast<const uint8_t*>(kv);
+  a.idx = idx;
+  a.s_q = s_q;
+  a.topk = plan->topk;
+  a.n_kv = static_cast<int>(n_kv);
+  a.num_splits = 1;
+  a.num_blocks = nb;
+  a.sched = 1;
+  a.num_ctas = P;
+  a.direct_whole = 1;
+  a.scale_log2 = sm_scale * 1.4426950408889634f;
+  a.o_acc = reinterpret_cast<float*>(ws);
+  a.lse_acc = reinterpret_cast<float*>(ws + L.lse_off);
+  a.counters = flags;
+  a.ready = flags + plan->s_q_max;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.inv_scale = out_inv_scale;
+  a.lse_out = lse_out;
+  a.sink = sink;
+  a.amax = amax_out;
+  a.status = dev->status;
+  a.wait_limit_ns = kWaitLimitNs;
+  return cuda_status(skv::launch_mla_decode(tq, a, cs));
+}
 }  // namespace
 
 extern "C" {
+
+int mla_workspace_init(const mla_plan_t* plan, void* workspace, void* stream) {
+  if (plan == nullptr) return MLA_ERR_INVALID_ARG;
+  if (plan->workspace_bytes == 0) return MLA_OK;
+  if (workspace == nullptr || !aligned(workspace, 256)) return MLA_ERR_WORKSPACE;
+  DeviceState* dev = nullptr;
+  const int st = device_state(&dev);
+  if (st != MLA_OK) return st;
+  return cuda_status(cudaMemsetAsync(workspace, 0, plan->workspace_bytes, static_cast<cudaStream_t>(stream)));
+}
 
 int mla_split_combine(const mla_plan_t* plan, int s_q, const void* workspace, const float* sink, int out_dtype,
                       float out_inv_scale, void* out, float* lse_out, float* amax_out, void* stream) {
@@ -304,6 +416,8 @@ int mla_sparse_decode_direct(int s_q, int topk, const void* q, const void* kv, i
   a.n_kv = static_cast<int>(n_kv);
   a.num_splits = 1;
   a.num_blocks = (topk + kMlaBlockRows - 1) / kMlaBlockRows;
+  a.sched = 0;
+  a.direct_whole = 1;
   a.scale_log2 = sm_scale * 1.4426950408889634f;
   a.out = out;
   a.out_dtype = out_dtype;
@@ -313,13 +427,17 @@ int mla_sparse_decode_direct(int s_q, int topk, const void* q, const void* kv, i
   a.amax = amax_out;
   a.status = dev->status;
   a.wait_limit_ns = kWaitLimitNs;
-  return cuda_status(skv::launch_mla_decode(tq, a, true, cs));
+  return cuda_status(skv::launch_mla_decode(tq, a, cs));
 }
 
 int mla_sparse_decode(const mla_plan_t* plan, int s_q, const void* q, const void* kv, int64_t n_kv,
                       const int32_t* idx, float sm_scale, const float* sink, int out_dtype, float out_inv_scale,
                       void* out, float* lse_out, float* amax_out, void* workspace, void* stream) {
   if (plan == nullptr) return MLA_ERR_INVALID_ARG;
+  if (plan->balanced_ctas > 0 && plan->num_sms > 0 && plan->num_blocks > 0 && s_q >= 1 &&
+      balanced_per(s_q, plan->num_blocks, plan->num_sms) > 0)
+    return mla_decode_balanced(plan, s_q, q, kv, n_kv, idx, sm_scale, sink, out_dtype, out_inv_scale, out, lse_out,
+                               amax_out, workspace, stream);
   if (plan->num_splits == 1) {
     if (s_q > plan->s_q_max) return MLA_ERR_INVALID_ARG;
     return mla_sparse_decode_direct(s_q, plan->topk, q, kv, n_kv, idx, sm_scale, sink, out_dtype, out_inv_scale,
@@ -623,6 +741,9 @@ int mla_sparse_decode_noalloc(int s_q, int topk, const void* q, const void* kv, 
   mla_plan_t plan;
   int st = mla_decode_plan(s_q, kMlaHeads, kMlaDqk, kMlaDv, topk, 0, 0, num_splits, &plan);
   if (st != MLA_OK) return st;
+  // the (token, split) jobs: their workspace is num_splits * s_q partial rows
+  plan.balanced_ctas = 0;
+  plan.workspace_bytes = plan.num_splits > 1 ? round_up(plan.lse_acc_offset + plan.lse_acc_bytes, 256) : 0;
   if (plan.workspace_bytes > MLA_NOALLOC_SCRATCH_BYTES) return MLA_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (plan.workspace_bytes > 0 && (st = noalloc_scratch(&scratch)) != MLA_OK) return st;

@@ -20,12 +20,24 @@ struct MlaArgs {
   int s_q;
   int topk;
   int n_kv;
-  int num_splits;       // 1 for the direct path
-  int num_blocks;       // ceil(topk / 64)
+  int num_splits;       // uniform schedule: splits per token (1 for the direct path)
+  int num_blocks;       // ceil(topk / 64): 64-row blocks per token
+  int sched;            // 0: one (token, split) job per CTA, grid s_q * num_splits;
+                        // 1: balanced, the s_q * num_blocks blocks cut into num_ctas
+                        //    near-equal contiguous ranges, one per CTA (grid num_ctas)
+  int num_ctas;         // balanced schedule: CTAs (<= s_q * num_blocks)
+  int direct_whole;     // a job that covers a whole token writes the final output
+                        // (sink, cast, LSE, amax) instead of a partial
   float scale_log2;     // sm_scale * log2(e)
-  // split path: partial workspace
-  float* o_acc;         // [S][s_q][64][512]
-  float* lse_acc;       // [S][s_q][64]
+  // Partial workspace. Uniform: [S][s_q][64][512] and [S][s_q][64]. Balanced:
+  // [2 * num_ctas][64][512] and [2 * num_ctas][64] (slot 2p: the first job of CTA
+  // p, slot 2p + 1: its last, when those are pieces of a token cut by a range
+  // boundary), with per-token piece counters [s_q] and per-slot ready flags
+  // [2 * num_ctas], all zero when the launch starts.
+  float* o_acc;
+  float* lse_acc;
+  uint32_t* counters;
+  uint32_t* ready;
   // direct path: final output
   void* out;            // [s_q][64][512] of out_dtype
   int out_dtype;
@@ -37,6 +49,24 @@ struct MlaArgs {
   uint64_t wait_limit_ns;
 };
 
+// Balanced schedule arithmetic, shared by the host and the decode kernel: U
+// units (64-row blocks, token-major) cut into P contiguous ranges, the first
+// U % P of them one unit longer. Requires 1 <= P <= U.
+__host__ __device__ inline int bal_begin(int p, int U, int P) {
+  const int base = U / P, rem = U % P;
+  return p * base + (p < rem ? p : rem);
+}
+// The range (CTA) that holds unit u.
+__host__ __device__ inline int bal_cta_of(int u, int U, int P) {
+  const int base = U / P, rem = U % P;
+  const int big = rem * (base + 1);
+  return u < big ? u / (base + 1) : rem + (u - big) / base;
+}
+// Partial slot of token t in CTA p: 2p for the CTA's first job, 2p + 1 for its last.
+__host__ __device__ inline int bal_slot(int p, int t, int nb, int U, int P) {
+  return 2 * p + (t == bal_begin(p, U, P) / nb ? 0 : 1);
+}
+
 // Dynamic shared memory the MLA decode kernel needs.
 int mla_decode_smem_bytes();
 // One-time per-device set-up (shared-memory opt-in of the kernels); called by the
@@ -45,7 +75,7 @@ cudaError_t prepare_mla_kernels();
 cudaError_t prepare_sdpa_kernels();
 
 // tm_q: Q viewed as 2-D [s_q*64 rows][576] bf16, box 64x64, 128B swizzle.
-cudaError_t launch_mla_decode(const CUtensorMap& tm_q, const MlaArgs& a, bool direct, cudaStream_t stream);
+cudaError_t launch_mla_decode(const CUtensorMap& tm_q, const MlaArgs& a, cudaStream_t stream);
 
 // Log-sum-exp combine over `rows` output rows of width d (512 or 128).
 struct CombineArgs {

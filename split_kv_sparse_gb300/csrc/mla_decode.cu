@@ -1,43 +1,68 @@
 // Split-KV sparse-MLA decode kernel for sm_103a (tcgen05 MMAs, TMEM accumulators,
 // cp.async row gathers).
 //
-// What one CTA computes (FlashMLA PR #25, "What changes"): the job
-// (query token t, KV split s) walks the top-k entries [row0, row1) of its own
-// block range, gathers those rows of the shared latent KV cache, and produces
-// for each of the 64 heads either
-//   split path:  O_acc = sum_r e^{s_r} V_r / sum_r e^{s_r} (fp32) and the log2 LSE,
-//   direct path: the same O with the attention sink folded into the
-//                denominator, cast to fp32 / bf16 / e4m3, plus LSE and amax.
+// What one job computes (FlashMLA PR #25, "What changes"): the job (query token
+// t, a range [row0, row1) of its top-k entries) gathers those rows of the shared
+// latent KV cache and produces, for each of the 64 heads,
+//   a partial:   O = sum_r e^{s_r} V_r / sum_r e^{s_r} (fp32) and the log2 LSE, or
+//   final rows:  the same O with the attention sink folded into the denominator,
+//                cast to fp32 / bf16 / e4m3, plus LSE and amax (a job that
+//                covers all of its token's entries).
 //
-// Layout of the work (one CTA per job, 256 threads, 64 gathered rows per step):
-//   warps 0-2  loads: Q once by TMA (9 tiles of 64 heads x 64 dims); per step
-//              the 64 gathered rows as 4608 16-byte cp.async copies (each row
-//              is 72 contiguous 16-byte pieces; a warp instruction covers 512
-//              contiguous bytes of a row), written in the 128-byte-swizzled
-//              layout into one half of a ring of two 64-row halves; an invalid
-//              index copies zeros and reads nothing. Completion is tracked per
-//              thread by cp.async.mbarrier.arrive.
+// Which jobs a CTA runs (the schedule):
+//   uniform   one (token, split) job per CTA: split s of S takes a near-equal run
+//             of 64-row blocks, remainder to the leading splits (cuDNN-frontend
+//             PR #768, SM120 FP8 commit); grid s_q * S.
+//   balanced  the s_q * nb blocks of all tokens, token-major, are cut into
+//             num_ctas near-equal contiguous ranges, one per CTA, so every SM
+//             walks the same number of rows whatever s_q is. A CTA runs one job
+//             per token its range touches. A whole token gets its final rows. A
+//             token cut by range boundaries is finished by whichever of its
+//             pieces counts itself last on a per-token counter: the others leave
+//             a partial and a ready flag; the last one merges them with its own O
+//             by the log-sum-exp rule of the combine ("The Split-K Dispatch",
+//             "The LSE Combine Strategy") and writes the final rows. It waits
+//             only on pieces that have already counted themselves, so their CTAs
+//             are running, and it leaves the counter and the flags at zero again.
+//
+// Layout of the work (256 threads, 64 gathered rows per step; the steps of all
+// of a CTA's jobs form one pipeline over a ring of two 64-row halves):
+//   warps 0-1  row gathers: warp w copies rows 32w..32w+31 of the step; lane i
+//              takes 16-byte piece i mod 8 of every 64-dim chunk of rows
+//              32w + 4m + i/8 (m = 0..7), so one warp instruction copies four
+//              whole 128-byte lines; each copy is one instruction with constant
+//              offsets on both addresses, into the 128-byte-swizzled layout. An
+//              invalid index copies zeros and reads nothing. Completion:
+//              cp.async.mbarrier.arrive.
+//   warp 2     Q of each job by TMA (9 tiles of 64 heads x 64 dims), once the
+//              previous job's last QK has finished with the buffer (a barrier
+//              with one phase per job: a waiter on an mbarrier parity must never
+//              fall two phases behind, which a per-step barrier would allow here).
 //   warp 3     tcgen05 issue (one thread), all descriptors precomputed:
-//                S[64 heads x 64 rows]  = Q . K_half^T                  (M=64, N=64, K=576)
-//                O^T[512 x 64 heads]   += V_half^T . (P_hi + P_lo)^T    (4 x (M=128, N=64, K=64), twice)
+//                S[64 heads x 64 rows]  = Q . K_half^T                (M=64, N=64, K=576)
+//                O^T[512 x 64 heads]   += V_half^T . P_hi^T, then . P_lo^T (4 x (M=128, N=64, K=64) each)
 //              V is read straight out of the gathered rows as an MN-major
 //              operand; Q, K and P^T are K-major; all tiles use the 128-byte
-//              swizzle. Each QK and each PV is one unbroken run of MMAs.
+//              swizzle. Each QK is one unbroken run of its 36 MMAs.
 //   warps 4-7  softmax: an M=64 accumulator keeps head 16w+i in lane i of TMEM
 //              sub-partition w, so warp 4+w owns heads 16w..16w+15; its lanes
 //              0-15 take rows 0-31 and lanes 16-31 rows 32-63 of the step (one
 //              16x32bx2 TMEM load). A head's running max and row sum live in two
 //              lanes of one warp; only a rescale of O^T (rare, lazy) is shared
 //              with the other warps, through a per-step barrier that is arrived
-//              on early and waited on late. Then the epilogue.
+//              on early and waited on late. P_hi is published before P_lo, whose
+//              one buffer must first be released by the previous PV. At the end
+//              of each job: the epilogue, straight from TMEM to global memory.
 //
 // Precision: p = 2^(x - m_ref) is stored as P_hi = p truncated to bf16 and
 // P_lo = bf16(p - P_hi); the PV product uses both, so P enters O with ~2^-15
 // relative error instead of the 2^-8 of a single bf16. The fp32 sum of p (the
-// softmax denominator, and the LSE) stays in per-thread partials, reduced once
-// at the end; it matches the P the product used to the same ~2^-15.
+// softmax denominator, and the LSE) is kept per thread and reduced at the end of
+// the job; it matches the P the product used to the same ~2^-15.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
+
+#include <type_traits>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -47,43 +72,42 @@ namespace skv {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kProducers = 96;                      // warps 0-2
-constexpr int kPiecesPerRow = 72;                   // 1152 B / 16 B
-constexpr int kPiecesPerThread = kMlaBlockRows * kPiecesPerRow / kProducers;   // 48
+constexpr int kLoaders = 64;                        // warps 0-1
 constexpr int kChunks = 9;                          // 576 dims = 9 column chunks of 64 (128 B)
 constexpr int kSlotBytes = 16384;                   // one column chunk of both halves
 constexpr int kHalfBytes = 8192;                    // one column chunk of one 64-row half
 constexpr int kQChunkBytes = 8192;                  // 64 heads x 128 B
 constexpr int kRingBytes = kChunks * kSlotBytes;    // 147456
 constexpr int kQBytes = kChunks * kQChunkBytes;     // 73728
+constexpr int kRowBytes = kMlaDqk * 2;              // 1152
 
 // Shared memory map. The dynamic shared memory base is 1024-byte aligned (the
 // kernel checks it and refuses to run otherwise), so no slack is reserved.
 constexpr int kOffRing = 0;
 constexpr int kOffQ = kOffRing + kRingBytes;        // 147456
-constexpr int kOffPlo = kOffQ + kQBytes;            // 221184: P_lo, 64 rows x 64 heads bf16
+constexpr int kOffPlo = kOffQ + kQBytes;            // 221184: P_lo^T, 64 heads x 64 rows bf16
 constexpr int kOffBars = kOffPlo + kHalfBytes;      // 229376
-constexpr int kOffMisc = kOffBars + 128;            // [0] tmem base, [1] abort flag, [2..3] go,
-                                                    // [4..11] rescale masks [2][4], [12..15] final flags
+constexpr int kOffMisc = kOffBars + 192;            // [0] tmem base, [1] abort flag, [2] ticket, [3] merge wait,
+                                                    // [4..11] rescale masks [2][4], [12..15] failure flags
 constexpr int kOffAlpha = kOffMisc + 128;           // float[2][64] rescale factors by step parity
-constexpr int kOffInv = kOffAlpha + 512;            // float[64] 1/denominator (epilogue)
-constexpr int kOffIdx = kOffInv + 1024;             // int[2][64] row indices of the step, per half
-constexpr int kSmemBytes = kOffIdx + 512;           // 231680
+constexpr int kOffHead = kOffAlpha + 512;           // float[2][64] per-head epilogue scalars
+constexpr int kSmemBytes = kOffHead + 512;          // 230720
 
 enum {
-  B_QFULL = 0, B_FULL0, B_FULL1, B_EMPTY0, B_EMPTY1, B_SFULL0, B_SFULL1,
-  B_PFULL0, B_PFULL1, B_PVDONE, B_DRAIN, B_XCH0, B_XCH1, kNumBars
+  B_QFULL = 0, B_FULL0, B_FULL1, B_EMPTY0, B_EMPTY1, B_SFULL0, B_SFULL1, B_PHI0, B_PHI1,
+  B_PLO0, B_PLO1, B_PVDONE, B_DRAIN, B_XCH0, B_XCH1, B_OFREE, B_QFREE, B_MRG, kNumBars
 };
-static_assert(kNumBars * 8 <= 128, "barrier area");
+static_assert(kNumBars * 8 <= 192, "barrier area");
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 256;                    // S^T buffers at columns 256 and 320
+constexpr uint32_t kTmemS = 256;                    // S buffers at columns 256 and 320
 constexpr float kRescaleThreshold = 8.0f;           // p = 2^(x - m_ref) <= 256 between rescales
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Wait sites reported in the status word when a bounded wait runs out.
 enum : uint32_t {
-  W_PROD_EMPTY = 1, W_MMA_Q, W_MMA_STALL, W_SM_S, W_SM_PV, W_SM_PV_EPI, W_DRAIN_MMA, W_SM_X
+  W_PROD_EMPTY = 1, W_MMA_Q, W_MMA_STALL, W_SM_S, W_SM_PV, W_SM_PV_EPI, W_DRAIN_MMA, W_SM_X, W_PROD_Q,
+  W_MERGE
 };
 
 // 128-byte-swizzled byte offset of the 16-byte piece `piece` (0-7) of row `row`
@@ -92,7 +116,95 @@ __device__ __forceinline__ int sw128(int row, int piece) {
   return (row >> 3) * 1024 + (row & 7) * 128 + ((piece ^ (row & 7)) << 4);
 }
 
-template <bool kDirect>
+// The 9 copies of one lane for one row: its 16-byte piece of each 64-dim chunk.
+// `dst` is the piece's swizzled place in chunk 0, `src` its bytes in chunk 0;
+// chunk c adds c * kSlotBytes to the one and c * 128 to the other.
+template <int C>
+__device__ __forceinline__ void copy_row_chunks(uint32_t dst, const uint8_t* src, uint32_t sz) {
+  if constexpr (C < kChunks) {
+    cp_async_16_off2<C * kSlotBytes, C * 128>(dst, src, sz);
+    copy_row_chunks<C + 1>(dst, src, sz);
+  }
+}
+
+enum : int { J_FINAL = 0, J_PARTIAL = 1, J_PIECE = 2 };
+
+// One job of a CTA: token t, top-k entries [row0, row1) in nsteps steps of 64.
+//   J_FINAL    final rows of token t;
+//   J_PARTIAL  a (token, split) partial at workspace rows out_row .. + 63;
+//   J_PIECE    a piece of a token cut by the balanced schedule, partial slot `slot`.
+struct Job {
+  int t, row0, row1, nsteps, kind, slot;
+  size_t out_row;
+};
+
+__device__ __forceinline__ int num_jobs(const MlaArgs& a) {
+  if (a.sched == 0) return 1;
+  const int U = a.s_q * a.num_blocks, P = a.num_ctas, p = blockIdx.x;
+  const int u0 = bal_begin(p, U, P), u1 = bal_begin(p + 1, U, P);
+  return (u1 - 1) / a.num_blocks - u0 / a.num_blocks + 1;
+}
+
+__device__ __forceinline__ Job job_at(const MlaArgs& a, int j) {
+  Job r;
+  if (a.sched == 0) {
+    const int S = a.num_splits;
+    const int t = static_cast<int>(blockIdx.x) / S, s = static_cast<int>(blockIdx.x) - t * S;
+    const int base = a.num_blocks / S, rem = a.num_blocks - base * S;
+    const int blk0 = s * base + min(s, rem), nblk = base + (s < rem ? 1 : 0);
+    r.t = t;
+    r.row0 = min(blk0 * kMlaBlockRows, a.topk);
+    r.row1 = min((blk0 + nblk) * kMlaBlockRows, a.topk);
+    r.nsteps = (r.row1 - r.row0 + kMlaBlockRows - 1) / kMlaBlockRows;
+    r.kind = (a.direct_whole && S == 1) ? J_FINAL : J_PARTIAL;
+    r.slot = s;
+    r.out_row = r.kind == J_FINAL ? static_cast<size_t>(t) * kMlaHeads
+                                  : (static_cast<size_t>(s) * a.s_q + t) * kMlaHeads;
+  } else {
+    const int nb = a.num_blocks, U = a.s_q * nb, P = a.num_ctas, p = blockIdx.x;
+    const int u0 = bal_begin(p, U, P), u1 = bal_begin(p + 1, U, P);
+    const int t = u0 / nb + j;
+    const int b0 = max(u0, t * nb) - t * nb, b1 = min(u1, (t + 1) * nb) - t * nb;
+    r.t = t;
+    r.row0 = b0 * kMlaBlockRows;
+    r.row1 = min(b1 * kMlaBlockRows, a.topk);
+    r.nsteps = b1 - b0;
+    r.kind = (b0 == 0 && b1 == nb) ? J_FINAL : J_PIECE;
+    r.slot = 2 * p + (j == 0 ? 0 : 1);
+    r.out_row = r.kind == J_FINAL ? static_cast<size_t>(t) * kMlaHeads : static_cast<size_t>(r.slot) * kMlaHeads;
+  }
+  return r;
+}
+
+// Final rows of one O^T tile column set: v[c] for the 64 heads at dim d, cast
+// and stored; returns max |v|.
+__device__ __forceinline__ float store_final(const MlaArgs& a, int t, int d, const float (&v)[64]) {
+  float m = 0.f;
+  if (a.out_dtype == 0) {
+    float* st = static_cast<float*>(a.out) + static_cast<size_t>(t) * kMlaHeads * kMlaDv + d;
+#pragma unroll
+    for (int c = 0; c < 64; ++c) {
+      m = fmaxf(m, fabsf(v[c]));
+      st[c * kMlaDv] = v[c];
+    }
+  } else if (a.out_dtype == 1) {
+    __nv_bfloat16* st = static_cast<__nv_bfloat16*>(a.out) + static_cast<size_t>(t) * kMlaHeads * kMlaDv + d;
+#pragma unroll
+    for (int c = 0; c < 64; ++c) {
+      m = fmaxf(m, fabsf(v[c]));
+      st[c * kMlaDv] = __float2bfloat16_rn(v[c]);
+    }
+  } else {
+    uint8_t* st = static_cast<uint8_t*>(a.out) + static_cast<size_t>(t) * kMlaHeads * kMlaDv + d;
+#pragma unroll
+    for (int c = 0; c < 64; ++c) {
+      m = fmaxf(m, fabsf(v[c]));
+      st[c * kMlaDv] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(v[c] * a.inv_scale, __NV_SATFINITE, __NV_E4M3));
+    }
+  }
+  return m;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const MlaArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -100,27 +212,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- job decode: one place, shared by every role --------------------------
-  const int t = blockIdx.x / a.num_splits;
-  const int s = blockIdx.x - t * a.num_splits;
-  const int base = a.num_blocks / a.num_splits;
-  const int rem = a.num_blocks - base * a.num_splits;
-  const int blk0 = s * base + min(s, rem);
-  const int nblk = base + (s < rem ? 1 : 0);
-  const int row0 = min(blk0 * kMlaBlockRows, a.topk);
-  const int row1 = min((blk0 + nblk) * kMlaBlockRows, a.topk);
-  const int nsteps = (row1 - row0 + kMlaBlockRows - 1) / kMlaBlockRows;
-  const size_t out_row = kDirect ? static_cast<size_t>(t) * kMlaHeads
-                                 : (static_cast<size_t>(s) * a.s_q + t) * kMlaHeads;
+  // ---- jobs: the same decode in every role ---------------------------------
+  const int njobs = num_jobs(a);
+  const Job j0 = job_at(a, 0);
 
-  if (nsteps == 0) {
-    // A split with no block of its own: O = 0, LSE = -inf (only the split path
-    // can have one; the direct path always has topk >= 1 entries).
+  if (j0.nsteps == 0) {
+    // A split with no block of its own (uniform schedule only): O = 0, LSE = -inf.
     grid_launch_dependents();
-    float4* o = reinterpret_cast<float4*>(a.o_acc + out_row * kMlaDv);
+    float4* o = reinterpret_cast<float4*>(a.o_acc + j0.out_row * kMlaDv);
     for (int i = threadIdx.x; i < kMlaHeads * kMlaDv / 4; i += kThreads)
       o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (threadIdx.x < kMlaHeads) a.lse_acc[out_row + threadIdx.x] = -INFINITY;
+    if (threadIdx.x < kMlaHeads) a.lse_acc[j0.out_row + threadIdx.x] = -INFINITY;
     return;
   }
   if ((sbase & 1023u) != 0) {
@@ -133,41 +235,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBars + 8 * i; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  volatile uint32_t* vmisc = misc;
   volatile uint32_t* xch = reinterpret_cast<volatile uint32_t*>(misc + 4);   // [2][4] rescale masks
-  volatile int* fin = reinterpret_cast<volatile int*>(misc + 12);             // [4] final per-warp flags
+  volatile int* fin = reinterpret_cast<volatile int*>(misc + 12);             // [4] per-warp failure flags
   float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
-  float* inv_s = reinterpret_cast<float*>(smem + kOffInv);
+  float* hs = reinterpret_cast<float*>(smem + kOffHead);                       // [2][64] per-head scalars
   const WaitCtx wc{a.wait_limit_ns, a.status, abort_flag};
-  const int32_t* idx_t = a.idx + static_cast<size_t>(t) * a.topk;
 
   // The first row indices: fetched before the set-up barrier so the global
-  // memory latency overlaps TMEM allocation and barrier initialisation. Loader
-  // thread i < 64 takes row i of step 0; every softmax warp takes rows lane and
-  // lane + 32 of step 0.
-  int first_idx = -1, first_idx2 = -1;
+  // memory latency overlaps TMEM allocation and barrier initialisation. A
+  // loader lane takes rows 32w + lane/2 and 32w + 16 + lane/2 of step 0; a
+  // softmax lane takes rows lane and lane + 32.
+  int pre0 = -1, pre1 = -1;
   {
-    int r = -1;
-    if (threadIdx.x < kMlaBlockRows) r = row0 + static_cast<int>(threadIdx.x);
-    if (warp >= 4) r = row0 + lane;
-    if (r >= 0 && r < row1) first_idx = __ldg(idx_t + r);
-    if (warp >= 4 && r + 32 < row1) first_idx2 = __ldg(idx_t + r + 32);
-    if (first_idx < 0 || first_idx >= a.n_kv) first_idx = -1;
+    const int32_t* idx0 = a.idx + static_cast<size_t>(j0.t) * a.topk;
+    int r = -1, r2 = -1;
+    if (warp < 2) {
+      r = j0.row0 + 32 * warp + lane;
+    } else if (warp >= 4) {
+      r = j0.row0 + lane;
+      r2 = r + 32;
+    }
+    if (r >= 0 && r < j0.row1) pre0 = __ldg(idx0 + r);
+    if (r2 >= 0 && r2 < j0.row1) pre1 = __ldg(idx0 + r2);
   }
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
-    mbar_init(bar(B_FULL0), kProducers);   // one cp.async completion arrival per producer thread
-    mbar_init(bar(B_FULL1), kProducers);
+    mbar_init(bar(B_FULL0), kLoaders);     // one cp.async completion arrival per loader thread
+    mbar_init(bar(B_FULL1), kLoaders);
     mbar_init(bar(B_EMPTY0), 1);
     mbar_init(bar(B_EMPTY1), 1);
     mbar_init(bar(B_SFULL0), 1);
     mbar_init(bar(B_SFULL1), 1);
-    mbar_init(bar(B_PFULL0), 4);
-    mbar_init(bar(B_PFULL1), 4);
+    mbar_init(bar(B_PHI0), 4);             // one arrival per softmax warp
+    mbar_init(bar(B_PHI1), 4);
+    mbar_init(bar(B_PLO0), 4);
+    mbar_init(bar(B_PLO1), 4);
     mbar_init(bar(B_PVDONE), 1);
     mbar_init(bar(B_DRAIN), 1);
-    mbar_init(bar(B_XCH0), 4);             // one arrival per softmax warp
+    mbar_init(bar(B_XCH0), 4);
     mbar_init(bar(B_XCH1), 4);
+    mbar_init(bar(B_OFREE), 4);            // the epilogue's last TMEM read of O^T, per softmax warp
+    mbar_init(bar(B_QFREE), 1);            // a job's last QK has completed: its Q buffer is free
+    mbar_init(bar(B_MRG), 1);              // a merge's bulk copies of other pieces' partials
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -179,61 +290,80 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  // The combine (a programmatic dependent) may begin launching now; it waits
-  // for this whole grid to finish before it reads any partial.
+  // A programmatic dependent (the combine of the uniform schedule) may begin
+  // launching now; it waits for this whole grid before it reads any partial.
   grid_launch_dependents();
 
-  if (warp < 3) {
-    // ========================================================== loaders ===
-    const int ptid = threadIdx.x;          // 0..95
-    int* idx_s = reinterpret_cast<int*>(smem + kOffIdx);
-    volatile int* go = reinterpret_cast<volatile int*>(misc + 2);   // [2]: by step parity
-    if (ptid == 0) {
-      tma_prefetch_desc(&tm_q);
-      mbar_arrive_expect_tx(bar(B_QFULL), kQBytes);
+  if (warp < 2) {
+    // ====================================================== row gathers ===
+    const int pc = lane & 7;                       // this lane's 16-byte piece of a chunk
+    const int ro = lane >> 3;                      // and its row within each group of 4
+    int g = 0;
+    bool stop = false;
+    int ixl = pre0;                                // index of row 32w + lane of the step
 #pragma unroll 1
-      for (int c = 0; c < kChunks; ++c)
-        tma_load_2d(sbase + kOffQ + c * kQChunkBytes, &tm_q, 64 * c, kMlaHeads * t, bar(B_QFULL));
-    }
-    // thread ptid < 64 fetches the row index of row ptid of a step
-    auto fetch = [&](int k) -> int {
-      const int r = row0 + kMlaBlockRows * k + ptid;
-      int v = -1;
-      if (ptid < kMlaBlockRows && r < row1) {
-        v = __ldg(idx_t + r);
-        if (v < 0 || v >= a.n_kv) v = -1;
-      }
-      return v;
-    };
-    int cur = first_idx;
+    for (int j = 0; j < njobs && !stop; ++j) {
+      const Job jb = (j == 0) ? j0 : job_at(a, j);
+      const int32_t* idx_t = a.idx + static_cast<size_t>(jb.t) * a.topk;
+      auto fetch = [&](int k) -> int {
+        const int r = jb.row0 + kMlaBlockRows * k + 32 * warp + lane;
+        return r < jb.row1 ? __ldg(idx_t + r) : -1;
+      };
+      if (j > 0) ixl = fetch(0);
+      // Rows two steps ahead are requested into L2 as soon as their index is
+      // known: with two ring halves a step's rows are copied only once the step
+      // two before has finished with its half, so without this their DRAM
+      // latency would sit on the loop's critical chain.
+      int n1 = fetch(1), n2 = fetch(2);            // indices of steps k+1 and k+2
+      auto prefetch_row = [&](int ix) {
+        if (ix >= 0 && ix < a.n_kv) prefetch_l2_bulk(a.kv + static_cast<size_t>(ix) * kRowBytes, kRowBytes);
+      };
 #pragma unroll 1
-    for (int k = 0; k < nsteps; ++k) {
-      const int h = k & 1;
-      const int nxt = (k + 1 < nsteps) ? fetch(k + 1) : -1;   // in flight during the wait below
-      if (ptid < kMlaBlockRows) idx_s[h * kMlaBlockRows + ptid] = cur;
-      if (ptid == 0) go[h] = (k < 2) ? 1 : wait_bounded(bar(B_EMPTY0 + h), ((k >> 1) - 1) & 1, wc, W_PROD_EMPTY);
-      named_bar_sync(2, kProducers);     // the half is free and its row indices are visible
-      if (!go[h]) break;                 // every loader sees the same flag
-      const uint32_t half_base = sbase + kOffRing + h * kHalfBytes;
-      // all index reads first: a read after a cp.async (which writes shared
-      // memory) would have to wait for it
-      int ixr[kPiecesPerThread];
+      for (int k = 0; k < jb.nsteps; ++k, ++g) {
+        const int h = g & 1;
+        if (g >= 2) {
+          int ok = 1;
+          if (lane == 0) ok = wait_bounded(bar(B_EMPTY0 + h), ((g >> 1) - 1) & 1, wc, W_PROD_EMPTY);
+          if (!__shfl_sync(0xffffffffu, ok, 0)) {
+            stop = true;
+            break;
+          }
+        }
 #pragma unroll
-      for (int i = 0; i < kPiecesPerThread; ++i) ixr[i] = idx_s[h * kMlaBlockRows + (ptid + kProducers * i) / kPiecesPerRow];
-#pragma unroll
-      for (int i = 0; i < kPiecesPerThread; ++i) {
-        const int u = ptid + kProducers * i;
-        const int row = u / kPiecesPerRow;
-        const int seg = u - row * kPiecesPerRow;
-        const int ix = ixr[i];
-        const uint32_t dst = half_base + (seg >> 3) * kSlotBytes + sw128(row, seg & 7);
-        const uint8_t* src = a.kv + static_cast<size_t>(ix < 0 ? 0 : ix) * (kMlaDqk * 2) + seg * 16;
-        cp_async_16(dst, src, ix < 0 ? 0u : 16u);
+        for (int m = 0; m < 8; ++m) {
+          const int rl = 4 * m + ro;                   // row within the warp's 32
+          const int row = 32 * warp + rl;
+          const int ix = __shfl_sync(0xffffffffu, ixl, rl);
+          const bool valid = ix >= 0 && ix < a.n_kv;
+          const uint8_t* src = a.kv + static_cast<size_t>(valid ? ix : 0) * kRowBytes + pc * 16;
+          const uint32_t dst = sbase + kOffRing + h * kHalfBytes + static_cast<uint32_t>(sw128(row, pc));
+          copy_row_chunks<0>(dst, src, valid ? 16u : 0u);
+        }
+        cp_async_arrive_noinc(bar(B_FULL0 + h));
+        if (k == 0) prefetch_row(n1);
+        prefetch_row(n2);
+        ixl = n1;
+        n1 = n2;
+        n2 = fetch(k + 3);                         // arrives while this step is computed
       }
-      cp_async_arrive_noinc(bar(B_FULL0 + h));
-      cur = nxt;
     }
     cp_async_wait_all();   // nothing of this thread is still landing when the CTA exits
+  } else if (warp == 2) {
+    // ============================================================ Q loads ===
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+#pragma unroll 1
+      for (int j = 0; j < njobs; ++j) {
+        const Job jb = (j == 0) ? j0 : job_at(a, j);
+        // the buffer is free once the previous job's last QK has completed; that
+        // barrier has one phase per job, waited in order
+        if (j > 0 && !wait_bounded(bar(B_QFREE), (j - 1) & 1, wc, W_PROD_Q)) break;
+        mbar_arrive_expect_tx(bar(B_QFULL), kQBytes);
+#pragma unroll 1
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_2d(sbase + kOffQ + c * kQChunkBytes, &tm_q, 64 * c, kMlaHeads * jb.t, bar(B_QFULL));
+      }
+    }
   } else if (warp == 3) {
     // ========================================================= MMA issuer ===
     if (lane == 0) {
@@ -241,75 +371,107 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdescPV = idesc_make(128, 64, 1, true, false);   // A (V^T) MN-major, B (P^T) K-major
       // Descriptors of the operands' first K step; every other one differs only
       // in the start-address field (bits 0-13, address >> 4, no carry out of it
-      // below 256 KB), so the issue loop adds a constant.
-      // (half 1 is half 0 shifted by kHalfBytes)
+      // below 256 KB), so the issue code adds a constant. Half 1 is half 0
+      // shifted by kHalfBytes.
       const uint64_t d_k0 = sdesc_sw128(sbase + kOffRing, 16, 1024);
       const uint64_t d_v0 = sdesc_sw128(sbase + kOffRing, kSlotBytes, 1024);
       const uint64_t d_phi0 = sdesc_sw128(sbase + kOffRing + 8 * kSlotBytes, 16, 1024);
       constexpr uint64_t kHalfStep = kHalfBytes >> 4;
       const uint64_t d_q = sdesc_sw128(sbase + kOffQ, 16, 1024);
       const uint64_t d_plo = sdesc_sw128(sbase + kOffPlo, 16, 1024);
-      // QK(k): 9 column chunks of 64 dims x 4 MMAs of K=16 (32 bytes of a K-major
-      // row each), issued back to back with constant descriptor offsets
-      auto issue_qk = [&](int k) {
-        const uint32_t d = tmem + kTmemS + 64 * (k & 1);
-        const uint64_t ak = d_k0 + (k & 1) * kHalfStep;
+      // QK(g), chunks 3r .. 3r+2 (run r of 3): 12 MMAs of K=16 (32 bytes of a
+      // K-major row each) with constant descriptor offsets
+      auto qk_run = [&](int g, int r) {
+        const uint32_t d = tmem + kTmemS + 64 * (g & 1);
+        const uint64_t bk = d_k0 + (g & 1) * kHalfStep;
+        auto run = [&](auto c0) {
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f16(d, d_q + (c * kQChunkBytes) / 16 + 2 * kk, ak + (c * kSlotBytes) / 16 + 2 * kk, kIdescQK,
-                    (c | kk) != 0);
-      };
-      // PV(k): for each 128-dim tile j of V, K = the 64 rows in 4 steps of 16
-      // (2048 B of the MN-major V^T, 32 B of the K-major P^T each), first with
-      // P_hi, then with P_lo.
-      auto issue_pv = [&](int k) {
-        const uint64_t av = d_v0 + (k & 1) * kHalfStep;
-        const uint64_t bphi = d_phi0 + (k & 1) * kHalfStep;
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-          const uint64_t bp = part ? d_plo : bphi;
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
+          for (int c = decltype(c0)::value; c < decltype(c0)::value + 3; ++c)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_f16(tmem + 64 * j, av + (2 * j * kSlotBytes + kk * 2048) / 16, bp + 2 * kk, kIdescPV,
-                      (k > 0 || part > 0 || kk > 0));
-        }
+              mma_f16(d, d_q + (c * kQChunkBytes) / 16 + 2 * kk, bk + (c * kSlotBytes) / 16 + 2 * kk, kIdescQK,
+                      (c | kk) != 0);
+        };
+        if (r == 0) run(std::integral_constant<int, 0>{});
+        else if (r == 1) run(std::integral_constant<int, 3>{});
+        else run(std::integral_constant<int, 6>{});
       };
-      bool ok = wait_bounded(bar(B_QFULL), 0, wc, W_MMA_Q);
-      // PV(k) is issued as soon as softmax(k) has written P: its completion
-      // frees the half for the loads of step k+2, the loop's critical chain.
-      // QK(k) is issued once its rows have landed and its S^T buffer is free
-      // (softmax(k-2) is done, i.e. PV(k-2) was issued). tcgen05 runs them in
-      // issue order, each as one unbroken run of MMAs: instructions between two
-      // MMAs of a run stall the tensor pipe. When only one of the two can make
-      // progress the thread sleeps in try_wait on that barrier; otherwise it
-      // polls both.
-      int nqk = 0, npv = 0;
+      // PV(g) with P_hi (part 0) or P_lo (part 1): for each 128-dim tile j of V,
+      // K = the 64 rows in 4 steps of 16 (2048 B of the MN-major V^T, 32 B of
+      // the K-major P^T each); `first` starts a new O^T (first step of a job).
+      auto pv_part = [&](int g, int part, bool first) {
+        const uint64_t av = d_v0 + (g & 1) * kHalfStep;
+        const uint64_t bp = part ? d_plo : d_phi0 + (g & 1) * kHalfStep;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f16(tmem + 64 * j, av + (2 * j * kSlotBytes + kk * 2048) / 16, bp + 2 * kk, kIdescPV,
+                    (!first || part > 0 || kk > 0));
+      };
+      int total = 0;
+#pragma unroll 1
+      for (int j = 0; j < njobs; ++j) total += (j == 0) ? j0.nsteps : job_at(a, j).nsteps;
+      // Issue order, highest priority first:
+      //   PV_lo(g)  once softmax(g) has written P_lo; its completion frees the
+      //             half for the loads of step g+2 (the loop's critical chain);
+      //   PV_hi(g)  once softmax(g) has written P_hi (the first step of a job
+      //             also waits for the previous job's epilogue to read O^T);
+      //   QK(g)     once its rows (and, first in a job, its Q)
+      //             have landed and its S buffer is free: softmax(g-2) published
+      //             P_hi, i.e. PV_hi(g-2) was issued.
+      // tcgen05 runs the MMAs in issue order. When only one of them can make
+      // progress the thread sleeps in try_wait on its barrier; otherwise it
+      // polls them without blocking.
+      int nqk = 0, qrun = 0, nph = 0, npl = 0;
+      int qj = 0, qk = 0, qn = j0.nsteps;   // QK cursor: job, step within it, its steps
+      int hj = 0, hk = 0, hn = j0.nsteps;   // PV_hi cursor
+      bool ok = true;
       uint64_t t_idle = 0;
-      while (ok && npv < nsteps) {
-        const bool can_pv = npv < nqk;
-        const bool can_qk = nqk < nsteps && nqk <= npv + 1;
-        const uint32_t pbar = bar(B_PFULL0 + (npv & 1)), pph = (npv >> 1) & 1;
-        const uint32_t fbar = bar(B_FULL0 + (nqk & 1)), fph = (nqk >> 1) & 1;
+      while (ok && npl < total) {
+        const bool c_lo = npl < nph;
+        const bool c_hi = nph < nqk;
+        const bool c_qk = nqk < total && nqk <= nph + 1;
+        const bool c_qk_new = c_qk && qrun == 0;
+        const int ncand = (c_lo ? 1 : 0) + (c_hi ? 1 : 0) + (c_qk_new ? 1 : 0);
+        auto ready = [&](uint32_t b, uint32_t ph) { return ncand == 1 ? mbar_try_wait(b, ph) : mbar_test_wait(b, ph); };
         bool progress = false;
-        if (can_pv && (can_qk ? mbar_test_wait(pbar, pph) : mbar_try_wait(pbar, pph))) {
+        if (c_lo && ready(bar(B_PLO0 + (npl & 1)), (npl >> 1) & 1)) {
           tc_fence_after();
-          issue_pv(npv);
-          mma_commit(bar(B_EMPTY0 + (npv & 1)));
+          pv_part(npl, 1, false);
+          mma_commit(bar(B_EMPTY0 + (npl & 1)));
           mma_commit(bar(B_PVDONE));
-          ++npv;
+          ++npl;
           progress = true;
-        } else if (can_qk && (can_pv ? mbar_test_wait(fbar, fph) : mbar_try_wait(fbar, fph))) {
-          // the rows were written by other threads' cp.async (generic proxy);
-          // make them visible to the tensor core's reads (async proxy)
-          fence_proxy_async_smem();
+        } else if (c_hi && ready(bar(B_PHI0 + (nph & 1)), (nph >> 1) & 1) &&
+                   (hk > 0 || hj == 0 || mbar_try_wait(bar(B_OFREE), (hj - 1) & 1))) {
           tc_fence_after();
-          issue_qk(nqk);
-          mma_commit(bar(B_SFULL0 + (nqk & 1)));
-          ++nqk;
+          pv_part(nph, 0, hk == 0);
+          ++nph;
+          if (++hk == hn) {
+            hk = 0;
+            if (++hj < njobs) hn = job_at(a, hj).nsteps;
+          }
+          progress = true;
+        } else if (c_qk && (qrun > 0 || (ready(bar(B_FULL0 + (nqk & 1)), (nqk >> 1) & 1) &&
+                                         (qk > 0 || mbar_try_wait(bar(B_QFULL), qj & 1))))) {
+          if (qrun == 0) {
+            // the rows were written by other threads' cp.async (generic proxy);
+            // make them visible to the tensor core's reads (async proxy)
+            fence_proxy_async_smem();
+            tc_fence_after();
+          }
+          while (qrun < 3) qk_run(nqk, qrun++);   // one unbroken run of 36 MMAs
+          {
+            mma_commit(bar(B_SFULL0 + (nqk & 1)));
+            qrun = 0;
+            ++nqk;
+            if (++qk == qn) {
+              mma_commit(bar(B_QFREE));   // the job's QKs are all issued
+              qk = 0;
+              if (++qj < njobs) qn = job_at(a, qj).nsteps;
+            }
+          }
           progress = true;
         }
         if (progress) {
@@ -341,241 +503,446 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
     const int head = 16 * sp + (lane & 15);   // this thread's head
     const int rb = (lane >> 4) * 32;          // and its 32 rows rb..rb+31 of every step
-    float m_run = -INFINITY;   // reference max of the head (log2 units), shared by its two lanes
-    float lsum = 0.f;          // fp32 softmax denominator over this thread's rows
     int bad = 0;               // a bounded wait of this warp ran out
-    int ia = first_idx, ib = first_idx2;   // indices of rows lane and lane + 32 of the step
-
-#pragma unroll 1
-    for (int k = 0; k < nsteps; ++k) {
-      const int h = k & 1;
-      // which of this thread's 32 rows hold a valid index
-      const uint32_t vlo = __ballot_sync(0xffffffffu, ia >= 0 && ia < a.n_kv);
-      const uint32_t vhi = __ballot_sync(0xffffffffu, ib >= 0 && ib < a.n_kv);
-      const uint32_t vm = rb ? vhi : vlo;
-      if (k + 1 < nsteps) {   // the next step's indices, in flight during this step
-        const int rn = row0 + kMlaBlockRows * (k + 1) + lane;
-        ia = rn < row1 ? __ldg(idx_t + rn) : -1;
-        ib = rn + 32 < row1 ? __ldg(idx_t + rn + 32) : -1;
-      }
-
+    float amax_l = 0.f;        // max |O| over the final rows this thread wrote
+    int g = 0;                 // step index over all of this CTA's jobs
+    int nmrg = 0;              // phases of B_MRG used so far
+    int pending = 0;           // 1 + slot of a stored partial whose ready flag is still to be set
+    auto bounded = [&](uint32_t b, uint32_t ph, uint32_t site) {
       int w = 1;
-      if (lane == 0) w = wait_bounded(bar(B_SFULL0 + h), (k >> 1) & 1, wc, W_SM_S);
+      if (lane == 0) w = wait_bounded(b, ph, wc, site);
       w = __shfl_sync(0xffffffffu, w, 0);
       if (!w) bad = 1;
-      tc_fence_after();
+      return w != 0;
+    };
 
-      float x[32];
-      float mx = -INFINITY;
-      if (w) {
-        uint32_t raw[32];
-        tmem_ld_16x32bx2_x32_h32(tmem + lane_base + kTmemS + 64 * h, raw);
-        tmem_wait_ld_x32(raw);
-        if (vm == 0xffffffffu) {
+#pragma unroll 1
+    for (int j = 0; j < njobs && !bad; ++j) {
+      const Job jb = (j == 0) ? j0 : job_at(a, j);
+      const int32_t* idx_t = a.idx + static_cast<size_t>(jb.t) * a.topk;
+      float m_run = -INFINITY;   // reference max of the head (log2 units), shared by its two lanes
+      float lsum = 0.f;          // fp32 softmax denominator over this thread's rows
+      int ia = pre0, ib = pre1;  // indices of rows lane and lane + 32 of the step
+      if (j > 0) {
+        const int r = jb.row0 + lane;
+        ia = r < jb.row1 ? __ldg(idx_t + r) : -1;
+        ib = r + 32 < jb.row1 ? __ldg(idx_t + r + 32) : -1;
+      }
+
+#pragma unroll 1
+      for (int k = 0; k < jb.nsteps; ++k, ++g) {
+        const int h = g & 1;
+        // which of this thread's 32 rows hold a valid index
+        const uint32_t vlo = __ballot_sync(0xffffffffu, ia >= 0 && ia < a.n_kv);
+        const uint32_t vhi = __ballot_sync(0xffffffffu, ib >= 0 && ib < a.n_kv);
+        const uint32_t vm = rb ? vhi : vlo;
+        if (k + 1 < jb.nsteps) {   // the next step's indices, in flight during this step
+          const int rn = jb.row0 + kMlaBlockRows * (k + 1) + lane;
+          ia = rn < jb.row1 ? __ldg(idx_t + rn) : -1;
+          ib = rn + 32 < jb.row1 ? __ldg(idx_t + rn + 32) : -1;
+        }
+
+        // A piece takes its ticket as its last step begins (the round trip
+        // overlaps the wait below): the last piece to count itself merges. Every
+        // piece that counted is running, so waiting on it cannot deadlock.
+        if (jb.kind == J_PIECE && k == jb.nsteps - 1 && tid == 0 && !bad)
+          misc[2] = atomicAdd(&a.counters[jb.t], 1u);
+        const bool w = bounded(bar(B_SFULL0 + h), (g >> 1) & 1, W_SM_S);
+        tc_fence_after();
+        float x[32];
+        float mx = -INFINITY;
+        if (w) {
+          uint32_t raw[32];
+          tmem_ld_16x32bx2_x32_h32(tmem + lane_base + kTmemS + 64 * h, raw);
+          tmem_wait_ld_x32(raw);
+          if (vm == 0xffffffffu) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            x[i] = __uint_as_float(raw[i]) * a.scale_log2;
-            mx = fmaxf(mx, x[i]);
+            for (int i = 0; i < 32; ++i) {
+              x[i] = __uint_as_float(raw[i]) * a.scale_log2;
+              mx = fmaxf(mx, x[i]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              x[i] = ((vm >> i) & 1u) ? __uint_as_float(raw[i]) * a.scale_log2 : -INFINITY;
+              mx = fmaxf(mx, x[i]);
+            }
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            x[i] = ((vm >> i) & 1u) ? __uint_as_float(raw[i]) * a.scale_log2 : -INFINITY;
-            mx = fmaxf(mx, x[i]);
-          }
+          for (int i = 0; i < 32; ++i) x[i] = -INFINITY;
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = -INFINITY;
-      }
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));   // over the step's 64 rows
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));   // over the step's 64 rows
 
-      // Lazy rescale: move the reference max only when a score exceeds it by
-      // more than the threshold (always on the first valid row of a head). Both
-      // lanes of the head see the same mx and take the same decision.
-      const bool need = mx > m_run + kRescaleThreshold;
-      if (need) {
-        const float al = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - mx);
-        lsum *= al;
-        m_run = mx;
-        if (lane < 16) alpha_s[h * 64 + head] = al;
-      }
-      const uint32_t rmask = __ballot_sync(0xffffffffu, need) & 0xffffu;
-      __syncwarp();
-      if (lane == 0) {
-        xch[h * 4 + sp] = rmask | (bad ? 0x10000u : 0u);
-        mbar_arrive(bar(B_XCH0 + h));      // release: the mask and the factors above
-      }
+        // Lazy rescale: move the reference max only when a score exceeds it by
+        // more than the threshold (always on the first valid row of a head). Both
+        // lanes of the head see the same mx and take the same decision.
+        const bool need = mx > m_run + kRescaleThreshold;
+        if (need) {
+          const float al = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - mx);
+          lsum *= al;
+          m_run = mx;
+          if (lane < 16) alpha_s[h * 64 + head] = al;
+        }
+        const uint32_t rmask = __ballot_sync(0xffffffffu, need) & 0xffffu;
+        if (pending) __threadfence();   // the previous job's partial, long since stored
+        __syncwarp();
+        if (lane == 0) {
+          xch[h * 4 + sp] = rmask | (bad ? 0x10000u : 0u);
+          mbar_arrive(bar(B_XCH0 + h));      // release: the mask and the factors above
+        }
 
-      // p = 2^(x - m_ref); a masked row gives 0
+        // p = 2^(x - m_ref); a masked row gives 0
 #pragma unroll
-      for (int i = 0; i < 32; ++i) x[i] = (x[i] == -INFINITY) ? 0.f : ex2_approx(x[i] - m_run);
-      {
-        float t[16];
+        for (int i = 0; i < 32; ++i) x[i] = (x[i] == -INFINITY) ? 0.f : ex2_approx(x[i] - m_run);
+        {
+          float ts[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) t[i] = x[i] + x[i + 16];
+          for (int i = 0; i < 16; ++i) ts[i] = x[i] + x[i + 16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] += t[i + 8];
+          for (int i = 0; i < 8; ++i) ts[i] += ts[i + 8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) t[i] += t[i + 4];
-        lsum += (t[0] + t[2]) + (t[1] + t[3]);
-      }
-      // P_hi = p with its mantissa cut to bf16 (exact bit truncation, no
-      // conversion); P_lo = bf16(p - P_hi), two rows per packed conversion.
-      // |P_lo| < 2^-7 p, so P_hi + P_lo matches p to 2^-15.
-      uint32_t hi[16], lo[16];
+          for (int i = 0; i < 4; ++i) ts[i] += ts[i + 4];
+          lsum += (ts[0] + ts[2]) + (ts[1] + ts[3]);
+        }
+        // P_hi = p with its mantissa cut to bf16 (exact bit truncation, no
+        // conversion); P_lo = bf16(p - P_hi), two rows per packed conversion.
+        // |P_lo| < 2^-7 p, so P_hi + P_lo matches p to 2^-15.
+        uint32_t hi[16], lo[16];
 #pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        const uint32_t b0 = __float_as_uint(x[i]) & 0xFFFF0000u;
-        const uint32_t b1 = __float_as_uint(x[i + 1]) & 0xFFFF0000u;
-        const __nv_bfloat162 lo2 =
-            __floats2bfloat162_rn(x[i] - __uint_as_float(b0), x[i + 1] - __uint_as_float(b1));
-        hi[i / 2] = (b0 >> 16) | b1;
-        lo[i / 2] = *reinterpret_cast<const uint32_t*>(&lo2);
-      }
+        for (int i = 0; i < 32; i += 2) {
+          const uint32_t b0 = __float_as_uint(x[i]) & 0xFFFF0000u;
+          const uint32_t b1 = __float_as_uint(x[i + 1]) & 0xFFFF0000u;
+          const __nv_bfloat162 lo2 =
+              __floats2bfloat162_rn(x[i] - __uint_as_float(b0), x[i + 1] - __uint_as_float(b1));
+          hi[i / 2] = (b0 >> 16) | b1;
+          lo[i / 2] = *reinterpret_cast<const uint32_t*>(&lo2);
+        }
 
-      // The other warps' rescale masks for this step.
-      int wx = 1;
-      if (lane == 0) wx = wait_bounded(bar(B_XCH0 + h), (k >> 1) & 1, wc, W_SM_X);
-      wx = __shfl_sync(0xffffffffu, wx, 0);
-      if (!wx) bad = 1;
-      const uint32_t x0 = xch[h * 4 + 0], x1 = xch[h * 4 + 1], x2 = xch[h * 4 + 2], x3 = xch[h * 4 + 3];
-      if (((x0 | x1 | x2 | x3) & 0x10000u) || !wx) {
-        bad = 1;
-        break;   // every softmax warp sees the same masks and leaves together
-      }
-      // PV(k-1) must be complete before O^T is rescaled and before P_lo (one
-      // buffer for all steps) is overwritten.
-      if (k >= 1) {
-        int wp = 1;
-        if (lane == 0) wp = wait_bounded(bar(B_PVDONE), (k - 1) & 1, wc, W_SM_PV);
-        wp = __shfl_sync(0xffffffffu, wp, 0);
-        if (!wp) bad = 1;
-        tc_fence_after();
+        // The other warps' rescale masks for this step.
+        const bool wx = bounded(bar(B_XCH0 + h), (g >> 1) & 1, W_SM_X);
+        if (pending) {
+          // every softmax thread has fenced its stores of that partial: publish it
+          if (tid == 0 && wx) st_release_gpu(a.ready + (pending - 1), 1u);
+          pending = 0;
+        }
+        const uint32_t x0 = xch[h * 4 + 0], x1 = xch[h * 4 + 1], x2 = xch[h * 4 + 2], x3 = xch[h * 4 + 3];
+        if (((x0 | x1 | x2 | x3) & 0x10000u) || !wx) {
+          bad = 1;
+          break;   // every softmax warp sees the same masks and leaves together
+        }
         const uint64_t resc = static_cast<uint64_t>(x0) | (static_cast<uint64_t>(x1) << 16) |
                               (static_cast<uint64_t>(x2) << 32) | (static_cast<uint64_t>(x3) << 48);
-        if (resc != 0 && !bad) {
-          // O^T holds PV of steps < k: scale the columns of the rescaled heads
-          // in the 32 dims (TMEM lanes) of each tile this warp can reach
-#pragma unroll 1
-          for (int j = 0; j < 8; ++j) {   // 4 O^T tiles x 2 halves of 32 head columns
-            const int c0 = 32 * (j & 1);
-            if (((resc >> c0) & 0xffffffffull) == 0) continue;
-            uint32_t o[32];
-            float al[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) al[i] = ((resc >> (c0 + i)) & 1ull) ? alpha_s[h * 64 + c0 + i] : 1.f;
-            const uint32_t col = 64 * (j >> 1) + c0;
-            tmem_ld_32x32b_x32(tmem + lane_base + col, o);
-            tmem_wait_ld_x32(o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * al[i]);
-            tmem_st_32x32b_x32(tmem + lane_base + col, o);
-          }
-          tmem_wait_st();
-        }
-      }
-      // P^T as a K-major operand: N = heads, K = rows; the 64 rows of one head
-      // are one 128-byte line of the swizzled tile, this thread's 32 rows are
-      // its pieces rb/8 .. rb/8+3.
-      {
+        // P^T as a K-major operand: N = heads, K = rows; the 64 rows of one head
+        // are one 128-byte line of the swizzled tile, this thread's 32 rows are
+        // its pieces rb/8 .. rb/8+3.
         uint8_t* p_hi = smem + kOffRing + 8 * kSlotBytes + h * kHalfBytes;
         uint8_t* p_lo = smem + kOffPlo;
+        auto store_p = [&](uint8_t* dst, const uint32_t (&v)[16]) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int off = sw128(head, (rb >> 3) + q);
-          *reinterpret_cast<uint4*>(p_hi + off) = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
-          *reinterpret_cast<uint4*>(p_lo + off) = make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(dst + sw128(head, (rb >> 3) + q)) =
+                make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        };
+        auto publish = [&](int b) {   // generic-proxy stores -> the tensor core's reads
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(b));
+        };
+        if (resc == 0 || k == 0) {
+          // O^T needs no rescale before PV_hi(g) (or holds nothing of this job
+          // yet): publish P_hi now; P_lo's buffer is free once PV(g-1) is done.
+          store_p(p_hi, hi);
+          publish(B_PHI0 + h);
+          if (g >= 1) {
+            bounded(bar(B_PVDONE), (g - 1) & 1, W_SM_PV);
+            tc_fence_after();
+          }
+          store_p(p_lo, lo);
+          publish(B_PLO0 + h);
+        } else {
+          // O^T holds PV of this job's earlier steps: once PV(g-1) is done, scale
+          // the columns of the rescaled heads in the 32 dims (TMEM lanes) of each
+          // tile this warp can reach, then publish both halves of P.
+          bounded(bar(B_PVDONE), (g - 1) & 1, W_SM_PV);
+          tc_fence_after();
+          if (!bad) {
+#pragma unroll 1
+            for (int q = 0; q < 8; ++q) {   // 4 O^T tiles x 2 halves of 32 head columns
+              const int c0 = 32 * (q & 1);
+              if (((resc >> c0) & 0xffffffffull) == 0) continue;
+              uint32_t o[32];
+              float al[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) al[i] = ((resc >> (c0 + i)) & 1ull) ? alpha_s[h * 64 + c0 + i] : 1.f;
+              const uint32_t col = 64 * (q >> 1) + c0;
+              tmem_ld_32x32b_x32(tmem + lane_base + col, o);
+              tmem_wait_ld_x32(o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * al[i]);
+              tmem_st_32x32b_x32(tmem + lane_base + col, o);
+            }
+            tmem_wait_st();
+          }
+          store_p(p_hi, hi);
+          store_p(p_lo, lo);
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(bar(B_PHI0 + h));
+            mbar_arrive(bar(B_PLO0 + h));
+          }
         }
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_PFULL0 + h));
-    }
 
-    // ---- epilogue ---------------------------------------------------------
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);
-    if (lane == 0) fin[sp] = bad;
-    if (lane < 16) {
-      float lse = -INFINITY, inv = 0.f;
-      if (lsum > 0.f) {
-        lse = m_run + log2f(lsum);
+      // ---- epilogue of job j ------------------------------------------------
+      // Every softmax warp reaches each named barrier below (a failed wait only
+      // ends the job loop after the exchange that follows it), so none can wait
+      // there forever. Per-head scalars hs[0..1][64]: 1/denominator and the job's
+      // own LSE.
+      lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);
+      if (!bad) {
+        bounded(bar(B_PVDONE), (g - 1) & 1, W_SM_PV_EPI);   // O^T is complete
+        tc_fence_after();
+      }
+      const float lse_own = lsum > 0.f ? m_run + log2f(lsum) : -INFINITY;
+      if (lane < 16) {
         float den = lsum;
-        if (kDirect && a.sink != nullptr) den += exp2f(a.sink[head] * kLog2e - m_run);
-        inv = 1.f / den;
-      }
-      inv_s[head] = inv;
-      if (kDirect) {
-        if (a.lse_out != nullptr) a.lse_out[out_row + head] = lse;
-      } else {
-        a.lse_acc[out_row + head] = lse;
-      }
-    }
-    named_bar_sync(1, 128);
-    const bool any_bad = fin[0] | fin[1] | fin[2] | fin[3];
-    int wp = 0;
-    if (!any_bad) {
-      if (lane == 0) wp = wait_bounded(bar(B_PVDONE), (nsteps - 1) & 1, wc, W_SM_PV_EPI);
-      wp = __shfl_sync(0xffffffffu, wp, 0);
-      tc_fence_after();
-    }
-    if (!any_bad && wp) {
-      // Stage the [64 heads][512] output tile in the ring (free now: every load
-      // has landed and every MMA has completed), then copy it to global memory
-      // with one bulk copy; a job's output rows are contiguous there.
-      float amax_l = 0.f;
-      float inv[64];   // in registers: no shared-memory reload between the stores
-#pragma unroll
-      for (int c = 0; c < 64; ++c) inv[c] = inv_s[c];
-      const int esize = (!kDirect || a.out_dtype == 0) ? 4 : (a.out_dtype == 1 ? 2 : 1);
-      uint8_t* stage = smem + kOffRing;
-#pragma unroll 1
-      for (int j = 0; j < 4; ++j) {
-        uint32_t o[64];
-        tmem_ld_32x32b_x64(tmem + lane_base + 64 * j, o);
-        tmem_wait_ld_x64(o);
-        const int d = 128 * j + 32 * sp + lane;
-        if (esize == 4) {
-          float* st = reinterpret_cast<float*>(stage) + d;
-#pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const float v = __uint_as_float(o[c]) * inv[c];
-            amax_l = fmaxf(amax_l, fabsf(v));
-            st[c * kMlaDv] = v;
+        if (jb.kind == J_FINAL && a.sink != nullptr && lsum > 0.f) den += exp2f(a.sink[head] * kLog2e - m_run);
+        hs[head] = lsum > 0.f ? 1.f / den : 0.f;
+        hs[64 + head] = lse_own;
+        if (!bad) {
+          if (jb.kind == J_FINAL) {
+            if (a.lse_out != nullptr) a.lse_out[jb.out_row + head] = lse_own;
+          } else {
+            a.lse_acc[jb.out_row + head] = lse_own;
           }
-        } else if (esize == 2) {
-          __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stage) + d;
+        }
+      }
+      if (lane == 0) fin[sp] = bad;
+      named_bar_sync(1, 128);
+      if (fin[0] | fin[1] | fin[2] | fin[3]) {
+        bad = 1;
+        break;   // every softmax warp leaves together
+      }
+      // the pieces of this token (balanced schedule): CTAs pa..pb
+      const int nb = a.num_blocks, U = a.s_q * nb, P = a.num_ctas;
+      int pa = 0, npieces = 1;
+      if (jb.kind == J_PIECE) {
+        pa = bal_cta_of(jb.t * nb, U, P);
+        npieces = bal_cta_of((jb.t + 1) * nb - 1, U, P) - pa + 1;
+      }
+      const bool merge = jb.kind == J_PIECE && static_cast<int>(vmisc[2]) == npieces - 1;
+      const bool to_final = jb.kind == J_FINAL || merge;
+
+      // A merge in the CTA's last job stages the other pieces' partial tiles in
+      // shared memory by bulk copies (the ring and Q buffers are idle then; the
+      // TMA engine keeps many requests in flight, plain loads from a thread
+      // would not): one tile of each other piece at a time, or all four tiles
+      // at once when there is a single other piece.
+      const int n_other = npieces - 1;
+      const bool staged = merge && j == njobs - 1 && n_other <= 6;
+      const bool all_tiles = staged && n_other == 1;
+      auto issue_stage = [&](int q0, int nq) {   // (tid 0) tiles q0 .. q0+nq-1 of every other piece
+        if (*abort_flag) return;
+        fence_proxy_async_all();
+        mbar_arrive_expect_tx(bar(B_MRG), static_cast<uint32_t>(n_other * nq) * 32768u);
+        int oi = 0;
+        for (int pq = 0; pq < npieces; ++pq) {
+          if (pa + pq == static_cast<int>(blockIdx.x)) continue;
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(
+              a.o_acc + static_cast<size_t>(bal_slot(pa + pq, jb.t, nb, U, P)) * kMlaHeads * kMlaDv);
+          for (int qq = 0; qq < nq; ++qq)
+            bulk_load(sbase + static_cast<uint32_t>((all_tiles ? q0 + qq : oi) * 32768),
+                      src + static_cast<size_t>(q0 + qq) * 32768, 32768u, bar(B_MRG));
+          ++oi;
+        }
+      };
+      auto wait_stage = [&]() {
+        const bool ok = bounded(bar(B_MRG), nmrg & 1, W_MERGE);
+        ++nmrg;
+        return ok;
+      };
+      if (merge) {
+        // Last piece of a cut token: wait until the other pieces' partials are
+        // visible (their CTAs have counted themselves, so they are running),
+        // then merge by the combine's rule with the sink, as final rows.
+        if (tid == 0) {
+          uint32_t okw = 1;
+          const uint64_t t0 = globaltimer_ns();
+          for (int q = 0; q < npieces && okw; ++q) {
+            if (pa + q == static_cast<int>(blockIdx.x)) continue;
+            const uint32_t* f = a.ready + bal_slot(pa + q, jb.t, nb, U, P);
+            while (ld_acquire_gpu(f) == 0u) {
+              if (*abort_flag || globaltimer_ns() - t0 > a.wait_limit_ns) {
+                okw = 0;
+                *abort_flag = 1;
+                atomicOr(&a.status[0], 1u);
+                atomicCAS(&a.status[1], 0u, W_MERGE);
+                break;
+              }
+            }
+          }
+          if (okw) {
+            // leave the counter and the flags zero for the next call (every piece
+            // has counted itself and set its flag: nobody touches them again)
+            for (int q = 0; q < npieces; ++q)
+              if (pa + q != static_cast<int>(blockIdx.x)) a.ready[bal_slot(pa + q, jb.t, nb, U, P)] = 0u;
+            a.counters[jb.t] = 0u;
+          }
+          misc[3] = okw;
+        }
+        named_bar_sync(1, 128);
+        if (!vmisc[3]) {
+          bad = 1;
+          break;
+        }
+        if (tid == 0 && staged) issue_stage(0, all_tiles ? 4 : 1);   // in flight during the factors below
+        // Pieces are folded in token order, the own piece in the very form a
+        // stored partial has (O * (1/l) in fp32, its LSE), so the result does not
+        // depend on which piece happened to end last.
+        if (lane < 16) {
+          // the pieces' LSEs (all loads in flight together) into the table, then
+          // the max, the weights and w_q / den in place
+          float* coef = reinterpret_cast<float*>(smem + kOffPlo);
+#pragma unroll 4
+          for (int q = 0; q < npieces; ++q)
+            coef[q * 64 + head] = pa + q == static_cast<int>(blockIdx.x)
+                                      ? lse_own
+                                      : __ldcg(a.lse_acc + static_cast<size_t>(bal_slot(pa + q, jb.t, nb, U, P)) * kMlaHeads + head);
+          float M = -INFINITY;
+          for (int q = 0; q < npieces; ++q) M = fmaxf(M, coef[q * 64 + head]);
+          float wsum = 0.f, inv_den = 0.f;
+          if (M != -INFINITY) {
+            for (int q = 0; q < npieces; ++q) {
+              const float l = coef[q * 64 + head];
+              const float w = l == -INFINITY ? 0.f : exp2f(l - M);
+              coef[q * 64 + head] = w;
+              wsum += w;
+            }
+            float den = wsum;
+            if (a.sink != nullptr) den += exp2f(a.sink[head] * kLog2e - M);
+            inv_den = 1.f / den;
+          }
+          for (int q = 0; q < npieces; ++q) coef[q * 64 + head] = M == -INFINITY ? 0.f : coef[q * 64 + head] * inv_den;
+          if (a.lse_out != nullptr)
+            a.lse_out[static_cast<size_t>(jb.t) * kMlaHeads + head] = M == -INFINITY ? -INFINITY : M + log2f(wsum);
+        }
+        named_bar_sync(1, 128);
+        if (all_tiles && !wait_stage()) {   // (no named barrier follows on this path)
+          bad = 1;
+          break;
+        }
+      }
+
+
+      // O^T tile q holds dims 128q .. 128q+127 in its lanes and the 64 heads in
+      // its columns: this thread handles dim d of every head; for each head the
+      // warp's 32 lanes touch 32 consecutive dims. A balanced piece's partial is
+      // kept in this same order (O^T, [512 dims][64 heads]), so the piece that
+      // merges it reads each thread's 64 values as 16-byte loads.
+      const float* coef = reinterpret_cast<const float*>(smem + kOffPlo);
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        const int dl = 32 * sp + lane;   // dim within the tile
+        const int d = 128 * q + dl;
+        float v[64];
+        if (!merge) {
+          uint32_t o[64];
+          tmem_ld_32x32b_x64(tmem + lane_base + 64 * q, o);
+          tmem_wait_ld_x64(o);
+          // the per-head factor read into registers before any store below
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const float v = __uint_as_float(o[c]) * inv[c];
-            amax_l = fmaxf(amax_l, fabsf(v));
-            st[c * kMlaDv] = __float2bfloat16_rn(v);
+          for (int c = 0; c < 64; c += 4) {
+            const float4 fv = *reinterpret_cast<const float4*>(hs + c);
+            v[c] = __uint_as_float(o[c]) * fv.x;
+            v[c + 1] = __uint_as_float(o[c + 1]) * fv.y;
+            v[c + 2] = __uint_as_float(o[c + 2]) * fv.z;
+            v[c + 3] = __uint_as_float(o[c + 3]) * fv.w;
           }
         } else {
-          uint8_t* st = stage + d;
+          // sum over the pieces, in token order, of w_q / den * O_q; the own
+          // piece enters as O * (1/l), re-read from TMEM at its turn
+          // (a failed wait only marks this warp bad: every warp still reaches the
+          // named barrier at the end of the tile)
+          if (staged && !all_tiles && !wait_stage()) bad = 1;
+          int oi = 0;   // index of the piece among the other pieces
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const float v = __uint_as_float(o[c]) * inv[c];
-            amax_l = fmaxf(amax_l, fabsf(v));
-            st[c * kMlaDv] =
-                static_cast<uint8_t>(__nv_cvt_float_to_fp8(v * a.inv_scale, __NV_SATFINITE, __NV_E4M3));
+          for (int c = 0; c < 64; ++c) v[c] = 0.f;
+#pragma unroll 1
+          for (int pq = 0; pq < npieces; ++pq) {
+            const float* cf = coef + pq * 64;
+            if (pa + pq == static_cast<int>(blockIdx.x)) {
+              uint32_t ow[64];
+              tmem_ld_32x32b_x64(tmem + lane_base + 64 * q, ow);
+              tmem_wait_ld_x64(ow);
+#pragma unroll
+              for (int c = 0; c < 64; ++c) v[c] = fmaf(cf[c], __uint_as_float(ow[c]) * hs[c], v[c]);
+            } else {
+              float4 t4[16];
+              if (staged) {
+                const float4* sl = reinterpret_cast<const float4*>(smem + (all_tiles ? q : oi) * 32768) + dl;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) t4[k] = sl[k * 128];
+              } else {
+                const float4* src = reinterpret_cast<const float4*>(
+                    a.o_acc + static_cast<size_t>(bal_slot(pa + pq, jb.t, nb, U, P)) * kMlaHeads * kMlaDv) + q * 2048 + dl;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) t4[k] = __ldcg(src + k * 128);
+              }
+              ++oi;
+#pragma unroll
+              for (int k = 0; k < 16; ++k) {
+                v[4 * k] = fmaf(cf[4 * k], t4[k].x, v[4 * k]);
+                v[4 * k + 1] = fmaf(cf[4 * k + 1], t4[k].y, v[4 * k + 1]);
+                v[4 * k + 2] = fmaf(cf[4 * k + 2], t4[k].z, v[4 * k + 2]);
+                v[4 * k + 3] = fmaf(cf[4 * k + 3], t4[k].w, v[4 * k + 3]);
+              }
+            }
           }
         }
-      }
-      fence_proxy_async_smem();          // the bulk copy reads the tile through the async proxy
-      named_bar_sync(1, 128);
-      if (tid == 0) {
-        uint8_t* gdst = kDirect ? static_cast<uint8_t*>(a.out) + out_row * kMlaDv * esize
-                                : reinterpret_cast<uint8_t*>(a.o_acc + out_row * kMlaDv);
-        bulk_store(gdst, sbase + kOffRing, kMlaHeads * kMlaDv * esize);
-        bulk_commit_and_wait_all();
-      }
-      if (kDirect && a.amax != nullptr) {
+        if (q == 3) {
+          // this warp's last read of O^T: the next job's first PV may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_OFREE));
+        }
+        if (staged && !all_tiles) {
+          named_bar_sync(1, 128);   // the slots are read: the next tile's copies may land
+          if (tid == 0 && q < 3) issue_stage(q + 1, 1);
+        }
+        if (to_final) {
+          amax_l = fmaxf(amax_l, store_final(a, jb.t, d, v));
+        } else if (jb.kind == J_PIECE) {
+          // [tile][k][dim in tile][4 heads]: a warp writes 512 contiguous bytes
+          float4* st = reinterpret_cast<float4*>(a.o_acc + jb.out_row * kMlaDv) + q * 2048 + dl;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax_l = fmaxf(amax_l, __shfl_xor_sync(0xffffffffu, amax_l, o));
-        if (lane == 0) atomicMax(reinterpret_cast<int*>(a.amax), __float_as_int(amax_l));
+          for (int k = 0; k < 16; ++k) st[k * 128] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        } else {
+          float* st = a.o_acc + jb.out_row * kMlaDv + d;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) st[c * kMlaDv] = v[c];
+        }
       }
+      if (bad) break;
+      if (jb.kind == J_PIECE && !merge) {
+        if (j + 1 < njobs) {
+          // published during the next step, once the stores have drained
+          pending = jb.slot + 1;
+        } else {
+          // publish this piece: every thread's stores, then the ready flag
+          __threadfence();
+          named_bar_sync(1, 128);
+          if (tid == 0) st_release_gpu(a.ready + jb.slot, 1u);
+        }
+      }
+    }
+    if (a.amax != nullptr && !bad) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax_l = fmaxf(amax_l, __shfl_xor_sync(0xffffffffu, amax_l, o));
+      if (lane == 0 && amax_l > 0.f) atomicMax(reinterpret_cast<int*>(a.amax), __float_as_int(amax_l));
     }
   }
 
@@ -594,18 +961,13 @@ int mla_decode_smem_bytes() { return kSmemBytes; }
 
 cudaError_t prepare_mla_kernels() {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kSmemBytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(mla_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  return cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
 }
 
-cudaError_t launch_mla_decode(const CUtensorMap& tm_q, const MlaArgs& a, bool direct, cudaStream_t stream) {
-  const dim3 grid(static_cast<unsigned>(a.s_q) * static_cast<unsigned>(a.num_splits));
-  if (direct)
-    mla_decode_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tm_q, a);
-  else
-    mla_decode_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tm_q, a);
+cudaError_t launch_mla_decode(const CUtensorMap& tm_q, const MlaArgs& a, cudaStream_t stream) {
+  const dim3 grid(a.sched == 0 ? static_cast<unsigned>(a.s_q) * static_cast<unsigned>(a.num_splits)
+                               : static_cast<unsigned>(a.num_ctas));
+  mla_decode_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, a);
   return cudaGetLastError();
 }
 

@@ -101,6 +101,20 @@ static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, 
   }
 }
 
+// ------------------------------------------------- flags in global memory --
+
+// Load with acquire semantics at GPU scope: reads after it see what the writer
+// published before its release.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Store with release semantics at GPU scope.
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // ------------------------------------------------------------------- fences --
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -166,6 +180,35 @@ __device__ __forceinline__ void bulk_commit_and_wait_all() {
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
+}
+// The same with a constant byte offset folded into the source address.
+template <int kOff>
+__device__ __forceinline__ void cp_async_16_off(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1+%3], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes), "n"(kOff)
+               : "memory");
+}
+// ... with constant offsets on both addresses.
+template <int kDstOff, int kSrcOff>
+__device__ __forceinline__ void cp_async_16_off2(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0+%3], [%1+%4], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes),
+               "n"(kDstOff), "n"(kSrcOff)
+               : "memory");
+}
+// Bulk global -> shared copy (TMA engine), completion counted on `bar` in bytes;
+// both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t sdst, const void* gsrc, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(sdst),
+               "l"(gsrc), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// Orders this thread's earlier memory accesses (any state space, generic proxy)
+// before its later async-proxy operations.
+__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
+// Starts bringing `bytes` (a multiple of 16) at a 16-byte aligned global address
+// into L2; no completion to wait for.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 // Arrives on `bar` once every cp.async this thread issued so far has landed
 // (the barrier's expected count includes this arrival).

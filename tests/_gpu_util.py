@@ -33,13 +33,18 @@ def check_status():
 
 
 def run_mla(inp, S: int, out_dtype: str = "f32", inv_scale: float = 1.0, with_amax: bool = False,
-            keep_workspace: bool = False):
-    """Whole decode step through mla_sparse_decode (direct path when S == 1)."""
+            keep_workspace: bool = False, num_sms: int = 0):
+    """Whole decode step through mla_sparse_decode: S > 0 forces the (token,
+    split) jobs (the direct path when S == 1); S == 0 takes the automatic plan,
+    whose one-shot call runs the balanced schedule over num_sms SMs (0 = the
+    device's)."""
     dev = torch.device("cuda")
     q, kv, idx = inp.q.to(dev), inp.kv.to(dev), inp.idx.to(dev)
     sink = inp.sink.to(dev) if inp.sink is not None else None
-    plan = b.mla_decode_plan(inp.s_q, inp.topk, force_splits=S)
-    ws = torch.empty(max(plan.workspace_bytes, 1), dtype=torch.uint8, device=dev) if plan.workspace_bytes else None
+    plan = b.mla_decode_plan(inp.s_q, inp.topk, force_splits=S, num_sms=num_sms)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev) if plan.workspace_bytes else None
+    if ws is not None:
+        b.mla_workspace_init(plan, ws)
     out = torch.empty(inp.s_q, 64, 512, dtype=TORCH_OUT[out_dtype], device=dev)
     lse = torch.empty(inp.s_q, 64, dtype=torch.float32, device=dev)
     amax = torch.empty(1, dtype=torch.float32, device=dev) if with_amax else None

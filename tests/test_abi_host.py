@@ -81,7 +81,22 @@ def test_plan_is_deterministic_and_follows_rule():
                 best = -(-nblk // smax)
                 assert -(-nblk // S) == best
                 assert all(-(-nblk // c) > best for c in range(1, S))
-                assert (p1.workspace_bytes == 0) == (S == 1)
+                # uniform workspace (0 for one split), and with the automatic
+                # choice also the balanced schedule's partial slots, counters and flags
+                ru = lambda x: -(-x // 256) * 256
+                uni = 0 if S == 1 else ru(ru(S * s_q * 64 * 512 * 4) + S * s_q * 64 * 4)
+                per = -(-(s_q * nblk) // sms)
+                mk_uniform = -(-(s_q * S) // sms) * -(-nblk // S)
+                enabled = 2 <= per < mk_uniform and -(-nblk // per) + 1 <= 32
+                C = min(sms, s_q * nblk) if enabled else 0
+                # partials [2C][64][512] then LSEs [2C][64]; counters [s_q] and
+                # flags [2C] at the very end, past both schedules' partials
+                partials = ru(ru(2 * C * 64 * 512 * 4) + 2 * C * 64 * 4)
+                flags = ru((s_q + 2 * C) * 4)
+                assert p1.balanced_ctas == C
+                assert p1.workspace_bytes == (max(uni, partials) + flags if enabled else uni)
+                pf = b.mla_decode_plan(s_q, topk, num_sms=sms, force_splits=S)
+                assert pf.balanced_ctas == 0 and (pf.workspace_bytes == 0) == (S == 1)
 
 
 def test_plan_examples():
@@ -176,3 +191,49 @@ def test_dense_plan():
 
 def test_build_targets_sm103a_only():
     assert bld.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def _bal_begin(p, U, P):
+    base, rem = divmod(U, P)
+    return p * base + min(p, rem)
+
+
+def test_balanced_schedule_covers_every_block_once():
+    """The balanced one-shot schedule, restated on the host: P contiguous ranges
+    of the token-major block list, near-equal; each range's jobs one per token it
+    touches; every (token, block) lands in exactly one job, a token held by one
+    CTA is whole, and only a CTA's first and last job can be pieces (its two
+    partial slots)."""
+    for sms in [148, 152]:
+        for s_q in [1, 3, 6, 16, 95, 96, 97, 384]:
+            for nb in [1, 2, 10, 32]:
+                U = s_q * nb
+                per = -(-U // sms)
+                P = -(-U // per)
+                assert P <= min(sms, U)
+                sizes = [_bal_begin(p + 1, U, P) - _bal_begin(p, U, P) for p in range(P)]
+                assert max(sizes) == per and max(sizes) - min(sizes) <= 1
+                seen = {}
+                for p in range(P):
+                    u0, u1 = _bal_begin(p, U, P), _bal_begin(p + 1, U, P)
+                    jobs = list(range(u0 // nb, (u1 - 1) // nb + 1))
+                    for j, t in enumerate(jobs):
+                        b0, b1 = max(u0, t * nb) - t * nb, min(u1, (t + 1) * nb) - t * nb
+                        assert 0 <= b0 < b1 <= nb
+                        if not (b0 == 0 and b1 == nb):
+                            assert j in (0, len(jobs) - 1)
+                        for blk in range(b0, b1):
+                            assert (t, blk) not in seen
+                            seen[(t, blk)] = p
+                assert len(seen) == U
+
+
+def test_balanced_schedule_choice_examples():
+    # s_q = 96, 384 on 152 SMs: the uniform grid walks 10 and 30 blocks on its
+    # busiest SM, the balanced schedule 7 and 26
+    assert b.mla_decode_plan(96, 640, num_sms=152).balanced_ctas == 152
+    assert b.mla_decode_plan(384, 640, num_sms=152).balanced_ctas == 152
+    # s_q = 1, 16: the grid already spreads as evenly (10 x 1 block, 80 x 2 blocks)
+    assert b.mla_decode_plan(1, 640, num_sms=152).balanced_ctas == 0
+    assert b.mla_decode_plan(16, 640, num_sms=152).balanced_ctas == 0
+    assert b.mla_decode_plan(96, 640, num_sms=152, force_splits=1).balanced_ctas == 0

@@ -173,6 +173,7 @@ def test_cuda_graph_capture_and_replay():
     plan = b.mla_decode_plan(16, 640)          # one plan for the whole s_q <= 16 bucket
     assert plan.num_splits > 1
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    b.mla_workspace_init(plan, ws)
     out = torch.empty(6, 64, 512, dtype=torch.uint8, device=dev)
     lse = torch.empty(6, 64, dtype=torch.float32, device=dev)
     s = torch.cuda.Stream()
@@ -230,8 +231,11 @@ def test_host_errors_on_gpu():
 
 @pytest.mark.parametrize("s_q", [96, 384])
 def test_full_size_sampled(s_q):
+    """The bench's configuration: the automatic plan (balanced schedule over the
+    device's SMs), FP8 output; tokens sampled so the oracle finishes in seconds."""
     inp = wl.mla_inputs(s_q, 131072, 640, seed=0)
-    r = run_mla(inp, b.mla_decode_plan(s_q, 640).num_splits, out_dtype="e4m3", inv_scale=64.0)
+    r = run_mla(inp, 0, out_dtype="e4m3", inv_scale=64.0)
+    assert r["plan"].balanced_ctas > 0
     rng = np.random.default_rng(s_q)
     ts = np.sort(rng.choice(s_q, 6, replace=False))
     sub = wl.MlaInputs(q=inp.q[ts], kv=inp.kv, idx=inp.idx[ts], sink=None, sm_scale=inp.sm_scale)
@@ -249,3 +253,80 @@ def test_full_size_forced_splits_sampled():
         r = run_mla(inp, S)
         assert_o_close(r["out"].numpy()[ts], O)
         assert_lse_close(r["lse"][ts], L)
+
+
+# ---- balanced schedule: range boundaries cutting tokens anywhere ----------------------
+
+@pytest.mark.parametrize("s_q,topk,num_sms", [
+    (2, 640, 5),      # 20 blocks over 5 CTAs of 4: each token in 3 pieces
+    (3, 640, 4),      # 30 blocks over 4 CTAs (8, 8, 7, 7): CTAs holding pieces of two tokens
+    (5, 640, 2),      # 50 blocks over 2 CTAs of 25: whole tokens beside the pieces of a cut one
+    (7, 200, 5),      # ragged top-k (4 blocks, the last of 8 rows), 28 blocks over 5 CTAs
+    (4, 640, 3),      # 40 blocks over 3 CTAs (14, 13, 13)
+])
+@pytest.mark.parametrize("with_sink", [False, True])
+def test_balanced_schedule_matches_oracle(s_q, topk, num_sms, with_sink):
+    inp = wl.mla_inputs(s_q, 32768, topk, seed=300 + s_q * 7 + num_sms, with_sink=with_sink,
+                        index_mode="window" if topk >= 128 else "uniform")
+    O, L = oracle_mla(inp)
+    r = run_mla(inp, 0, num_sms=num_sms)
+    assert r["plan"].balanced_ctas > 0
+    assert_o_close(r["out"].numpy(), O)
+    assert_lse_close(r["lse"], L)
+
+
+@pytest.mark.parametrize("out_dtype", ["bf16", "e4m3"])
+def test_balanced_schedule_casts_and_amax(out_dtype):
+    """Whole tokens and merged cut tokens are cast by the kernel; the amax is the
+    max over both."""
+    inp = wl.mla_inputs(5, 32768, 640, seed=41, v_mean=1.0, with_sink=True)
+    O, L = oracle_mla(inp)
+    r = run_mla(inp, 0, out_dtype=out_dtype, inv_scale=64.0, with_amax=True, num_sms=4)   # 50 over 4
+    assert_cast_close(r["out"], O, out_dtype, 64.0)
+    assert_lse_close(r["lse"], L)
+    assert abs(r["amax"] - float(np.abs(O).max())) <= 2e-3 * float(np.abs(O).max())
+
+
+def test_balanced_schedule_padding_and_empty_pieces():
+    """Padded and out-of-range indices; a piece whose rows are all masked is an
+    empty partial (LSE = -inf) and drops out of the merge; a token with no valid
+    row at all is O = 0, LSE = -inf."""
+    inp = wl.mla_inputs(4, 32768, 640, seed=43)
+    idx = inp.idx.clone()
+    idx[1, 0:256] = -1             # token 1's first piece (blocks 0-3, in CTA 0) holds no valid row
+    idx[3, :] = -1                 # token 3 (whole, in CTA 2): nothing valid
+    idx[2, 100:110] = 40000        # out of range: masked
+    inp = wl.MlaInputs(q=inp.q, kv=inp.kv, idx=idx, sink=None, sm_scale=inp.sm_scale)
+    O, L = oracle_mla(inp)
+    r = run_mla(inp, 0, num_sms=3)       # 40 blocks over 3 CTAs (14, 13, 13)
+    assert r["plan"].balanced_ctas > 0
+    assert_o_close(r["out"].numpy(), O)
+    assert_lse_close(r["lse"], L)
+
+
+def test_balanced_schedule_repeated_calls():
+    """Two calls in a row on one workspace, initialised once: each call leaves the
+    per-token counters and ready flags at the end of the workspace at zero again,
+    so the second call gives the same, correct result."""
+    inp = wl.mla_inputs(3, 32768, 640, seed=47, with_sink=True)
+    O, L = oracle_mla(inp)
+    dev = torch.device("cuda")
+    plan = b.mla_decode_plan(3, 640, num_sms=4)
+    assert plan.balanced_ctas > 0
+    ws = torch.full((plan.workspace_bytes,), 0xA5, dtype=torch.uint8, device=dev)
+    b.mla_workspace_init(plan, ws)
+    flag_bytes = -(-((3 + 2 * plan.balanced_ctas) * 4) // 256) * 256
+    outs = []
+    for _ in range(2):
+        out = torch.empty(3, 64, 512, dtype=torch.float32, device=dev)
+        lse = torch.empty(3, 64, dtype=torch.float32, device=dev)
+        b.mla_sparse_decode(plan, 3, inp.q.to(dev), inp.kv.to(dev), inp.n_kv, inp.idx.to(dev), inp.sm_scale,
+                            inp.sink.to(dev), "f32", 1.0, out, lse, None, ws)
+        torch.cuda.synchronize()
+        check_status()
+        assert int(ws[plan.workspace_bytes - flag_bytes:].count_nonzero()) == 0
+        outs.append((out.cpu(), lse.cpu()))
+    for out, lse in outs:
+        assert_o_close(out.numpy(), O)
+        assert_lse_close(lse.double().numpy(), L)
+    assert torch.equal(outs[0][0], outs[1][0])
