@@ -209,7 +209,7 @@ class Case:
                                            self.ws, stream=self.stream)
 
     def launches(self) -> int:
-        """Kernels one call launches (the balanced call also clears its counters)."""
+        """Kernels one call launches."""
         return 1 if (self.balanced or self.S == 1) else 2
 
     def schedule(self) -> str:
@@ -329,14 +329,18 @@ def run_gpu(args):
     if not args.no_sweep:
         for s_q in SWEEP_SQ:
             inp = inp_main if s_q == args.s_q else inputs(s_q)
-            # forced (token, split) grids, then the planner's choice (S = 0: the
-            # balanced schedule of the one-shot call)
-            for S in list(SWEEP_S) + [0]:
+            # forced (token, split) grids, the planner's choice (S = 0) and the
+            # balanced one-shot schedule where it applies (S = -1)
+            for S in list(SWEEP_S) + [0, -1]:
                 c = Case(b, torch, kv, inp, S)
+                if S == -1 and not c.balanced:
+                    del c
+                    continue
                 us = statistics.fmean(c.time(c.g_call, args.sweep_steps, 3, flush))
                 ks = statistics.fmean(c.time(c.g_kernel, args.sweep_steps, 3, flush))
                 cb = balanced_bytes(s_q, c.plan.num_sms) if c.balanced else algorithmic_bytes(s_q, S, "call")
-                sweep.append({"s_q": s_q, "num_splits": S if S else "planner", "planner": S == 0,
+                sweep.append({"s_q": s_q, "num_splits": {0: "planner", -1: "balanced"}.get(S, S),
+                              "planner": S == 0,
                               "schedule": c.schedule(), "us_per_call": round(us, 2),
                               "split_kernel_us": round(ks, 2), "alg_bytes": cb,
                               "gb_s": round(cb / (us * 1e-6) / 1e9, 1),
@@ -410,7 +414,9 @@ def known_traffic(s_q, S):
         h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     except OSError:
         return None
-    table = {}   # (source hash, s_q, S) -> dram bytes per launch
+    table = {   # (source hash, s_q, S) -> dram bytes per launch (profiles/mla_decode_kernel_sq96_direct.md)
+        ("889e27a4e83ea856", 96, 1): 55_534_592,
+    }
     return table.get((h, s_q, S))
 
 

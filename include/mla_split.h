@@ -76,6 +76,7 @@ extern "C" {
 
 /* Largest split count any plan may use. */
 #define MLA_MAX_SPLITS 64
+#define MLA_FORCE_BALANCED (-1)   /* force_splits value: the balanced schedule wherever it applies */
 
 /* ======================================================================= *
  *  Sparse MLA decode                                                       *
@@ -138,13 +139,16 @@ typedef struct {
  * Automatic rule: among split counts S with s_q_max * S <= num_sms (at least 1),
  * take the smallest S that reaches the fewest blocks per split, ceil(num_blocks / S).
  * With force_splits == 0 the plan also enables the balanced schedule for the
- * one-shot call when it beats that grid at s_q_max: with per = ceil(s_q_max *
- * num_blocks / num_sms), when 2 <= per < ceil(s_q_max * S / num_sms) *
- * ceil(num_blocks / S) (the most blocks any SM walks under the grid) and
- * ceil(num_blocks / per) + 1 <= 32. It then sets balanced_ctas = min(num_sms,
- * s_q_max * num_blocks) and sizes the workspace for both schedules: the larger
- * of the two partial areas plus the balanced counters at the end. With
- * force_splits > 0 the one-shot call runs the (token, split) jobs.
+ * one-shot call when it is expected to beat that grid at s_q_max: with per =
+ * ceil(s_q_max * num_blocks / num_sms), when 2 <= per, ceil(num_blocks / per) + 1
+ * <= 32 and per + 6 < ceil(s_q_max * S / num_sms) * ceil(num_blocks / S) (the
+ * most blocks any SM walks under the grid; 6 blocks is the schedule's measured
+ * cost of job boundaries and merging). force_splits == MLA_FORCE_BALANCED keeps
+ * the automatic S and enables the balanced schedule whenever the first two
+ * conditions hold. Enabling it sets balanced_ctas = min(num_sms, s_q_max *
+ * num_blocks) and sizes the workspace for both schedules: the larger of the two
+ * partial areas plus the balanced counters at the end. With force_splits > 0
+ * the one-shot call runs the (token, split) jobs.
  * Errors: MLA_ERR_UNSUPPORTED unless h_q == 64, d_qk == 576, d_v == 512;
  *         MLA_ERR_INVALID_ARG for s_q_max < 1, topk < 1, out == NULL, or bad split counts. */
 MLA_API int mla_decode_plan(int s_q_max, int h_q, int d_qk, int d_v, int topk,

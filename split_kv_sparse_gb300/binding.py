@@ -21,6 +21,7 @@ MLA_STATUS_TIMEOUT = 0x1
 MLA_STATUS_BAD_SHAPE = 0x2
 MLA_STATUS_BAD_ALIGN = 0x4
 MLA_MAX_SPLITS = 64
+MLA_FORCE_BALANCED = -1
 OUT_DTYPES = {"f32": MLA_OUT_F32, "bf16": MLA_OUT_BF16, "e4m3": MLA_OUT_E4M3}
 
 # Every symbol the header declares (checked by the library-load test).

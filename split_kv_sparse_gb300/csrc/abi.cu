@@ -113,6 +113,12 @@ int64_t balanced_per(int64_t s_q, int nb, int num_sms) {
 int64_t uniform_makespan(int64_t s_q, int nb, int S, int num_sms) {
   return (s_q * S + num_sms - 1) / num_sms * ((nb + S - 1) / S);
 }
+// What the balanced schedule costs beyond its blocks, in 64-row block times: a
+// CTA's job boundary (the piece's partial store before the next token's softmax
+// can start) and the last piece's merge. Measured on GB300 at s_q = 96 and 384
+// (topk 640): the schedule ran as slow as per + 5.5 to per + 5.7 blocks of the
+// uniform grid.
+constexpr int64_t kBalancedOverheadBlocks = 6;
 
 BalancedLayout balanced_layout(int ctas, int s_q_max) {
   BalancedLayout L;
@@ -201,7 +207,9 @@ int mla_decode_plan(int s_q_max, int h_q, int d_qk, int d_v, int topk, int num_s
   if (h_q != kMlaHeads || d_qk != kMlaDqk || d_v != kMlaDv) return MLA_ERR_UNSUPPORTED;
   if (s_q_max < 1 || topk < 1 || num_sms < 0) return MLA_ERR_INVALID_ARG;
   if (max_splits < 0 || max_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID_ARG;
-  if (force_splits < 0 || force_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID_ARG;
+  if (force_splits < MLA_FORCE_BALANCED || force_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID_ARG;
+  const bool want_balanced = force_splits == MLA_FORCE_BALANCED;
+  if (want_balanced) force_splits = 0;
   if (num_sms == 0) {
     DeviceState* d = nullptr;
     const int st = device_state(&d);
@@ -241,7 +249,8 @@ int mla_decode_plan(int s_q_max, int h_q, int d_qk, int d_v, int topk, int num_s
     out->workspace_bytes = round_up(out->lse_acc_offset + out->lse_acc_bytes, 256);
   }
   const int64_t per = balanced_per(s_q_max, nblk, num_sms);
-  if (force_splits == 0 && per > 0 && per < uniform_makespan(s_q_max, nblk, S, num_sms)) {
+  if (force_splits == 0 && per > 0 &&
+      (want_balanced || per + kBalancedOverheadBlocks < uniform_makespan(s_q_max, nblk, S, num_sms))) {
     // the one-shot call spreads all tokens' blocks over at most num_sms CTAs
     const int64_t units = static_cast<int64_t>(s_q_max) * nblk;
     out->balanced_ctas = static_cast<int32_t>(std::min<int64_t>(units, num_sms));

@@ -35,9 +35,9 @@ def check_status():
 def run_mla(inp, S: int, out_dtype: str = "f32", inv_scale: float = 1.0, with_amax: bool = False,
             keep_workspace: bool = False, num_sms: int = 0):
     """Whole decode step through mla_sparse_decode: S > 0 forces the (token,
-    split) jobs (the direct path when S == 1); S == 0 takes the automatic plan,
-    whose one-shot call runs the balanced schedule over num_sms SMs (0 = the
-    device's)."""
+    split) jobs (the direct path when S == 1); S == 0 takes the automatic plan;
+    S == MLA_FORCE_BALANCED runs the balanced schedule where it applies. num_sms
+    is the SM count the plan spreads the work over (0 = the device's)."""
     dev = torch.device("cuda")
     q, kv, idx = inp.q.to(dev), inp.kv.to(dev), inp.idx.to(dev)
     sink = inp.sink.to(dev) if inp.sink is not None else None

@@ -87,7 +87,8 @@ def test_plan_is_deterministic_and_follows_rule():
                 uni = 0 if S == 1 else ru(ru(S * s_q * 64 * 512 * 4) + S * s_q * 64 * 4)
                 per = -(-(s_q * nblk) // sms)
                 mk_uniform = -(-(s_q * S) // sms) * -(-nblk // S)
-                enabled = 2 <= per < mk_uniform and -(-nblk // per) + 1 <= 32
+                applies = per >= 2 and -(-nblk // per) + 1 <= 32
+                enabled = applies and per + 6 < mk_uniform
                 C = min(sms, s_q * nblk) if enabled else 0
                 # partials [2C][64][512] then LSEs [2C][64]; counters [s_q] and
                 # flags [2C] at the very end, past both schedules' partials
@@ -97,6 +98,9 @@ def test_plan_is_deterministic_and_follows_rule():
                 assert p1.workspace_bytes == (max(uni, partials) + flags if enabled else uni)
                 pf = b.mla_decode_plan(s_q, topk, num_sms=sms, force_splits=S)
                 assert pf.balanced_ctas == 0 and (pf.workspace_bytes == 0) == (S == 1)
+                pb = b.mla_decode_plan(s_q, topk, num_sms=sms, force_splits=b.MLA_FORCE_BALANCED)
+                assert pb.num_splits == S
+                assert pb.balanced_ctas == (min(sms, s_q * nblk) if applies else 0)
 
 
 def test_plan_examples():
@@ -110,7 +114,7 @@ def test_plan_examples():
 
 @pytest.mark.parametrize("kw,code", [
     (dict(h_q=32), 2), (dict(d_qk=512), 2), (dict(d_v=576), 2),
-    (dict(force_splits=65), 1), (dict(max_splits=-1), 1), (dict(num_sms=-1), 1),
+    (dict(force_splits=65), 1), (dict(force_splits=-2), 1), (dict(max_splits=-1), 1), (dict(num_sms=-1), 1),
 ])
 def test_plan_errors(kw, code):
     with pytest.raises(b.SplitKVError) as e:
@@ -230,9 +234,13 @@ def test_balanced_schedule_covers_every_block_once():
 
 def test_balanced_schedule_choice_examples():
     # s_q = 96, 384 on 152 SMs: the uniform grid walks 10 and 30 blocks on its
-    # busiest SM, the balanced schedule 7 and 26
-    assert b.mla_decode_plan(96, 640, num_sms=152).balanced_ctas == 152
-    assert b.mla_decode_plan(384, 640, num_sms=152).balanced_ctas == 152
+    # busiest SM, the balanced schedule 7 and 26 plus its overhead of 6
+    assert b.mla_decode_plan(96, 640, num_sms=152).balanced_ctas == 0
+    assert b.mla_decode_plan(384, 640, num_sms=152).balanced_ctas == 0
+    assert b.mla_decode_plan(96, 640, num_sms=152, force_splits=-1).balanced_ctas == 152
+    assert b.mla_decode_plan(384, 640, num_sms=152, force_splits=-1).balanced_ctas == 152
+    # s_q = 160: two waves of 10 blocks against 11 + 6
+    assert b.mla_decode_plan(160, 640, num_sms=152).balanced_ctas == 152
     # s_q = 1, 16: the grid already spreads as evenly (10 x 1 block, 80 x 2 blocks)
     assert b.mla_decode_plan(1, 640, num_sms=152).balanced_ctas == 0
     assert b.mla_decode_plan(16, 640, num_sms=152).balanced_ctas == 0

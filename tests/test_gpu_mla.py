@@ -229,13 +229,15 @@ def test_host_errors_on_gpu():
 
 # ---- full-size workload, in the bench's launch configuration, sampled tokens ----------
 
+@pytest.mark.parametrize("S", [0, b.MLA_FORCE_BALANCED])
 @pytest.mark.parametrize("s_q", [96, 384])
-def test_full_size_sampled(s_q):
-    """The bench's configuration: the automatic plan (balanced schedule over the
-    device's SMs), FP8 output; tokens sampled so the oracle finishes in seconds."""
+def test_full_size_sampled(s_q, S):
+    """The bench's configuration: the automatic plan, and the balanced schedule
+    over the device's SMs, FP8 output; tokens sampled so the oracle finishes in
+    seconds."""
     inp = wl.mla_inputs(s_q, 131072, 640, seed=0)
-    r = run_mla(inp, 0, out_dtype="e4m3", inv_scale=64.0)
-    assert r["plan"].balanced_ctas > 0
+    r = run_mla(inp, S, out_dtype="e4m3", inv_scale=64.0)
+    assert (r["plan"].balanced_ctas > 0) == (S == b.MLA_FORCE_BALANCED)
     rng = np.random.default_rng(s_q)
     ts = np.sort(rng.choice(s_q, 6, replace=False))
     sub = wl.MlaInputs(q=inp.q[ts], kv=inp.kv, idx=inp.idx[ts], sink=None, sm_scale=inp.sm_scale)
@@ -269,7 +271,7 @@ def test_balanced_schedule_matches_oracle(s_q, topk, num_sms, with_sink):
     inp = wl.mla_inputs(s_q, 32768, topk, seed=300 + s_q * 7 + num_sms, with_sink=with_sink,
                         index_mode="window" if topk >= 128 else "uniform")
     O, L = oracle_mla(inp)
-    r = run_mla(inp, 0, num_sms=num_sms)
+    r = run_mla(inp, b.MLA_FORCE_BALANCED, num_sms=num_sms)
     assert r["plan"].balanced_ctas > 0
     assert_o_close(r["out"].numpy(), O)
     assert_lse_close(r["lse"], L)
@@ -281,7 +283,8 @@ def test_balanced_schedule_casts_and_amax(out_dtype):
     max over both."""
     inp = wl.mla_inputs(5, 32768, 640, seed=41, v_mean=1.0, with_sink=True)
     O, L = oracle_mla(inp)
-    r = run_mla(inp, 0, out_dtype=out_dtype, inv_scale=64.0, with_amax=True, num_sms=4)   # 50 over 4
+    r = run_mla(inp, b.MLA_FORCE_BALANCED, out_dtype=out_dtype, inv_scale=64.0, with_amax=True,
+                num_sms=4)   # 50 over 4
     assert_cast_close(r["out"], O, out_dtype, 64.0)
     assert_lse_close(r["lse"], L)
     assert abs(r["amax"] - float(np.abs(O).max())) <= 2e-3 * float(np.abs(O).max())
@@ -298,7 +301,7 @@ def test_balanced_schedule_padding_and_empty_pieces():
     idx[2, 100:110] = 40000        # out of range: masked
     inp = wl.MlaInputs(q=inp.q, kv=inp.kv, idx=idx, sink=None, sm_scale=inp.sm_scale)
     O, L = oracle_mla(inp)
-    r = run_mla(inp, 0, num_sms=3)       # 40 blocks over 3 CTAs (14, 13, 13)
+    r = run_mla(inp, b.MLA_FORCE_BALANCED, num_sms=3)       # 40 blocks over 3 CTAs (14, 13, 13)
     assert r["plan"].balanced_ctas > 0
     assert_o_close(r["out"].numpy(), O)
     assert_lse_close(r["lse"], L)
@@ -311,7 +314,7 @@ def test_balanced_schedule_repeated_calls():
     inp = wl.mla_inputs(3, 32768, 640, seed=47, with_sink=True)
     O, L = oracle_mla(inp)
     dev = torch.device("cuda")
-    plan = b.mla_decode_plan(3, 640, num_sms=4)
+    plan = b.mla_decode_plan(3, 640, num_sms=4, force_splits=b.MLA_FORCE_BALANCED)
     assert plan.balanced_ctas > 0
     ws = torch.full((plan.workspace_bytes,), 0xA5, dtype=torch.uint8, device=dev)
     b.mla_workspace_init(plan, ws)
