@@ -103,6 +103,10 @@ typedef struct {
   int32_t num_sms;      /* SM count the split choice was made for                  */
   int32_t balanced_ctas; /* > 0: mla_sparse_decode runs the balanced schedule with at
                             most this many CTAs (see below); 0: the (token, split) jobs */
+  int32_t dim_groups;   /* CTAs per (token, split) job: 1, 2 or 4. Each computes the
+                           job's scores and softmax and 512/dim_groups of its output
+                           dims, so PV and the output stores of one job spread over
+                           dim_groups SMs (used when s_q_max * num_splits leaves SMs idle) */
   uint64_t o_acc_bytes;     /* num_splits * s_q_max * h_q * d_v * 4                */
   uint64_t lse_acc_offset;  /* o_acc_bytes rounded up to 256                       */
   uint64_t lse_acc_bytes;   /* num_splits * s_q_max * h_q * 4                      */
@@ -138,6 +142,7 @@ typedef struct {
  *                even above num_blocks (the extra splits are empty).
  * Automatic rule: among split counts S with s_q_max * S <= num_sms (at least 1),
  * take the smallest S that reaches the fewest blocks per split, ceil(num_blocks / S).
+ * dim_groups is the largest of 4, 2, 1 with s_q_max * S * dim_groups <= num_sms.
  * With force_splits == 0 the plan also enables the balanced schedule for the
  * one-shot call when it is expected to beat that grid at s_q_max: with per =
  * ceil(s_q_max * num_blocks / num_sms), when 2 <= per, ceil(num_blocks / per) + 1

@@ -43,7 +43,8 @@ class MlaPlan(ctypes.Structure):
     _fields_ = [("s_q_max", ctypes.c_int32), ("h_q", ctypes.c_int32), ("d_qk", ctypes.c_int32),
                 ("d_v", ctypes.c_int32), ("topk", ctypes.c_int32), ("block_rows", ctypes.c_int32),
                 ("num_blocks", ctypes.c_int32), ("num_splits", ctypes.c_int32), ("num_sms", ctypes.c_int32),
-                ("balanced_ctas", ctypes.c_int32), ("o_acc_bytes", ctypes.c_uint64),
+                ("balanced_ctas", ctypes.c_int32), ("dim_groups", ctypes.c_int32),
+                ("o_acc_bytes", ctypes.c_uint64),
                 ("lse_acc_offset", ctypes.c_uint64), ("lse_acc_bytes", ctypes.c_uint64),
                 ("workspace_bytes", ctypes.c_uint64)]
 

@@ -119,6 +119,13 @@ int64_t uniform_makespan(int64_t s_q, int nb, int S, int num_sms) {
 // (topk 640): the schedule ran as slow as per + 5.5 to per + 5.7 blocks of the
 // uniform grid.
 constexpr int64_t kBalancedOverheadBlocks = 6;
+// CTAs per (token, split) job: the largest of 4, 2, 1 that still fits `jobs`
+// jobs on num_sms SMs at one CTA each.
+int dim_groups_for(int64_t jobs, int num_sms) {
+  for (int d = 4; d > 1; d /= 2)
+    if (jobs * d <= num_sms) return d;
+  return 1;
+}
 
 BalancedLayout balanced_layout(int ctas, int s_q_max) {
   BalancedLayout L;
@@ -242,6 +249,7 @@ int mla_decode_plan(int s_q_max, int h_q, int d_qk, int d_v, int topk, int num_s
   out->num_blocks = nblk;
   out->num_splits = S;
   out->num_sms = num_sms;
+  out->dim_groups = dim_groups_for(static_cast<int64_t>(s_q_max) * S, num_sms);
   if (S > 1) {
     out->o_acc_bytes = static_cast<uint64_t>(S) * s_q_max * h_q * d_v * 4ull;
     out->lse_acc_offset = round_up(out->o_acc_bytes, 256);
@@ -280,6 +288,7 @@ int mla_sparse_decode_split(const mla_plan_t* plan, int s_q, const void* q, cons
   a.n_kv = static_cast<int>(n_kv);
   a.num_splits = plan->num_splits;
   a.num_blocks = plan->num_blocks;
+  a.dim_groups = plan->dim_groups;
   a.sched = 0;
   a.direct_whole = 0;
   a.scale_log2 = sm_scale * 1.4426950408889634f;
@@ -364,6 +373,7 @@ int mla_decode_balanced(const mla_plan_t* plan, int s_q, const void* q, const vo
   a.n_kv = static_cast<int>(n_kv);
   a.num_splits = 1;
   a.num_blocks = nb;
+  a.dim_groups = 1;
   a.sched = 1;
   a.num_ctas = P;
   a.direct_whole = 1;
@@ -402,9 +412,14 @@ int mla_split_combine(const mla_plan_t* plan, int s_q, const void* workspace, co
                           stream);
 }
 
-int mla_sparse_decode_direct(int s_q, int topk, const void* q, const void* kv, int64_t n_kv, const int32_t* idx,
-                             float sm_scale, const float* sink, int out_dtype, float out_inv_scale, void* out,
-                             float* lse_out, float* amax_out, void* stream) {
+}  // extern "C"
+
+namespace {
+// The unsplit launch with `dim_groups` CTAs per token (0: chosen from the
+// device's SM count).
+int mla_direct_impl(int s_q, int topk, const void* q, const void* kv, int64_t n_kv, const int32_t* idx,
+                    float sm_scale, const float* sink, int out_dtype, float out_inv_scale, void* out, float* lse_out,
+                    float* amax_out, int dim_groups, void* stream) {
   int st = check_mla_inputs(s_q, topk, q, kv, n_kv, idx, sm_scale);
   if (st != MLA_OK) return st;
   if (out == nullptr || !aligned(out, 16) || !valid_out_dtype(out_dtype)) return MLA_ERR_INVALID_ARG;
@@ -425,6 +440,7 @@ int mla_sparse_decode_direct(int s_q, int topk, const void* q, const void* kv, i
   a.n_kv = static_cast<int>(n_kv);
   a.num_splits = 1;
   a.num_blocks = (topk + kMlaBlockRows - 1) / kMlaBlockRows;
+  a.dim_groups = dim_groups > 0 ? dim_groups : dim_groups_for(s_q, dev->num_sms);
   a.sched = 0;
   a.direct_whole = 1;
   a.scale_log2 = sm_scale * 1.4426950408889634f;
@@ -438,6 +454,16 @@ int mla_sparse_decode_direct(int s_q, int topk, const void* q, const void* kv, i
   a.wait_limit_ns = kWaitLimitNs;
   return cuda_status(skv::launch_mla_decode(tq, a, cs));
 }
+}  // namespace
+
+extern "C" {
+
+int mla_sparse_decode_direct(int s_q, int topk, const void* q, const void* kv, int64_t n_kv, const int32_t* idx,
+                             float sm_scale, const float* sink, int out_dtype, float out_inv_scale, void* out,
+                             float* lse_out, float* amax_out, void* stream) {
+  return mla_direct_impl(s_q, topk, q, kv, n_kv, idx, sm_scale, sink, out_dtype, out_inv_scale, out, lse_out,
+                         amax_out, 0, stream);
+}
 
 int mla_sparse_decode(const mla_plan_t* plan, int s_q, const void* q, const void* kv, int64_t n_kv,
                       const int32_t* idx, float sm_scale, const float* sink, int out_dtype, float out_inv_scale,
@@ -449,8 +475,8 @@ int mla_sparse_decode(const mla_plan_t* plan, int s_q, const void* q, const void
                                amax_out, workspace, stream);
   if (plan->num_splits == 1) {
     if (s_q > plan->s_q_max) return MLA_ERR_INVALID_ARG;
-    return mla_sparse_decode_direct(s_q, plan->topk, q, kv, n_kv, idx, sm_scale, sink, out_dtype, out_inv_scale,
-                                    out, lse_out, amax_out, stream);
+    return mla_direct_impl(s_q, plan->topk, q, kv, n_kv, idx, sm_scale, sink, out_dtype, out_inv_scale, out,
+                           lse_out, amax_out, plan->dim_groups, stream);
   }
   // validate the combine's own arguments before launching anything
   if (out == nullptr || !aligned(out, 16) || !valid_out_dtype(out_dtype)) return MLA_ERR_INVALID_ARG;

@@ -6,8 +6,9 @@
 // One warp per (output row, 128-wide column slice), so even one decode token
 // (64 rows x 4 slices of the 512-wide O) spreads over 32 CTAs: the lanes read
 // the row's split LSEs, take M = max_s LSE_s and w_s = 2^(LSE_s - M), then
-// stream their slice of the fp32 partials of the splits with w_s > 0 (empty
-// splits are never read) as float4 loads, four splits in flight at a time.
+// stream their slice of the fp32 partials as float4 loads, 8 or 16 splits in
+// flight at a time (the first batch requested together with the LSEs), skipping
+// every split with w_s = 0 (empty).
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -31,10 +32,12 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-template <int D>
-__global__ void __launch_bounds__(kWarps * 32) combine_kernel(const CombineArgs a) {
+// kBatch: splits' slices in flight at a time. 8 keeps a thread within 64
+// registers, so 32 warps fit an SM and a few thousand rows run in one wave; 16
+// (more registers) serves combines over more than 8 splits.
+template <int D, int kBatch>
+__global__ void __launch_bounds__(kWarps * 32, kBatch == 8 ? 4 : 1) combine_kernel(const CombineArgs a) {
   constexpr int kSlices = D / 128;   // 128 floats = one float4 per lane
-  constexpr int V = 1;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int item = blockIdx.x * kWarps + warp;
@@ -45,6 +48,15 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const CombineArgs 
   const int S = a.num_splits;
   const size_t rows = static_cast<size_t>(a.rows);
 
+  auto src_of = [&](int s) {
+    return reinterpret_cast<const float4*>(a.o_acc + (static_cast<size_t>(s) * rows + row) * D + slice * 128) + lane;
+  };
+  // The first kBatch splits' slices are requested together with the LSEs, before
+  // the weights are known (one memory round trip for S <= kBatch); a split whose
+  // weight turns out 0 (empty) is then skipped, whatever its slice holds.
+  float4 x[kBatch];
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) x[u] = u < S ? __ldcs(src_of(u)) : make_float4(0.f, 0.f, 0.f, 0.f);
   const float l0 = lane < S ? a.lse_acc[static_cast<size_t>(lane) * rows + row] : -INFINITY;
   const float l1 = lane + 32 < S ? a.lse_acc[static_cast<size_t>(lane + 32) * rows + row] : -INFINITY;
   const float M = warp_max(fmaxf(l0, l1));
@@ -52,36 +64,31 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const CombineArgs 
   const float w0 = (l0 == -INFINITY) ? 0.f : exp2f(l0 - M);
   const float w1 = (l1 == -INFINITY) ? 0.f : exp2f(l1 - M);
   const float wsum = warp_sum(w0 + w1);
+  auto weight = [&](int s) { return __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31); };
 
-  float4 acc[V];
-#pragma unroll
-  for (int v = 0; v < V; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (!empty) {
-#pragma unroll 1
-    for (int s0 = 0; s0 < S; s0 += 4) {
-      float ws[4];
-      float4 x[4][V];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int s = s0 + u;
-        const float w = (s < S) ? __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31) : 0.f;
-        ws[u] = w;
-        const float4* src =
-            reinterpret_cast<const float4*>(a.o_acc + (static_cast<size_t>(s) * rows + row) * D + slice * 128);
-#pragma unroll
-        for (int v = 0; v < V; ++v)
-          x[u][v] = (w != 0.f) ? __ldcs(src + lane + 32 * v) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int v = 0; v < V; ++v) {
-          acc[v].x = fmaf(ws[u], x[u][v].x, acc[v].x);
-          acc[v].y = fmaf(ws[u], x[u][v].y, acc[v].y);
-          acc[v].z = fmaf(ws[u], x[u][v].z, acc[v].z);
-          acc[v].w = fmaf(ws[u], x[u][v].w, acc[v].w);
-        }
+  // acc = sum over s, in split order, of w_s * O_s
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto fold = [&](float w, const float4& v) {
+    if (w != 0.f) {
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
     }
+  };
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u)
+    if (u < S) fold(weight(u), x[u]);
+#pragma unroll 1
+  for (int s0 = kBatch; s0 < S; s0 += kBatch) {
+    float ws[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      ws[u] = s0 + u < S ? weight(s0 + u) : 0.f;
+      x[u] = ws[u] != 0.f ? __ldcs(src_of(s0 + u)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) fold(ws[u], x[u]);
   }
   float inv = 0.f;
   if (!empty) {
@@ -89,36 +96,28 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const CombineArgs 
     if (a.sink != nullptr) den += exp2f(a.sink[row % a.heads] * kLog2e - M);
     inv = 1.f / den;
   }
-  float amax_l = 0.f;
-#pragma unroll
-  for (int v = 0; v < V; ++v) {
-    acc[v].x *= inv;
-    acc[v].y *= inv;
-    acc[v].z *= inv;
-    acc[v].w *= inv;
-    amax_l = fmaxf(amax_l, fmaxf(fmaxf(fabsf(acc[v].x), fabsf(acc[v].y)),
-                                 fmaxf(fabsf(acc[v].z), fabsf(acc[v].w))));
-  }
+  acc.x *= inv;
+  acc.y *= inv;
+  acc.z *= inv;
+  acc.w *= inv;
+  float amax_l = fmaxf(fmaxf(fabsf(acc.x), fabsf(acc.y)), fmaxf(fabsf(acc.z), fabsf(acc.w)));
   const size_t base = static_cast<size_t>(row) * D + slice * 128;
-#pragma unroll
-  for (int v = 0; v < V; ++v) {
-    const int e = 4 * (lane + 32 * v);
-    if (a.out_dtype == 0) {
-      reinterpret_cast<float4*>(static_cast<float*>(a.out) + base)[lane + 32 * v] = acc[v];
-    } else if (a.out_dtype == 1) {
-      __nv_bfloat162 lo = __floats2bfloat162_rn(acc[v].x, acc[v].y);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(acc[v].z, acc[v].w);
-      uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&lo);
-      pk.y = *reinterpret_cast<uint32_t*>(&hi);
-      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + base + e) = pk;
-    } else {
-      const float2 lo = make_float2(acc[v].x * a.inv_scale, acc[v].y * a.inv_scale);
-      const float2 hi = make_float2(acc[v].z * a.inv_scale, acc[v].w * a.inv_scale);
-      const uint32_t c01 = __nv_cvt_float2_to_fp8x2(lo, __NV_SATFINITE, __NV_E4M3);
-      const uint32_t c23 = __nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, __NV_E4M3);
-      *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.out) + base + e) = (c01 & 0xFFFFu) | (c23 << 16);
-    }
+  const int e = 4 * lane;
+  if (a.out_dtype == 0) {
+    reinterpret_cast<float4*>(static_cast<float*>(a.out) + base)[lane] = acc;
+  } else if (a.out_dtype == 1) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + base + e) = pk;
+  } else {
+    const float2 lo = make_float2(acc.x * a.inv_scale, acc.y * a.inv_scale);
+    const float2 hi = make_float2(acc.z * a.inv_scale, acc.w * a.inv_scale);
+    const uint32_t c01 = __nv_cvt_float2_to_fp8x2(lo, __NV_SATFINITE, __NV_E4M3);
+    const uint32_t c23 = __nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, __NV_E4M3);
+    *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.out) + base + e) = (c01 & 0xFFFFu) | (c23 << 16);
   }
   if (slice == 0 && lane == 0 && a.lse_out != nullptr) a.lse_out[row] = empty ? -INFINITY : M + log2f(wsum);
   if (a.amax != nullptr) {
@@ -145,8 +144,9 @@ cudaError_t launch_combine(const CombineArgs& a, bool zero_amax, bool pdl, cudaS
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (a.d == 512) return cudaLaunchKernelEx(&cfg, combine_kernel<512>, a);
-  if (a.d == 128) return cudaLaunchKernelEx(&cfg, combine_kernel<128>, a);
+  const bool wide = a.num_splits > 8;
+  if (a.d == 512) return cudaLaunchKernelEx(&cfg, wide ? combine_kernel<512, 16> : combine_kernel<512, 8>, a);
+  if (a.d == 128) return cudaLaunchKernelEx(&cfg, wide ? combine_kernel<128, 16> : combine_kernel<128, 8>, a);
   return cudaErrorInvalidValue;
 }
 

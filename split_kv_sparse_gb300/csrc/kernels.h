@@ -22,7 +22,10 @@ struct MlaArgs {
   int n_kv;
   int num_splits;       // uniform schedule: splits per token (1 for the direct path)
   int num_blocks;       // ceil(topk / 64): 64-row blocks per token
-  int sched;            // 0: one (token, split) job per CTA, grid s_q * num_splits;
+  int dim_groups;       // uniform schedule: CTAs per (token, split) job (1, 2 or 4); CTA
+                        // g of a job computes the same scores and softmax and the
+                        // output dims [512 g / dim_groups, 512 (g + 1) / dim_groups)
+  int sched;            // 0: (token, split) jobs, grid s_q * num_splits * dim_groups;
                         // 1: balanced, the s_q * num_blocks blocks cut into num_ctas
                         //    near-equal contiguous ranges, one per CTA (grid num_ctas)
   int num_ctas;         // balanced schedule: CTAs (<= s_q * num_blocks)

@@ -135,6 +135,7 @@ enum : int { J_FINAL = 0, J_PARTIAL = 1, J_PIECE = 2 };
 //   J_PIECE    a piece of a token cut by the balanced schedule, partial slot `slot`.
 struct Job {
   int t, row0, row1, nsteps, kind, slot;
+  int q0, nq;   // the 128-dim tiles of O^T this CTA computes: q0 .. q0+nq-1
   size_t out_row;
 };
 
@@ -148,8 +149,11 @@ __device__ __forceinline__ int num_jobs(const MlaArgs& a) {
 __device__ __forceinline__ Job job_at(const MlaArgs& a, int j) {
   Job r;
   if (a.sched == 0) {
-    const int S = a.num_splits;
-    const int t = static_cast<int>(blockIdx.x) / S, s = static_cast<int>(blockIdx.x) - t * S;
+    const int S = a.num_splits, D = a.dim_groups;
+    const int job = static_cast<int>(blockIdx.x) / D, dg = static_cast<int>(blockIdx.x) - job * D;
+    const int t = job / S, s = job - t * S;
+    r.nq = 4 / D;
+    r.q0 = dg * r.nq;
     const int base = a.num_blocks / S, rem = a.num_blocks - base * S;
     const int blk0 = s * base + min(s, rem), nblk = base + (s < rem ? 1 : 0);
     r.t = t;
@@ -171,6 +175,8 @@ __device__ __forceinline__ Job job_at(const MlaArgs& a, int j) {
     r.nsteps = b1 - b0;
     r.kind = (b0 == 0 && b1 == nb) ? J_FINAL : J_PIECE;
     r.slot = 2 * p + (j == 0 ? 0 : 1);
+    r.q0 = 0;
+    r.nq = 4;
     r.out_row = r.kind == J_FINAL ? static_cast<size_t>(t) * kMlaHeads : static_cast<size_t>(r.slot) * kMlaHeads;
   }
   return r;
@@ -217,12 +223,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Job j0 = job_at(a, 0);
 
   if (j0.nsteps == 0) {
-    // A split with no block of its own (uniform schedule only): O = 0, LSE = -inf.
+    // A split with no block of its own (uniform schedule only): O = 0 over this
+    // CTA's dims, LSE = -inf (written by the CTA of the first dims).
     grid_launch_dependents();
     float4* o = reinterpret_cast<float4*>(a.o_acc + j0.out_row * kMlaDv);
-    for (int i = threadIdx.x; i < kMlaHeads * kMlaDv / 4; i += kThreads)
-      o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (threadIdx.x < kMlaHeads) a.lse_acc[j0.out_row + threadIdx.x] = -INFINITY;
+    const int per_head = 32 * j0.nq;   // float4s of one head row this CTA owns
+    for (int i = threadIdx.x; i < kMlaHeads * per_head; i += kThreads) {
+      const int h = i / per_head;
+      o[h * (kMlaDv / 4) + 32 * j0.q0 + (i - h * per_head)] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (j0.q0 == 0 && threadIdx.x < kMlaHeads) a.lse_acc[j0.out_row + threadIdx.x] = -INFINITY;
     return;
   }
   if ((sbase & 1023u) != 0) {
@@ -399,15 +409,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       // PV(g) with P_hi (part 0) or P_lo (part 1): for each 128-dim tile j of V,
       // K = the 64 rows in 4 steps of 16 (2048 B of the MN-major V^T, 32 B of
       // the K-major P^T each); `first` starts a new O^T (first step of a job).
+      // Only the CTA's own tiles tq0 .. tq1-1 (all four unless the job's dims are
+      // spread over several CTAs).
+      const int tq0 = j0.q0, tq1 = j0.q0 + j0.nq;
       auto pv_part = [&](int g, int part, bool first) {
         const uint64_t av = d_v0 + (g & 1) * kHalfStep;
         const uint64_t bp = part ? d_plo : d_phi0 + (g & 1) * kHalfStep;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int j = 0; j < 4; ++j) {
+          if (j < tq0 || j >= tq1) continue;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_f16(tmem + 64 * j, av + (2 * j * kSlotBytes + kk * 2048) / 16, bp + 2 * kk, kIdescPV,
                     (!first || part > 0 || kk > 0));
+        }
       };
       int total = 0;
 #pragma unroll 1
@@ -669,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           if (!bad) {
 #pragma unroll 1
-            for (int q = 0; q < 8; ++q) {   // 4 O^T tiles x 2 halves of 32 head columns
+            for (int q = 2 * jb.q0; q < 2 * (jb.q0 + jb.nq); ++q) {   // own O^T tiles x 2 halves of 32 heads
               const int c0 = 32 * (q & 1);
               if (((resc >> c0) & 0xffffffffull) == 0) continue;
               uint32_t o[32];
@@ -713,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (jb.kind == J_FINAL && a.sink != nullptr && lsum > 0.f) den += exp2f(a.sink[head] * kLog2e - m_run);
         hs[head] = lsum > 0.f ? 1.f / den : 0.f;
         hs[64 + head] = lse_own;
-        if (!bad) {
+        if (!bad && jb.q0 == 0) {   // (every CTA of a job has the same LSE)
           if (jb.kind == J_FINAL) {
             if (a.lse_out != nullptr) a.lse_out[jb.out_row + head] = lse_own;
           } else {
@@ -845,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // merges it reads each thread's 64 values as 16-byte loads.
       const float* coef = reinterpret_cast<const float*>(smem + kOffPlo);
 #pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
+      for (int q = jb.q0; q < jb.q0 + jb.nq; ++q) {
         const int dl = 32 * sp + lane;   // dim within the tile
         const int d = 128 * q + dl;
         float v[64];
@@ -903,7 +918,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (q == 3) {
+        if (q == jb.q0 + jb.nq - 1) {
           // this warp's last read of O^T: the next job's first PV may overwrite it
           tc_fence_before();
           __syncwarp();
@@ -965,7 +980,9 @@ cudaError_t prepare_mla_kernels() {
 }
 
 cudaError_t launch_mla_decode(const CUtensorMap& tm_q, const MlaArgs& a, cudaStream_t stream) {
-  const dim3 grid(a.sched == 0 ? static_cast<unsigned>(a.s_q) * static_cast<unsigned>(a.num_splits)
+  if (a.sched == 0 && a.dim_groups != 1 && a.dim_groups != 2 && a.dim_groups != 4) return cudaErrorInvalidValue;
+  const dim3 grid(a.sched == 0 ? static_cast<unsigned>(a.s_q) * static_cast<unsigned>(a.num_splits) *
+                                     static_cast<unsigned>(a.dim_groups)
                                : static_cast<unsigned>(a.num_ctas));
   mla_decode_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, a);
   return cudaGetLastError();

@@ -95,6 +95,8 @@ def test_plan_is_deterministic_and_follows_rule():
                 partials = ru(ru(2 * C * 64 * 512 * 4) + 2 * C * 64 * 4)
                 flags = ru((s_q + 2 * C) * 4)
                 assert p1.balanced_ctas == C
+                # CTAs per (token, split) job: 4, 2 or 1, whatever still fits the SMs
+                assert p1.dim_groups == next(d for d in (4, 2, 1) if s_q * S * d <= sms or d == 1)
                 assert p1.workspace_bytes == (max(uni, partials) + flags if enabled else uni)
                 pf = b.mla_decode_plan(s_q, topk, num_sms=sms, force_splits=S)
                 assert pf.balanced_ctas == 0 and (pf.workspace_bytes == 0) == (S == 1)
@@ -105,6 +107,11 @@ def test_plan_is_deterministic_and_follows_rule():
 
 def test_plan_examples():
     assert b.mla_decode_plan(1, 640, num_sms=152).num_splits == 10
+    assert b.mla_decode_plan(1, 640, num_sms=152).dim_groups == 4      # 40 CTAs
+    assert b.mla_decode_plan(6, 640, num_sms=152).dim_groups == 2      # 120 CTAs
+    assert b.mla_decode_plan(16, 640, num_sms=152).dim_groups == 1     # 80 CTAs
+    assert b.mla_decode_plan(1, 640, num_sms=20).dim_groups == 2
+    assert b.mla_decode_plan(1, 640, num_sms=10).dim_groups == 1
     assert b.mla_decode_plan(16, 640, num_sms=152).num_splits == 5
     assert b.mla_decode_plan(96, 640, num_sms=152).num_splits == 1
     assert b.mla_decode_plan(1, 640, num_sms=152, max_splits=4).num_splits == 4

@@ -65,6 +65,25 @@ def test_split_partials_match_oracle(S):
         assert_lse_close(r["lse_acc"][s], L_s[s], what=f"partial LSE split {s}")
 
 
+@pytest.mark.parametrize("num_sms,D", [(152, 4), (40, 2), (20, 1)])
+@pytest.mark.parametrize("S", [1, 5])
+def test_dim_groups(S, num_sms, D):
+    """A (token, split) job's dims spread over D CTAs (chosen by the plan from the SM
+    count): partials, final O, LSE and amax as with one CTA per job."""
+    inp = wl.mla_inputs(4, 32768, 640, seed=61, v_mean=1.0, with_sink=True)
+    O, L = oracle_mla(inp)
+    r = run_mla(inp, S, out_dtype="bf16", with_amax=True, keep_workspace=True, num_sms=num_sms)
+    assert r["plan"].dim_groups == (D if S == 5 else max(d for d in (4, 2, 1) if 4 * d <= num_sms or d == 1))
+    assert_cast_close(r["out"], O, "bf16")
+    assert_lse_close(r["lse"], L)
+    assert abs(r["amax"] - float(np.abs(O).max())) <= 2e-3 * float(np.abs(O).max())
+    if S > 1:
+        O_s, L_s = om.split_partials(inp.q, inp.kv, inp.idx, inp.sm_scale, S)
+        for s in range(S):
+            assert_o_close(r["o_acc"][s], O_s[s], what=f"partial O split {s}")
+            assert_lse_close(r["lse_acc"][s], L_s[s], what=f"partial LSE split {s}")
+
+
 def test_degenerate_more_splits_than_blocks():
     """s_q = 4, topk = 64 with per-token valid counts in [1, 64] (rest -1), 16 splits over 1 block."""
     inp = wl.mla_inputs(4, 32768, 64, seed=3, index_mode="padded", with_sink=True)
