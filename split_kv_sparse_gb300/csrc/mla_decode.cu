@@ -182,30 +182,92 @@ __device__ __forceinline__ Job job_at(const MlaArgs& a, int j) {
   return r;
 }
 
-// Final rows of one O^T tile column set: v[c] for the 64 heads at dim d, cast
-// and stored; returns max |v|.
-__device__ __forceinline__ float store_final(const MlaArgs& a, int t, int d, const float (&v)[64]) {
+// 4x4 transpose of 32-bit words across the four lanes whose lane bits `b` and
+// `2b` differ (lane i holds m[0..3]; afterwards it holds word i of each of the
+// four lanes, in lane order). Two butterfly stages of two exchanges each.
+__device__ __forceinline__ void transpose4_words(uint32_t (&m)[4], int lane, int b) {
+  const bool hi1 = (lane & (2 * b)) != 0, hi0 = (lane & b) != 0;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {   // distance 2 in the quad: swap the off-diagonal 2x2 blocks
+    const uint32_t snd = hi1 ? m[r] : m[r + 2];
+    const uint32_t rcv = __shfl_xor_sync(0xffffffffu, snd, 2 * b);
+    if (hi1) m[r] = rcv; else m[r + 2] = rcv;
+  }
+#pragma unroll
+  for (int r = 0; r < 4; r += 2) {   // distance 1: swap within each 2x2 block
+    const uint32_t snd = hi0 ? m[r] : m[r + 1];
+    const uint32_t rcv = __shfl_xor_sync(0xffffffffu, snd, b);
+    if (hi0) m[r] = rcv; else m[r + 1] = rcv;
+  }
+}
+
+// Final rows of one O^T tile column set, cast and stored; returns max |v| of
+// this thread's values. Lane l of the warp holds v[c] = O[head c][d0 + l] for the
+// 64 heads; d0 (a multiple of 32) is the same for the whole warp, and every lane
+// of the warp calls this together. fp32 rows are stored as they are (each store
+// instruction covers 128 contiguous bytes of one head). bf16 and e4m3 codes are
+// first moved across lanes so that each lane holds 16 contiguous bytes of one
+// head row, stored with one 16-byte store per head and half-row group.
+__device__ __forceinline__ float store_final(const MlaArgs& a, int t, int d0, int lane, const float (&v)[64]) {
   float m = 0.f;
+#pragma unroll
+  for (int c = 0; c < 64; ++c) m = fmaxf(m, fabsf(v[c]));
+  const size_t row0 = static_cast<size_t>(t) * kMlaHeads * kMlaDv + d0;   // head 0, dim d0
   if (a.out_dtype == 0) {
-    float* st = static_cast<float*>(a.out) + static_cast<size_t>(t) * kMlaHeads * kMlaDv + d;
+    float* st = static_cast<float*>(a.out) + row0 + lane;
 #pragma unroll
-    for (int c = 0; c < 64; ++c) {
-      m = fmaxf(m, fabsf(v[c]));
-      st[c * kMlaDv] = v[c];
-    }
+    for (int c = 0; c < 64; ++c) st[c * kMlaDv] = v[c];
   } else if (a.out_dtype == 1) {
-    __nv_bfloat16* st = static_cast<__nv_bfloat16*>(a.out) + static_cast<size_t>(t) * kMlaHeads * kMlaDv + d;
+    // w[k]: heads 2k, 2k+1 at dim d0 + lane. Lane pairs swap halves, so lane
+    // 2i+j holds head 2k+j at dims 2i, 2i+1; then the four lanes 8h+2i'+j
+    // (i' = 0..3) transpose groups of four words, so lane 8h+2i'+j holds, for k
+    // = 4G+i', head 2k+j at dims 8h .. 8h+7.
+    const bool odd = (lane & 1) != 0;
 #pragma unroll
-    for (int c = 0; c < 64; ++c) {
-      m = fmaxf(m, fabsf(v[c]));
-      st[c * kMlaDv] = __float2bfloat16_rn(v[c]);
+    for (int G = 0; G < 8; ++G) {
+      uint32_t w[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int k = 4 * G + r;
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+        const uint32_t x = *reinterpret_cast<const uint32_t*>(&h2);
+        const uint32_t y = __shfl_xor_sync(0xffffffffu, x, 1);
+        // even lane: (own head 2k, partner's head 2k); odd: (partner's 2k+1, own 2k+1)
+        w[r] = odd ? __byte_perm(x, y, 0x3276) : __byte_perm(x, y, 0x5410);
+      }
+      transpose4_words(w, lane, 2);
+      const int ip = (lane >> 1) & 3, j = lane & 1, hq = lane >> 3;
+      const int head = 2 * (4 * G + ip) + j;
+      __nv_bfloat16* st = static_cast<__nv_bfloat16*>(a.out) + row0 + static_cast<size_t>(head) * kMlaDv + 8 * hq;
+      *reinterpret_cast<uint4*>(st) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   } else {
-    uint8_t* st = static_cast<uint8_t*>(a.out) + static_cast<size_t>(t) * kMlaHeads * kMlaDv + d;
+    // w[k]: heads 4k .. 4k+3 at dim d0 + lane, one byte each. A 4x4 byte
+    // transpose in each lane quad gives lane 4i+j head 4k+j at dims 4i .. 4i+3;
+    // then the four lanes 16h+4i'+j transpose groups of four words, so lane
+    // 16h+4i'+j holds, for k = 4G+i', head 4k+j at dims 16h .. 16h+15.
+    const int j = lane & 3;
+    const uint32_t sel1 = (j & 2) ? 0x3276u : 0x5410u;
+    const uint32_t sel2 = (j & 1) ? 0x3715u : 0x6240u;
 #pragma unroll
-    for (int c = 0; c < 64; ++c) {
-      m = fmaxf(m, fabsf(v[c]));
-      st[c * kMlaDv] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(v[c] * a.inv_scale, __NV_SATFINITE, __NV_E4M3));
+    for (int G = 0; G < 4; ++G) {
+      uint32_t w[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int k = 4 * G + r;
+        const uint32_t c01 = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * k] * a.inv_scale, v[4 * k + 1] * a.inv_scale),
+                                                      __NV_SATFINITE, __NV_E4M3);
+        const uint32_t c23 = __nv_cvt_float2_to_fp8x2(
+            make_float2(v[4 * k + 2] * a.inv_scale, v[4 * k + 3] * a.inv_scale), __NV_SATFINITE, __NV_E4M3);
+        uint32_t x = (c01 & 0xFFFFu) | (c23 << 16);
+        x = __byte_perm(x, __shfl_xor_sync(0xffffffffu, x, 2), sel1);
+        w[r] = __byte_perm(x, __shfl_xor_sync(0xffffffffu, x, 1), sel2);
+      }
+      transpose4_words(w, lane, 4);
+      const int ip = (lane >> 2) & 3, hq = lane >> 4;
+      const int head = 4 * (4 * G + ip) + j;
+      uint8_t* st = static_cast<uint8_t*>(a.out) + row0 + static_cast<size_t>(head) * kMlaDv + 16 * hq;
+      *reinterpret_cast<uint4*>(st) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
   return m;
@@ -929,7 +991,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (tid == 0 && q < 3) issue_stage(q + 1, 1);
         }
         if (to_final) {
-          amax_l = fmaxf(amax_l, store_final(a, jb.t, d, v));
+          amax_l = fmaxf(amax_l, store_final(a, jb.t, d - lane, lane, v));
         } else if (jb.kind == J_PIECE) {
           // [tile][k][dim in tile][4 heads]: a warp writes 512 contiguous bytes
           float4* st = reinterpret_cast<float4*>(a.o_acc + jb.out_row * kMlaDv) + q * 2048 + dl;
