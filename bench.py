@@ -415,7 +415,7 @@ def known_traffic(s_q, S):
     except OSError:
         return None
     table = {   # (source hash, s_q, S) -> dram bytes per launch (profiles/mla_decode_kernel_sq96_direct.md)
-        ("889e27a4e83ea856", 96, 1): 55_534_592,
+        ("33d4418cd7b0cfac", 96, 1): 55_557_632,
     }
     return table.get((h, s_q, S))
 
