@@ -247,6 +247,67 @@ class Case:
         return [1000.0 * e0.elapsed_time(e1) for e0, e1 in ev]
 
 
+DENSE_DESC = ("dense FP8 GQA split-KV SDPA decode: batch 8, 32 query / 8 KV heads, d=128, 1-16 query tokens per "
+              "sequence, causal KV lengths uniform in [1024,16384], e4m3 Q/K/V ~N(0,1) with per-tensor descales, "
+              "bf16 O, seed 0")
+
+
+def dense_bytes(sq, skv, h_q: int, h_kv: int, d: int, S: int) -> int:
+    """Algorithmic bytes of one dense call: every sequence's K and V (e4m3, all KV
+    heads), Q (e4m3), bf16 O and fp32 LSE; S > 1 adds the fp32 partial O + LSE,
+    written by the split kernel and read by the combine."""
+    total_q = int(sum(sq))
+    kv = 2 * int(sum(skv)) * h_kv * d
+    q = total_q * h_q * d
+    out = total_q * h_q * (d * 2 + 4)
+    partial = 2 * S * total_q * h_q * (d + 1) * 4 if S > 1 else 0
+    return kv + q + out + partial
+
+
+class DenseCase:
+    """Device inputs, a plan, outputs and CUDA graphs for one dense split count."""
+
+    def __init__(self, b, torch, inp, S):
+        self.b, self.torch, self.inp = b, torch, inp
+        dev = torch.device("cuda")
+        self.sq = (inp.cu_seqlens_q[1:] - inp.cu_seqlens_q[:-1]).tolist()
+        self.skv = (inp.cu_seqlens_kv[1:] - inp.cu_seqlens_kv[:-1]).tolist()
+        self.total_q, self.total_kv = int(inp.cu_seqlens_q[-1]), int(inp.cu_seqlens_kv[-1])
+        self.plan = b.sdpa_fp8_decode_plan(inp.batch, inp.h_q, inp.h_kv, inp.d, 16, self.total_q, max(self.skv),
+                                           force_splits=S)
+        self.S = self.plan.num_splits
+        self.q, self.k, self.v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+        self.cq, self.ck = inp.cu_seqlens_q.to(dev), inp.cu_seqlens_kv.to(dev)
+        self.ds = [torch.tensor([x], dtype=torch.float32, device=dev)
+                   for x in (inp.descale_q, inp.descale_k, inp.descale_v)]
+        self.ws = (torch.empty(self.plan.workspace_bytes, dtype=torch.uint8, device=dev)
+                   if self.plan.workspace_bytes else None)
+        self.out = torch.empty(self.total_q, inp.h_q, inp.d, dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(self.total_q, inp.h_q, dtype=torch.float32, device=dev)
+        self.stream = torch.cuda.Stream()
+        self.g_call = Case._capture(self, self._call)
+        self.g_kernel = Case._capture(self, self._kernel)
+
+    def _call(self):
+        self.b.sdpa_fp8_decode(self.plan, self.total_q, self.total_kv, self.q, self.k, self.v, self.cq, self.ck,
+                               self.ds[0], self.ds[1], self.ds[2], self.inp.sm_scale, "bf16", 1.0, self.out,
+                               self.lse, None, self.ws, stream=self.stream)
+
+    def _kernel(self):
+        if self.S == 1:
+            self._call()
+        else:
+            self.b.sdpa_fp8_decode_split(self.plan, self.total_q, self.total_kv, self.q, self.k, self.v, self.cq,
+                                         self.ck, self.ds[0], self.ds[1], self.ds[2], self.inp.sm_scale, self.ws,
+                                         stream=self.stream)
+
+    def time(self, graph, steps, warmup, flush):
+        return Case.time(self, graph, steps, warmup, flush)
+
+    def bytes(self) -> int:
+        return dense_bytes(self.sq, self.skv, self.inp.h_q, self.inp.h_kv, self.inp.d, self.S)
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -325,9 +386,9 @@ def run_gpu(args):
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
 
     # ---- sweep: s_q x splits (and the planner's choice) -------------------------------
-    sweep = []
+    sweep, dense_sweep = [], []
     if not args.no_sweep:
-        for s_q in SWEEP_SQ:
+        for s_q in (() if args.no_mla_sweep else SWEEP_SQ):
             inp = inp_main if s_q == args.s_q else inputs(s_q)
             # forced (token, split) grids, the planner's choice (S = 0) and the
             # balanced one-shot schedule where it applies (S = -1)
@@ -346,6 +407,20 @@ def run_gpu(args):
                               "gb_s": round(cb / (us * 1e-6) / 1e9, 1),
                               "frac_of_peak": round(cb / (us * 1e-6) / 1e9 / peak, 4)})
                 del c
+        torch.cuda.synchronize()
+        # the dense FP8 GQA variant (same partial / LSE protocol), forced split
+        # counts and the planner's choice
+        dinp = wl.sdpa_inputs(8, 32, 8, 128, seed=0)
+        for S in list(SWEEP_S) + [0]:
+            c = DenseCase(b, torch, dinp, S)
+            us = statistics.fmean(c.time(c.g_call, args.sweep_steps, 3, flush))
+            ks = statistics.fmean(c.time(c.g_kernel, args.sweep_steps, 3, flush))
+            cb = c.bytes()
+            dense_sweep.append({"num_splits": S if S else "planner", "planner": S == 0, "splits_used": c.S,
+                                "us_per_call": round(us, 2), "split_kernel_us": round(ks, 2), "alg_bytes": cb,
+                                "gb_s": round(cb / (us * 1e-6) / 1e9, 1),
+                                "frac_of_peak": round(cb / (us * 1e-6) / 1e9 / peak, 4)})
+            del c
         torch.cuda.synchronize()
     sampler.stop()
     clocks = sampler.summary()
@@ -387,6 +462,7 @@ def run_gpu(args):
             "clocks": clocks,
             "cpu_baseline": cpu,
             "sweep": sweep,
+            "dense_sweep": {"workload": DENSE_DESC, "points": dense_sweep} if dense_sweep else None,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -499,6 +575,7 @@ def main():
     ap.add_argument("--s-q", type=int, default=96)
     ap.add_argument("--sweep-steps", type=int, default=50)
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-mla-sweep", action="store_true", help="run only the dense part of the sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--_cpu-worker", action="store_true", help=argparse.SUPPRESS)

@@ -58,7 +58,7 @@ constexpr int kSmemBytes = kSmemUsed + 1024;
 enum {
   B_QFULL = 0, B_SFULL_STAGE0, B_SFULL_STAGE1, B_SFULL_STAGE2, B_SEMPTY0, B_SEMPTY1, B_SEMPTY2,
   B_SREADY0, B_SREADY1, B_PFULL0, B_PFULL1, B_V16FULL0, B_V16FULL1, B_V16EMPTY0, B_V16EMPTY1,
-  B_FINAL, B_DRAIN, kNumBars
+  B_FINAL, B_DRAIN, B_PVDONE, kNumBars
 };
 static_assert(kNumBars * 8 <= 256, "barrier area");
 
@@ -68,7 +68,7 @@ constexpr float kRescaleThreshold = 8.0f;
 
 enum : uint32_t {
   W_PROD = 101, W_MMA_Q, W_MMA_P, W_MMA_V, W_MMA_FULL, W_SM_S, W_SM_FINAL, W_CV_FULL, W_CV_EMPTY,
-  W_DRAIN_MMA2, W_DRAIN_TMA2
+  W_DRAIN_MMA2, W_DRAIN_TMA2, W_SM_PV
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -157,6 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(B_FINAL), 1);
     mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_PVDONE), 1);             // one phase per tile's PV
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -227,35 +228,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_f16(tmem, sdesc_sw128(v16 + kk * 2048, 16384, 1024),
                   sdesc_sw128(pt + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), kIdescPV, (t > 0 || kk > 0));
       };
-      bool ok = wait_bounded(bar(B_QFULL), 0, wc, W_MMA_Q);
-#pragma unroll 1
-      for (int t = 0; ok && t < nt; ++t) {
-        if (t >= 1) {
-          const int u = t - 1;
-          ok = wait_bounded(bar(B_PFULL0 + (u & 1)), (u >> 1) & 1, wc, W_MMA_P) &&
-               wait_bounded(bar(B_V16FULL0 + (u & 1)), (u >> 1) & 1, wc, W_MMA_V);
-          if (!ok) break;
+      // Per tile t: QK(t) as soon as its K tile has landed (its S buffer was
+      // read by softmax(t-2), whose P the previous iteration waited for), then
+      // PV(t-1) once softmax(t-1) has written P(t-1). So the scores of tile t
+      // are computed while the softmax of tile t-1 runs.
+      auto pv_step = [&](int u) {
+        const bool w = wait_bounded(bar(B_PFULL0 + (u & 1)), (u >> 1) & 1, wc, W_MMA_P) &&
+                       wait_bounded(bar(B_V16FULL0 + (u & 1)), (u >> 1) & 1, wc, W_MMA_V);
+        if (w) {
           tc_fence_after();
           issue_pv(u);
           mma_commit(bar(B_V16EMPTY0 + (u & 1)));
+          mma_commit(bar(B_PVDONE));
         }
+        return w;
+      };
+      bool ok = wait_bounded(bar(B_QFULL), 0, wc, W_MMA_Q);
+#pragma unroll 1
+      for (int t = 0; ok && t < nt; ++t) {
         ok = wait_bounded(bar(B_SFULL_STAGE0 + t % kStages), (t / kStages) & 1, wc, W_MMA_FULL);
         if (!ok) break;
         tc_fence_after();
         issue_qk(t);
         mma_commit(bar(B_SREADY0 + (t & 1)));
         mma_commit(bar(B_SEMPTY0 + t % kStages));
+        if (t >= 1) ok = pv_step(t - 1);
       }
       if (ok) {
-        const int u = nt - 1;
-        ok = wait_bounded(bar(B_PFULL0 + (u & 1)), (u >> 1) & 1, wc, W_MMA_P) &&
-             wait_bounded(bar(B_V16FULL0 + (u & 1)), (u >> 1) & 1, wc, W_MMA_V);
-        if (ok) {
-          tc_fence_after();
-          issue_pv(u);
-          mma_commit(bar(B_V16EMPTY0 + (u & 1)));
-          mma_commit(bar(B_FINAL));
-        }
+        ok = pv_step(nt - 1);
+        if (ok) mma_commit(bar(B_FINAL));
       }
       if (!ok) {
         mma_commit(bar(B_DRAIN));
@@ -320,6 +321,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int i = 0; i < 64; ++i) lpart[i] = 0.f;
     int bad = 0;
+    // Only the first R of the 64 rows are real: work on 8-row blocks up to R and
+    // leave the rest at -inf (their P rows are never written; the O columns they
+    // produce are never read).
+    const int nb8 = (R + 7) >> 3;
 #pragma unroll 1
     for (int t = 0; t < nt; ++t) {
       const int keyrel = (tile0 + t) * kTile + 32 * sp + lane;   // this thread's key, sequence-relative
@@ -334,14 +339,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_32x32b_x64(tmem + lane_base + kTmemS + 64 * (t & 1), raw);
         tmem_wait_ld_x64(raw);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) x[i] = keyrel <= lim[i] ? __uint_as_float(raw[i]) * sc : -INFINITY;
+        for (int c8 = 0; c8 < 8; ++c8) {
+          if (c8 < nb8) {
+#pragma unroll
+            for (int j = 8 * c8; j < 8 * c8 + 8; ++j)
+              x[j] = keyrel <= lim[j] ? __uint_as_float(raw[j]) * sc : -INFINITY;
+          } else {
+#pragma unroll
+            for (int j = 8 * c8; j < 8 * c8 + 8; ++j) x[j] = -INFINITY;
+          }
+        }
       } else {
 #pragma unroll
         for (int i = 0; i < 64; ++i) x[i] = -INFINITY;
       }
       bool need = false;
 #pragma unroll
-      for (int i = 0; i < 64; ++i) need |= x[i] > m_use[i] + kRescaleThreshold;
+      for (int c8 = 0; c8 < 8; ++c8)
+        if (c8 < nb8) {
+#pragma unroll
+          for (int j = 8 * c8; j < 8 * c8 + 8; ++j) need |= x[j] > m_use[j] + kRescaleThreshold;
+        }
       const unsigned vote = __ballot_sync(0xffffffffu, need);
       if (lane == 0) flags[(t & 1) * 4 + wi] = (vote != 0u ? 1 : 0) | (bad ? 2 : 0);
       named_bar_sync(1, 128);
@@ -368,7 +386,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 64; ++i) lpart[i] *= alpha[i];
         if (t >= 1) {
-          // S^T(t) ready implies every earlier PV has completed: O^T is final up to tile t-1
+          // O^T must hold PV(t-1) before it is scaled. S^T(t) ready already
+          // implies PV(t-2) is done, so this waits for one phase at most.
+          int wp = 1;
+          if (lane == 0) wp = wait_bounded(bar(B_PVDONE), (t - 1) & 1, wc, W_SM_PV);
+          if (!__shfl_sync(0xffffffffu, wp, 0)) bad = 1;
+          tc_fence_after();
 #pragma unroll 1
           for (int j = 0; j < 2; ++j) {
             uint32_t o[32];
@@ -389,18 +412,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kb = key >> 6, kc = (key & 63) >> 3, kbyte = (key & 7) * 2;
       // all reads of m_use before the first store (stores could alias it)
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        x[i] = (x[i] == -INFINITY) ? 0.f : ex2_approx(x[i] - m_use[i]);
-        lpart[i] += x[i];
-      }
+      for (int c8 = 0; c8 < 8; ++c8)
+        if (c8 < nb8) {
 #pragma unroll
-      for (int i = 0; i < 64; i += 2) {
-        const __half2 ph = __floats2half2_rn(x[i], x[i + 1]);
-        const int off0 = kb * 8192 + (i >> 3) * 1024 + (i & 7) * 128 + ((kc ^ (i & 7)) << 4) + kbyte;
-        const int off1 = kb * 8192 + ((i + 1) >> 3) * 1024 + ((i + 1) & 7) * 128 + ((kc ^ ((i + 1) & 7)) << 4) + kbyte;
-        *reinterpret_cast<__half*>(pt + off0) = __low2half(ph);
-        *reinterpret_cast<__half*>(pt + off1) = __high2half(ph);
-      }
+          for (int i = 8 * c8; i < 8 * c8 + 8; ++i) {
+            x[i] = (x[i] == -INFINITY) ? 0.f : ex2_approx(x[i] - m_use[i]);
+            lpart[i] += x[i];
+          }
+        }
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8)
+        if (c8 < nb8) {
+#pragma unroll
+          for (int i = 8 * c8; i < 8 * c8 + 8; i += 2) {
+            const __half2 ph = __floats2half2_rn(x[i], x[i + 1]);
+            const int off0 = kb * 8192 + (i >> 3) * 1024 + (i & 7) * 128 + ((kc ^ (i & 7)) << 4) + kbyte;
+            const int off1 =
+                kb * 8192 + ((i + 1) >> 3) * 1024 + ((i + 1) & 7) * 128 + ((kc ^ ((i + 1) & 7)) << 4) + kbyte;
+            *reinterpret_cast<__half*>(pt + off0) = __low2half(ph);
+            *reinterpret_cast<__half*>(pt + off1) = __high2half(ph);
+          }
+        }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
