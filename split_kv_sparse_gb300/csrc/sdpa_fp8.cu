@@ -5,15 +5,16 @@
 // into split-major slots (or, unsplit, a direct bf16/fp32/e4m3 epilogue that
 // also computes the amax).
 //
-// One CTA per job (sequence b, KV head g, split s), 256 threads:
+// One CTA per job (sequence b, KV head g, split s), 320 threads:
 //   warp 0     TMA: the job's Q rows once (the group's h_q/h_kv heads of up to
 //              64/group tokens = 64 rows x 128 B), then per tile K and V
 //              (128 keys x 128 B each, e4m3) into a 3-stage ring.
-//   warp 1     tcgen05 issue:  S^T[128 keys x 64 rows] = K . Q^T   (kind::f8f6f4, K=128)
+//   warp 1     tcgen05 issue:  S[64 rows x 128 keys] = Q . K^T     (kind::f8f6f4, K=128)
 //                              O^T[128 d x 64 rows] += V^T . P^T   (kind::f16, f16 operands)
-//   warps 2-5  softmax over keys (TMEM lane = key), lazy rescale of O^T,
+//   warps 2-5  softmax over the keys of each query row (S = Q.K^T, M=64: a row
+//              per lane pair, the tile's keys in its columns), lazy rescale of O^T,
 //              P^T in f16, then the epilogue.
-//   warps 6-7  convert each V tile from e4m3 to f16 (exact) into the
+//   warps 6-9  convert each V tile from e4m3 to f16 (exact) into the
 //              MN-major 128-byte-swizzled layout the PV MMA reads.
 // The QK product of e4m3 codes is exact in fp32; descales multiply the scores
 // (dq*dk*sm_scale) and the output (dv).
@@ -28,7 +29,8 @@
 namespace skv {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 320;
+constexpr int kConverters = 4;             // warps 6-9: one key row of the V tile per thread
 constexpr int kD = 128;
 constexpr int kTile = 128;                 // keys per tile (split unit)
 constexpr int kRows = 64;                  // query rows per job (tokens x group heads)
@@ -45,14 +47,9 @@ constexpr int kOffP = kOffV16 + 2 * kV16Bytes;               // 163840
 constexpr int kOffQ = kOffP + 2 * kPBytes;                   // 196608
 constexpr int kOffBars = kOffQ + kQBytes;                    // 204800
 constexpr int kOffMisc = kOffBars + 256;
-constexpr int kOffMuse = kOffMisc + 128;
-constexpr int kOffAlpha = kOffMuse + 256;
-constexpr int kOffMnew = kOffAlpha + 256;
-constexpr int kOffTmax = kOffMnew + 256;
-constexpr int kOffLred = kOffTmax + 1024;
-constexpr int kOffInv = kOffLred + 1024;
-constexpr int kOffLim = kOffInv + 256;                       // int[64] last visible key per row
-constexpr int kSmemUsed = kOffLim + 256;
+constexpr int kOffAlpha = kOffMisc + 128;                    // float[2][64] rescale factors by tile parity
+constexpr int kOffInv = kOffAlpha + 512;                     // float[64] dv / l per row
+constexpr int kSmemUsed = kOffInv + 256;
 constexpr int kSmemBytes = kSmemUsed + 1024;
 
 enum {
@@ -62,8 +59,8 @@ enum {
 };
 static_assert(kNumBars * 8 <= 256, "barrier area");
 
-constexpr uint32_t kTmemCols = 256;        // O^T at [0, 64), S^T buffers at 64 and 128
-constexpr uint32_t kTmemS = 64;
+constexpr uint32_t kTmemCols = 512;        // O^T at [0, 64), S buffers (128 keys each) at 128 and 256
+constexpr uint32_t kTmemS = 128;
 constexpr float kRescaleThreshold = 8.0f;
 
 enum : uint32_t {
@@ -134,25 +131,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   volatile int* flags = reinterpret_cast<volatile int*>(misc + 4);
-  float* m_use = reinterpret_cast<float*>(smem + kOffMuse);
-  float* alpha = reinterpret_cast<float*>(smem + kOffAlpha);
-  float* m_new = reinterpret_cast<float*>(smem + kOffMnew);
-  float* tmax = reinterpret_cast<float*>(smem + kOffTmax);
-  float* lred = reinterpret_cast<float*>(smem + kOffLred);
+  float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
   float* inv_s = reinterpret_cast<float*>(smem + kOffInv);
-  int* lim = reinterpret_cast<int*>(smem + kOffLim);
   const WaitCtx wc{a.wait_limit_ns, a.status, abort_flag};
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar(B_SFULL_STAGE0 + i), 1);
-      mbar_init(bar(B_SEMPTY0 + i), 3);            // QK commit + 2 converter warps
+      mbar_init(bar(B_SEMPTY0 + i), 1 + kConverters);   // QK commit + the converter warps
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_SREADY0 + i), 1);
       mbar_init(bar(B_PFULL0 + i), 4);
-      mbar_init(bar(B_V16FULL0 + i), 2);
+      mbar_init(bar(B_V16FULL0 + i), kConverters);
       mbar_init(bar(B_V16EMPTY0 + i), 1);
     }
     mbar_init(bar(B_FINAL), 1);
@@ -160,13 +152,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_PVDONE), 1);             // one phase per tile's PV
     *abort_flag = 0;
     mbar_init_fence();
-  }
-  if (threadIdx.x >= 64 && threadIdx.x < 128) {
-    const int rho = threadIdx.x - 64;
-    m_use[rho] = -INFINITY;
-    // last key (sequence-relative) row rho may see inside this split: bottom-right causal
-    const int pos = kvlen - sq + rho / group;
-    lim[rho] = rho < R ? min(key_end - 1, pos) : -1;
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(misc), kTmemCols);
@@ -210,14 +195,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ========================================================= MMA issuer ===
     if (lane == 0) {
-      constexpr uint32_t kIdescQK = idesc_make(128, 64, 0, false, false);   // e4m3 x e4m3
+      constexpr uint32_t kIdescQK = idesc_make(64, 128, 0, false, false);   // e4m3 x e4m3, M=64 rows, N=128 keys
       constexpr uint32_t kIdescPV = idesc_make(128, 64, 0, true, false);    // f16, A MN-major
       auto issue_qk = [&](int t) {
         const uint32_t kt = sbase + kOffStage + (t % kStages) * kStageBytes;
-        const uint32_t d = tmem + kTmemS + 64 * (t & 1);
+        const uint32_t d = tmem + kTmemS + 128 * (t & 1);
+        // A = Q (64 rows x 128 B), B = the K tile (128 keys x 128 B), both K-major;
+        // K = 32 e4m3 codes (32 bytes) per MMA
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_f8(d, sdesc_sw128(kt + kk * 32, 16, 1024), sdesc_sw128(sbase + kOffQ + kk * 32, 16, 1024),
+          mma_f8(d, sdesc_sw128(sbase + kOffQ + kk * 32, 16, 1024), sdesc_sw128(kt + kk * 32, 16, 1024),
                  kIdescQK, kk != 0);
       };
       auto issue_pv = [&](int t) {
@@ -265,7 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 6) {
     // ==================================================== V e4m3 -> f16 ===
-    const int ct = threadIdx.x - 192;       // 0..63: key rows ct and ct + 64 of each tile
+    const int key = threadIdx.x - 192;      // 0..127: this thread's key row of each tile
+    const int r8 = key & 7;
 #pragma unroll 1
     for (int t = 0; t < nt; ++t) {
       const int st = t % kStages;
@@ -276,15 +264,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       w = __shfl_sync(0xffffffffu, w, 0);
       if (!w) break;   // the abort flag is set; the other roles stop on their own waits
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int key = ct + 64 * rr;
-        const int r8 = key & 7;
+      {
         const uint8_t* vrow = smem + kOffStage + st * kStageBytes + kKVTileBytes + (key >> 3) * 1024 + r8 * 128;
         uint8_t* v16 = smem + kOffV16 + (t & 1) * kV16Bytes + (key >> 3) * 1024 + r8 * 128;
+        uint4 row[8];   // the whole 128-byte row first: eight loads in flight
+#pragma unroll
+        for (int c = 0; c < 8; ++c) row[c] = *reinterpret_cast<const uint4*>(vrow + ((c ^ r8) << 4));
 #pragma unroll
         for (int c = 0; c < 8; ++c) {            // 16 e4m3 values (d = 16c .. 16c+15) per chunk
-          const uint4 raw = *reinterpret_cast<const uint4*>(vrow + ((c ^ r8) << 4));
+          const uint4 raw = row[c];
           const uint32_t wds[4] = {raw.x, raw.y, raw.z, raw.w};
           uint32_t h[8];
 #pragma unroll
@@ -310,162 +298,157 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ============================================== softmax + epilogue ====
+    // S = Q.K^T is an M=64 accumulator: row r (token r / group, head r % group)
+    // sits in lane r % 16 of sub-partition r / 16, the tile's 128 keys in its
+    // columns. Lanes i and i + 16 of a warp hold row 16 sp + i: keys 0-63 and
+    // 64-127 (tcgen05.ld 16x32bx2), so a row's max and sum take one shuffle.
     const int sp = warp & 3;
     const int wi = warp - 2;
-    const int tid = threadIdx.x - 64;
     const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
+    const int row = 16 * sp + (lane & 15);
+    const int kh = lane >> 4;                       // key half of the tile
+    const bool live = row < R;
+    // last key (sequence-relative) this row may see inside this split: bottom-right causal
+    const int lim_r = live ? min(key_end - 1, kvlen - sq + row / group) : -1;
     const float sc = dq * dk * a.scale_log2;
-    // fp32 softmax denominators per row over the keys this thread has held;
-    // reduced over threads once, in the epilogue (P in f16 matches p to 2^-12)
-    float lpart[64];
-#pragma unroll
-    for (int i = 0; i < 64; ++i) lpart[i] = 0.f;
+    float m_run = -INFINITY;   // the row's reference max (log2 units), shared by its two lanes
+    float lsum = 0.f;          // fp32 softmax denominator over this thread's keys
     int bad = 0;
-    // Only the first R of the 64 rows are real: work on 8-row blocks up to R and
-    // leave the rest at -inf (their P rows are never written; the O columns they
-    // produce are never read).
-    const int nb8 = (R + 7) >> 3;
 #pragma unroll 1
     for (int t = 0; t < nt; ++t) {
-      const int keyrel = (tile0 + t) * kTile + 32 * sp + lane;   // this thread's key, sequence-relative
+      const int key0 = (tile0 + t) * kTile + 64 * kh;   // this thread's first key, sequence-relative
       int w = 1;
       if (lane == 0) w = wait_bounded(bar(B_SREADY0 + (t & 1)), (t >> 1) & 1, wc, W_SM_S);
       w = __shfl_sync(0xffffffffu, w, 0);
       if (!w) bad = 1;
       tc_fence_after();
       float x[64];
-      if (w) {
+      float mx = -INFINITY;
+      {
         uint32_t raw[64];
-        tmem_ld_32x32b_x64(tmem + lane_base + kTmemS + 64 * (t & 1), raw);
+        tmem_ld_16x32bx2_x64_h64(tmem + lane_base + kTmemS + 128 * (t & 1), raw);
         tmem_wait_ld_x64(raw);
+        if (w && key0 + 63 <= lim_r) {
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          if (c8 < nb8) {
-#pragma unroll
-            for (int j = 8 * c8; j < 8 * c8 + 8; ++j)
-              x[j] = keyrel <= lim[j] ? __uint_as_float(raw[j]) * sc : -INFINITY;
-          } else {
-#pragma unroll
-            for (int j = 8 * c8; j < 8 * c8 + 8; ++j) x[j] = -INFINITY;
+          for (int i = 0; i < 64; ++i) {
+            x[i] = __uint_as_float(raw[i]) * sc;
+            mx = fmaxf(mx, x[i]);
           }
-        }
-      } else {
+        } else if (w) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) x[i] = -INFINITY;
+          for (int i = 0; i < 64; ++i) {
+            x[i] = key0 + i <= lim_r ? __uint_as_float(raw[i]) * sc : -INFINITY;
+            mx = fmaxf(mx, x[i]);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) x[i] = -INFINITY;
+        }
       }
-      bool need = false;
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      // Lazy rescale: move the reference only when a score exceeds it by more
+      // than the threshold (always on the row's first visible key). Both lanes
+      // of the row see the same mx and take the same decision.
+      const bool need = mx > m_run + kRescaleThreshold;
+      float al = 1.f;
+      if (need) {
+        al = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - mx);
+        lsum *= al;
+        m_run = mx;
+      }
+      float* alpha = alpha_s + 64 * (t & 1);
+      if (lane < 16) alpha[row] = al;
+      const unsigned rmask = __ballot_sync(0xffffffffu, need) & 0xffffu;
+      if (lane == 0) flags[(t & 1) * 4 + wi] = static_cast<int>(rmask) | (bad ? 0x10000 : 0);
+      // p = 2^(x - m_ref); an invisible key gives 0
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8)
-        if (c8 < nb8) {
+      for (int i = 0; i < 64; ++i) x[i] = (x[i] == -INFINITY) ? 0.f : ex2_approx(x[i] - m_run);
+      {
+        float ts[32];
 #pragma unroll
-          for (int j = 8 * c8; j < 8 * c8 + 8; ++j) need |= x[j] > m_use[j] + kRescaleThreshold;
+        for (int i = 0; i < 32; ++i) ts[i] = x[i] + x[i + 32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ts[i] += ts[i + 16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ts[i] += ts[i + 8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ts[i] += ts[i + 4];
+        lsum += (ts[0] + ts[2]) + (ts[1] + ts[3]);
+      }
+      // P (f16) as the K-major B operand of PV: N = rows, K = keys; the row's 64
+      // keys of this half are one 128-byte line of swizzle atom kh, stored as
+      // eight 16-byte pieces (rows past R are never read back: not stored)
+      uint8_t* pt = smem + kOffP + (t & 1) * kPBytes + kh * 8192 + (row >> 3) * 1024 + (row & 7) * 128;
+      if (live) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t h4[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const __half2 ph = __floats2half2_rn(x[8 * c + 2 * j], x[8 * c + 2 * j + 1]);
+            h4[j] = *reinterpret_cast<const uint32_t*>(&ph);
+          }
+          *reinterpret_cast<uint4*>(pt + ((c ^ (row & 7)) << 4)) = make_uint4(h4[0], h4[1], h4[2], h4[3]);
         }
-      const unsigned vote = __ballot_sync(0xffffffffu, need);
-      if (lane == 0) flags[(t & 1) * 4 + wi] = (vote != 0u ? 1 : 0) | (bad ? 2 : 0);
+      }
+      // the other warps' rescale masks: O^T holds every row in all four warps' lanes
       named_bar_sync(1, 128);
-      const int f = flags[(t & 1) * 4 + 0] | flags[(t & 1) * 4 + 1] | flags[(t & 1) * 4 + 2] |
-                    flags[(t & 1) * 4 + 3];
-      if (f & 2) {
+      const int f0 = flags[(t & 1) * 4 + 0], f1 = flags[(t & 1) * 4 + 1], f2 = flags[(t & 1) * 4 + 2],
+                f3 = flags[(t & 1) * 4 + 3];
+      if ((f0 | f1 | f2 | f3) & 0x10000) {
         bad = 1;
-        break;
+        break;   // every softmax warp sees the same flags and leaves together
       }
-      if (f & 1) {
-        float mx0, mx1;
-        warp_transpose_reduce<true>(x, lane, mx0, mx1);
-        tmax[wi * 64 + 2 * lane] = mx0;
-        tmax[wi * 64 + 2 * lane + 1] = mx1;
-        named_bar_sync(1, 128);
-        if (tid < 64) {
-          const float tm = fmaxf(fmaxf(tmax[tid], tmax[64 + tid]), fmaxf(tmax[128 + tid], tmax[192 + tid]));
-          const float mo = m_use[tid];
-          const float mn = fmaxf(mo, tm);
-          alpha[tid] = (mn == -INFINITY) ? 1.f : ex2_approx(mo - mn);
-          m_new[tid] = mn;
-        }
-        named_bar_sync(1, 128);
-#pragma unroll
-        for (int i = 0; i < 64; ++i) lpart[i] *= alpha[i];
-        if (t >= 1) {
-          // O^T must hold PV(t-1) before it is scaled. S^T(t) ready already
-          // implies PV(t-2) is done, so this waits for one phase at most.
-          int wp = 1;
-          if (lane == 0) wp = wait_bounded(bar(B_PVDONE), (t - 1) & 1, wc, W_SM_PV);
-          if (!__shfl_sync(0xffffffffu, wp, 0)) bad = 1;
-          tc_fence_after();
+      const uint64_t resc = static_cast<uint64_t>(f0 & 0xffff) | (static_cast<uint64_t>(f1 & 0xffff) << 16) |
+                            (static_cast<uint64_t>(f2 & 0xffff) << 32) | (static_cast<uint64_t>(f3 & 0xffff) << 48);
+      if (resc != 0 && t >= 1) {
+        // O^T must hold PV(t-1) before it is scaled. S^T(t) ready already
+        // implies PV(t-2) is done, so this waits for one phase at most.
+        int wp = 1;
+        if (lane == 0) wp = wait_bounded(bar(B_PVDONE), (t - 1) & 1, wc, W_SM_PV);
+        if (!__shfl_sync(0xffffffffu, wp, 0)) bad = 1;
+        tc_fence_after();
 #pragma unroll 1
-          for (int j = 0; j < 2; ++j) {
-            uint32_t o[32];
-            tmem_ld_32x32b_x32(tmem + lane_base + 32 * j, o);
-            tmem_wait_ld_x32(o);
+        for (int j = 0; j < 2; ++j) {
+          if (((resc >> (32 * j)) & 0xffffffffull) == 0) continue;
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(tmem + lane_base + 32 * j, o);
+          tmem_wait_ld_x32(o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha[32 * j + i]);
-            tmem_st_32x32b_x32(tmem + lane_base + 32 * j, o);
-          }
-          tmem_wait_st();
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha[32 * j + i]);
+          tmem_st_32x32b_x32(tmem + lane_base + 32 * j, o);
         }
-        if (tid < 64) m_use[tid] = m_new[tid];
-        named_bar_sync(1, 128);
+        tmem_wait_st();
       }
-      // P^T (f16, K-major over keys, two 64-key swizzle atoms) for this tile
-      uint8_t* pt = smem + kOffP + (t & 1) * kPBytes;
-      const int key = 32 * sp + lane;
-      const int kb = key >> 6, kc = (key & 63) >> 3, kbyte = (key & 7) * 2;
-      // all reads of m_use before the first store (stores could alias it)
-#pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8)
-        if (c8 < nb8) {
-#pragma unroll
-          for (int i = 8 * c8; i < 8 * c8 + 8; ++i) {
-            x[i] = (x[i] == -INFINITY) ? 0.f : ex2_approx(x[i] - m_use[i]);
-            lpart[i] += x[i];
-          }
-        }
-#pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8)
-        if (c8 < nb8) {
-#pragma unroll
-          for (int i = 8 * c8; i < 8 * c8 + 8; i += 2) {
-            const __half2 ph = __floats2half2_rn(x[i], x[i + 1]);
-            const int off0 = kb * 8192 + (i >> 3) * 1024 + (i & 7) * 128 + ((kc ^ (i & 7)) << 4) + kbyte;
-            const int off1 =
-                kb * 8192 + ((i + 1) >> 3) * 1024 + ((i + 1) & 7) * 128 + ((kc ^ ((i + 1) & 7)) << 4) + kbyte;
-            *reinterpret_cast<__half*>(pt + off0) = __low2half(ph);
-            *reinterpret_cast<__half*>(pt + off1) = __high2half(ph);
-          }
-        }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PFULL0 + (t & 1)));
+      // alpha and the flags of this tile's parity are rewritten two tiles on, past
+      // the named barrier of the next tile, which every warp reaches only after
+      // reading them here
     }
 
     // ---- epilogue ---------------------------------------------------------
-    {
-      float ls0, ls1;
-      warp_transpose_reduce<false>(lpart, lane, ls0, ls1);
-      lred[wi * 64 + 2 * lane] = ls0;
-      lred[wi * 64 + 2 * lane + 1] = ls1;
-    }
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);   // the row's two key halves
     if (lane == 0) flags[8 + wi] = bad;
-    named_bar_sync(1, 128);
-    const bool any_bad = flags[8] | flags[9] | flags[10] | flags[11];
-    if (tid < 64) {
-      const float l = (lred[tid] + lred[64 + tid]) + (lred[128 + tid] + lred[192 + tid]);
+    if (lane < 16 && live) {
       float lse = -INFINITY, inv = 0.f;
-      if (l > 0.f) {
-        lse = m_use[tid] + log2f(l);
-        inv = dv / l;
+      if (lsum > 0.f) {
+        lse = m_run + log2f(lsum);
+        inv = dv / lsum;
       }
-      inv_s[tid] = inv;
-      if (tid < R) {
+      inv_s[row] = inv;
+      if (!bad) {
         if (direct) {
-          if (a.lse_out != nullptr) a.lse_out[out_index(tid)] = lse;
+          if (a.lse_out != nullptr) a.lse_out[out_index(row)] = lse;
         } else {
-          a.lse_acc[out_index(tid)] = lse;
+          a.lse_acc[out_index(row)] = lse;
         }
       }
     }
     named_bar_sync(1, 128);
+    const bool any_bad = flags[8] | flags[9] | flags[10] | flags[11];
     if (!any_bad) {
       int w = 1;
       if (lane == 0) w = wait_bounded(bar(B_FINAL), 0, wc, W_SM_FINAL);
