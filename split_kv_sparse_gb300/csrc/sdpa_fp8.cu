@@ -29,6 +29,19 @@
 namespace skv {
 namespace {
 
+// Four e4m3 codes (bytes 0..3 of w) to four f16 values, exactly (every e4m3
+// value is an f16 value): bytes 0, 1 -> lo, bytes 2, 3 -> hi, low half first.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n"
+      "  .reg .b16 a, b;\n"
+      "  mov.b32 {a, b}, %2;\n"
+      "  cvt.rn.f16x2.e4m3x2 %0, a;\n"
+      "  cvt.rn.f16x2.e4m3x2 %1, b;\n"
+      "}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
 constexpr int kThreads = 320;
 constexpr int kConverters = 4;             // warps 6-9: one key row of the V tile per thread
 constexpr int kD = 128;
@@ -276,12 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t wds[4] = {raw.x, raw.y, raw.z, raw.w};
           uint32_t h[8];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wds[j] & 0xFFFFu), __NV_E4M3);
-            const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wds[j] >> 16), __NV_E4M3);
-            h[2 * j] = static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16);
-            h[2 * j + 1] = static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16);
-          }
+          for (int j = 0; j < 4; ++j) e4m3x4_to_f16x4(wds[j], h[2 * j], h[2 * j + 1]);
           // d = 16c .. 16c+7 -> MN atom (16c)/64, 16-B chunk ((16c)%64)/8; then +8
           const int d0 = 16 * c;
           const int a0 = d0 >> 6, c0 = (d0 & 63) >> 3;
@@ -324,16 +332,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       float x[64];
       float mx = -INFINITY;
+      bool all_vis = false;   // x holds raw scores (every key visible) rather than scaled ones
       {
         uint32_t raw[64];
         tmem_ld_16x32bx2_x64_h64(tmem + lane_base + kTmemS + 128 * (t & 1), raw);
         tmem_wait_ld_x64(raw);
         if (w && key0 + 63 <= lim_r) {
+          // every key visible: the max of the raw scores (sc > 0), the scale
+          // folded into the exponent below
+          float mr = __uint_as_float(raw[0]);
 #pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            x[i] = __uint_as_float(raw[i]) * sc;
-            mx = fmaxf(mx, x[i]);
-          }
+          for (int i = 1; i < 64; ++i) mr = fmaxf(mr, __uint_as_float(raw[i]));
+#pragma unroll
+          for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(raw[i]);
+          mx = mr * sc;
+          all_vis = true;
         } else if (w) {
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
@@ -361,8 +374,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const unsigned rmask = __ballot_sync(0xffffffffu, need) & 0xffffu;
       if (lane == 0) flags[(t & 1) * 4 + wi] = static_cast<int>(rmask) | (bad ? 0x10000 : 0);
       // p = 2^(x - m_ref); an invisible key gives 0
+      if (all_vis) {
+        const float nm = -m_run;
 #pragma unroll
-      for (int i = 0; i < 64; ++i) x[i] = (x[i] == -INFINITY) ? 0.f : ex2_approx(x[i] - m_run);
+        for (int i = 0; i < 64; ++i) x[i] = ex2_approx(fmaf(x[i], sc, nm));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) x[i] = (x[i] == -INFINITY) ? 0.f : ex2_approx(x[i] - m_run);
+      }
       {
         float ts[32];
 #pragma unroll
