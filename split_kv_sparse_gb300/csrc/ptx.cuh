@@ -77,12 +77,10 @@ struct WaitCtx {
   volatile int* abort_flag; // shared
 };
 
-// Waits for the phase with the given parity of `bar`. Gives up after
-// ctx.limit_ns (or when another role of this CTA has aborted), records the
-// timeout in the status word and returns false. Never traps.
-static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtx& ctx,
-                                          uint32_t site) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The waiting part of wait_bounded, out of line: the common case (the phase
+// has already completed) costs no call.
+static __device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity, const WaitCtx& ctx,
+                                               uint32_t site) {
   uint64_t t0 = 0;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -99,6 +97,14 @@ static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, 
       }
     }
   }
+}
+
+// Waits for the phase with the given parity of `bar`. Gives up after
+// ctx.limit_ns (or when another role of this CTA has aborted), records the
+// timeout in the status word and returns false. Never traps.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtx& ctx, uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bounded_slow(bar, parity, ctx, site);
 }
 
 // ------------------------------------------------- flags in global memory --
