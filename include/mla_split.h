@@ -250,9 +250,11 @@ typedef struct {
   uint64_t workspace_bytes;
 } sdpa_plan_t;
 
-/* Split count for the dense path: S with batch * h_kv * S <= num_sms (at least 1),
- * smallest S reaching the fewest tiles per split for a sequence of max_kv keys;
- * force_splits > 0 overrides. Errors as for mla_decode_plan (d must be 128). */
+/* Split count for the dense path: among S with batch * h_kv * S <= 2 * num_sms (at
+ * least 1; two waves of CTAs, since in a ragged batch the jobs of shorter
+ * sequences end early), the smallest S reaching the fewest tiles per split for a
+ * sequence of max_kv keys; force_splits > 0 overrides. Errors as for
+ * mla_decode_plan (d must be 128). */
 MLA_API int sdpa_fp8_decode_plan(int batch, int h_q, int h_kv, int d, int max_q_per_seq,
                          int total_q_max, int max_kv, int num_sms, int max_splits,
                          int force_splits, sdpa_plan_t* out);

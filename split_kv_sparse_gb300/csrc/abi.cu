@@ -515,7 +515,9 @@ int sdpa_fp8_decode_plan(int batch, int h_q, int h_kv, int d, int max_q_per_seq,
   int S = force_splits;
   if (S == 0) {
     const int cap = max_splits > 0 ? max_splits : MLA_MAX_SPLITS;
-    int smax = num_sms / (batch * h_kv);
+    // up to two waves of CTAs: the plan knows only the longest sequence, and in
+    // a ragged batch the jobs of shorter ones end early and free their SMs
+    int smax = 2 * num_sms / (batch * h_kv);
     if (smax > cap) smax = cap;
     if (smax > ntiles) smax = ntiles;
     if (smax < 1) smax = 1;

@@ -190,7 +190,8 @@ def test_no_device_is_reported_not_crashed():
 
 def test_dense_plan():
     p = b.sdpa_fp8_decode_plan(8, 32, 8, 128, 16, 128, 16384, num_sms=152)
-    assert p.num_splits >= 1 and 8 * 8 * p.num_splits <= 152
+    assert p.num_splits >= 1 and 8 * 8 * p.num_splits <= 2 * 152
+    assert p.num_splits == 4    # 128 tiles: 4 splits of 32 (256 CTAs)
     assert p.o_acc_bytes == (p.num_splits * 128 * 32 * 128 * 4 if p.num_splits > 1 else 0)
     with pytest.raises(b.SplitKVError) as e:
         b.sdpa_fp8_decode_plan(8, 32, 8, 64, 16, 128, 16384, num_sms=152)
