@@ -497,9 +497,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       //   QK(g)     once its rows (and, first in a job, its Q)
       //             have landed and its S buffer is free: softmax(g-2) published
       //             P_hi, i.e. PV_hi(g-2) was issued.
-      // tcgen05 runs the MMAs in issue order. When only one of them can make
-      // progress the thread sleeps in try_wait on its barrier; otherwise it
-      // polls them without blocking.
+      // tcgen05 runs the MMAs in issue order. The thread polls the barriers
+      // without blocking (a suspended try_wait can wake well after the phase
+      // completes).
       int nqk = 0, qrun = 0, nph = 0, npl = 0;
       int qj = 0, qk = 0, qn = j0.nsteps;   // QK cursor: job, step within it, its steps
       int hj = 0, hk = 0, hn = j0.nsteps;   // PV_hi cursor
@@ -509,9 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool c_lo = npl < nph;
         const bool c_hi = nph < nqk;
         const bool c_qk = nqk < total && nqk <= nph + 1;
-        const bool c_qk_new = c_qk && qrun == 0;
-        const int ncand = (c_lo ? 1 : 0) + (c_hi ? 1 : 0) + (c_qk_new ? 1 : 0);
-        auto ready = [&](uint32_t b, uint32_t ph) { return ncand == 1 ? mbar_try_wait(b, ph) : mbar_test_wait(b, ph); };
+        auto ready = [&](uint32_t b, uint32_t ph) { return mbar_test_wait(b, ph); };
         bool progress = false;
         if (c_lo && ready(bar(B_PLO0 + (npl & 1)), (npl >> 1) & 1)) {
           tc_fence_after();

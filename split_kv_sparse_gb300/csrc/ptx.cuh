@@ -83,7 +83,8 @@ static __device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t par
                                                uint32_t site) {
   uint64_t t0 = 0;
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    // polled: a try_wait may suspend the thread past the phase's completion
+    if (mbar_test_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*ctx.abort_flag) return false;
       const uint64_t now = globaltimer_ns();
