@@ -141,7 +141,11 @@ typedef struct {
  *   force_splits 0 = automatic; > 0 uses exactly that many splits (<= MLA_MAX_SPLITS),
  *                even above num_blocks (the extra splits are empty).
  * Automatic rule: among split counts S with s_q_max * S <= num_sms (at least 1),
- * take the smallest S that reaches the fewest blocks per split, ceil(num_blocks / S).
+ * take the smallest S that reaches the fewest blocks per split, counting
+ * max(2, ceil(num_blocks / S)): a split of two 64-row blocks costs about what a
+ * split of one does, and fewer splits leave SMs to dim groups and partials to
+ * the combine (measured on GB300, topk 640: s_q = 10 takes 5 splits x 2 dim
+ * groups, 21.6 us, where 10 splits x 1 took 25.3 us).
  * dim_groups is the largest of 4, 2, 1 with s_q_max * S * dim_groups <= num_sms.
  * With force_splits == 0 the plan also enables the balanced schedule for the
  * one-shot call when it is expected to beat that grid at s_q_max: with per =

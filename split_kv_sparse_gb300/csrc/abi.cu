@@ -231,10 +231,15 @@ int mla_decode_plan(int s_q_max, int h_q, int d_qk, int d_v, int topk, int num_s
     if (smax > cap) smax = cap;
     if (smax > nblk) smax = nblk;
     if (smax < 1) smax = 1;
-    const int best = (nblk + smax - 1) / smax;   // fewest blocks any split must walk
+    // A split of two 64-row blocks costs about what a split of one does (the
+    // second block's rows land while the first is computed), while every extra
+    // split adds a partial to write and to combine and takes SMs the job's dim
+    // groups could use: the blocks a split walks count as at least two.
+    auto eff_blocks = [&](int c) { return std::max(2, (nblk + c - 1) / c); };
+    const int best = eff_blocks(smax);
     S = smax;
     for (int c = 1; c <= smax; ++c)
-      if ((nblk + c - 1) / c == best) {
+      if (eff_blocks(c) == best) {
         S = c;
         break;
       }

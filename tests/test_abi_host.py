@@ -78,9 +78,10 @@ def test_plan_is_deterministic_and_follows_rule():
                 assert 1 <= S <= nblk
                 assert s_q * S <= max(sms, s_q)
                 smax = max(1, min(sms // s_q, nblk, 64))
-                best = -(-nblk // smax)
-                assert -(-nblk // S) == best
-                assert all(-(-nblk // c) > best for c in range(1, S))
+                eff = lambda c: max(2, -(-nblk // c))   # one- and two-block splits count alike
+                best = eff(smax)
+                assert eff(S) == best
+                assert all(eff(c) > best for c in range(1, S))
                 # uniform workspace (0 for one split), and with the automatic
                 # choice also the balanced schedule's partial slots, counters and flags
                 ru = lambda x: -(-x // 256) * 256
@@ -106,15 +107,18 @@ def test_plan_is_deterministic_and_follows_rule():
 
 
 def test_plan_examples():
-    assert b.mla_decode_plan(1, 640, num_sms=152).num_splits == 10
-    assert b.mla_decode_plan(1, 640, num_sms=152).dim_groups == 4      # 40 CTAs
-    assert b.mla_decode_plan(6, 640, num_sms=152).dim_groups == 2      # 120 CTAs
-    assert b.mla_decode_plan(16, 640, num_sms=152).dim_groups == 1     # 80 CTAs
-    assert b.mla_decode_plan(1, 640, num_sms=20).dim_groups == 2
-    assert b.mla_decode_plan(1, 640, num_sms=10).dim_groups == 1
+    assert b.mla_decode_plan(1, 640, num_sms=152).num_splits == 5      # 2 blocks each
+    assert b.mla_decode_plan(1, 640, num_sms=152).dim_groups == 4      # 20 CTAs
+    assert b.mla_decode_plan(6, 640, num_sms=152).dim_groups == 4      # 5 splits, 120 CTAs
+    assert b.mla_decode_plan(10, 640, num_sms=152).dim_groups == 2     # 5 splits, 100 CTAs
+    assert b.mla_decode_plan(16, 640, num_sms=152).dim_groups == 1     # 5 splits, 80 CTAs
+    assert b.mla_decode_plan(1, 640, num_sms=10).dim_groups == 2       # 5 splits
+    assert b.mla_decode_plan(1, 640, num_sms=5).dim_groups == 1
+    assert b.mla_decode_plan(1, 128, num_sms=152).num_splits == 1     # 2 blocks: no split
     assert b.mla_decode_plan(16, 640, num_sms=152).num_splits == 5
     assert b.mla_decode_plan(96, 640, num_sms=152).num_splits == 1
     assert b.mla_decode_plan(1, 640, num_sms=152, max_splits=4).num_splits == 4
+    assert b.mla_decode_plan(1, 640, num_sms=152, max_splits=8).num_splits == 5
     p = b.mla_decode_plan(4, 64, num_sms=152, force_splits=16)   # more splits than blocks
     assert p.num_splits == 16 and p.num_blocks == 1
 
