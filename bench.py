@@ -491,7 +491,7 @@ def known_traffic(s_q, S):
     except OSError:
         return None
     table = {   # (source hash, s_q, S) -> dram bytes per launch (profiles/mla_decode_kernel_sq96_direct.md)
-        ("33d4418cd7b0cfac", 96, 1): 55_557_632,
+        ("176f9c28bf327e45", 96, 1): 55_575_040,
     }
     return table.get((h, s_q, S))
 
