@@ -4,10 +4,12 @@ measured HBM peak) across s_q x num_splits, on synthetic data shaped like the
 FlashMLA PR #25 workload (h_q = 64, d_qk = 576, d_v = 512, topk = 128 + 512,
 one bf16 latent KV cache of 131072 rows, FP8 e4m3 output with a per-tensor scale).
 
-One "step" is one decode call: the split kernel plus the combine (or the
-direct-epilogue kernel when the plan picks one split), replayed as a CUDA graph
-with inputs resident in HBM; L2 is flushed (256 MiB write, untimed) before every
-timed call and each call is timed with CUDA events on its stream.
+One "step" is one decode call through mla_sparse_decode: the split kernel plus
+the combine, the direct-epilogue kernel when the plan picks one split, or the
+balanced kernel, replayed as a CUDA graph with inputs resident in HBM; L2 is
+flushed (256 MiB write, untimed) before every timed call and each call is timed
+with CUDA events on its stream. The line also carries an s_q x num_splits sweep
+and the dense FP8 GQA variant's sweep (the same partial / LSE protocol).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--s-q 96] [--impl ours|reference]
 

@@ -12,7 +12,9 @@
 // Which jobs a CTA runs (the schedule):
 //   uniform   one (token, split) job per CTA: split s of S takes a near-equal run
 //             of 64-row blocks, remainder to the leading splits (cuDNN-frontend
-//             PR #768, SM120 FP8 commit); grid s_q * S.
+//             PR #768, SM120 FP8 commit). With dim_groups D > 1 a job runs on D
+//             CTAs that compute the same scores and softmax and each write
+//             512/D of the output dims; grid s_q * S * D.
 //   balanced  the s_q * nb blocks of all tokens, token-major, are cut into
 //             num_ctas near-equal contiguous ranges, one per CTA, so every SM
 //             walks the same number of rows whatever s_q is. A CTA runs one job
@@ -498,9 +500,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       //             have landed and its S buffer is free: softmax(g-2) published
       //             P_hi, i.e. PV_hi(g-2) was issued.
       // tcgen05 runs the MMAs in issue order. The thread polls the barriers
-      // without blocking (a suspended try_wait can wake well after the phase
-      // completes).
-      int nqk = 0, qrun = 0, nph = 0, npl = 0;
+      // without blocking (test_wait; measured a little faster here than
+      // letting try_wait suspend the thread).
+      int nqk = 0, nph = 0, npl = 0;
       int qj = 0, qk = 0, qn = j0.nsteps;   // QK cursor: job, step within it, its steps
       int hj = 0, hk = 0, hn = j0.nsteps;   // PV_hi cursor
       bool ok = true;
@@ -519,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++npl;
           progress = true;
         } else if (c_hi && ready(bar(B_PHI0 + (nph & 1)), (nph >> 1) & 1) &&
-                   (hk > 0 || hj == 0 || mbar_try_wait(bar(B_OFREE), (hj - 1) & 1))) {
+                   (hk > 0 || hj == 0 || ready(bar(B_OFREE), (hj - 1) & 1))) {
           tc_fence_after();
           pv_part(nph, 0, hk == 0);
           ++nph;
@@ -528,24 +530,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (++hj < njobs) hn = job_at(a, hj).nsteps;
           }
           progress = true;
-        } else if (c_qk && (qrun > 0 || (ready(bar(B_FULL0 + (nqk & 1)), (nqk >> 1) & 1) &&
-                                         (qk > 0 || mbar_try_wait(bar(B_QFULL), qj & 1))))) {
-          if (qrun == 0) {
-            // the rows were written by other threads' cp.async (generic proxy);
-            // make them visible to the tensor core's reads (async proxy)
-            fence_proxy_async_smem();
-            tc_fence_after();
-          }
-          while (qrun < 3) qk_run(nqk, qrun++);   // one unbroken run of 36 MMAs
-          {
-            mma_commit(bar(B_SFULL0 + (nqk & 1)));
-            qrun = 0;
-            ++nqk;
-            if (++qk == qn) {
-              mma_commit(bar(B_QFREE));   // the job's QKs are all issued
-              qk = 0;
-              if (++qj < njobs) qn = job_at(a, qj).nsteps;
-            }
+        } else if (c_qk && ready(bar(B_FULL0 + (nqk & 1)), (nqk >> 1) & 1) &&
+                   (qk > 0 || ready(bar(B_QFULL), qj & 1))) {
+          // the rows were written by other threads' cp.async (generic proxy);
+          // make them visible to the tensor core's reads (async proxy)
+          fence_proxy_async_smem();
+          tc_fence_after();
+#pragma unroll
+          for (int r = 0; r < 3; ++r) qk_run(nqk, r);   // one unbroken run of 36 MMAs
+          mma_commit(bar(B_SFULL0 + (nqk & 1)));
+          ++nqk;
+          if (++qk == qn) {
+            mma_commit(bar(B_QFREE));   // the job's QKs are all issued
+            qk = 0;
+            if (++qj < njobs) qn = job_at(a, qj).nsteps;
           }
           progress = true;
         }

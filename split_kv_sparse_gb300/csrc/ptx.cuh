@@ -83,7 +83,7 @@ static __device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t par
                                                uint32_t site) {
   uint64_t t0 = 0;
   for (uint32_t it = 1;; ++it) {
-    // polled: a try_wait may suspend the thread past the phase's completion
+    // polled with test_wait: measured a little faster than a suspending try_wait
     if (mbar_test_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*ctx.abort_flag) return false;
