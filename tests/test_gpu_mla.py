@@ -265,6 +265,56 @@ def test_full_size_sampled(s_q, S):
     assert_lse_close(r["lse"][ts], L)
 
 
+def test_many_tokens_sampled():
+    """1000 tokens: seven waves of (token) CTAs on 152 SMs, the automatic plan."""
+    inp = wl.mla_inputs(1000, 131072, 640, seed=6)
+    r = run_mla(inp, 0, out_dtype="bf16")
+    ts = np.array([0, 151, 152, 607, 999])
+    sub = wl.MlaInputs(q=inp.q[ts], kv=inp.kv, idx=inp.idx[ts], sink=None, sm_scale=inp.sm_scale)
+    O, L = oracle_mla(sub)
+    assert_cast_close(r["out"][ts], O, "bf16")
+    assert_lse_close(r["lse"][ts], L)
+
+
+def test_long_topk():
+    """topk 4096 (64 blocks): many splits of several blocks each."""
+    inp = wl.mla_inputs(2, 32768, 4096, seed=8, index_mode="uniform", with_sink=True)
+    O, L = oracle_mla(inp)
+    for S in (0, 7, 64):
+        r = run_mla(inp, S)
+        assert_o_close(r["out"].numpy(), O, what=f"O S={S}")
+        assert_lse_close(r["lse"], L, what=f"LSE S={S}")
+
+
+def test_cache_past_two_gigabytes():
+    """A 2.1M-row cache (2.4 GB, row offsets past 2^31 bytes), made of copies of a
+    32768-row seeded cache; the indices reach the last rows."""
+    base = wl.mla_inputs(3, 32768, 640, seed=12, index_mode="uniform")
+    n_kv = 2_100_000
+    dev = torch.device("cuda")
+    kv = base.kv.to(dev).repeat(-(-n_kv // 32768), 1)[:n_kv].contiguous()
+    g = torch.Generator().manual_seed(12)
+    idx = torch.randint(n_kv - 300_000, n_kv, (3, 640), generator=g, dtype=torch.int64)
+    idx[:, :64] = torch.arange(n_kv - 64, n_kv)          # the very last rows
+    idx = idx.to(torch.int32)
+    sub = wl.MlaInputs(q=base.q, kv=base.kv, idx=(idx.long() % 32768).to(torch.int32), sink=None,
+                       sm_scale=base.sm_scale)
+    O, L = oracle_mla(sub)
+    for S in (1, 4):
+        plan = b.mla_decode_plan(3, 640, force_splits=S)
+        ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev) if plan.workspace_bytes else None
+        out = torch.empty(3, 64, 512, dtype=torch.float32, device=dev)
+        lse = torch.empty(3, 64, dtype=torch.float32, device=dev)
+        b.mla_sparse_decode(plan, 3, base.q.to(dev), kv, n_kv, idx.to(dev), base.sm_scale, None, "f32", 1.0, out,
+                            lse, None, ws)
+        torch.cuda.synchronize()
+        check_status()
+        assert_o_close(out.cpu().numpy(), O, what=f"O S={S}")
+        assert_lse_close(lse.cpu().double().numpy(), L, what=f"LSE S={S}")
+    del kv
+    torch.cuda.empty_cache()
+
+
 def test_full_size_forced_splits_sampled():
     inp = wl.mla_inputs(16, 131072, 640, seed=4, with_sink=True)
     ts = np.array([0, 7, 15])
