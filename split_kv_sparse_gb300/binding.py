@@ -53,7 +53,7 @@ class SdpaPlan(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("h_q", ctypes.c_int32), ("h_kv", ctypes.c_int32),
                 ("d", ctypes.c_int32), ("max_q_per_seq", ctypes.c_int32), ("total_q_max", ctypes.c_int32),
                 ("max_kv", ctypes.c_int32), ("key_tile", ctypes.c_int32), ("num_splits", ctypes.c_int32),
-                ("num_sms", ctypes.c_int32), ("o_acc_bytes", ctypes.c_uint64),
+                ("num_sms", ctypes.c_int32), ("adaptive_splits", ctypes.c_int32), ("o_acc_bytes", ctypes.c_uint64),
                 ("lse_acc_offset", ctypes.c_uint64), ("lse_acc_bytes", ctypes.c_uint64),
                 ("workspace_bytes", ctypes.c_uint64)]
 

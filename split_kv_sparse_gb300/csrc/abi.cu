@@ -119,6 +119,8 @@ int64_t uniform_makespan(int64_t s_q, int nb, int S, int num_sms) {
 // (topk 640): the schedule ran as slow as per + 5.5 to per + 5.7 blocks of the
 // uniform grid.
 constexpr int64_t kBalancedOverheadBlocks = 6;
+// The most splits the dense planner's per-sequence rule gives one sequence.
+constexpr int kDenseMaxAdaptiveSplits = 16;
 // CTAs per (token, split) job: the largest of 4, 2, 1 that still fits `jobs`
 // jobs on num_sms SMs at one CTA each.
 int dim_groups_for(int64_t jobs, int num_sms) {
@@ -518,21 +520,16 @@ int sdpa_fp8_decode_plan(int batch, int h_q, int h_kv, int d, int max_q_per_seq,
   }
   const int ntiles = (max_kv + 127) / 128;
   int S = force_splits;
+  int adaptive = 0;
   if (S == 0) {
+    // Each sequence gets its own split count, from the KV lengths, on the GPU:
+    // the batch's tiles x KV heads are spread over one wave of SMs (T tiles per
+    // split), so a ragged batch does not leave SMs idle behind its longest
+    // sequence. S bounds the count (and sizes the workspace).
     const int cap = max_splits > 0 ? max_splits : MLA_MAX_SPLITS;
-    // up to two waves of CTAs: the plan knows only the longest sequence, and in
-    // a ragged batch the jobs of shorter ones end early and free their SMs
-    int smax = 2 * num_sms / (batch * h_kv);
-    if (smax > cap) smax = cap;
-    if (smax > ntiles) smax = ntiles;
-    if (smax < 1) smax = 1;
-    const int best = (ntiles + smax - 1) / smax;
-    S = smax;
-    for (int c = 1; c <= smax; ++c)
-      if ((ntiles + c - 1) / c == best) {
-        S = c;
-        break;
-      }
+    S = std::min(std::min(cap, kDenseMaxAdaptiveSplits), ntiles);
+    if (S < 1) S = 1;
+    adaptive = S > 1 ? 1 : 0;
   }
   out->batch = batch;
   out->h_q = h_q;
@@ -544,6 +541,7 @@ int sdpa_fp8_decode_plan(int batch, int h_q, int h_kv, int d, int max_q_per_seq,
   out->key_tile = 128;
   out->num_splits = S;
   out->num_sms = num_sms;
+  out->adaptive_splits = adaptive;
   if (S > 1) {
     out->o_acc_bytes = static_cast<uint64_t>(S) * total_q_max * h_q * d * 4ull;
     out->lse_acc_offset = round_up(out->o_acc_bytes, 256);
@@ -557,8 +555,10 @@ namespace {
 int sdpa_launch(int batch, int h_q, int h_kv, int total_q, int64_t total_kv, int num_splits, const void* q,
                 const void* k, const void* v, const int32_t* cu_q, const int32_t* cu_kv, const float* dq,
                 const float* dk, const float* dv, float sm_scale, float* o_acc, float* lse_acc, void* out,
-                int out_dtype, float inv_scale, float* lse_out, float* amax, bool direct, void* stream) {
+                int out_dtype, float inv_scale, float* lse_out, float* amax, bool direct, void* stream,
+                int adaptive = 0, int num_sms = 0) {
   if (batch < 1 || h_kv < 1 || h_q < h_kv || h_q % h_kv != 0) return MLA_ERR_INVALID_ARG;
+  if (adaptive && (direct || num_sms < 1)) return MLA_ERR_INVALID_ARG;
   const int group = h_q / h_kv;
   if (64 % group != 0) return MLA_ERR_UNSUPPORTED;
   if (q == nullptr || k == nullptr || v == nullptr || cu_q == nullptr || cu_kv == nullptr)
@@ -601,6 +601,8 @@ int sdpa_launch(int batch, int h_q, int h_kv, int total_q, int64_t total_kv, int
   a.h_kv = h_kv;
   a.total_q = total_q;
   a.num_splits = num_splits;
+  a.adaptive = adaptive;
+  a.num_sms = num_sms;
   a.scale_log2 = sm_scale * 1.4426950408889634f;
   a.o_acc = o_acc;
   a.lse_acc = lse_acc;
@@ -655,7 +657,7 @@ int sdpa_fp8_decode_split(const sdpa_plan_t* plan, int total_q, int64_t total_kv
                      cu_seqlens_q, cu_seqlens_kv, descale_q, descale_k, descale_v, sm_scale,
                      static_cast<float*>(workspace),
                      reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan->lse_acc_offset), nullptr, 0,
-                     1.f, nullptr, nullptr, false, stream);
+                     1.f, nullptr, nullptr, false, stream, plan->adaptive_splits, plan->num_sms);
 }
 
 int sdpa_split_combine(const sdpa_plan_t* plan, int total_q, const void* workspace, int out_dtype,

@@ -111,6 +111,8 @@ struct SdpaArgs {
   const float* descale_k;
   const float* descale_v;
   int batch, h_q, h_kv, total_q, num_splits;
+  int adaptive;                 // per-sequence split counts (<= num_splits) from the KV lengths
+  int num_sms;                  // SM count the adaptive rule spreads the work over
   float scale_log2;
   float* o_acc;                 // split path [S][total_q][h_q][128]
   float* lse_acc;               // [S][total_q][h_q]

@@ -92,11 +92,54 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   // ---- job decode (shared by every role) ------------------------------------
-  const int S = a.num_splits;
-  const int s = blockIdx.x % S;
-  const int bg = blockIdx.x / S;
-  const int g = bg % a.h_kv;
-  const int b = bg / a.h_kv;
+  const int S = a.num_splits;   // splits per sequence (adaptive: the most any sequence gets)
+  int b = 0, g = 0, s = 0, Sb = S;
+  if (!a.adaptive) {
+    s = blockIdx.x % S;
+    const int bg = blockIdx.x / S;
+    g = bg % a.h_kv;
+    b = bg / a.h_kv;
+  } else {
+    // Sequence bb gets clamp(ceil(tiles / T), 1, S) near-equal splits, with T
+    // the fewest tiles per split for which the batch's jobs (x KV heads) fit one
+    // wave of num_sms CTAs (or every sequence has one split). Jobs are listed
+    // sequence by sequence, (split, KV head) within one; a CTA past the last job
+    // has nothing to do.
+    int total = 0, longest = 1;
+    for (int bb = 0; bb < a.batch; ++bb) {
+      const int tb = (__ldg(a.cu_kv + bb + 1) - __ldg(a.cu_kv + bb) + kTile - 1) / kTile;
+      total += tb;
+      longest = max(longest, tb);
+    }
+    auto jobs = [&](int tt) {
+      int n = 0;
+      for (int bb = 0; bb < a.batch; ++bb) {
+        const int tb = (__ldg(a.cu_kv + bb + 1) - __ldg(a.cu_kv + bb) + kTile - 1) / kTile;
+        n += min(S, max(1, (tb + tt - 1) / tt));
+      }
+      return n * a.h_kv;
+    };
+    int T = max(1, (total * a.h_kv + a.num_sms - 1) / a.num_sms);
+    while (T < longest && jobs(T) > a.num_sms) ++T;
+    int j = blockIdx.x;
+    b = -1;
+    for (int bb = 0; bb < a.batch; ++bb) {
+      const int tb = (__ldg(a.cu_kv + bb + 1) - __ldg(a.cu_kv + bb) + kTile - 1) / kTile;
+      const int sb = min(S, max(1, (tb + T - 1) / T));
+      if (j < sb * a.h_kv) {
+        b = bb;
+        Sb = sb;
+        s = j / a.h_kv;
+        g = j - s * a.h_kv;
+        break;
+      }
+      j -= sb * a.h_kv;
+    }
+    if (b < 0) {
+      grid_launch_dependents();
+      return;
+    }
+  }
   const int group = a.h_q / a.h_kv;
   const int q0 = a.cu_q[b];
   const int sq = a.cu_q[b + 1] - q0;
@@ -104,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kvlen = a.cu_kv[b + 1] - k0;
   const int R = sq * group;                              // valid rows, <= 64
   const int ntiles_all = (kvlen + kTile - 1) / kTile;
-  const int base = ntiles_all / S, rem = ntiles_all - base * S;
+  const int base = ntiles_all / Sb, rem = ntiles_all - base * Sb;
   const int tile0 = s * base + min(s, rem);
   const int nt = base + (s < rem ? 1 : 0);
   const int key_end = min((tile0 + nt) * kTile, kvlen);  // exclusive, sequence-relative
@@ -122,6 +165,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     grid_launch_dependents();
     if (threadIdx.x == 0) atomicOr(&a.status[0], 2u);
     return;
+  }
+  if (a.adaptive && s == 0 && !direct) {
+    // the splits this sequence does not use: LSE = -inf, so the combine gives
+    // them weight 0 and never reads their O
+    for (int i = threadIdx.x; i < R * (S - Sb); i += kThreads) {
+      const int rho = i % R, sp = Sb + i / R;
+      const size_t tok = static_cast<size_t>(q0 + rho / group);
+      const size_t head = static_cast<size_t>(g * group + rho % group);
+      a.lse_acc[(static_cast<size_t>(sp) * a.total_q + tok) * a.h_q + head] = -INFINITY;
+    }
   }
   if (nt == 0 || R <= 0) {
     // nothing to attend in this split: O = 0, LSE = -inf for the job's rows
@@ -529,7 +582,11 @@ cudaError_t prepare_sdpa_kernels() {
 
 cudaError_t launch_sdpa_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                const SdpaArgs& a, bool direct, cudaStream_t stream) {
-  const dim3 grid(static_cast<unsigned>(a.batch) * a.h_kv * a.num_splits);
+  // adaptive: at most num_sms jobs, unless every sequence has one split
+  const long long all = static_cast<long long>(a.batch) * a.h_kv * a.num_splits;
+  const long long one = static_cast<long long>(a.batch) * a.h_kv;
+  const long long bound = a.adaptive ? (one > a.num_sms ? one : static_cast<long long>(a.num_sms)) : all;
+  const dim3 grid(static_cast<unsigned>(bound < all ? bound : all));
   sdpa_decode_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, a, direct ? 1 : 0);
   return cudaGetLastError();
 }

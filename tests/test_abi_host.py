@@ -194,8 +194,11 @@ def test_no_device_is_reported_not_crashed():
 
 def test_dense_plan():
     p = b.sdpa_fp8_decode_plan(8, 32, 8, 128, 16, 128, 16384, num_sms=152)
-    assert p.num_splits >= 1 and 8 * 8 * p.num_splits <= 2 * 152
-    assert p.num_splits == 4    # 128 tiles: 4 splits of 32 (256 CTAs)
+    assert p.num_splits == 16 and p.adaptive_splits == 1   # per-sequence counts, at most 16
+    pf = b.sdpa_fp8_decode_plan(8, 32, 8, 128, 16, 128, 16384, num_sms=152, force_splits=4)
+    assert pf.num_splits == 4 and pf.adaptive_splits == 0
+    p1 = b.sdpa_fp8_decode_plan(8, 32, 8, 128, 16, 128, 100, num_sms=152)   # one tile: no split
+    assert p1.num_splits == 1 and p1.adaptive_splits == 0 and p1.workspace_bytes == 0
     assert p.o_acc_bytes == (p.num_splits * 128 * 32 * 128 * 4 if p.num_splits > 1 else 0)
     with pytest.raises(b.SplitKVError) as e:
         b.sdpa_fp8_decode_plan(8, 32, 8, 64, 16, 128, 16384, num_sms=152)

@@ -92,6 +92,25 @@ def test_group_sizes(h_q, h_kv, q_per_seq):
         _check(inp, run_sdpa(inp, S), O, L)
 
 
+def test_adaptive_splits_on_a_ragged_batch():
+    """The planner's per-sequence split counts: a long sequence beside short ones.
+    Final O / LSE as the oracle; the split slots a sequence does not use hold
+    LSE = -inf."""
+    inp = wl.sdpa_inputs(4, 8, 2, 128, q_per_seq=(1, 4), kv_len=(100, 20000), seed=9)
+    O, L = osd.attention(inp)
+    r = run_sdpa(inp, 0, keep_workspace=True)
+    assert r["plan"].adaptive_splits == 1
+    _check(inp, r, O, L)
+    skv = (inp.cu_seqlens_kv[1:] - inp.cu_seqlens_kv[:-1]).tolist()
+    cq = inp.cu_seqlens_q.tolist()
+    # some sequence uses fewer splits than the bound: its last slot is -inf, its first is not
+    unused = [b for b in range(4) if np.all(np.isneginf(r["lse_acc"][-1, cq[b]:cq[b + 1]]))]
+    assert unused, "every sequence used every split slot"
+    for b in unused:
+        assert np.all(np.isfinite(r["lse_acc"][0, cq[b]:cq[b + 1]]))
+    assert max(skv) > 8 * 128
+
+
 def test_single_key_sequences():
     inp = wl.sdpa_inputs(4, 8, 2, 128, q_per_seq=(1, 1), kv_len=(1, 1), seed=3)
     O, L = osd.attention(inp)
