@@ -254,15 +254,32 @@ DENSE_DESC = ("dense FP8 GQA split-KV SDPA decode: batch 8, 32 query / 8 KV head
               "bf16 O, seed 0")
 
 
-def dense_bytes(sq, skv, h_q: int, h_kv: int, d: int, S: int) -> int:
+def dense_splits(skv, h_kv: int, S: int, num_sms: int):
+    """Per-sequence split counts of the dense planner's adaptive rule (restated
+    from sdpa_fp8_decode_plan): clamp(ceil(tiles / T), 1, S) with T the fewest
+    tiles per split from ceil(sum tiles * h_kv / num_sms) up whose jobs fit
+    num_sms CTAs."""
+    tiles = [-(-int(k) // 128) for k in skv]
+    longest = max([1] + tiles)
+    jobs = lambda T: sum(min(S, max(1, -(-t // T))) for t in tiles) * h_kv
+    T = max(1, -(-(sum(tiles) * h_kv) // num_sms))
+    while T < longest and jobs(T) > num_sms:
+        T += 1
+    return [min(S, max(1, -(-t // T))) for t in tiles]
+
+
+def dense_bytes(sq, skv, h_q: int, h_kv: int, d: int, S: int, splits=None) -> int:
     """Algorithmic bytes of one dense call: every sequence's K and V (e4m3, all KV
-    heads), Q (e4m3), bf16 O and fp32 LSE; S > 1 adds the fp32 partial O + LSE,
-    written by the split kernel and read by the combine."""
+    heads), Q (e4m3), bf16 O and fp32 LSE; with splits, the fp32 partial O + LSE of
+    every split a sequence uses, written by the split kernel and read by the
+    combine (splits: per-sequence counts, else S for every sequence)."""
     total_q = int(sum(sq))
     kv = 2 * int(sum(skv)) * h_kv * d
     q = total_q * h_q * d
     out = total_q * h_q * (d * 2 + 4)
-    partial = 2 * S * total_q * h_q * (d + 1) * 4 if S > 1 else 0
+    if splits is None:
+        splits = [S] * len(sq)
+    partial = 0 if S == 1 else sum(2 * n * int(t) * h_q * (d + 1) * 4 for n, t in zip(splits, sq))
     return kv + q + out + partial
 
 
@@ -307,7 +324,9 @@ class DenseCase:
         return Case.time(self, graph, steps, warmup, flush)
 
     def bytes(self) -> int:
-        return dense_bytes(self.sq, self.skv, self.inp.h_q, self.inp.h_kv, self.inp.d, self.S)
+        splits = (dense_splits(self.skv, self.inp.h_kv, self.S, self.plan.num_sms) if self.plan.adaptive_splits
+                  else None)
+        return dense_bytes(self.sq, self.skv, self.inp.h_q, self.inp.h_kv, self.inp.d, self.S, splits)
 
 
 def run_gpu(args):
@@ -419,6 +438,8 @@ def run_gpu(args):
             ks = statistics.fmean(c.time(c.g_kernel, args.sweep_steps, 3, flush))
             cb = c.bytes()
             dense_sweep.append({"num_splits": S if S else "planner", "planner": S == 0, "splits_used": c.S,
+                                "per_sequence_splits": (dense_splits(c.skv, 8, c.S, c.plan.num_sms)
+                                                        if c.plan.adaptive_splits else None),
                                 "us_per_call": round(us, 2), "split_kernel_us": round(ks, 2), "alg_bytes": cb,
                                 "gb_s": round(cb / (us * 1e-6) / 1e9, 1),
                                 "frac_of_peak": round(cb / (us * 1e-6) / 1e9 / peak, 4)})
