@@ -488,78 +488,117 @@ __global__ void __launch_bounds__(kThreads, 1)
                     (!first || part > 0 || kk > 0));
         }
       };
-      int total = 0;
-#pragma unroll 1
-      for (int j = 0; j < njobs; ++j) total += (j == 0) ? j0.nsteps : job_at(a, j).nsteps;
-      // Issue order, highest priority first:
-      //   PV_lo(g)  once softmax(g) has written P_lo; its completion frees the
-      //             half for the loads of step g+2 (the loop's critical chain);
-      //   PV_hi(g)  once softmax(g) has written P_hi (the first step of a job
-      //             also waits for the previous job's epilogue to read O^T);
-      //   QK(g)     once its rows (and, first in a job, its Q)
-      //             have landed and its S buffer is free: softmax(g-2) published
-      //             P_hi, i.e. PV_hi(g-2) was issued.
-      // tcgen05 runs the MMAs in issue order. The thread polls the barriers
-      // without blocking (test_wait; measured a little faster here than
-      // letting try_wait suspend the thread).
-      int nqk = 0, nph = 0, npl = 0;
-      int qj = 0, qk = 0, qn = j0.nsteps;   // QK cursor: job, step within it, its steps
-      int hj = 0, hk = 0, hn = j0.nsteps;   // PV_hi cursor
       bool ok = true;
-      uint64_t t_idle = 0;
-      while (ok && npl < total) {
-        const bool c_lo = npl < nph;
-        const bool c_hi = nph < nqk;
-        const bool c_qk = nqk < total && nqk <= nph + 1;
-        auto ready = [&](uint32_t b, uint32_t ph) { return mbar_test_wait(b, ph); };
-        bool progress = false;
-        if (c_lo && ready(bar(B_PLO0 + (npl & 1)), (npl >> 1) & 1)) {
-          tc_fence_after();
-          pv_part(npl, 1, false);
-          mma_commit(bar(B_EMPTY0 + (npl & 1)));
-          mma_commit(bar(B_PVDONE));
-          ++npl;
-          progress = true;
-        } else if (c_hi && ready(bar(B_PHI0 + (nph & 1)), (nph >> 1) & 1) &&
-                   (hk > 0 || hj == 0 || ready(bar(B_OFREE), (hj - 1) & 1))) {
-          tc_fence_after();
-          pv_part(nph, 0, hk == 0);
-          ++nph;
-          if (++hk == hn) {
-            hk = 0;
-            if (++hj < njobs) hn = job_at(a, hj).nsteps;
-          }
-          progress = true;
-        } else if (c_qk && ready(bar(B_FULL0 + (nqk & 1)), (nqk >> 1) & 1) &&
-                   (qk > 0 || ready(bar(B_QFULL), qj & 1))) {
-          // the rows were written by other threads' cp.async (generic proxy);
-          // make them visible to the tensor core's reads (async proxy)
-          fence_proxy_async_smem();
-          tc_fence_after();
+      if (a.sched == 0) {
+        // Uniform schedule, one job: a fixed order by pairs of steps,
+        //   QK(g) QK(g+1) PV_hi(g) PV_lo(g) PV_hi(g+1) PV_lo(g+1),
+        // each group issued after its own bounded wait. Every wait's producer was
+        // issued earlier in this order (rows of g+1 come after PV_lo(g-1), P_lo(g)
+        // after PV_lo(g-1) is done, S(g)'s buffer is free once PV_hi(g-2) is
+        // issued), so the order cannot deadlock. Measured faster than the polling
+        // loop of the balanced schedule below, by 4-6 % over s_q = 1 .. 384.
+        const int n = j0.nsteps;
+        auto wait = [&](uint32_t b, uint32_t ph, uint32_t site) {
+          if (ok && !wait_bounded(b, ph, wc, site)) ok = false;
+          return ok;
+        };
+        for (int g = 0; g < n && ok; g += 2) {
+          for (int h = g; h < g + 2 && h < n; ++h) {
+            if (!wait(bar(B_FULL0 + (h & 1)), (h >> 1) & 1, W_MMA_STALL)) break;
+            if (h == 0 && !wait(bar(B_QFULL), 0, W_MMA_Q)) break;
+            // the rows were written by other threads' cp.async (generic proxy);
+            // make them visible to the tensor core's reads (async proxy)
+            fence_proxy_async_smem();
+            tc_fence_after();
 #pragma unroll
-          for (int r = 0; r < 3; ++r) qk_run(nqk, r);   // one unbroken run of 36 MMAs
-          mma_commit(bar(B_SFULL0 + (nqk & 1)));
-          ++nqk;
-          if (++qk == qn) {
-            mma_commit(bar(B_QFREE));   // the job's QKs are all issued
-            qk = 0;
-            if (++qj < njobs) qn = job_at(a, qj).nsteps;
+            for (int r = 0; r < 3; ++r) qk_run(h, r);   // one unbroken run of 36 MMAs
+            mma_commit(bar(B_SFULL0 + (h & 1)));
+            if (h == n - 1) mma_commit(bar(B_QFREE));   // the job's QKs are all issued
           }
-          progress = true;
+          for (int h = g; h < g + 2 && h < n && ok; ++h) {
+            if (!wait(bar(B_PHI0 + (h & 1)), (h >> 1) & 1, W_MMA_STALL)) break;
+            tc_fence_after();
+            pv_part(h, 0, h == 0);
+            if (!wait(bar(B_PLO0 + (h & 1)), (h >> 1) & 1, W_MMA_STALL)) break;
+            tc_fence_after();
+            pv_part(h, 1, false);
+            mma_commit(bar(B_EMPTY0 + (h & 1)));   // the half is free for the rows of step h+2
+            mma_commit(bar(B_PVDONE));
+          }
         }
-        if (progress) {
-          t_idle = 0;
-        } else {
-          const uint64_t now = globaltimer_ns();
-          if (*abort_flag) {
-            ok = false;
-          } else if (t_idle == 0) {
-            t_idle = now;
-          } else if (now - t_idle > a.wait_limit_ns) {
-            *abort_flag = 1;
-            atomicOr(&a.status[0], 1u);
-            atomicCAS(&a.status[1], 0u, W_MMA_STALL);
-            ok = false;
+      } else {
+        int total = 0;
+#pragma unroll 1
+        for (int j = 0; j < njobs; ++j) total += (j == 0) ? j0.nsteps : job_at(a, j).nsteps;
+        // Issue order, highest priority first:
+        //   PV_lo(g)  once softmax(g) has written P_lo; its completion frees the
+        //             half for the loads of step g+2 (the loop's critical chain);
+        //   PV_hi(g)  once softmax(g) has written P_hi (the first step of a job
+        //             also waits for the previous job's epilogue to read O^T);
+        //   QK(g)     once its rows (and, first in a job, its Q)
+        //             have landed and its S buffer is free: softmax(g-2) published
+        //             P_hi, i.e. PV_hi(g-2) was issued.
+        // tcgen05 runs the MMAs in issue order. The thread polls the barriers
+        // without blocking (test_wait; measured a little faster here than
+        // letting try_wait suspend the thread).
+        int nqk = 0, nph = 0, npl = 0;
+        int qj = 0, qk = 0, qn = j0.nsteps;   // QK cursor: job, step within it, its steps
+        int hj = 0, hk = 0, hn = j0.nsteps;   // PV_hi cursor
+        uint64_t t_idle = 0;
+        while (ok && npl < total) {
+          const bool c_lo = npl < nph;
+          const bool c_hi = nph < nqk;
+          const bool c_qk = nqk < total && nqk <= nph + 1;
+          auto ready = [&](uint32_t b, uint32_t ph) { return mbar_test_wait(b, ph); };
+          bool progress = false;
+          if (c_lo && ready(bar(B_PLO0 + (npl & 1)), (npl >> 1) & 1)) {
+            tc_fence_after();
+            pv_part(npl, 1, false);
+            mma_commit(bar(B_EMPTY0 + (npl & 1)));
+            mma_commit(bar(B_PVDONE));
+            ++npl;
+            progress = true;
+          } else if (c_hi && ready(bar(B_PHI0 + (nph & 1)), (nph >> 1) & 1) &&
+                     (hk > 0 || hj == 0 || ready(bar(B_OFREE), (hj - 1) & 1))) {
+            tc_fence_after();
+            pv_part(nph, 0, hk == 0);
+            ++nph;
+            if (++hk == hn) {
+              hk = 0;
+              if (++hj < njobs) hn = job_at(a, hj).nsteps;
+            }
+            progress = true;
+          } else if (c_qk && ready(bar(B_FULL0 + (nqk & 1)), (nqk >> 1) & 1) &&
+                     (qk > 0 || ready(bar(B_QFULL), qj & 1))) {
+            // the rows were written by other threads' cp.async (generic proxy);
+            // make them visible to the tensor core's reads (async proxy)
+            fence_proxy_async_smem();
+            tc_fence_after();
+#pragma unroll
+            for (int r = 0; r < 3; ++r) qk_run(nqk, r);   // one unbroken run of 36 MMAs
+            mma_commit(bar(B_SFULL0 + (nqk & 1)));
+            ++nqk;
+            if (++qk == qn) {
+              mma_commit(bar(B_QFREE));   // the job's QKs are all issued
+              qk = 0;
+              if (++qj < njobs) qn = job_at(a, qj).nsteps;
+            }
+            progress = true;
+          }
+          if (progress) {
+            t_idle = 0;
+          } else {
+            const uint64_t now = globaltimer_ns();
+            if (*abort_flag) {
+              ok = false;
+            } else if (t_idle == 0) {
+              t_idle = now;
+            } else if (now - t_idle > a.wait_limit_ns) {
+              *abort_flag = 1;
+              atomicOr(&a.status[0], 1u);
+              atomicCAS(&a.status[1], 0u, W_MMA_STALL);
+              ok = false;
+            }
           }
         }
       }
