@@ -230,6 +230,30 @@ MLA_API int mla_sparse_decode(const mla_plan_t* plan, int s_q,
                       void* out, float* lse_out, float* amax_out,
                       void* workspace, void* stream);
 
+/* The same decode step with the step's inputs and results in host memory, for a
+ * caller whose queries and indices arrive from the host and whose output is read
+ * there. In order on `stream`: q and idx are copied from host memory into the
+ * caller's device buffers, mla_sparse_decode runs on those, and out (and lse)
+ * are copied back into host memory; one cudaMemcpyAsync per buffer. With
+ * page-locked host buffers every copy is asynchronous and the call returns at
+ * once; with pageable ones the runtime may finish a copy before returning. The
+ * host results are complete once the stream has passed the call. The KV cache,
+ * sink, workspace and amax stay on the device (decode state).
+ *   q_host   bf16 [s_q][h_q][576]            copied into q_dev (device, same size, 16-byte aligned)
+ *   idx_host int32 [s_q][plan->topk]         copied into idx_dev (device, same size)
+ *   out_dev  [s_q][h_q][512] of out_dtype    copied into out_host
+ *   lse_dev, lse_host  fp32 [s_q][h_q], both NULL or both set
+ * Other arguments as mla_sparse_decode. A NULL buffer (other than the lse pair,
+ * sink, amax_out and workspace as mla_sparse_decode allows) or a lone lse
+ * pointer gives MLA_ERR_INVALID_ARG before anything is queued; a failed copy
+ * gives MLA_ERR_CUDA. */
+MLA_API int mla_sparse_decode_host(const mla_plan_t* plan, int s_q,
+                           const void* q_host, void* q_dev, const void* kv, int64_t n_kv,
+                           const int32_t* idx_host, int32_t* idx_dev, float sm_scale, const float* sink,
+                           int out_dtype, float out_inv_scale,
+                           void* out_dev, void* out_host, float* lse_dev, float* lse_host,
+                           float* amax_out, void* workspace, void* stream);
+
 /* ======================================================================= *
  *  Dense FP8 GQA split-KV SDPA decode (cuDNN-frontend PR #768 form)        *
  * ======================================================================= */

@@ -27,9 +27,10 @@ OUT_DTYPES = {"f32": MLA_OUT_F32, "bf16": MLA_OUT_BF16, "e4m3": MLA_OUT_E4M3}
 # Every symbol the header declares (checked by the library-load test).
 EXPORTS = [
     "mla_decode_plan", "mla_sparse_decode_split", "mla_split_combine", "mla_sparse_decode_direct",
-    "mla_sparse_decode", "sdpa_fp8_decode_plan", "sdpa_fp8_decode_split", "sdpa_split_combine",
-    "sdpa_fp8_decode_direct", "sdpa_fp8_decode", "mla_get_status", "mla_selftest_wait_timeout",
-    "mla_status_string", "mla_abi_version", "mla_sparse_decode_noalloc", "mla_workspace_init",
+    "mla_sparse_decode", "mla_sparse_decode_host", "sdpa_fp8_decode_plan", "sdpa_fp8_decode_split",
+    "sdpa_split_combine", "sdpa_fp8_decode_direct", "sdpa_fp8_decode", "mla_get_status",
+    "mla_selftest_wait_timeout", "mla_status_string", "mla_abi_version", "mla_sparse_decode_noalloc",
+    "mla_workspace_init",
 ]
 
 
@@ -71,6 +72,8 @@ _SIGS = {
     "mla_split_combine": [ctypes.POINTER(MlaPlan), _I, _P, _P, _I, _F, _P, _P, _P, _P],
     "mla_sparse_decode_direct": [_I, _I, _P, _P, _I64, _P, _F, _P, _I, _F, _P, _P, _P, _P],
     "mla_sparse_decode": [ctypes.POINTER(MlaPlan), _I, _P, _P, _I64, _P, _F, _P, _I, _F, _P, _P, _P, _P, _P],
+    "mla_sparse_decode_host": [ctypes.POINTER(MlaPlan), _I, _P, _P, _P, _I64, _P, _P, _F, _P, _I, _F, _P, _P, _P,
+                               _P, _P, _P, _P],
     "sdpa_fp8_decode_plan": [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(SdpaPlan)],
     "sdpa_fp8_decode_split": [ctypes.POINTER(SdpaPlan), _I, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _F, _P, _P],
     "sdpa_split_combine": [ctypes.POINTER(SdpaPlan), _I, _P, _I, _F, _P, _P, _P, _P],
@@ -174,6 +177,18 @@ def mla_sparse_decode(plan: MlaPlan, s_q: int, q, kv, n_kv: int, idx, sm_scale: 
                                    _ptr(sink), _dtype(out_dtype), out_inv_scale, _ptr(out), _ptr(lse_out),
                                    _ptr(amax_out), _ptr(workspace), _stream(stream)),
            "mla_sparse_decode")
+
+
+def mla_sparse_decode_host(plan: MlaPlan, s_q: int, q_host, q_dev, kv, n_kv: int, idx_host, idx_dev,
+                           sm_scale: float, sink, out_dtype, out_inv_scale: float, out_dev, out_host,
+                           lse_dev=None, lse_host=None, amax_out=None, workspace=None, stream=None):
+    """The decode step with q / idx / out / lse in host memory (pinned for asynchronous copies): the
+    library copies them through the given device buffers around mla_sparse_decode, on `stream`."""
+    _check(lib().mla_sparse_decode_host(ctypes.byref(plan), s_q, _ptr(q_host), _ptr(q_dev), _ptr(kv), n_kv,
+                                        _ptr(idx_host), _ptr(idx_dev), sm_scale, _ptr(sink), _dtype(out_dtype),
+                                        out_inv_scale, _ptr(out_dev), _ptr(out_host), _ptr(lse_dev),
+                                        _ptr(lse_host), _ptr(amax_out), _ptr(workspace), _stream(stream)),
+           "mla_sparse_decode_host")
 
 
 # -------------------------------------------------------------------- dense --

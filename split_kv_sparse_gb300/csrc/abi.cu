@@ -499,6 +499,36 @@ int mla_sparse_decode(const mla_plan_t* plan, int s_q, const void* q, const void
                           stream);
 }
 
+int mla_sparse_decode_host(const mla_plan_t* plan, int s_q, const void* q_host, void* q_dev, const void* kv,
+                           int64_t n_kv, const int32_t* idx_host, int32_t* idx_dev, float sm_scale,
+                           const float* sink, int out_dtype, float out_inv_scale, void* out_dev, void* out_host,
+                           float* lse_dev, float* lse_host, float* amax_out, void* workspace, void* stream) {
+  if (plan == nullptr || s_q < 1 || plan->topk < 1 || plan->h_q != kMlaHeads) return MLA_ERR_INVALID_ARG;
+  if (q_host == nullptr || q_dev == nullptr || idx_host == nullptr || idx_dev == nullptr || out_dev == nullptr ||
+      out_host == nullptr || (lse_dev == nullptr) != (lse_host == nullptr) || !valid_out_dtype(out_dtype))
+    return MLA_ERR_INVALID_ARG;
+  const size_t rows = static_cast<size_t>(s_q) * kMlaHeads;
+  const size_t q_bytes = rows * kMlaDqk * 2;
+  const size_t idx_bytes = static_cast<size_t>(s_q) * plan->topk * sizeof(int32_t);
+  const size_t out_bytes = rows * kMlaDv * (out_dtype == MLA_OUT_F32 ? 4 : out_dtype == MLA_OUT_BF16 ? 2 : 1);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  auto copy = [&](void* dst, const void* src, size_t n, cudaMemcpyKind kind) {
+    if (cudaMemcpyAsync(dst, src, n, kind, st) == cudaSuccess) return true;
+    cudaGetLastError();
+    return false;
+  };
+  if (!copy(q_dev, q_host, q_bytes, cudaMemcpyHostToDevice) ||
+      !copy(idx_dev, idx_host, idx_bytes, cudaMemcpyHostToDevice))
+    return MLA_ERR_CUDA;
+  const int rc = mla_sparse_decode(plan, s_q, q_dev, kv, n_kv, idx_dev, sm_scale, sink, out_dtype, out_inv_scale,
+                                   out_dev, lse_dev, amax_out, workspace, stream);
+  if (rc != MLA_OK) return rc;
+  if (!copy(out_host, out_dev, out_bytes, cudaMemcpyDeviceToHost)) return MLA_ERR_CUDA;
+  if (lse_dev != nullptr && !copy(lse_host, lse_dev, rows * sizeof(float), cudaMemcpyDeviceToHost))
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
 // ---------------------------------------------------------------- dense -----
 
 int sdpa_fp8_decode_plan(int batch, int h_q, int h_kv, int d, int max_q_per_seq, int total_q_max, int max_kv,

@@ -166,6 +166,28 @@ def test_split_call_argument_checks_before_device_work():
     assert e.value.status == 1
 
 
+def test_host_buffer_call_argument_checks_before_device_work():
+    """mla_sparse_decode_host rejects a missing buffer, a lone LSE pointer or a bad output type
+    before it queues a copy."""
+    plan = b.mla_decode_plan(4, 640, num_sms=152, force_splits=1)
+    fake = 1 << 20   # never dereferenced
+    full = dict(q_host=fake, q_dev=fake, idx_host=fake, idx_dev=fake, out_dev=fake, out_host=fake,
+                lse_dev=None, lse_host=None, out_dtype="e4m3")
+    cases = [dict(q_host=None), dict(q_dev=None), dict(idx_host=None), dict(idx_dev=None), dict(out_dev=None),
+             dict(out_host=None), dict(lse_dev=fake), dict(lse_host=fake), dict(out_dtype=7)]
+    for c in cases:
+        a = full | c
+        with pytest.raises(b.SplitKVError) as e:
+            b.mla_sparse_decode_host(plan, 2, a["q_host"], a["q_dev"], fake, 100, a["idx_host"], a["idx_dev"],
+                                     0.1, None, a["out_dtype"], 64.0, a["out_dev"], a["out_host"],
+                                     a["lse_dev"], a["lse_host"], stream=0)
+        assert e.value.status == 1, c
+    with pytest.raises(b.SplitKVError) as e:   # s_q < 1
+        b.mla_sparse_decode_host(plan, 0, fake, fake, fake, 100, fake, fake, 0.1, None, "e4m3", 64.0, fake, fake,
+                                 stream=0)
+    assert e.value.status == 1
+
+
 def test_combine_argument_checks():
     plan = b.mla_decode_plan(4, 640, num_sms=152, force_splits=4)
     fake = 1 << 20

@@ -402,3 +402,35 @@ def test_balanced_schedule_repeated_calls():
         assert_o_close(out.numpy(), O)
         assert_lse_close(lse.double().numpy(), L)
     assert torch.equal(outs[0][0], outs[1][0])
+
+
+@pytest.mark.parametrize("s_q,S", [(6, 0), (96, 0), (16, b.MLA_FORCE_BALANCED)])
+def test_host_buffer_call(s_q, S):
+    """mla_sparse_decode_host: queries and indices from pinned host memory, FP8 output and LSE back to
+    host memory, all on one stream; the same bytes as the device-buffer call, and the oracle's values."""
+    inp = wl.mla_inputs(s_q, 32768, 640, seed=77, with_sink=True)
+    dev = torch.device("cuda")
+    kv, sink = inp.kv.to(dev), inp.sink.to(dev)
+    plan = b.mla_decode_plan(s_q, 640, force_splits=S)
+    ws = torch.empty(max(plan.workspace_bytes, 1), dtype=torch.uint8, device=dev)
+    if plan.workspace_bytes:
+        b.mla_workspace_init(plan, ws)
+    q_h, idx_h = inp.q.pin_memory(), inp.idx.pin_memory()
+    q_d, idx_d = torch.empty_like(inp.q, device=dev), torch.empty_like(inp.idx, device=dev)
+    out_d = torch.empty(s_q, 64, 512, dtype=torch.uint8, device=dev)
+    out_h = torch.zeros(s_q, 64, 512, dtype=torch.uint8).pin_memory()
+    lse_d = torch.empty(s_q, 64, dtype=torch.float32, device=dev)
+    lse_h = torch.zeros(s_q, 64, dtype=torch.float32).pin_memory()
+    st = torch.cuda.Stream()
+    b.mla_sparse_decode_host(plan, s_q, q_h, q_d, kv, inp.n_kv, idx_h, idx_d, inp.sm_scale, sink, "e4m3", 64.0,
+                             out_d, out_h, lse_d, lse_h, None, ws if plan.workspace_bytes else None, stream=st)
+    st.synchronize()
+    check_status()
+    r = run_mla(inp, S, out_dtype="e4m3", inv_scale=64.0)
+    assert torch.equal(out_h, r["out"])
+    assert np.array_equal(lse_h.double().numpy(), r["lse"])
+    ts = np.array([0, s_q - 1])
+    sub = wl.MlaInputs(q=inp.q[ts], kv=inp.kv, idx=inp.idx[ts], sink=inp.sink, sm_scale=inp.sm_scale)
+    O, L = oracle_mla(sub)
+    assert_cast_close(out_h[ts], O, "e4m3", 64.0)
+    assert_lse_close(lse_h[ts].double().numpy(), L)
