@@ -246,7 +246,8 @@ MLA_API int mla_sparse_decode(const mla_plan_t* plan, int s_q,
  * Other arguments as mla_sparse_decode. A NULL buffer (other than the lse pair,
  * sink, amax_out and workspace as mla_sparse_decode allows) or a lone lse
  * pointer gives MLA_ERR_INVALID_ARG before anything is queued; a failed copy
- * gives MLA_ERR_CUDA. */
+ * gives MLA_ERR_CUDA. This entry point has no counterpart in the pages: it is a
+ * packaging of mla_sparse_decode for host-resident inputs and outputs. */
 MLA_API int mla_sparse_decode_host(const mla_plan_t* plan, int s_q,
                            const void* q_host, void* q_dev, const void* kv, int64_t n_kv,
                            const int32_t* idx_host, int32_t* idx_dev, float sm_scale, const float* sink,
