@@ -150,9 +150,9 @@ typedef struct {
  * With force_splits == 0 the plan also enables the balanced schedule for the
  * one-shot call when it is expected to beat that grid at s_q_max: with per =
  * ceil(s_q_max * num_blocks / num_sms), when 2 <= per, ceil(num_blocks / per) + 1
- * <= 32 and per + 6 < ceil(s_q_max * S / num_sms) * ceil(num_blocks / S) (the
- * most blocks any SM walks under the grid; 6 blocks is the schedule's measured
- * cost of job boundaries and merging). force_splits == MLA_FORCE_BALANCED keeps
+ * <= 32 and per + 5 < ceil(s_q_max * S / num_sms) * ceil(num_blocks / S) (the
+ * most blocks any SM walks under the grid; 5 blocks stands for the schedule's
+ * measured cost of job boundaries and merging). force_splits == MLA_FORCE_BALANCED keeps
  * the automatic S and enables the balanced schedule whenever the first two
  * conditions hold. Enabling it sets balanced_ctas = min(num_sms, s_q_max *
  * num_blocks) and sizes the workspace for both schedules: the larger of the two

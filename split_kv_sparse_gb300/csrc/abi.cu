@@ -115,10 +115,12 @@ int64_t uniform_makespan(int64_t s_q, int nb, int S, int num_sms) {
 }
 // What the balanced schedule costs beyond its blocks, in 64-row block times: a
 // CTA's job boundary (the piece's partial store before the next token's softmax
-// can start) and the last piece's merge. Measured on GB300 at s_q = 96 and 384
-// (topk 640): the schedule ran as slow as per + 5.5 to per + 5.7 blocks of the
-// uniform grid.
-constexpr int64_t kBalancedOverheadBlocks = 6;
+// can start) and the last piece's merge. It depends on how many tokens are cut;
+// measured on GB300 (topk 640, 152 SMs), in blocks of the uniform grid: about 5
+// at s_q = 160 and 200, 6 at 250, 7 to 7.5 at 96 and 384, under 1 at 300 (whole
+// tokens only). With 5 the rule below picks the faster schedule at every
+// measured s_q (96, 120, 160, 200, 250, 300, 384).
+constexpr int64_t kBalancedOverheadBlocks = 5;
 // The most splits the dense planner's per-sequence rule gives one sequence.
 constexpr int kDenseMaxAdaptiveSplits = 16;
 // CTAs per (token, split) job: the largest of 4, 2, 1 that still fits `jobs`

@@ -89,7 +89,7 @@ def test_plan_is_deterministic_and_follows_rule():
                 per = -(-(s_q * nblk) // sms)
                 mk_uniform = -(-(s_q * S) // sms) * -(-nblk // S)
                 applies = per >= 2 and -(-nblk // per) + 1 <= 32
-                enabled = applies and per + 6 < mk_uniform
+                enabled = applies and per + 5 < mk_uniform
                 C = min(sms, s_q * nblk) if enabled else 0
                 # partials [2C][64][512] then LSEs [2C][64]; counters [s_q] and
                 # flags [2C] at the very end, past both schedules' partials
@@ -271,13 +271,17 @@ def test_balanced_schedule_covers_every_block_once():
 
 def test_balanced_schedule_choice_examples():
     # s_q = 96, 384 on 152 SMs: the uniform grid walks 10 and 30 blocks on its
-    # busiest SM, the balanced schedule 7 and 26 plus its overhead of 6
+    # busiest SM, the balanced schedule 7 and 26 plus its overhead of 5
     assert b.mla_decode_plan(96, 640, num_sms=152).balanced_ctas == 0
     assert b.mla_decode_plan(384, 640, num_sms=152).balanced_ctas == 0
     assert b.mla_decode_plan(96, 640, num_sms=152, force_splits=-1).balanced_ctas == 152
     assert b.mla_decode_plan(384, 640, num_sms=152, force_splits=-1).balanced_ctas == 152
-    # s_q = 160: two waves of 10 blocks against 11 + 6
+    # s_q = 160, 200: two waves of 10 blocks against 11 + 5 and 14 + 5; s_q = 250, 300:
+    # 17 + 5 and 20 + 5 against the same two waves
     assert b.mla_decode_plan(160, 640, num_sms=152).balanced_ctas == 152
+    assert b.mla_decode_plan(200, 640, num_sms=152).balanced_ctas == 152
+    assert b.mla_decode_plan(250, 640, num_sms=152).balanced_ctas == 0
+    assert b.mla_decode_plan(300, 640, num_sms=152).balanced_ctas == 0
     # s_q = 1, 16: the grid already spreads as evenly (10 x 1 block, 80 x 2 blocks)
     assert b.mla_decode_plan(1, 640, num_sms=152).balanced_ctas == 0
     assert b.mla_decode_plan(16, 640, num_sms=152).balanced_ctas == 0
