@@ -514,7 +514,7 @@ def known_traffic(s_q, S):
     except OSError:
         return None
     table = {   # (source hash, s_q, S) -> dram bytes per launch (profiles/mla_decode_kernel_sq96_direct.md)
-        ("ff85a18d6e38d51e", 96, 1): 55_632_128,
+        ("5fd6d0fb3f19d7c4", 96, 1): 55_383_296,
     }
     return table.get((h, s_q, S))
 
