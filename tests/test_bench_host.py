@@ -1,4 +1,5 @@
-"""Host-side pieces of bench.py: the byte model and the multi-rank aggregation.
+"""Host-side pieces of bench.py: the byte model, the multi-rank aggregation and the
+reference arm (the fp64 oracle on the host's cores, which needs no GPU).
 
 bench.py runs one independent replica per GPU under torchrun (the sparse path
 shards by token with no exchange); the only cross-rank step is the max of the
@@ -47,3 +48,24 @@ def test_two_gloo_ranks_take_the_max():
         p.join(timeout=60)
         assert p.exitcode == 0
     assert res[0] == res[1] == [11.0, 5.0]
+
+
+def test_reference_arm_line_on_cpu():
+    """bench.py --impl reference times the fp64 oracle on the host's cores and prints the contract's
+    line (impl, metric, unit, value, cpu_baseline, e2e with no copies); a rank other than 0 prints
+    nothing and exits 0."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "1", "--warmup", "3"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "us/call" and line["higher_is_better"] is False
+    assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": "us/call", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2")
+    r1 = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=root, env=env)
+    assert r1.returncode == 0 and r1.stdout.strip() == ""
