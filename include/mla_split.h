@@ -371,21 +371,25 @@ MLA_API int mla_selftest_wait_timeout(uint64_t limit_ns, void* stream);
  * device image (MLA_NOALLOC_SCRATCH_BYTES); every GPU that loads the library
  * holds that array until the process exits. The caller still passes q, kv, idx,
  * sink and the outputs, as for mla_sparse_decode; the plan is made internally
- * for this s_q (num_splits: 0 = the automatic choice, > 0 forces that many).
+ * for this s_q (num_splits: 0 = the automatic choice among the split counts
+ * whose workspace fits the array, so it is never refused; > 0 forces that many).
  * This entry point has no counterpart in the pages: it is a packaging of the
  * same split + combine for that kind of caller.
  *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
- *   - A call whose workspace would exceed MLA_NOALLOC_SCRATCH_BYTES
+ *   - A forced num_splits whose workspace would exceed MLA_NOALLOC_SCRATCH_BYTES
  *     (num_splits * s_q * 64 * (512 + 1) * 4 bytes, rounded up) returns
- *     MLA_ERR_WORKSPACE and launches nothing; use fewer splits or
- *     mla_sparse_decode with a caller workspace.
+ *     MLA_ERR_WORKSPACE and launches nothing; use fewer splits, the automatic
+ *     choice, or mla_sparse_decode with a caller workspace.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind; the split pass overwrites every slot it needs before the combine
  *     reads it, so no clearing is needed. Calls that overlap on the GPU (on
  *     different streams, or from several threads) race on the array: order them.
  *   - The first call on a device resolves the array's device address for that
- *     device (cudaGetSymbolAddress); make that first call before capturing a
- *     stream into a CUDA graph. */
+ *     device (cudaGetSymbolAddress) and keeps it for the life of the process;
+ *     make that first call before capturing a stream into a CUDA graph. As with
+ *     the rest of this library's per-device state (the status word, the kernel
+ *     attributes), a device reset (cudaDeviceReset) is not supported: the
+ *     process must not call into the library after one. */
 MLA_API int mla_sparse_decode_noalloc(int s_q, int topk, const void* q, const void* kv, int64_t n_kv,
                                       const int32_t* idx, float sm_scale, const float* sink,
                                       int num_splits, int out_dtype, float out_inv_scale,

@@ -91,6 +91,13 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 uint64_t round_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
+// Workspace of the (token, split) schedule: fp32 O partials [S][s_q][64][512],
+// then fp32 LSE partials [S][s_q][64] at the next 256-byte boundary.
+uint64_t split_workspace_bytes(int S, int s_q) {
+  const uint64_t o = static_cast<uint64_t>(S) * s_q * kMlaHeads * kMlaDv * 4ull;
+  return round_up(round_up(o, 256) + static_cast<uint64_t>(S) * s_q * kMlaHeads * 4ull, 256);
+}
+
 // Workspace of the balanced schedule for at most `ctas` CTAs and `s_q_max` tokens:
 //   fp32 O partials [2 * ctas][64][512] at 0, fp32 LSE partials [2 * ctas][64]
 //   after them; its uint32 per-token piece counters [s_q_max] and per-slot ready
@@ -814,8 +821,18 @@ int mla_sparse_decode_noalloc(int s_q, int topk, const void* q, const void* kv, 
                               float sm_scale, const float* sink, int num_splits, int out_dtype, float out_inv_scale,
                               void* out, float* lse_out, float* amax_out, void* stream) {
   if (num_splits < 0 || num_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID_ARG;
+  if (s_q < 1) return MLA_ERR_INVALID_ARG;
+  // The automatic choice only considers split counts whose workspace fits the
+  // array, so it never refuses an ordinary shape; a forced count is taken as
+  // asked and refused below if it does not fit.
+  int max_splits = 0;
+  if (num_splits == 0) {
+    max_splits = 1;
+    for (int S = 2; S <= MLA_MAX_SPLITS; ++S)
+      if (split_workspace_bytes(S, s_q) <= MLA_NOALLOC_SCRATCH_BYTES) max_splits = S;
+  }
   mla_plan_t plan;
-  int st = mla_decode_plan(s_q, kMlaHeads, kMlaDqk, kMlaDv, topk, 0, 0, num_splits, &plan);
+  int st = mla_decode_plan(s_q, kMlaHeads, kMlaDqk, kMlaDv, topk, 0, max_splits, num_splits, &plan);
   if (st != MLA_OK) return st;
   // the (token, split) jobs: their workspace is num_splits * s_q partial rows
   plan.balanced_ctas = 0;

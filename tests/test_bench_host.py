@@ -21,6 +21,17 @@ def test_algorithmic_bytes_model():
     assert bench.algorithmic_bytes(96, 1) == 96 * (per_tok + 32768 + 256)
 
 
+def test_sweep_point_bytes_use_the_plans_split_count():
+    """A swept point's bytes come from the schedule the plan runs: the planner's point
+    (requested count 0) counts the partials of the splits it actually uses."""
+    per_tok = 64 * 576 * 2 + 640 * 4 + 640 * 1152
+    # s_q = 1, the planner's 5 splits: 813,568 + 2 * 5 * 131,328 + 33,024 = 2,159,872 B
+    assert bench.point_bytes(1, 5, False, 152) == 2_159_872
+    assert bench.point_bytes(1, 5, False, 152) == per_tok + 2 * 5 * (131072 + 256) + 64 * 512 + 256
+    assert bench.point_bytes(96, 1, False, 152) == bench.algorithmic_bytes(96, 1)
+    assert bench.point_bytes(96, 1, True, 152) == bench.balanced_bytes(96, 152)
+
+
 def test_single_process_max_is_identity():
     assert bench.max_over_ranks([1.5, 2.0]) == [1.5, 2.0]
 
