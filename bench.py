@@ -97,6 +97,13 @@ def balanced_bytes(s_q: int, num_sms: int) -> int:
     return s_q * (per_tok_in + out) + 2 * (pieces - cut) * partial
 
 
+def point_bytes(s_q: int, splits_used: int, balanced: bool, num_sms: int) -> int:
+    """Algorithmic bytes of one swept call, from the schedule the plan actually runs:
+    the balanced schedule's, else the (token, split) grid's with the plan's split
+    count (for the planner's point too, whose requested count is 0)."""
+    return balanced_bytes(s_q, num_sms) if balanced else algorithmic_bytes(s_q, splits_used, "call")
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -169,17 +176,38 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------- GPU arm --
 
-class Case:
-    """Device inputs, a plan, outputs and CUDA graphs for one (s_q, S) point."""
+L2_FALLBACK = 129 * 1000 * 1000
+MAX_LAYERS = 320
 
-    def __init__(self, b, torch, kv, inp, S):
+
+def unique_bytes(s_q: int) -> int:
+    """Bytes one call reads at most (queries, indices, gathered rows), ignoring the rows
+    that tokens share: the footprint a rotation of caches has to exceed."""
+    return s_q * (H_Q * D_QK * 2 + TOPK * 4 + TOPK * D_QK * 2)
+
+
+def layers_for(s_q: int, l2_bytes: int) -> int:
+    """How many per-layer caches (and query/index sets) a timed run rotates through so
+    that what one call reads has left L2 by the time the same layer comes round again:
+    at least 3x L2 of other calls' reads, at least 4 layers, at most MAX_LAYERS."""
+    return max(4, min(MAX_LAYERS, -(-3 * l2_bytes // unique_bytes(s_q))))
+
+
+class Case:
+    """Plan, per-layer inputs, outputs and CUDA graphs for one (s_q, S) point.
+
+    A decode step runs once per model layer, each layer with its own KV cache, so the
+    same layer's rows come round again only after every other layer's reads have
+    passed through L2. The timed runs do the same: consecutive calls rotate over
+    `layers` caches (views of one allocation) and per-layer queries / indices whose
+    total exceeds L2 several times, back to back in one CUDA graph."""
+
+    def __init__(self, b, torch, kv_all, qs, idxs, sm_scale, S):
         self.b, self.torch = b, torch
-        dev = kv.device
-        self.s_q = inp.s_q
-        self.q = inp.q.to(dev)
-        self.idx = inp.idx.to(dev)
-        self.kv = kv
-        self.sm_scale = inp.sm_scale
+        self.layers = len(qs)
+        self.s_q = qs[0].shape[0]
+        self.kv_all, self.qs, self.idxs, self.sm_scale = kv_all, qs, idxs, sm_scale
+        dev = kv_all.device
         self.plan = b.mla_decode_plan(self.s_q, TOPK, force_splits=S) if S else b.mla_decode_plan(self.s_q, TOPK)
         self.S = self.plan.num_splits
         # the automatic plan's one-shot call runs the balanced schedule (one kernel)
@@ -189,6 +217,7 @@ class Case:
         if self.balanced:
             self.P, self.per, self.cut, self.pieces = balanced_schedule(self.s_q, self.plan.num_blocks,
                                                                         self.plan.num_sms)
+        # calls on one stream run one after another, so the layers share one workspace
         self.ws = (torch.empty(self.plan.workspace_bytes, dtype=torch.uint8, device=dev)
                    if self.plan.workspace_bytes else None)
         if self.ws is not None:
@@ -196,19 +225,20 @@ class Case:
         self.out = torch.empty(self.s_q, H_Q, D_V, dtype=torch.uint8, device=dev)
         self.lse = torch.empty(self.s_q, H_Q, dtype=torch.float32, device=dev)
         self.stream = torch.cuda.Stream()
-        self.g_call = self._capture(self._call)
-        self.g_kernel = self._capture(self._kernel)
+        self.g_call = self._capture(lambda: [self._call(l) for l in range(self.layers)])
+        self.g_kernel = self._capture(lambda: [self._kernel(l) for l in range(self.layers)])
+        self._single = {}
 
-    def _call(self):
-        self.b.mla_sparse_decode(self.plan, self.s_q, self.q, self.kv, N_KV, self.idx, self.sm_scale, None,
-                                 "e4m3", INV_SCALE, self.out, self.lse, None, self.ws, stream=self.stream)
+    def _call(self, l):
+        self.b.mla_sparse_decode(self.plan, self.s_q, self.qs[l], self.kv_all[l], N_KV, self.idxs[l], self.sm_scale,
+                                 None, "e4m3", INV_SCALE, self.out, self.lse, None, self.ws, stream=self.stream)
 
-    def _kernel(self):
+    def _kernel(self, l):
         if self.balanced or self.S == 1:
-            self._call()
+            self._call(l)
         else:
-            self.b.mla_sparse_decode_split(self.plan, self.s_q, self.q, self.kv, N_KV, self.idx, self.sm_scale,
-                                           self.ws, stream=self.stream)
+            self.b.mla_sparse_decode_split(self.plan, self.s_q, self.qs[l], self.kv_all[l], N_KV, self.idxs[l],
+                                           self.sm_scale, self.ws, stream=self.stream)
 
     def launches(self) -> int:
         """Kernels one call launches."""
@@ -231,22 +261,52 @@ class Case:
         torch.cuda.synchronize()
         return g
 
-    def time(self, graph, steps, warmup, flush):
-        """Per-call device time (µs) with L2 flushed before every call."""
+    def _single_graph(self, kind, l):
+        key = (kind, l)
+        if key not in self._single:
+            self._single[key] = self._capture(lambda: (self._call if kind == "call" else self._kernel)(l))
+        return self._single[key]
+
+    def time(self, kind, steps, warmup):
+        """Mean device time (µs) of `steps` consecutive calls (kind "call": the whole
+        decode call; "kernel": the split / direct / balanced kernel alone), rotating
+        over the layers, bracketed by one pair of CUDA events on the case's stream."""
         torch = self.torch
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        graph = self.g_call if kind == "call" else self.g_kernel
+        full, rest = divmod(steps, self.layers)
+        singles = [self._single_graph(kind, l) for l in range(rest)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(self.stream):
-            for _ in range(warmup):
-                flush.zero_()
+            for _ in range(max(1, -(-warmup // self.layers))):
                 graph.replay()
+            torch.cuda.synchronize()
+            e0.record(self.stream)
+            for _ in range(full):
+                graph.replay()
+            for g in singles:
+                g.replay()
+            e1.record(self.stream)
+        torch.cuda.synchronize()
+        return 1000.0 * e0.elapsed_time(e1) / steps
+
+    def time_flushed(self, reps, flush):
+        """Per-call time of single calls (layer 0) with L2 flushed before each, each call
+        bracketed by its own pair of CUDA events (includes the event / graph-launch floor)."""
+        torch = self.torch
+        g = self._single_graph("call", 0)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        with torch.cuda.stream(self.stream):
+            for _ in range(3):
+                flush.zero_()
+                g.replay()
             torch.cuda.synchronize()
             for e0, e1 in ev:
                 flush.zero_()
                 e0.record(self.stream)
-                graph.replay()
+                g.replay()
                 e1.record(self.stream)
         torch.cuda.synchronize()
-        return [1000.0 * e0.elapsed_time(e1) for e0, e1 in ev]
+        return statistics.fmean(1000.0 * e0.elapsed_time(e1) for e0, e1 in ev)
 
 
 DENSE_DESC = ("dense FP8 GQA split-KV SDPA decode: batch 8, 32 query / 8 KV heads, d=128, 1-16 query tokens per "
@@ -283,19 +343,25 @@ def dense_bytes(sq, skv, h_q: int, h_kv: int, d: int, S: int, splits=None) -> in
     return kv + q + out + partial
 
 
-class DenseCase:
-    """Device inputs, a plan, outputs and CUDA graphs for one dense split count."""
+DENSE_LAYERS = 4
 
-    def __init__(self, b, torch, inp, S):
+
+class DenseCase:
+    """Plan, outputs and CUDA graphs for one dense split count; consecutive timed calls
+    rotate over DENSE_LAYERS copies of the inputs (143 MB of K / V each), as the layers
+    of a model would."""
+
+    def __init__(self, b, torch, inp, S, layers=DENSE_LAYERS):
         self.b, self.torch, self.inp = b, torch, inp
         dev = torch.device("cuda")
+        self.layers = layers
         self.sq = (inp.cu_seqlens_q[1:] - inp.cu_seqlens_q[:-1]).tolist()
         self.skv = (inp.cu_seqlens_kv[1:] - inp.cu_seqlens_kv[:-1]).tolist()
         self.total_q, self.total_kv = int(inp.cu_seqlens_q[-1]), int(inp.cu_seqlens_kv[-1])
         self.plan = b.sdpa_fp8_decode_plan(inp.batch, inp.h_q, inp.h_kv, inp.d, 16, self.total_q, max(self.skv),
                                            force_splits=S)
         self.S = self.plan.num_splits
-        self.q, self.k, self.v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+        self.qkv = [(inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)) for _ in range(layers)]
         self.cq, self.ck = inp.cu_seqlens_q.to(dev), inp.cu_seqlens_kv.to(dev)
         self.ds = [torch.tensor([x], dtype=torch.float32, device=dev)
                    for x in (inp.descale_q, inp.descale_k, inp.descale_v)]
@@ -304,24 +370,33 @@ class DenseCase:
         self.out = torch.empty(self.total_q, inp.h_q, inp.d, dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty(self.total_q, inp.h_q, dtype=torch.float32, device=dev)
         self.stream = torch.cuda.Stream()
-        self.g_call = Case._capture(self, self._call)
-        self.g_kernel = Case._capture(self, self._kernel)
+        self.g_call = Case._capture(self, lambda: [self._call(l) for l in range(layers)])
+        self.g_kernel = Case._capture(self, lambda: [self._kernel(l) for l in range(layers)])
+        self._single = {}
 
-    def _call(self):
-        self.b.sdpa_fp8_decode(self.plan, self.total_q, self.total_kv, self.q, self.k, self.v, self.cq, self.ck,
+    def _call(self, l):
+        q, k, v = self.qkv[l]
+        self.b.sdpa_fp8_decode(self.plan, self.total_q, self.total_kv, q, k, v, self.cq, self.ck,
                                self.ds[0], self.ds[1], self.ds[2], self.inp.sm_scale, "bf16", 1.0, self.out,
                                self.lse, None, self.ws, stream=self.stream)
 
-    def _kernel(self):
+    def _kernel(self, l):
         if self.S == 1:
-            self._call()
+            self._call(l)
         else:
-            self.b.sdpa_fp8_decode_split(self.plan, self.total_q, self.total_kv, self.q, self.k, self.v, self.cq,
+            q, k, v = self.qkv[l]
+            self.b.sdpa_fp8_decode_split(self.plan, self.total_q, self.total_kv, q, k, v, self.cq,
                                          self.ck, self.ds[0], self.ds[1], self.ds[2], self.inp.sm_scale, self.ws,
                                          stream=self.stream)
 
-    def time(self, graph, steps, warmup, flush):
-        return Case.time(self, graph, steps, warmup, flush)
+    def _capture(self, fn):
+        return Case._capture(self, fn)
+
+    def time(self, kind, steps, warmup):
+        return Case.time(self, kind, steps, warmup)
+
+    def _single_graph(self, kind, l):
+        return Case._single_graph(self, kind, l)
 
     def bytes(self) -> int:
         splits = (dense_splits(self.skv, self.inp.h_kv, self.S, self.plan.num_sms) if self.plan.adaptive_splits
@@ -345,97 +420,116 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     peak, peak_src = load_peaks()
 
-    # inputs: one KV cache shared by every s_q (generated once), Q / indices per s_q
+    # inputs: one seeded 131072-row cache, replicated as the per-layer caches of the
+    # timed rotation (views of one allocation), and per-layer queries / indices per s_q
+    l2_bytes = int(getattr(torch.cuda.get_device_properties(local), "L2_cache_size", 0) or L2_FALLBACK)
+    s_q_list = [args.s_q] + ([] if (args.no_sweep or args.no_mla_sweep) else [s for s in SWEEP_SQ if s != args.s_q])
+    n_layers_max = max(layers_for(s, l2_bytes) for s in s_q_list)
     base = wl.mla_inputs(1, N_KV, TOPK, seed=0)
-    kv = base.kv.to(dev)
+    kv_all = torch.empty(n_layers_max, N_KV, D_QK, dtype=torch.bfloat16, device=dev)
+    kv_all[0].copy_(base.kv.to(dev))
+    kv_all[1:].copy_(kv_all[0].expand(n_layers_max - 1, N_KV, D_QK))
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    def inputs(s_q):
-        inp = wl.mla_inputs(s_q, N_KV, TOPK, seed=1000 + s_q) if s_q != 1 else base
-        return wl.MlaInputs(q=inp.q, kv=base.kv, idx=inp.idx, sink=None, sm_scale=inp.sm_scale)
+    def layer_inputs(s_q):
+        R = layers_for(s_q, l2_bytes)
+        qs, idxs = [], []
+        for l in range(R):
+            q, idx = wl.mla_queries(s_q, N_KV, TOPK, seed=1000 + s_q + 7919 * l)
+            qs.append(q.to(dev))
+            idxs.append(idx.to(dev))
+        return qs, idxs
 
-    inp_main = inputs(args.s_q)
-    case = Case(b, torch, kv, inp_main, 0)
+    main_qs, main_idxs = layer_inputs(args.s_q)
+    case = Case(b, torch, kv_all, main_qs, main_idxs, base.sm_scale, 0)
 
     props = torch.cuda.get_device_properties(local)
     sampler = ClockSampler(getattr(props, "uuid", None) and f"GPU-{props.uuid}" or str(local))
     sampler.start()
     time.sleep(0.2)
 
-    # ---- headline: whole call, cold L2 ------------------------------------------------
+    # ---- headline: K consecutive decode calls over the rotating layers -------------------
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     sampler.mark()
     t_wall0 = time.perf_counter()
-    call_us = case.time(case.g_call, args.steps, args.warmup, flush)
+    mean_call = case.time("call", args.steps, args.warmup)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t_wall0
     sampler.mark()
-    kern_us = case.time(case.g_kernel, args.steps, max(3, args.warmup // 2), flush)
+    mean_kern = case.time("kernel", args.steps, max(3, args.warmup // 2))
+    flushed = case.time_flushed(min(args.steps, 200), flush)
     if world > 1:
         dist.barrier()
 
-    mean_call, mean_kern = max_over_ranks([statistics.fmean(call_us), statistics.fmean(kern_us)], dev)
+    mean_call, mean_kern, flushed = max_over_ranks([mean_call, mean_kern, flushed], dev)
 
     kbytes = (balanced_bytes(args.s_q, case.plan.num_sms) if case.balanced
               else algorithmic_bytes(args.s_q, case.S, "split"))
     achieved = kbytes / (mean_kern * 1e-6) / 1e9
 
     # ---- end to end through the C ABI with host buffers ---------------------------------
-    # mla_sparse_decode_host: the library copies Q and the indices in from pinned host
-    # memory, decodes, and copies the FP8 output and the LSE back, on the case's stream
-    q_h = inp_main.q.pin_memory()
-    idx_h = inp_main.idx.pin_memory()
+    # mla_sparse_decode_host: per call the library copies that layer's queries and indices
+    # in from pinned host memory, decodes, and copies the FP8 output and the LSE back, on
+    # the case's stream; consecutive calls rotate over the layers
+    q_h = [q.cpu().pin_memory() for q in main_qs]
+    idx_h = [i.cpu().pin_memory() for i in main_idxs]
     out_h = torch.empty(case.out.shape, dtype=case.out.dtype).pin_memory()
     lse_h = torch.empty(case.lse.shape, dtype=case.lse.dtype).pin_memory()
-    e2e = []
+    n_e2e = min(args.steps, 500)
+
+    def host_call(l):
+        b.mla_sparse_decode_host(case.plan, case.s_q, q_h[l], case.qs[l], case.kv_all[l], N_KV, idx_h[l],
+                                 case.idxs[l], case.sm_scale, None, "e4m3", INV_SCALE, case.out, out_h, case.lse,
+                                 lse_h, None, case.ws, stream=case.stream)
     with torch.cuda.stream(case.stream):
-        for i in range(args.warmup + min(args.steps, 500)):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(case.stream)
-            b.mla_sparse_decode_host(case.plan, case.s_q, q_h, case.q, case.kv, N_KV, idx_h, case.idx,
-                                     case.sm_scale, None, "e4m3", INV_SCALE, case.out, out_h, case.lse, lse_h,
-                                     None, case.ws, stream=case.stream)
-            e1.record(case.stream)
-            if i >= args.warmup:
-                e2e.append((e0, e1))
+        for i in range(args.warmup):
+            host_call(i % case.layers)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(case.stream)
+        for i in range(n_e2e):
+            host_call(i % case.layers)
+        e1.record(case.stream)
     torch.cuda.synchronize()
-    e2e_us = statistics.fmean(1000.0 * a.elapsed_time(c) for a, c in e2e)
-    h2d = q_h.numel() * q_h.element_size() + idx_h.numel() * idx_h.element_size()
+    e2e_us = max_over_ranks([1000.0 * e0.elapsed_time(e1) / n_e2e], dev)[0]
+    h2d = q_h[0].numel() * q_h[0].element_size() + idx_h[0].numel() * idx_h[0].element_size()
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
 
     # ---- sweep: s_q x splits (and the planner's choice) -------------------------------
     sweep, dense_sweep = [], []
     if not args.no_sweep:
         for s_q in (() if args.no_mla_sweep else SWEEP_SQ):
-            inp = inp_main if s_q == args.s_q else inputs(s_q)
+            qs, idxs = (main_qs, main_idxs) if s_q == args.s_q else layer_inputs(s_q)
             # forced (token, split) grids, the planner's choice (S = 0) and the
             # balanced one-shot schedule where it applies (S = -1)
             for S in list(SWEEP_S) + [0, -1]:
-                c = Case(b, torch, kv, inp, S)
+                c = Case(b, torch, kv_all, qs, idxs, base.sm_scale, S)
                 if S == -1 and not c.balanced:
                     del c
                     continue
-                us = statistics.fmean(c.time(c.g_call, args.sweep_steps, 3, flush))
-                ks = statistics.fmean(c.time(c.g_kernel, args.sweep_steps, 3, flush))
-                cb = balanced_bytes(s_q, c.plan.num_sms) if c.balanced else algorithmic_bytes(s_q, S, "call")
+                steps = max(args.sweep_steps, c.layers)
+                us = c.time("call", steps, c.layers)
+                ks = c.time("kernel", steps, c.layers)
+                cb = point_bytes(s_q, c.S, c.balanced, c.plan.num_sms)
                 sweep.append({"s_q": s_q, "num_splits": {0: "planner", -1: "balanced"}.get(S, S),
-                              "planner": S == 0,
+                              "planner": S == 0, "layers": c.layers, "steps": steps,
                               "schedule": c.schedule(), "us_per_call": round(us, 2),
                               "split_kernel_us": round(ks, 2), "alg_bytes": cb,
                               "gb_s": round(cb / (us * 1e-6) / 1e9, 1),
                               "frac_of_peak": round(cb / (us * 1e-6) / 1e9 / peak, 4)})
                 del c
+            del qs, idxs
         torch.cuda.synchronize()
         # the dense FP8 GQA variant (same partial / LSE protocol), forced split
         # counts and the planner's choice
         dinp = wl.sdpa_inputs(8, 32, 8, 128, seed=0)
         for S in list(SWEEP_S) + [0]:
             c = DenseCase(b, torch, dinp, S)
-            us = statistics.fmean(c.time(c.g_call, args.sweep_steps, 3, flush))
-            ks = statistics.fmean(c.time(c.g_kernel, args.sweep_steps, 3, flush))
+            steps = max(args.sweep_steps, c.layers)
+            us = c.time("call", steps, c.layers)
+            ks = c.time("kernel", steps, c.layers)
             cb = c.bytes()
             dense_sweep.append({"num_splits": S if S else "planner", "planner": S == 0, "splits_used": c.S,
                                 "per_sequence_splits": (dense_splits(c.skv, 8, c.S, c.plan.num_sms)
@@ -465,8 +559,15 @@ def run_gpu(args):
             "config": {"workload": workload_name(args.s_q), "s_q": args.s_q, "schedule": case.schedule(),
                        "n_kv": N_KV, "topk": TOPK, "h_q": H_Q, "d_qk": D_QK, "d_v": D_V,
                        "output": "e4m3", "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-                       "l2": "flushed before every timed call (256 MiB write, untimed)",
-                       "timing": "CUDA graph replay of one decode call, CUDA events on its stream, mean of steps",
+                       "l2": (f"inputs larger than L2: consecutive calls rotate over {case.layers} per-layer "
+                              f"KV caches ({N_KV} rows each) and query / index sets, "
+                              f"{case.layers * unique_bytes(args.s_q) / 1e6:.0f} MB read per rotation against "
+                              f"{l2_bytes / 1e6:.0f} MB of L2"),
+                       "timing": ("the K steps as consecutive decode calls (CUDA graphs of one call per layer), "
+                                  "one pair of CUDA events on the launching stream around all K; value = "
+                                  "elapsed / K"),
+                       "layers": case.layers,
+                       "single_call_l2_flushed_us": round(flushed, 3),
                        "wall_s_timed_region": round(wall, 4)},
             "roofline": {"bound": "hbm", "kernel": ("mla_decode_kernel (balanced, in-kernel merge)" if case.balanced
                                                     else "mla_decode_kernel (split pass)" if case.S > 1
@@ -480,7 +581,8 @@ def run_gpu(args):
             "e2e": {"value": round(e2e_us, 3), "unit": "us/call", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
                     "note": "mla_sparse_decode_host: H2D of Q and indices from pinned host memory, the decode, "
-                            "D2H of FP8 O and LSE, in one C-ABI call; the KV cache is resident decode state"},
+                            "D2H of FP8 O and LSE, in one C-ABI call per step, rotating over the layers; the "
+                            "KV caches are resident decode state"},
             "gpu_launches": args.steps * case.launches(),
             "clocks": clocks,
             "cpu_baseline": cpu,
@@ -506,14 +608,14 @@ def max_over_ranks(values, device=None):
 
 def known_traffic(s_q, S):
     """DRAM bytes per launch of the dominant kernel from an ncu capture of the current kernel
-    source (profiles/), or None when no capture matches it."""
+    source, or None when no capture matches it (the source hash keys the table)."""
     import hashlib
     src = os.path.join(ROOT, "split_kv_sparse_gb300", "csrc", "mla_decode.cu")
     try:
         h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     except OSError:
         return None
-    table = {   # (source hash, s_q, S) -> dram bytes per launch (profiles/mla_decode_kernel_sq96_direct.md)
+    table = {   # (source hash, s_q, S) -> dram bytes per launch
         ("5fd6d0fb3f19d7c4", 96, 1): 55_383_296,
     }
     return table.get((h, s_q, S))

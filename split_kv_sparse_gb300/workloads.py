@@ -118,6 +118,16 @@ def mla_inputs(s_q: int, n_kv: int, topk: int = 640, *, seed: int = 0,
                      sm_scale=1.0 / math.sqrt(D_QK))
 
 
+def mla_queries(s_q: int, n_kv: int, topk: int = 640, *, seed: int = 0, h_q: int = H_Q):
+    """Queries and "128 + 512" indices of one decode step without a cache (for callers that
+    bring their own cache, e.g. one per model layer): Q ~ N(0, 1) bf16 [s_q, h_q, 576] and
+    int32 indices [s_q, topk] drawn as in mla_inputs's "window" mode."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    q = rng.standard_normal((s_q, h_q, D_QK), dtype=np.float32)
+    idx = window_plus_uniform_indices(rng, s_q, n_kv, 128, topk - 128)
+    return _bf16(q), torch.from_numpy(idx)
+
+
 # --------------------------------------------------------------------------------------
 # Dense FP8 GQA decode (cuDNN-frontend PR #768 form)
 # --------------------------------------------------------------------------------------
