@@ -356,6 +356,20 @@ MLA_API int mla_get_status(uint32_t* status_out, uint32_t* site_out);
  * of the bounded waits without hanging or faulting the GPU. */
 MLA_API int mla_selftest_wait_timeout(uint64_t limit_ns, void* stream);
 
+/* Sets the time limit of the decode kernels' pipeline waits (every mbarrier
+ * wait of mla_decode's and the dense kernel's roles, and the balanced schedule's
+ * wait on other pieces' ready flags) for the calls launched after it, process
+ * wide. limit_ns = 0 restores the default of 2 s; otherwise 100 ns .. 10 s, else
+ * MLA_ERR_INVALID_ARG. A wait that runs out records MLA_STATUS_TIMEOUT and the
+ * wait's site in the status word (mla_get_status) and aborts its CTA: the other
+ * roles stop at their next wait, the CTA waits (up to 2 s, whatever this limit)
+ * for its own copies and MMAs in flight, frees its tensor memory and exits; the
+ * call's outputs are then undefined, and a balanced-schedule workspace must be
+ * cleared again (mla_workspace_init) before the next call. For tests of that
+ * abort path: a limit far below a step's latency makes real waits run out. The
+ * pages have no counterpart (failure handling of this library). */
+MLA_API int mla_set_wait_limit_ns(uint64_t limit_ns);
+
 /* ======================================================================= *
  *  Decode without allocation                                               *
  * ======================================================================= */

@@ -30,7 +30,7 @@ EXPORTS = [
     "mla_sparse_decode", "mla_sparse_decode_host", "sdpa_fp8_decode_plan", "sdpa_fp8_decode_split",
     "sdpa_split_combine", "sdpa_fp8_decode_direct", "sdpa_fp8_decode", "mla_get_status",
     "mla_selftest_wait_timeout", "mla_status_string", "mla_abi_version", "mla_sparse_decode_noalloc",
-    "mla_workspace_init",
+    "mla_workspace_init", "mla_set_wait_limit_ns",
 ]
 
 
@@ -87,6 +87,7 @@ _SIGS = {
     "mla_abi_version": [],
     "mla_sparse_decode_noalloc": [_I, _I, _P, _P, _I64, _P, _F, _P, _I, _I, _F, _P, _P, _P, _P],
     "mla_workspace_init": [ctypes.POINTER(MlaPlan), _P, _P],
+    "mla_set_wait_limit_ns": [_U64],
 }
 
 
@@ -252,6 +253,11 @@ def mla_get_status():
     st, site = ctypes.c_uint32(0), ctypes.c_uint32(0)
     _check(lib().mla_get_status(ctypes.byref(st), ctypes.byref(site)), "mla_get_status")
     return st.value, site.value
+
+
+def mla_set_wait_limit_ns(limit_ns: int):
+    """Time limit of the decode kernels' pipeline waits for later calls (0 = the 2 s default)."""
+    _check(lib().mla_set_wait_limit_ns(limit_ns), "mla_set_wait_limit_ns")
 
 
 def mla_selftest_wait_timeout(limit_ns: int, stream=None):

@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "kernels.h"
@@ -22,6 +23,10 @@ using skv::kMlaHeads;
 __device__ uint32_t g_status[2];
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
+// The limit the decode kernels give their pipeline waits (mla_set_wait_limit_ns
+// shortens it for tests); an aborting CTA always waits up to kWaitLimitNs for its
+// own copies and MMAs in flight.
+std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
 constexpr int kMaxDevices = 64;
 
 struct DeviceState {
@@ -311,7 +316,8 @@ int mla_sparse_decode_split(const mla_plan_t* plan, int s_q, const void* q, cons
   a.o_acc = static_cast<float*>(workspace);
   a.lse_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan->lse_acc_offset);
   a.status = dev->status;
-  a.wait_limit_ns = kWaitLimitNs;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.drain_limit_ns = kWaitLimitNs;
   return cuda_status(skv::launch_mla_decode(tq, a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -405,7 +411,8 @@ int mla_decode_balanced(const mla_plan_t* plan, int s_q, const void* q, const vo
   a.sink = sink;
   a.amax = amax_out;
   a.status = dev->status;
-  a.wait_limit_ns = kWaitLimitNs;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.drain_limit_ns = kWaitLimitNs;
   return cuda_status(skv::launch_mla_decode(tq, a, cs));
 }
 }  // namespace
@@ -467,7 +474,8 @@ int mla_direct_impl(int s_q, int topk, const void* q, const void* kv, int64_t n_
   a.sink = sink;
   a.amax = amax_out;
   a.status = dev->status;
-  a.wait_limit_ns = kWaitLimitNs;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.drain_limit_ns = kWaitLimitNs;
   return cuda_status(skv::launch_mla_decode(tq, a, cs));
 }
 }  // namespace
@@ -651,7 +659,8 @@ int sdpa_launch(int batch, int h_q, int h_kv, int total_q, int64_t total_kv, int
   a.lse_out = lse_out;
   a.amax = amax;
   a.status = dev->status;
-  a.wait_limit_ns = kWaitLimitNs;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.drain_limit_ns = kWaitLimitNs;
   return cuda_status(skv::launch_sdpa_decode(tq, tk, tv, a, direct, cs));
 }
 int sdpa_combine_impl(const sdpa_plan_t* plan, int total_q, const void* workspace, int out_dtype,
@@ -764,6 +773,13 @@ int mla_get_status(uint32_t* status_out, uint32_t* site_out) {
   }
   if (status_out != nullptr) *status_out = h[0];
   if (site_out != nullptr) *site_out = h[1];
+  return MLA_OK;
+}
+
+int mla_set_wait_limit_ns(uint64_t limit_ns) {
+  if (limit_ns == 0) limit_ns = kWaitLimitNs;
+  if (limit_ns < 100ull || limit_ns > 10000000000ull) return MLA_ERR_INVALID_ARG;
+  g_wait_limit_ns.store(limit_ns);
   return MLA_OK;
 }
 

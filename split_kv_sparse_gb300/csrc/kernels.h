@@ -49,7 +49,8 @@ struct MlaArgs {
   const float* sink;    // [64] or null
   float* amax;          // scalar or null (zeroed by the launcher)
   uint32_t* status;     // device status words [2]
-  uint64_t wait_limit_ns;
+  uint64_t wait_limit_ns;   // a pipeline wait that runs longer records a timeout and aborts the CTA
+  uint64_t drain_limit_ns;  // how long an aborting CTA waits for its own copies and MMAs in flight
 };
 
 // Balanced schedule arithmetic, shared by the host and the decode kernel: U
@@ -122,7 +123,8 @@ struct SdpaArgs {
   float* lse_out;
   float* amax;
   uint32_t* status;
-  uint64_t wait_limit_ns;
+  uint64_t wait_limit_ns;   // as in MlaArgs
+  uint64_t drain_limit_ns;
 };
 int sdpa_decode_smem_bytes();
 // tm_q: Q viewed as 3-D [total_q][h_q][128] e4m3, box {128 d, group heads, 64/group tokens}.

@@ -95,10 +95,17 @@ constexpr int kOffAlpha = kOffMisc + 128;           // float[2][64] rescale fact
 constexpr int kOffHead = kOffAlpha + 512;           // float[2][64] per-head epilogue scalars
 constexpr int kSmemBytes = kOffHead + 512;          // 230720
 
+// The ring half of each step is filled and released in two chunk groups: A =
+// column chunks 0-3 (the V dims of O^T tiles 0 and 1) and B = chunks 4-8 (tiles
+// 2 and 3 and the RoPE chunk, which holds P_hi once the scores are computed). A
+// group is refilled as soon as the PV MMAs that read it are done, so the rows of
+// step g + 2 start landing while PV(g) still runs.
 enum {
-  B_QFULL = 0, B_FULL0, B_FULL1, B_EMPTY0, B_EMPTY1, B_SFULL0, B_SFULL1, B_PHI0, B_PHI1,
-  B_PLO0, B_PLO1, B_PVDONE, B_DRAIN, B_XCH0, B_XCH1, B_OFREE, B_QFREE, B_MRG, kNumBars
+  B_QFULL = 0, B_FULLA0, B_FULLA1, B_FULLB0, B_FULLB1, B_EMPTYA0, B_EMPTYA1, B_EMPTYB0, B_EMPTYB1,
+  B_SFULL0, B_SFULL1, B_PHI0, B_PHI1, B_PLO0, B_PLO1, B_PVDONE, B_DRAIN, B_XCH0, B_XCH1, B_OFREE,
+  B_QFREE, B_MRG, kNumBars
 };
+constexpr int kGroupSplit = 4;                      // chunks [0, 4) form group A, [4, 9) group B
 static_assert(kNumBars * 8 <= 192, "barrier area");
 
 constexpr uint32_t kTmemCols = 512;
@@ -109,7 +116,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Wait sites reported in the status word when a bounded wait runs out.
 enum : uint32_t {
   W_PROD_EMPTY = 1, W_MMA_Q, W_MMA_STALL, W_SM_S, W_SM_PV, W_SM_PV_EPI, W_DRAIN_MMA, W_SM_X, W_PROD_Q,
-  W_MERGE
+  W_MERGE, W_DRAIN_Q, W_DRAIN_MRG
 };
 
 // 128-byte-swizzled byte offset of the 16-byte piece `piece` (0-7) of row `row`
@@ -118,14 +125,14 @@ __device__ __forceinline__ int sw128(int row, int piece) {
   return (row >> 3) * 1024 + (row & 7) * 128 + ((piece ^ (row & 7)) << 4);
 }
 
-// The 9 copies of one lane for one row: its 16-byte piece of each 64-dim chunk.
-// `dst` is the piece's swizzled place in chunk 0, `src` its bytes in chunk 0;
-// chunk c adds c * kSlotBytes to the one and c * 128 to the other.
-template <int C>
+// The copies of one lane for one row: its 16-byte piece of each 64-dim chunk
+// C .. kEnd-1. `dst` is the piece's swizzled place in chunk 0, `src` its bytes
+// in chunk 0; chunk c adds c * kSlotBytes to the one and c * 128 to the other.
+template <int C, int kEnd>
 __device__ __forceinline__ void copy_row_chunks(uint32_t dst, const uint8_t* src, uint32_t sz) {
-  if constexpr (C < kChunks) {
+  if constexpr (C < kEnd) {
     cp_async_16_off2<C * kSlotBytes, C * 128>(dst, src, sz);
-    copy_row_chunks<C + 1>(dst, src, sz);
+    copy_row_chunks<C + 1, kEnd>(dst, src, sz);
   }
 }
 
@@ -336,10 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
-    mbar_init(bar(B_FULL0), kLoaders);     // one cp.async completion arrival per loader thread
-    mbar_init(bar(B_FULL1), kLoaders);
-    mbar_init(bar(B_EMPTY0), 1);
-    mbar_init(bar(B_EMPTY1), 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar(B_FULLA0 + i), kLoaders);   // one cp.async completion arrival per loader thread
+      mbar_init(bar(B_EMPTYA0 + i), 1);         // one MMA commit
+    }
     mbar_init(bar(B_SFULL0), 1);
     mbar_init(bar(B_SFULL1), 1);
     mbar_init(bar(B_PHI0), 4);             // one arrival per softmax warp
@@ -387,21 +394,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Rows two steps ahead are requested into L2 as soon as their index is
       // known: with two ring halves a step's rows are copied only once the step
       // two before has finished with its half, so without this their DRAM
-      // latency would sit on the loop's critical chain.
+      // latency would sit on the loop's critical chain. One prefetch per
+      // 128-byte line from the load/store path (a bulk prefetch per row goes
+      // through the copy engine, which takes the requests one at a time).
       int n1 = fetch(1), n2 = fetch(2);            // indices of steps k+1 and k+2
       auto prefetch_row = [&](int ix) {
-        if (ix >= 0 && ix < a.n_kv) prefetch_l2_bulk(a.kv + static_cast<size_t>(ix) * kRowBytes, kRowBytes);
+        if (ix >= 0 && ix < a.n_kv) {
+          const uint8_t* r = a.kv + static_cast<size_t>(ix) * kRowBytes;
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) prefetch_l2_line(r + 128 * c);
+        }
       };
-#pragma unroll 1
-      for (int k = 0; k < jb.nsteps; ++k, ++g) {
-        const int h = g & 1;
+      // one chunk group of the step's 64 rows: wait until the MMAs of step g - 2
+      // are done with it, copy, and arrive on its FULL barrier when the copies land
+      auto copy_group = [&](auto grp, int g, int h) -> bool {
+        constexpr int G = decltype(grp)::value;
         if (g >= 2) {
           int ok = 1;
-          if (lane == 0) ok = wait_bounded(bar(B_EMPTY0 + h), ((g >> 1) - 1) & 1, wc, W_PROD_EMPTY);
-          if (!__shfl_sync(0xffffffffu, ok, 0)) {
-            stop = true;
-            break;
-          }
+          if (lane == 0) ok = wait_bounded(bar((G == 0 ? B_EMPTYA0 : B_EMPTYB0) + h), ((g >> 1) - 1) & 1, wc,
+                                           W_PROD_EMPTY);
+          if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
         }
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
@@ -411,9 +423,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool valid = ix >= 0 && ix < a.n_kv;
           const uint8_t* src = a.kv + static_cast<size_t>(valid ? ix : 0) * kRowBytes + pc * 16;
           const uint32_t dst = sbase + kOffRing + h * kHalfBytes + static_cast<uint32_t>(sw128(row, pc));
-          copy_row_chunks<0>(dst, src, valid ? 16u : 0u);
+          if constexpr (G == 0) copy_row_chunks<0, kGroupSplit>(dst, src, valid ? 16u : 0u);
+          else copy_row_chunks<kGroupSplit, kChunks>(dst, src, valid ? 16u : 0u);
         }
-        cp_async_arrive_noinc(bar(B_FULL0 + h));
+        cp_async_arrive_noinc(bar((G == 0 ? B_FULLA0 : B_FULLB0) + h));
+        return true;
+      };
+#pragma unroll 1
+      for (int k = 0; k < jb.nsteps; ++k, ++g) {
+        const int h = g & 1;
+        if (!copy_group(std::integral_constant<int, 0>{}, g, h) ||
+            !copy_group(std::integral_constant<int, 1>{}, g, h)) {
+          stop = true;
+          break;
+        }
         if (k == 0) prefetch_row(n1);
         prefetch_row(n2);
         ixl = n1;
@@ -426,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============================================================ Q loads ===
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
+      int issued = 0;
 #pragma unroll 1
       for (int j = 0; j < njobs; ++j) {
         const Job jb = (j == 0) ? j0 : job_at(a, j);
@@ -436,119 +460,146 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         for (int c = 0; c < kChunks; ++c)
           tma_load_2d(sbase + kOffQ + c * kQChunkBytes, &tm_q, 64 * c, kMlaHeads * jb.t, bar(B_QFULL));
+        ++issued;
       }
+      // Nothing this thread started may still be writing shared memory when the
+      // CTA exits: wait for the last Q load (each load is issued only after the
+      // previous one was consumed, so it is the only one that can be in flight;
+      // already landed, unless the CTA is aborting).
+      if (issued > 0 && !wait_drain(bar(B_QFULL), (issued - 1) & 1, a.drain_limit_ns))
+        atomicCAS(&a.status[1], 0u, W_DRAIN_Q);
     }
   } else if (warp == 3) {
     // ========================================================= MMA issuer ===
     if (lane == 0) {
       constexpr uint32_t kIdescQK = idesc_make(64, 64, 1, false, false);   // A (Q), B (K rows) K-major
       constexpr uint32_t kIdescPV = idesc_make(128, 64, 1, true, false);   // A (V^T) MN-major, B (P^T) K-major
-      // Descriptors of the operands' first K step; every other one differs only
-      // in the start-address field (bits 0-13, address >> 4, no carry out of it
-      // below 256 KB), so the issue code adds a constant. Half 1 is half 0
-      // shifted by kHalfBytes.
-      const uint64_t d_k0 = sdesc_sw128(sbase + kOffRing, 16, 1024);
-      const uint64_t d_v0 = sdesc_sw128(sbase + kOffRing, kSlotBytes, 1024);
-      const uint64_t d_phi0 = sdesc_sw128(sbase + kOffRing + 8 * kSlotBytes, 16, 1024);
-      constexpr uint64_t kHalfStep = kHalfBytes >> 4;
-      const uint64_t d_q = sdesc_sw128(sbase + kOffQ, 16, 1024);
-      const uint64_t d_plo = sdesc_sw128(sbase + kOffPlo, 16, 1024);
-      // QK(g), chunks 3r .. 3r+2 (run r of 3): 12 MMAs of K=16 (32 bytes of a
-      // K-major row each) with constant descriptor offsets
-      auto qk_run = [&](int g, int r) {
+      // Operand descriptors as 32-bit words. Every descriptor's high word is the
+      // same (128-byte swizzle, 1024-byte atom stride); the low word holds the
+      // start address (bits 0-13, address >> 4, no carry out of it below 256 KB)
+      // and the leading-byte offset, so another K step, chunk, tile or ring half
+      // is an add to the low word, and within a group of MMAs that add is a
+      // compile-time constant. The groups are fully unrolled: tcgen05.mma is
+      // issued by one thread, and every instruction between two MMAs delays the
+      // next one (measured with a probe of this stream: 48-51 cycles per MMA
+      // unrolled, 60-64 with the descriptors stepped in a rolled loop).
+      const uint32_t w_hi = static_cast<uint32_t>(sdesc_sw128(sbase, 16, 1024) >> 32);
+      const uint32_t w_k0 = static_cast<uint32_t>(sdesc_sw128(sbase + kOffRing, 16, 1024));
+      const uint32_t w_v0 = static_cast<uint32_t>(sdesc_sw128(sbase + kOffRing, kSlotBytes, 1024));
+      const uint32_t w_phi0 = static_cast<uint32_t>(sdesc_sw128(sbase + kOffRing + 8 * kSlotBytes, 16, 1024));
+      const uint32_t w_q = static_cast<uint32_t>(sdesc_sw128(sbase + kOffQ, 16, 1024));
+      const uint32_t w_plo = static_cast<uint32_t>(sdesc_sw128(sbase + kOffPlo, 16, 1024));
+      constexpr uint32_t kHalfStep = kHalfBytes >> 4;
+      // QK(g) over chunks C0 .. C1-1: 4 MMAs of K=16 (32 bytes of a K-major row)
+      // per 64-dim chunk, all into S buffer g & 1.
+      auto qk_chunks = [&](int g, auto c0, auto c1) {
+        constexpr int C0 = decltype(c0)::value, C1 = decltype(c1)::value;
         const uint32_t d = tmem + kTmemS + 64 * (g & 1);
-        const uint64_t bk = d_k0 + (g & 1) * kHalfStep;
-        auto run = [&](auto c0) {
+        const uint32_t bk = w_k0 + (g & 1) * kHalfStep;
 #pragma unroll
-          for (int c = decltype(c0)::value; c < decltype(c0)::value + 3; ++c)
+        for (int c = C0; c < C1; ++c) {
+          if (c == 0) mma_f16_wc<0>(d, w_q, bk, w_hi, kIdescQK);
+          else mma_f16_wc<1>(d, w_q + c * (kQChunkBytes >> 4), bk + c * (kSlotBytes >> 4), w_hi, kIdescQK);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f16(d, d_q + (c * kQChunkBytes) / 16 + 2 * kk, bk + (c * kSlotBytes) / 16 + 2 * kk, kIdescQK,
-                      (c | kk) != 0);
-        };
-        if (r == 0) run(std::integral_constant<int, 0>{});
-        else if (r == 1) run(std::integral_constant<int, 3>{});
-        else run(std::integral_constant<int, 6>{});
-      };
-      // PV(g) with P_hi (part 0) or P_lo (part 1): for each 128-dim tile j of V,
-      // K = the 64 rows in 4 steps of 16 (2048 B of the MN-major V^T, 32 B of
-      // the K-major P^T each); `first` starts a new O^T (first step of a job).
-      // Only the CTA's own tiles tq0 .. tq1-1 (all four unless the job's dims are
-      // spread over several CTAs).
-      const int tq0 = j0.q0, tq1 = j0.q0 + j0.nq;
-      auto pv_part = [&](int g, int part, bool first) {
-        const uint64_t av = d_v0 + (g & 1) * kHalfStep;
-        const uint64_t bp = part ? d_plo : d_phi0 + (g & 1) * kHalfStep;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (j < tq0 || j >= tq1) continue;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f16(tmem + 64 * j, av + (2 * j * kSlotBytes + kk * 2048) / 16, bp + 2 * kk, kIdescPV,
-                    (!first || part > 0 || kk > 0));
+          for (int kk = 1; kk < 4; ++kk)
+            mma_f16_wc<1>(d, w_q + c * (kQChunkBytes >> 4) + 2 * kk, bk + c * (kSlotBytes >> 4) + 2 * kk, w_hi,
+                          kIdescQK);
         }
       };
-      // The balanced loop below issues the same MMAs from rolled loops: a few
-      // lines of code instead of three unrolled runs. Measured: the uniform
-      // calls at s_q = 1, 6, 16 ran 1-2 us faster with the balanced loop's issue
-      // code small, and the balanced calls no slower.
-      auto qk_compact = [&](int g) {
-        const uint32_t d = tmem + kTmemS + 64 * (g & 1);
-        const uint64_t bk = d_k0 + (g & 1) * kHalfStep;
-#pragma unroll 1
-        for (int c = 0; c < kChunks; ++c)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f16(d, d_q + (c * kQChunkBytes) / 16 + 2 * kk, bk + (c * kSlotBytes) / 16 + 2 * kk, kIdescQK,
-                    (c | kk) != 0);
+      // PV(g) for O^T tile j (dims 128 j .. 128 j + 127) with P_hi (part 0) or P_lo
+      // (part 1): K = the 64 rows in 4 steps of 16 (2048 B of the MN-major V^T, 32
+      // B of the K-major P^T each); `fresh` starts a new O^T (first step of a job).
+      auto pv_tile = [&](int g, int part, int j, bool fresh) {
+        const uint32_t av = w_v0 + (g & 1) * kHalfStep + j * ((2 * kSlotBytes) >> 4);
+        const uint32_t bp = part ? w_plo : w_phi0 + (g & 1) * kHalfStep;
+        const uint32_t d = tmem + 64 * j;
+        if (fresh && part == 0) mma_f16_wc<0>(d, av, bp, w_hi, kIdescPV);
+        else mma_f16_wc<1>(d, av, bp, w_hi, kIdescPV);
+        mma_f16_wc<1>(d, av + (2048 >> 4), bp + 2, w_hi, kIdescPV);
+        mma_f16_wc<1>(d, av + (4096 >> 4), bp + 4, w_hi, kIdescPV);
+        mma_f16_wc<1>(d, av + (6144 >> 4), bp + 6, w_hi, kIdescPV);
       };
-      auto pv_compact = [&](int g, int part, bool first) {
-        const uint64_t av = d_v0 + (g & 1) * kHalfStep;
-        const uint64_t bp = part ? d_plo : d_phi0 + (g & 1) * kHalfStep;
-#pragma unroll 1
-        for (int j = tq0; j < tq1; ++j)
+      // tiles j0 .. j1-1 of one part (the 4 tiles unrolled, each skipped unless in range)
+      auto pv_tiles = [&](int g, int part, int j0, int j1, bool fresh) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f16(tmem + 64 * j, av + (2 * j * kSlotBytes + kk * 2048) / 16, bp + 2 * kk, kIdescPV,
-                    (!first || part > 0 || kk > 0));
+        for (int j = 0; j < 4; ++j)
+          if (j >= j0 && j < j1) pv_tile(g, part, j, fresh);
       };
+      // This CTA's O^T tiles: tq0 .. tq1-1 (all four unless the job's dims are
+      // spread over several CTAs); those below tqa read chunk group A.
+      const int tq0 = j0.q0, tq1 = j0.q0 + j0.nq;
+      const int tqa = min(max(tq0, kGroupSplit / 2), tq1);
       bool ok = true;
+      auto wait = [&](uint32_t b, uint32_t ph, uint32_t site) {
+        if (ok && !wait_bounded(b, ph, wc, site)) ok = false;
+        return ok;
+      };
+      // the rows were written by other threads' cp.async (generic proxy); make
+      // them visible to the tensor core's reads (async proxy)
+      auto rows_visible = [&]() {
+        fence_proxy_async_smem();
+        tc_fence_after();
+      };
+      // QK(g) in its two chunk groups, each after its rows have landed
+      auto issue_qk = [&](int g, bool first_of_job, int qphase, bool last_of_job) {
+        const int h = g & 1;
+        if (!wait(bar(B_FULLA0 + h), (g >> 1) & 1, W_MMA_STALL)) return false;
+        if (first_of_job && !wait(bar(B_QFULL), qphase & 1, W_MMA_Q)) return false;
+        rows_visible();
+        qk_chunks(g, std::integral_constant<int, 0>{}, std::integral_constant<int, kGroupSplit>{});
+        if (!wait(bar(B_FULLB0 + h), (g >> 1) & 1, W_MMA_STALL)) return false;
+        rows_visible();
+        qk_chunks(g, std::integral_constant<int, kGroupSplit>{}, std::integral_constant<int, kChunks>{});
+        mma_commit(bar(B_SFULL0 + h));
+        if (last_of_job) mma_commit(bar(B_QFREE));   // the job's QKs are all issued
+        return true;
+      };
+      // PV(g) with the release of its chunk groups: tile-major (P_hi and P_lo of a
+      // tile together, so group A frees after the first two tiles) when P_lo is
+      // published already, else all P_hi tiles first (P_lo's buffer is still being
+      // read by PV(g - 1) when PV(g) is issued right behind it).
+      auto issue_pv = [&](int g, bool first, bool tile_major) {
+        const int h = g & 1;
+        if (!wait(bar(B_PHI0 + h), (g >> 1) & 1, W_MMA_STALL)) return false;
+        if (tile_major && !wait(bar(B_PLO0 + h), (g >> 1) & 1, W_MMA_STALL)) return false;
+        tc_fence_after();
+        if (tile_major) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (j >= tq0 && j < tq1) {
+              pv_tile(g, 0, j, first);
+              pv_tile(g, 1, j, first);
+              if (j + 1 == tqa) mma_commit(bar(B_EMPTYA0 + h));   // after the last tile that reads group A
+            }
+          }
+          if (tqa == tq0) mma_commit(bar(B_EMPTYA0 + h));          // no tile of this CTA reads group A
+        } else {
+          pv_tiles(g, 0, tq0, tq1, first);
+          if (!wait(bar(B_PLO0 + h), (g >> 1) & 1, W_MMA_STALL)) return false;
+          tc_fence_after();
+          pv_tiles(g, 1, tq0, tqa, false);
+          mma_commit(bar(B_EMPTYA0 + h));
+          pv_tiles(g, 1, tqa, tq1, false);
+        }
+        mma_commit(bar(B_EMPTYB0 + h));   // the half is free for the rows of step g + 2
+        mma_commit(bar(B_PVDONE));
+        return true;
+      };
       if (a.sched == 0) {
         // Uniform schedule, one job: a fixed order by pairs of steps,
-        //   QK(g) QK(g+1) PV_hi(g) PV_lo(g) PV_hi(g+1) PV_lo(g+1),
-        // each group issued after its own bounded wait. Every wait's producer was
-        // issued earlier in this order (rows of g+1 come after PV_lo(g-1), P_lo(g)
-        // after PV_lo(g-1) is done, S(g)'s buffer is free once PV_hi(g-2) is
-        // issued), so the order cannot deadlock. Measured faster than the polling
-        // loop of the balanced schedule below, by 4-6 % over s_q = 1 .. 384.
+        //   QK(g) QK(g+1) PV(g) PV(g+1),
+        // each group issued after its own bounded waits. Every wait's producer was
+        // issued earlier in this order (the rows of g+1 come after PV(g-1) freed
+        // its half, P_lo(g) after PV(g-1) is done, S(g)'s buffer is free once
+        // PV(g-2) is issued), so the order cannot deadlock. QK(g+1) covers the
+        // softmax of g, PV(g) that of g+1; the chunk groups of step g's half are
+        // refilled with the rows of g+2 while PV(g+1) and QK(g+2) run.
         const int n = j0.nsteps;
-        auto wait = [&](uint32_t b, uint32_t ph, uint32_t site) {
-          if (ok && !wait_bounded(b, ph, wc, site)) ok = false;
-          return ok;
-        };
         for (int g = 0; g < n && ok; g += 2) {
-          for (int h = g; h < g + 2 && h < n; ++h) {
-            if (!wait(bar(B_FULL0 + (h & 1)), (h >> 1) & 1, W_MMA_STALL)) break;
-            if (h == 0 && !wait(bar(B_QFULL), 0, W_MMA_Q)) break;
-            // the rows were written by other threads' cp.async (generic proxy);
-            // make them visible to the tensor core's reads (async proxy)
-            fence_proxy_async_smem();
-            tc_fence_after();
-#pragma unroll
-            for (int r = 0; r < 3; ++r) qk_run(h, r);   // one unbroken run of 36 MMAs
-            mma_commit(bar(B_SFULL0 + (h & 1)));
-            if (h == n - 1) mma_commit(bar(B_QFREE));   // the job's QKs are all issued
-          }
-          for (int h = g; h < g + 2 && h < n && ok; ++h) {
-            if (!wait(bar(B_PHI0 + (h & 1)), (h >> 1) & 1, W_MMA_STALL)) break;
-            tc_fence_after();
-            pv_part(h, 0, h == 0);
-            if (!wait(bar(B_PLO0 + (h & 1)), (h >> 1) & 1, W_MMA_STALL)) break;
-            tc_fence_after();
-            pv_part(h, 1, false);
-            mma_commit(bar(B_EMPTY0 + (h & 1)));   // the half is free for the rows of step h+2
-            mma_commit(bar(B_PVDONE));
-          }
+          if (!issue_qk(g, g == 0, 0, g == n - 1)) break;
+          if (g + 1 < n && !issue_qk(g + 1, false, 0, g + 1 == n - 1)) break;
+          if (!issue_pv(g, g == 0, true)) break;
+          if (g + 1 < n && !issue_pv(g + 1, false, false)) break;
         }
       } else {
         int total = 0;
@@ -577,28 +628,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool progress = false;
           if (c_lo && ready(bar(B_PLO0 + (npl & 1)), (npl >> 1) & 1)) {
             tc_fence_after();
-            pv_compact(npl, 1, false);
-            mma_commit(bar(B_EMPTY0 + (npl & 1)));
+            pv_tiles(npl, 1, tq0, tq1, false);
+            mma_commit(bar(B_EMPTYA0 + (npl & 1)));
+            mma_commit(bar(B_EMPTYB0 + (npl & 1)));
             mma_commit(bar(B_PVDONE));
             ++npl;
             progress = true;
           } else if (c_hi && ready(bar(B_PHI0 + (nph & 1)), (nph >> 1) & 1) &&
                      (hk > 0 || hj == 0 || ready(bar(B_OFREE), (hj - 1) & 1))) {
             tc_fence_after();
-            pv_compact(nph, 0, hk == 0);
+            pv_tiles(nph, 0, tq0, tq1, hk == 0);
             ++nph;
             if (++hk == hn) {
               hk = 0;
               if (++hj < njobs) hn = job_at(a, hj).nsteps;
             }
             progress = true;
-          } else if (c_qk && ready(bar(B_FULL0 + (nqk & 1)), (nqk >> 1) & 1) &&
+          } else if (c_qk && ready(bar(B_FULLA0 + (nqk & 1)), (nqk >> 1) & 1) &&
+                     ready(bar(B_FULLB0 + (nqk & 1)), (nqk >> 1) & 1) &&
                      (qk > 0 || ready(bar(B_QFULL), qj & 1))) {
-            // the rows were written by other threads' cp.async (generic proxy);
-            // make them visible to the tensor core's reads (async proxy)
-            fence_proxy_async_smem();
-            tc_fence_after();
-            qk_compact(nqk);   // one unbroken run of 36 MMAs
+            rows_visible();
+            qk_chunks(nqk, std::integral_constant<int, 0>{}, std::integral_constant<int, kChunks>{});
             mma_commit(bar(B_SFULL0 + (nqk & 1)));
             ++nqk;
             if (++qk == qn) {
@@ -628,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         // no MMA may still be reading shared memory or writing TMEM when the CTA exits
         mma_commit(bar(B_DRAIN));
-        if (!wait_drain(bar(B_DRAIN), 0, a.wait_limit_ns)) atomicCAS(&a.status[1], 0u, W_DRAIN_MMA);
+        if (!wait_drain(bar(B_DRAIN), 0, a.drain_limit_ns)) atomicCAS(&a.status[1], 0u, W_DRAIN_MMA);
       }
     }
   } else {
@@ -642,6 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float amax_l = 0.f;        // max |O| over the final rows this thread wrote
     int g = 0;                 // step index over all of this CTA's jobs
     int nmrg = 0;              // phases of B_MRG used so far
+    int nmrg_issued = 0;       // (tid 0) phases of B_MRG whose bulk copies it started
     int pending = 0;           // 1 + slot of a stored partial whose ready flag is still to be set
     auto bounded = [&](uint32_t b, uint32_t ph, uint32_t site) {
       int w = 1;
@@ -884,6 +935,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (*abort_flag) return;
         fence_proxy_async_all();
         mbar_arrive_expect_tx(bar(B_MRG), static_cast<uint32_t>(n_other * nq) * 32768u);
+        ++nmrg_issued;
         int oi = 0;
         for (int pq = 0; pq < npieces; ++pq) {
           if (pa + pq == static_cast<int>(blockIdx.x)) continue;
@@ -1079,6 +1131,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int o = 16; o > 0; o >>= 1) amax_l = fmaxf(amax_l, __shfl_xor_sync(0xffffffffu, amax_l, o));
       if (lane == 0 && amax_l > 0.f) atomicMax(reinterpret_cast<int*>(a.amax), __float_as_int(amax_l));
     }
+    // no bulk copy of a merge may still be landing in shared memory when the CTA
+    // exits (one is in flight at most; it has landed unless the CTA is aborting)
+    if (tid == 0 && nmrg_issued > 0 && !wait_drain(bar(B_MRG), (nmrg_issued - 1) & 1, a.drain_limit_ns))
+      atomicCAS(&a.status[1], 0u, W_DRAIN_MRG);
   }
 
   // ---- teardown: every role reaches this point, TMEM is freed by its owner --

@@ -81,16 +81,13 @@ struct WaitCtx {
 // has already completed) costs no call.
 static __device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity, const WaitCtx& ctx,
                                                uint32_t site) {
-  uint64_t t0 = 0;
+  const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     // polled with test_wait: measured a little faster than a suspending try_wait
     if (mbar_test_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
+    if ((it & 15u) == 0) {
       if (*ctx.abort_flag) return false;
-      const uint64_t now = globaltimer_ns();
-      if (t0 == 0) {
-        t0 = now;
-      } else if (now - t0 > ctx.limit_ns) {
+      if (globaltimer_ns() - t0 > ctx.limit_ns) {
         *ctx.abort_flag = 1;
         atomicOr(&ctx.status[0], 1u);
         atomicCAS(&ctx.status[1], 0u, site);
@@ -102,9 +99,11 @@ static __device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t par
 
 // Waits for the phase with the given parity of `bar`. Gives up after
 // ctx.limit_ns (or when another role of this CTA has aborted), records the
-// timeout in the status word and returns false. Never traps.
+// timeout in the status word and returns false. Never traps. The first test
+// never suspends the thread (a suspending try_wait could sit out a wait of any
+// length inside the hardware's own window, where no limit is checked).
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtx& ctx, uint32_t site) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   return wait_bounded_slow(bar, parity, ctx, site);
 }
 
@@ -217,6 +216,10 @@ __device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.pr
 __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
+// Requests the 128-byte line holding `p` into L2 (no completion to wait for).
+__device__ __forceinline__ void prefetch_l2_line(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 // Arrives on `bar` once every cp.async this thread issued so far has landed
 // (the barrier's expected count includes this arrival).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
@@ -260,6 +263,42 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
       "  tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
       "}\n" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The same with each operand descriptor given as its two 32-bit words. The low
+// word holds the start-address field, so stepping an operand through a tile is
+// one 32-bit add; the high words of every 128-byte-swizzled operand with an
+// 8-row atom stride of 1024 bytes are equal, so one register serves both.
+__device__ __forceinline__ void mma_f16_w(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t ab_hi,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred p;\n"
+      "  .reg .b64 da, db;\n"
+      "  setp.ne.b32 p, %5, 0;\n"
+      "  mov.b64 da, {%1, %3};\n"
+      "  mov.b64 db, {%2, %3};\n"
+      "  tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(ab_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The same with a compile-time accumulate flag (folded into the predicate).
+template <int kAccumulate>
+__device__ __forceinline__ void mma_f16_wc(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t ab_hi,
+                                           uint32_t idesc) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred p;\n"
+      "  .reg .b64 da, db;\n"
+      "  setp.ne.b32 p, %5, 0;\n"
+      "  mov.b64 da, {%1, %3};\n"
+      "  mov.b64 db, {%2, %3};\n"
+      "  tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(ab_hi), "r"(idesc), "n"(kAccumulate)
       : "memory");
 }
 

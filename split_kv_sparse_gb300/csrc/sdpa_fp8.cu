@@ -253,10 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(dst + kKVTileBytes, &tm_v, 0, g, key, bar(B_SFULL_STAGE0 + st));
         last[st] = t;
       }
-      if (!ok)
-        for (int st = 0; st < kStages; ++st)
-          if (last[st] >= 0 && !wait_drain(bar(B_SFULL_STAGE0 + st), (last[st] / kStages) & 1, a.wait_limit_ns))
-            atomicCAS(&a.status[1], 0u, W_DRAIN_TMA2);
+      // Nothing this thread started may still be writing shared memory when the
+      // CTA exits: wait for the last load of every stage and for Q (all landed
+      // already, unless the CTA is aborting).
+      (void)ok;
+      for (int st = 0; st < kStages; ++st)
+        if (last[st] >= 0 && !wait_drain(bar(B_SFULL_STAGE0 + st), (last[st] / kStages) & 1, a.drain_limit_ns))
+          atomicCAS(&a.status[1], 0u, W_DRAIN_TMA2);
+      if (!wait_drain(bar(B_QFULL), 0, a.drain_limit_ns)) atomicCAS(&a.status[1], 0u, W_DRAIN_TMA2);
     }
   } else if (warp == 1) {
     // ========================================================= MMA issuer ===
@@ -313,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) {
         mma_commit(bar(B_DRAIN));
-        if (!wait_drain(bar(B_DRAIN), 0, a.wait_limit_ns)) atomicCAS(&a.status[1], 0u, W_DRAIN_MMA2);
+        if (!wait_drain(bar(B_DRAIN), 0, a.drain_limit_ns)) atomicCAS(&a.status[1], 0u, W_DRAIN_MMA2);
       }
     }
   } else if (warp >= 6) {

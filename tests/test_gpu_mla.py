@@ -308,6 +308,54 @@ def test_long_topk():
         assert_lse_close(r["lse"], L, what=f"LSE S={S}")
 
 
+@pytest.mark.parametrize("S", [1, 2])
+def test_dim_groups_on_long_top_k(S):
+    """A job's dims spread over four CTAs (the plan for two tokens on the device's SMs) on
+    topk 4096: 64 or 32 steps per CTA, so any drift in how a CTA releases ring
+    chunks to its loaders would show as a wrong row, a wrong result or a timeout."""
+    inp = wl.mla_inputs(2, 32768, 4096, seed=88, index_mode="uniform", with_sink=True)
+    O, L = oracle_mla(inp)
+    r = run_mla(inp, S)
+    assert r["plan"].dim_groups == 4
+    assert_o_close(r["out"].numpy(), O)
+    assert_lse_close(r["lse"], L)
+
+
+@pytest.mark.parametrize("s_q,S", [(1, 0), (6, 0), (96, 0), (16, b.MLA_FORCE_BALANCED), (2, 1)])
+def test_many_calls_back_to_back(s_q, S):
+    """200 consecutive decode calls in CUDA graphs, as the bench runs them: no wait
+    may run out, and the last call's output is the oracle's."""
+    inp = wl.mla_inputs(s_q, 32768, 640, seed=900 + s_q, with_sink=True)
+    dev = torch.device("cuda")
+    q, kv, idx, sink = inp.q.to(dev), inp.kv.to(dev), inp.idx.to(dev), inp.sink.to(dev)
+    plan = b.mla_decode_plan(s_q, 640, force_splits=S)
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
+    if plan.workspace_bytes:
+        b.mla_workspace_init(plan, ws)
+    out = torch.empty(s_q, 64, 512, dtype=torch.float32, device=dev)
+    lse = torch.empty(s_q, 64, dtype=torch.float32, device=dev)
+    st = torch.cuda.Stream()
+
+    def call():
+        b.mla_sparse_decode(plan, s_q, q, kv, inp.n_kv, idx, inp.sm_scale, sink, "f32", 1.0, out, lse, None,
+                            ws if plan.workspace_bytes else None, stream=st)
+    with torch.cuda.stream(st):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        for _ in range(50):
+            call()
+    with torch.cuda.stream(st):
+        for _ in range(4):
+            g.replay()
+    torch.cuda.synchronize()
+    check_status()
+    O, L = oracle_mla(inp)
+    assert_o_close(out.cpu().numpy(), O)
+    assert_lse_close(lse.cpu().double().numpy(), L)
+
+
 def test_cache_past_two_gigabytes():
     """A 2.1M-row cache (2.4 GB, row offsets past 2^31 bytes), made of copies of a
     32768-row seeded cache; the indices reach the last rows."""
