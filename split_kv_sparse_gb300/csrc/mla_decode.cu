@@ -89,11 +89,11 @@ constexpr int kOffRing = 0;
 constexpr int kOffQ = kOffRing + kRingBytes;        // 147456
 constexpr int kOffPlo = kOffQ + kQBytes;            // 221184: P_lo^T, 64 heads x 64 rows bf16
 constexpr int kOffBars = kOffPlo + kHalfBytes;      // 229376
-constexpr int kOffMisc = kOffBars + 192;            // [0] tmem base, [1] abort flag, [2] ticket, [3] merge wait,
+constexpr int kOffMisc = kOffBars + 256;            // [0] tmem base, [1] abort flag, [2] ticket, [3] merge wait,
                                                     // [4..11] rescale masks [2][4], [12..15] failure flags
 constexpr int kOffAlpha = kOffMisc + 128;           // float[2][64] rescale factors by step parity
 constexpr int kOffHead = kOffAlpha + 512;           // float[2][64] per-head epilogue scalars
-constexpr int kSmemBytes = kOffHead + 512;          // 230720
+constexpr int kSmemBytes = kOffHead + 512;          // 230784
 
 // The ring half of each step is filled and released in two chunk groups: A =
 // column chunks 0-3 (the V dims of O^T tiles 0 and 1) and B = chunks 4-8 (tiles
@@ -103,10 +103,10 @@ constexpr int kSmemBytes = kOffHead + 512;          // 230720
 enum {
   B_QFULL = 0, B_FULLA0, B_FULLA1, B_FULLB0, B_FULLB1, B_EMPTYA0, B_EMPTYA1, B_EMPTYB0, B_EMPTYB1,
   B_SFULL0, B_SFULL1, B_PHI0, B_PHI1, B_PLO0, B_PLO1, B_PVDONE, B_DRAIN, B_XCH0, B_XCH1, B_OFREE,
-  B_QFREE, B_MRG, kNumBars
+  B_QFREE, B_MRG, B_OT0, B_OT1, B_OT2, B_OT3, kNumBars
 };
 constexpr int kGroupSplit = 4;                      // chunks [0, 4) form group A, [4, 9) group B
-static_assert(kNumBars * 8 <= 192, "barrier area");
+static_assert(kNumBars * 8 <= 256, "barrier area");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 256;                    // S buffers at columns 256 and 320
@@ -360,6 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_OFREE), 4);            // the epilogue's last TMEM read of O^T, per softmax warp
     mbar_init(bar(B_QFREE), 1);            // a job's last QK has completed: its Q buffer is free
     mbar_init(bar(B_MRG), 1);              // a merge's bulk copies of other pieces' partials
+    for (int i = 0; i < 4; ++i) mbar_init(bar(B_OT0 + i), 1);   // O^T tile i of a job is complete
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -437,6 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           stop = true;
           break;
         }
+        // (Deferring the first prefetches until the first two steps' copies are on
+        // their way measured slower, at s_q = 1 and 96 alike.)
         if (k == 0) prefetch_row(n1);
         prefetch_row(n2);
         ixl = n1;
@@ -558,7 +561,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // tile together, so group A frees after the first two tiles) when P_lo is
       // published already, else all P_hi tiles first (P_lo's buffer is still being
       // read by PV(g - 1) when PV(g) is issued right behind it).
-      auto issue_pv = [&](int g, bool first, bool tile_major) {
+      // On the job's last step each O^T tile's completion is signalled on its own
+      // barrier (B_OT0 + j), so the epilogue reads a tile while the MMAs of the
+      // next ones still run.
+      auto issue_pv = [&](int g, bool first, bool tile_major, bool last) {
         const int h = g & 1;
         if (!wait(bar(B_PHI0 + h), (g >> 1) & 1, W_MMA_STALL)) return false;
         if (tile_major && !wait(bar(B_PLO0 + h), (g >> 1) & 1, W_MMA_STALL)) return false;
@@ -569,6 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j >= tq0 && j < tq1) {
               pv_tile(g, 0, j, first);
               pv_tile(g, 1, j, first);
+              if (last) mma_commit(bar(B_OT0 + j));
               if (j + 1 == tqa) mma_commit(bar(B_EMPTYA0 + h));   // after the last tile that reads group A
             }
           }
@@ -577,9 +584,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           pv_tiles(g, 0, tq0, tq1, first);
           if (!wait(bar(B_PLO0 + h), (g >> 1) & 1, W_MMA_STALL)) return false;
           tc_fence_after();
-          pv_tiles(g, 1, tq0, tqa, false);
-          mma_commit(bar(B_EMPTYA0 + h));
-          pv_tiles(g, 1, tqa, tq1, false);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (j >= tq0 && j < tq1) {
+              pv_tile(g, 1, j, false);
+              if (last) mma_commit(bar(B_OT0 + j));
+              if (j + 1 == tqa) mma_commit(bar(B_EMPTYA0 + h));
+            }
+          }
+          if (tqa == tq0) mma_commit(bar(B_EMPTYA0 + h));
         }
         mma_commit(bar(B_EMPTYB0 + h));   // the half is free for the rows of step g + 2
         mma_commit(bar(B_PVDONE));
@@ -598,8 +611,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int g = 0; g < n && ok; g += 2) {
           if (!issue_qk(g, g == 0, 0, g == n - 1)) break;
           if (g + 1 < n && !issue_qk(g + 1, false, 0, g + 1 == n - 1)) break;
-          if (!issue_pv(g, g == 0, true)) break;
-          if (g + 1 < n && !issue_pv(g + 1, false, false)) break;
+          if (!issue_pv(g, g == 0, true, g == n - 1)) break;
+          if (g + 1 < n && !issue_pv(g + 1, false, false, g + 1 == n - 1)) break;
         }
       } else {
         int total = 0;
@@ -889,7 +902,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // there forever. Per-head scalars hs[0..1][64]: 1/denominator and the job's
       // own LSE.
       lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);
-      if (!bad) {
+      if (!bad && a.sched != 0) {
         bounded(bar(B_PVDONE), (g - 1) & 1, W_SM_PV_EPI);   // O^T is complete
         tc_fence_after();
       }
@@ -1036,6 +1049,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int dl = 32 * sp + lane;   // dim within the tile
         const int d = 128 * q + dl;
         float v[64];
+        if (a.sched == 0) {   // (one job per CTA) tile q of O^T is complete
+          if (!bad) bounded(bar(B_OT0 + q), 0, W_SM_PV_EPI);
+          tc_fence_after();
+        }
         if (!merge) {
           uint32_t o[64];
           tmem_ld_32x32b_x64(tmem + lane_base + 64 * q, o);
