@@ -120,18 +120,16 @@ typedef struct {
  * of all tokens, token-major, are cut into P contiguous near-equal ranges, one per
  * CTA, with P the fewest CTAs that reach the smallest per-CTA block count on
  * num_sms SMs: per = ceil(s_q * num_blocks / num_sms), P = ceil(s_q * num_blocks / per).
- * A token inside one range is finished by that CTA (sink, cast, LSE, amax). The
- * pieces of a token cut by range boundaries are partials with the split
- * definition; the piece that ends last folds the others in by the combine's rule
- * and writes the token's final rows, so the call is one kernel. Workspace of this
- * schedule, with C = balanced_ctas: fp32 O partials [2*C][h_q][d_v] (in the
- * kernel's own element order) and fp32 LSE partials [2*C][h_q] from offset 0
- * (the LSE part 256-byte aligned), and uint32 per-token counters [s_q_max]
- * followed by ready flags [2*C] in the last round_up((s_q_max + 2*C) * 4, 256)
- * bytes of plan->workspace_bytes. Those counters and flags must be zero before
- * the first call: run mla_workspace_init once on a new workspace (each call
- * leaves them at zero again), and once more after a call that set
- * MLA_STATUS_TIMEOUT. */
+ * A token inside one range is finished by that CTA (sink, cast, LSE, amax). Each
+ * piece of a token cut by range boundaries is a partial with the split definition,
+ * written to slot = the piece's place among its token's pieces (0 for the piece
+ * that holds the token's first block) in the split layout [slot][s_q][h_q][d_v]
+ * (fp32) and [slot][s_q][h_q] (fp32 LSE, at the next 256-byte boundary after the
+ * O part sized for s_q_max); the combine, launched as the decode kernel's
+ * programmatic dependent, folds each cut token's pieces. So the call is two
+ * kernels and the workspace holds one partial slot per piece of the most cut
+ * token (over every s_q <= s_q_max the schedule applies to). Nothing in it needs
+ * to start at zero. */
 
 /* Choose the split count and size the workspace ("The Split-K Dispatch",
  * "Adaptive NSPLIT"; FlashMLA PR #25, "Measured": partial bytes
@@ -149,24 +147,23 @@ typedef struct {
  * dim_groups is the largest of 4, 2, 1 with s_q_max * S * dim_groups <= num_sms.
  * With force_splits == 0 the plan also enables the balanced schedule for the
  * one-shot call when it is expected to beat that grid at s_q_max: with per =
- * ceil(s_q_max * num_blocks / num_sms), when 2 <= per, ceil(num_blocks / per) + 1
- * <= 32 and per + 5 < ceil(s_q_max * S / num_sms) * ceil(num_blocks / S) (the
- * most blocks any SM walks under the grid; 5 blocks stands for the schedule's
- * measured cost of job boundaries and merging). force_splits == MLA_FORCE_BALANCED keeps
- * the automatic S and enables the balanced schedule whenever the first two
- * conditions hold. Enabling it sets balanced_ctas = min(num_sms, s_q_max *
- * num_blocks) and sizes the workspace for both schedules: the larger of the two
- * partial areas plus the balanced counters at the end. With force_splits > 0
- * the one-shot call runs the (token, split) jobs.
+ * ceil(s_q_max * num_blocks / num_sms), when 2 <= per and per + 5 <
+ * ceil(s_q_max * S / num_sms) * ceil(num_blocks / S) (the most blocks any SM walks
+ * under the grid; 5 blocks stands for the schedule's cost of job boundaries and of
+ * combining the pieces). force_splits == MLA_FORCE_BALANCED keeps the automatic S
+ * and enables the balanced schedule whenever 2 <= per. Enabling it sets
+ * balanced_ctas = min(num_sms, s_q_max * num_blocks) and sizes the workspace for
+ * both schedules: the larger of the two partial areas. With force_splits > 0 the
+ * one-shot call runs the (token, split) jobs.
  * Errors: MLA_ERR_UNSUPPORTED unless h_q == 64, d_qk == 576, d_v == 512;
  *         MLA_ERR_INVALID_ARG for s_q_max < 1, topk < 1, out == NULL, or bad split counts. */
 MLA_API int mla_decode_plan(int s_q_max, int h_q, int d_qk, int d_v, int topk,
                     int num_sms, int max_splits, int force_splits, mla_plan_t* out);
 
-/* Zeroes all plan->workspace_bytes of `workspace` on `stream`. Needed once on a
- * new workspace before the first mla_sparse_decode call of a plan with
- * balanced_ctas > 0 (its counters must start at zero), and after a call that
- * timed out; harmless otherwise. Returns MLA_OK at once when the plan needs no
+/* Zeroes all plan->workspace_bytes of `workspace` on `stream`. No schedule needs
+ * its workspace to start at zero (every partial slot a call reads was written by
+ * the same call); this is a convenience for callers that want a defined state.
+ * Returns MLA_OK at once when the plan needs no
  * workspace; MLA_ERR_WORKSPACE for a NULL or not 256-byte aligned workspace;
  * MLA_ERR_INVALID_ARG for plan == NULL; MLA_ERR_CUDA when the clear cannot be
  * queued. */
@@ -357,17 +354,15 @@ MLA_API int mla_get_status(uint32_t* status_out, uint32_t* site_out);
 MLA_API int mla_selftest_wait_timeout(uint64_t limit_ns, void* stream);
 
 /* Sets the time limit of the decode kernels' pipeline waits (every mbarrier
- * wait of mla_decode's and the dense kernel's roles, and the balanced schedule's
- * wait on other pieces' ready flags) for the calls launched after it, process
- * wide. limit_ns = 0 restores the default of 2 s; otherwise 100 ns .. 10 s, else
- * MLA_ERR_INVALID_ARG. A wait that runs out records MLA_STATUS_TIMEOUT and the
- * wait's site in the status word (mla_get_status) and aborts its CTA: the other
- * roles stop at their next wait, the CTA waits (up to 2 s, whatever this limit)
- * for its own copies and MMAs in flight, frees its tensor memory and exits; the
- * call's outputs are then undefined, and a balanced-schedule workspace must be
- * cleared again (mla_workspace_init) before the next call. For tests of that
- * abort path: a limit far below a step's latency makes real waits run out. The
- * pages have no counterpart (failure handling of this library). */
+ * wait of the sparse-MLA and the dense kernels' roles) for the calls launched
+ * after it, process wide. limit_ns = 0 restores the default of 2 s; otherwise
+ * 100 ns .. 10 s, else MLA_ERR_INVALID_ARG. A wait that runs out records
+ * MLA_STATUS_TIMEOUT and the wait's site in the status word (mla_get_status) and
+ * aborts its CTA: the other roles stop at their next wait, the CTA waits (up to
+ * 2 s, whatever this limit) for its own copies and MMAs in flight, frees its
+ * tensor memory and exits; the call's outputs are then undefined. For tests of
+ * that abort path: a limit far below a step's latency makes real waits run out.
+ * The pages have no counterpart (failure handling of this library). */
 MLA_API int mla_set_wait_limit_ns(uint64_t limit_ns);
 
 /* ======================================================================= *

@@ -103,35 +103,46 @@ uint64_t split_workspace_bytes(int S, int s_q) {
   return round_up(round_up(o, 256) + static_cast<uint64_t>(S) * s_q * kMlaHeads * 4ull, 256);
 }
 
-// Workspace of the balanced schedule for at most `ctas` CTAs and `s_q_max` tokens:
-//   fp32 O partials [2 * ctas][64][512] at 0, fp32 LSE partials [2 * ctas][64]
-//   after them; its uint32 per-token piece counters [s_q_max] and per-slot ready
-//   flags [2 * ctas] sit at the end of the plan's workspace (past what the
-//   uniform schedule uses too) and must start at zero (mla_workspace_init); each
-//   call leaves them at zero again.
-struct BalancedLayout {
-  uint64_t lse_off, partial_bytes, flag_bytes;
-};
 // Blocks per CTA of the balanced schedule for s_q tokens (0 when it does not
-// apply: fewer than 2 blocks per CTA, i.e. every block its own piece, or more
-// pieces per cut token than the merge's table holds).
+// apply: fewer than 2 blocks per CTA, i.e. every block its own piece).
 int64_t balanced_per(int64_t s_q, int nb, int num_sms) {
   const int64_t U = s_q * nb;
   const int64_t per = (U + num_sms - 1) / num_sms;
-  if (per < 2 || (nb + per - 1) / per + 1 > 32) return 0;
-  return per;
+  return per < 2 ? 0 : per;
+}
+// CTA ranges of the balanced schedule for s_q tokens: the fewest that reach the
+// smallest per-CTA block count on num_sms SMs.
+int balanced_ctas(int64_t s_q, int nb, int num_sms) {
+  const int64_t U = s_q * nb;
+  const int64_t per = (U + num_sms - 1) / num_sms;
+  return static_cast<int>((U + per - 1) / per);
+}
+// The most pieces one token is cut into by the balanced schedule, over every
+// s_q up to s_q_max at which the schedule applies: the partial slots its
+// workspace needs. Once a CTA range is longer than a token, no token spans more
+// than two ranges.
+int balanced_slots(int s_q_max, int nb, int num_sms) {
+  int most = 1;
+  for (int64_t s_q = 1; s_q <= s_q_max; ++s_q) {
+    const int64_t per = balanced_per(s_q, nb, num_sms);
+    if (per == 0) continue;
+    if (per > nb) return std::max(most, 2);
+    const int U = static_cast<int>(s_q * nb), P = balanced_ctas(s_q, nb, num_sms);
+    for (int64_t t = 0; t < s_q; ++t) {
+      const int n = skv::bal_cta_of(static_cast<int>((t + 1) * nb - 1), U, P) -
+                    skv::bal_cta_of(static_cast<int>(t * nb), U, P) + 1;
+      most = std::max(most, n);
+    }
+  }
+  return most;
 }
 // Blocks the busiest SM walks under the uniform (token, split) grid.
 int64_t uniform_makespan(int64_t s_q, int nb, int S, int num_sms) {
   return (s_q * S + num_sms - 1) / num_sms * ((nb + S - 1) / S);
 }
 // What the balanced schedule costs beyond its blocks, in 64-row block times: a
-// CTA's job boundary (the piece's partial store before the next token's softmax
-// can start) and the last piece's merge. It depends on how many tokens are cut;
-// measured on GB300 (topk 640, 152 SMs), in blocks of the uniform grid: about 5
-// at s_q = 160 and 200, 6 at 250, 7 to 7.5 at 96 and 384, under 1 at 300 (whole
-// tokens only). With 5 the rule below picks the faster schedule at every
-// measured s_q (96, 120, 160, 200, 250, 300, 384).
+// CTA's job boundary (the next token's Q, and its first PV waiting for the
+// previous job's epilogue) and the combine of the cut tokens' pieces.
 constexpr int64_t kBalancedOverheadBlocks = 5;
 // The most splits the dense planner's per-sequence rule gives one sequence.
 constexpr int kDenseMaxAdaptiveSplits = 16;
@@ -141,15 +152,6 @@ int dim_groups_for(int64_t jobs, int num_sms) {
   for (int d = 4; d > 1; d /= 2)
     if (jobs * d <= num_sms) return d;
   return 1;
-}
-
-BalancedLayout balanced_layout(int ctas, int s_q_max) {
-  BalancedLayout L;
-  const uint64_t slots = 2ull * static_cast<uint64_t>(ctas);
-  L.lse_off = round_up(slots * kMlaHeads * kMlaDv * 4ull, 256);
-  L.partial_bytes = round_up(L.lse_off + slots * kMlaHeads * 4ull, 256);
-  L.flag_bytes = round_up((static_cast<uint64_t>(s_q_max) + slots) * 4ull, 256);
-  return L;
 }
 
 int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
@@ -280,11 +282,12 @@ int mla_decode_plan(int s_q_max, int h_q, int d_qk, int d_v, int topk, int num_s
   const int64_t per = balanced_per(s_q_max, nblk, num_sms);
   if (force_splits == 0 && per > 0 &&
       (want_balanced || per + kBalancedOverheadBlocks < uniform_makespan(s_q_max, nblk, S, num_sms))) {
-    // the one-shot call spreads all tokens' blocks over at most num_sms CTAs
+    // the one-shot call spreads all tokens' blocks over at most num_sms CTAs; its
+    // workspace holds a partial slot per piece of the most cut token
     const int64_t units = static_cast<int64_t>(s_q_max) * nblk;
     out->balanced_ctas = static_cast<int32_t>(std::min<int64_t>(units, num_sms));
-    const BalancedLayout L = balanced_layout(out->balanced_ctas, s_q_max);
-    out->workspace_bytes = std::max(out->workspace_bytes, L.partial_bytes) + L.flag_bytes;
+    out->workspace_bytes =
+        std::max<uint64_t>(out->workspace_bytes, split_workspace_bytes(balanced_slots(s_q_max, nblk, num_sms), s_q_max));
   }
   return MLA_OK;
 }
@@ -356,8 +359,9 @@ int mla_combine_impl(const mla_plan_t* plan, int s_q, const void* workspace, con
 }
 
 // The one-shot call on the balanced schedule: every SM walks (nearly) the same
-// number of 64-row blocks whatever s_q is. One kernel: whole tokens are finished
-// by the CTA that holds them, a cut token by the CTA whose piece ends last.
+// number of 64-row blocks whatever s_q is. The decode kernel writes the final
+// rows of whole tokens and a partial per piece of every token cut by a range
+// boundary; the combine, launched as its programmatic dependent, folds those.
 int mla_decode_balanced(const mla_plan_t* plan, int s_q, const void* q, const void* kv, int64_t n_kv,
                         const int32_t* idx, float sm_scale, const float* sink, int out_dtype, float out_inv_scale,
                         void* out, float* lse_out, float* amax_out, void* workspace, void* stream) {
@@ -367,23 +371,22 @@ int mla_decode_balanced(const mla_plan_t* plan, int s_q, const void* q, const vo
   if (st != MLA_OK) return st;
   if (out == nullptr || !aligned(out, 16) || !valid_out_dtype(out_dtype)) return MLA_ERR_INVALID_ARG;
   if (out_dtype == MLA_OUT_E4M3 && !std::isfinite(out_inv_scale)) return MLA_ERR_INVALID_ARG;
-  const BalancedLayout L = balanced_layout(plan->balanced_ctas, plan->s_q_max);
-  if (workspace == nullptr || !aligned(workspace, 256) || plan->workspace_bytes < L.partial_bytes + L.flag_bytes)
-    return MLA_ERR_WORKSPACE;
-  // CTAs: the fewest that reach the smallest per-CTA block count on num_sms SMs
   const int nb = plan->num_blocks;
   const int64_t U = static_cast<int64_t>(s_q) * nb;
   if (U > 0x7FFFFFFFll) return MLA_ERR_INVALID_ARG;
-  const int64_t per = (U + plan->num_sms - 1) / plan->num_sms;
-  const int P = static_cast<int>((U + per - 1) / per);
+  const int P = balanced_ctas(s_q, nb, plan->num_sms);
   if (P > plan->balanced_ctas) return MLA_ERR_WORKSPACE;
+  const int slots = balanced_slots(plan->s_q_max, nb, plan->num_sms);
+  const uint64_t o_bytes = static_cast<uint64_t>(slots) * plan->s_q_max * kMlaHeads * kMlaDv * 4ull;
+  if (workspace == nullptr || !aligned(workspace, 256) ||
+      plan->workspace_bytes < split_workspace_bytes(slots, plan->s_q_max))
+    return MLA_ERR_WORKSPACE;
   DeviceState* dev = nullptr;
   if ((st = device_state(&dev)) != MLA_OK) return st;
   CUtensorMap tq;
   if ((st = mla_q_tensor_map(s_q, q, &tq)) != MLA_OK) return st;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  uint32_t* flags = reinterpret_cast<uint32_t*>(ws + plan->workspace_bytes - L.flag_bytes);
   if (amax_out != nullptr) {
     if ((st = cuda_status(cudaMemsetAsync(amax_out, 0, sizeof(float), cs))) != MLA_OK) return st;
   }
@@ -401,9 +404,7 @@ int mla_decode_balanced(const mla_plan_t* plan, int s_q, const void* q, const vo
   a.direct_whole = 1;
   a.scale_log2 = sm_scale * 1.4426950408889634f;
   a.o_acc = reinterpret_cast<float*>(ws);
-  a.lse_acc = reinterpret_cast<float*>(ws + L.lse_off);
-  a.counters = flags;
-  a.ready = flags + plan->s_q_max;
+  a.lse_acc = reinterpret_cast<float*>(ws + round_up(o_bytes, 256));
   a.out = out;
   a.out_dtype = out_dtype;
   a.inv_scale = out_inv_scale;
@@ -413,7 +414,24 @@ int mla_decode_balanced(const mla_plan_t* plan, int s_q, const void* q, const vo
   a.status = dev->status;
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.drain_limit_ns = kWaitLimitNs;
-  return cuda_status(skv::launch_mla_decode(tq, a, cs));
+  if ((st = cuda_status(skv::launch_mla_decode(tq, a, cs))) != MLA_OK) return st;
+  skv::CombineArgs c{};
+  c.o_acc = a.o_acc;
+  c.lse_acc = a.lse_acc;
+  c.num_splits = slots;
+  c.rows = s_q * kMlaHeads;
+  c.heads = kMlaHeads;
+  c.d = kMlaDv;
+  c.sink = sink;
+  c.out = out;
+  c.out_dtype = out_dtype;
+  c.inv_scale = out_inv_scale;
+  c.lse_out = lse_out;
+  c.amax = amax_out;
+  c.bal_nb = nb;
+  c.bal_units = static_cast<int>(U);
+  c.bal_ctas = P;
+  return cuda_status(skv::launch_combine(c, /*zero_amax=*/false, /*pdl=*/true, cs));
 }
 }  // namespace
 

@@ -45,7 +45,13 @@ __global__ void __launch_bounds__(kWarps * 32, kBatch == 8 ? 4 : 1) combine_kern
   const int slice = item - row * kSlices;
   grid_dependency_wait();      // the split pass has finished writing the partials
   if (row >= a.rows) return;   // whole warp leaves together
-  const int S = a.num_splits;
+  int S = a.num_splits;
+  if (a.bal_ctas > 0) {
+    const int t = row / a.heads;
+    const int pa = bal_cta_of(t * a.bal_nb, a.bal_units, a.bal_ctas);
+    S = bal_cta_of((t + 1) * a.bal_nb - 1, a.bal_units, a.bal_ctas) - pa + 1;
+    if (S == 1) return;        // a whole token: the decode kernel wrote its final rows
+  }
   const size_t rows = static_cast<size_t>(a.rows);
 
   auto src_of = [&](int s) {

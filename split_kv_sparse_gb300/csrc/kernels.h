@@ -32,15 +32,11 @@ struct MlaArgs {
   int direct_whole;     // a job that covers a whole token writes the final output
                         // (sink, cast, LSE, amax) instead of a partial
   float scale_log2;     // sm_scale * log2(e)
-  // Partial workspace. Uniform: [S][s_q][64][512] and [S][s_q][64]. Balanced:
-  // [2 * num_ctas][64][512] and [2 * num_ctas][64] (slot 2p: the first job of CTA
-  // p, slot 2p + 1: its last, when those are pieces of a token cut by a range
-  // boundary), with per-token piece counters [s_q] and per-slot ready flags
-  // [2 * num_ctas], all zero when the launch starts.
+  // Partial workspace: [slot][s_q][64][512] and [slot][s_q][64]. Uniform: slot =
+  // the split. Balanced: slot = a piece's place among the pieces of its token
+  // (a token cut by range boundaries); whole tokens write their final rows.
   float* o_acc;
   float* lse_acc;
-  uint32_t* counters;
-  uint32_t* ready;
   // direct path: final output
   void* out;            // [s_q][64][512] of out_dtype
   int out_dtype;
@@ -95,6 +91,11 @@ struct CombineArgs {
   float inv_scale;
   float* lse_out;       // [rows] or null
   float* amax;          // scalar or null
+  // Balanced sparse-MLA schedule (bal_ctas > 0): row r belongs to token r / heads,
+  // whose split count is the number of CTA ranges its bal_nb blocks fall in (the
+  // blocks of all tokens, bal_units of them, cut into bal_ctas ranges); a token in
+  // one range was finished by the decode kernel and is left alone.
+  int bal_nb, bal_units, bal_ctas;
 };
 // zero_amax: clear *amax first (a memset on the stream); pdl: launch as a
 // programmatic dependent of the preceding kernel on the stream.

@@ -18,14 +18,11 @@
 //   balanced  the s_q * nb blocks of all tokens, token-major, are cut into
 //             num_ctas near-equal contiguous ranges, one per CTA, so every SM
 //             walks the same number of rows whatever s_q is. A CTA runs one job
-//             per token its range touches. A whole token gets its final rows. A
-//             token cut by range boundaries is finished by whichever of its
-//             pieces counts itself last on a per-token counter: the others leave
-//             a partial and a ready flag; the last one merges them with its own O
-//             by the log-sum-exp rule of the combine ("The Split-K Dispatch",
-//             "The LSE Combine Strategy") and writes the final rows. It waits
-//             only on pieces that have already counted themselves, so their CTAs
-//             are running, and it leaves the counter and the flags at zero again.
+//             per token its range touches. A whole token gets its final rows; each
+//             piece of a token cut by range boundaries is a partial in the split
+//             layout, slot = the piece's place among its token's pieces, and the
+//             combine folds them by the log-sum-exp rule ("The Split-K Dispatch",
+//             "The LSE Combine Strategy").
 //
 // Layout of the work (256 threads, 64 gathered rows per step; the steps of all
 // of a CTA's jobs form one pipeline over a ring of two 64-row halves):
@@ -89,7 +86,7 @@ constexpr int kOffRing = 0;
 constexpr int kOffQ = kOffRing + kRingBytes;        // 147456
 constexpr int kOffPlo = kOffQ + kQBytes;            // 221184: P_lo^T, 64 heads x 64 rows bf16
 constexpr int kOffBars = kOffPlo + kHalfBytes;      // 229376
-constexpr int kOffMisc = kOffBars + 256;            // [0] tmem base, [1] abort flag, [2] ticket, [3] merge wait,
+constexpr int kOffMisc = kOffBars + 256;            // [0] tmem base, [1] abort flag,
                                                     // [4..11] rescale masks [2][4], [12..15] failure flags
 constexpr int kOffAlpha = kOffMisc + 128;           // float[2][64] rescale factors by step parity
 constexpr int kOffHead = kOffAlpha + 512;           // float[2][64] per-head epilogue scalars
@@ -103,7 +100,7 @@ constexpr int kSmemBytes = kOffHead + 512;          // 230784
 enum {
   B_QFULL = 0, B_FULLA0, B_FULLA1, B_FULLB0, B_FULLB1, B_EMPTYA0, B_EMPTYA1, B_EMPTYB0, B_EMPTYB1,
   B_SFULL0, B_SFULL1, B_PHI0, B_PHI1, B_PLO0, B_PLO1, B_PVDONE, B_DRAIN, B_XCH0, B_XCH1, B_OFREE,
-  B_QFREE, B_MRG, B_OT0, B_OT1, B_OT2, B_OT3, kNumBars
+  B_QFREE, B_OT0, B_OT1, B_OT2, B_OT3, kNumBars
 };
 constexpr int kGroupSplit = 4;                      // chunks [0, 4) form group A, [4, 9) group B
 static_assert(kNumBars * 8 <= 256, "barrier area");
@@ -116,7 +113,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Wait sites reported in the status word when a bounded wait runs out.
 enum : uint32_t {
   W_PROD_EMPTY = 1, W_MMA_Q, W_MMA_STALL, W_SM_S, W_SM_PV, W_SM_PV_EPI, W_DRAIN_MMA, W_SM_X, W_PROD_Q,
-  W_MERGE, W_DRAIN_Q, W_DRAIN_MRG
+  W_DRAIN_Q = 11
 };
 
 // 128-byte-swizzled byte offset of the 16-byte piece `piece` (0-7) of row `row`
@@ -136,12 +133,13 @@ __device__ __forceinline__ void copy_row_chunks(uint32_t dst, const uint8_t* src
   }
 }
 
-enum : int { J_FINAL = 0, J_PARTIAL = 1, J_PIECE = 2 };
+enum : int { J_FINAL = 0, J_PARTIAL = 1 };
 
 // One job of a CTA: token t, top-k entries [row0, row1) in nsteps steps of 64.
 //   J_FINAL    final rows of token t;
-//   J_PARTIAL  a (token, split) partial at workspace rows out_row .. + 63;
-//   J_PIECE    a piece of a token cut by the balanced schedule, partial slot `slot`.
+//   J_PARTIAL  a partial at workspace rows out_row .. + 63: a (token, split) job
+//              of the uniform schedule, or a piece of a token cut by the balanced
+//              schedule (slot = the piece's place among its token's pieces).
 struct Job {
   int t, row0, row1, nsteps, kind, slot;
   int q0, nq;   // the 128-dim tiles of O^T this CTA computes: q0 .. q0+nq-1
@@ -182,11 +180,12 @@ __device__ __forceinline__ Job job_at(const MlaArgs& a, int j) {
     r.row0 = b0 * kMlaBlockRows;
     r.row1 = min(b1 * kMlaBlockRows, a.topk);
     r.nsteps = b1 - b0;
-    r.kind = (b0 == 0 && b1 == nb) ? J_FINAL : J_PIECE;
-    r.slot = 2 * p + (j == 0 ? 0 : 1);
+    r.kind = (b0 == 0 && b1 == nb) ? J_FINAL : J_PARTIAL;
+    r.slot = p - bal_cta_of(t * nb, U, P);
     r.q0 = 0;
     r.nq = 4;
-    r.out_row = r.kind == J_FINAL ? static_cast<size_t>(t) * kMlaHeads : static_cast<size_t>(r.slot) * kMlaHeads;
+    r.out_row = r.kind == J_FINAL ? static_cast<size_t>(t) * kMlaHeads
+                                  : (static_cast<size_t>(r.slot) * a.s_q + t) * kMlaHeads;
   }
   return r;
 }
@@ -316,7 +315,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBars + 8 * i; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
-  volatile uint32_t* vmisc = misc;
   volatile uint32_t* xch = reinterpret_cast<volatile uint32_t*>(misc + 4);   // [2][4] rescale masks
   volatile int* fin = reinterpret_cast<volatile int*>(misc + 12);             // [4] per-warp failure flags
   float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
@@ -359,7 +357,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_XCH1), 4);
     mbar_init(bar(B_OFREE), 4);            // the epilogue's last TMEM read of O^T, per softmax warp
     mbar_init(bar(B_QFREE), 1);            // a job's last QK has completed: its Q buffer is free
-    mbar_init(bar(B_MRG), 1);              // a merge's bulk copies of other pieces' partials
     for (int i = 0; i < 4; ++i) mbar_init(bar(B_OT0 + i), 1);   // O^T tile i of a job is complete
     *abort_flag = 0;
     mbar_init_fence();
@@ -697,16 +694,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ============================================== softmax + epilogue ====
     const int sp = warp & 3;               // TMEM sub-partition (lanes 32sp..32sp+31)
-    const int tid = threadIdx.x - 128;     // 0..127
     const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
     const int head = 16 * sp + (lane & 15);   // this thread's head
     const int rb = (lane >> 4) * 32;          // and its 32 rows rb..rb+31 of every step
     int bad = 0;               // a bounded wait of this warp ran out
     float amax_l = 0.f;        // max |O| over the final rows this thread wrote
     int g = 0;                 // step index over all of this CTA's jobs
-    int nmrg = 0;              // phases of B_MRG used so far
-    int nmrg_issued = 0;       // (tid 0) phases of B_MRG whose bulk copies it started
-    int pending = 0;           // 1 + slot of a stored partial whose ready flag is still to be set
     auto bounded = [&](uint32_t b, uint32_t ph, uint32_t site) {
       int w = 1;
       if (lane == 0) w = wait_bounded(b, ph, wc, site);
@@ -741,11 +734,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           ib = rn + 32 < jb.row1 ? __ldg(idx_t + rn + 32) : -1;
         }
 
-        // A piece takes its ticket as its last step begins (the round trip
-        // overlaps the wait below): the last piece to count itself merges. Every
-        // piece that counted is running, so waiting on it cannot deadlock.
-        if (jb.kind == J_PIECE && k == jb.nsteps - 1 && tid == 0 && !bad)
-          misc[2] = atomicAdd(&a.counters[jb.t], 1u);
         const bool w = bounded(bar(B_SFULL0 + h), (g >> 1) & 1, W_SM_S);
         tc_fence_after();
         float x[32];
@@ -784,7 +772,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane < 16) alpha_s[h * 64 + head] = al;
         }
         const uint32_t rmask = __ballot_sync(0xffffffffu, need) & 0xffffu;
-        if (pending) __threadfence();   // the previous job's partial, long since stored
         __syncwarp();
         if (lane == 0) {
           xch[h * 4 + sp] = rmask | (bad ? 0x10000u : 0u);
@@ -820,11 +807,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // The other warps' rescale masks for this step.
         const bool wx = bounded(bar(B_XCH0 + h), (g >> 1) & 1, W_SM_X);
-        if (pending) {
-          // every softmax thread has fenced its stores of that partial: publish it
-          if (tid == 0 && wx) st_release_gpu(a.ready + (pending - 1), 1u);
-          pending = 0;
-        }
         const uint32_t x0 = xch[h * 4 + 0], x1 = xch[h * 4 + 1], x2 = xch[h * 4 + 2], x3 = xch[h * 4 + 3];
         if (((x0 | x1 | x2 | x3) & 0x10000u) || !wx) {
           bad = 1;
@@ -926,134 +908,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         bad = 1;
         break;   // every softmax warp leaves together
       }
-      // the pieces of this token (balanced schedule): CTAs pa..pb
-      const int nb = a.num_blocks, U = a.s_q * nb, P = a.num_ctas;
-      int pa = 0, npieces = 1;
-      if (jb.kind == J_PIECE) {
-        pa = bal_cta_of(jb.t * nb, U, P);
-        npieces = bal_cta_of((jb.t + 1) * nb - 1, U, P) - pa + 1;
-      }
-      const bool merge = jb.kind == J_PIECE && static_cast<int>(vmisc[2]) == npieces - 1;
-      const bool to_final = jb.kind == J_FINAL || merge;
-
-      // A merge in the CTA's last job stages the other pieces' partial tiles in
-      // shared memory by bulk copies (the ring and Q buffers are idle then; the
-      // TMA engine keeps many requests in flight, plain loads from a thread
-      // would not): one tile of each other piece at a time, or all four tiles
-      // at once when there is a single other piece.
-      const int n_other = npieces - 1;
-      const bool staged = merge && j == njobs - 1 && n_other <= 6;
-      const bool all_tiles = staged && n_other == 1;
-      auto issue_stage = [&](int q0, int nq) {   // (tid 0) tiles q0 .. q0+nq-1 of every other piece
-        if (*abort_flag) return;
-        fence_proxy_async_all();
-        mbar_arrive_expect_tx(bar(B_MRG), static_cast<uint32_t>(n_other * nq) * 32768u);
-        ++nmrg_issued;
-        int oi = 0;
-        for (int pq = 0; pq < npieces; ++pq) {
-          if (pa + pq == static_cast<int>(blockIdx.x)) continue;
-          const uint8_t* src = reinterpret_cast<const uint8_t*>(
-              a.o_acc + static_cast<size_t>(bal_slot(pa + pq, jb.t, nb, U, P)) * kMlaHeads * kMlaDv);
-          for (int qq = 0; qq < nq; ++qq)
-            bulk_load(sbase + static_cast<uint32_t>((all_tiles ? q0 + qq : oi) * 32768),
-                      src + static_cast<size_t>(q0 + qq) * 32768, 32768u, bar(B_MRG));
-          ++oi;
-        }
-      };
-      auto wait_stage = [&]() {
-        const bool ok = bounded(bar(B_MRG), nmrg & 1, W_MERGE);
-        ++nmrg;
-        return ok;
-      };
-      if (merge) {
-        // Last piece of a cut token: wait until the other pieces' partials are
-        // visible (their CTAs have counted themselves, so they are running),
-        // then merge by the combine's rule with the sink, as final rows.
-        if (tid == 0) {
-          uint32_t okw = 1;
-          const uint64_t t0 = globaltimer_ns();
-          for (int q = 0; q < npieces && okw; ++q) {
-            if (pa + q == static_cast<int>(blockIdx.x)) continue;
-            const uint32_t* f = a.ready + bal_slot(pa + q, jb.t, nb, U, P);
-            while (ld_acquire_gpu(f) == 0u) {
-              if (*abort_flag || globaltimer_ns() - t0 > a.wait_limit_ns) {
-                okw = 0;
-                *abort_flag = 1;
-                atomicOr(&a.status[0], 1u);
-                atomicCAS(&a.status[1], 0u, W_MERGE);
-                break;
-              }
-            }
-          }
-          if (okw) {
-            // leave the counter and the flags zero for the next call (every piece
-            // has counted itself and set its flag: nobody touches them again)
-            for (int q = 0; q < npieces; ++q)
-              if (pa + q != static_cast<int>(blockIdx.x)) a.ready[bal_slot(pa + q, jb.t, nb, U, P)] = 0u;
-            a.counters[jb.t] = 0u;
-          }
-          misc[3] = okw;
-        }
-        named_bar_sync(1, 128);
-        if (!vmisc[3]) {
-          bad = 1;
-          break;
-        }
-        if (tid == 0 && staged) issue_stage(0, all_tiles ? 4 : 1);   // in flight during the factors below
-        // Pieces are folded in token order, the own piece in the very form a
-        // stored partial has (O * (1/l) in fp32, its LSE), so the result does not
-        // depend on which piece happened to end last.
-        if (lane < 16) {
-          // the pieces' LSEs (all loads in flight together) into the table, then
-          // the max, the weights and w_q / den in place
-          float* coef = reinterpret_cast<float*>(smem + kOffPlo);
-#pragma unroll 4
-          for (int q = 0; q < npieces; ++q)
-            coef[q * 64 + head] = pa + q == static_cast<int>(blockIdx.x)
-                                      ? lse_own
-                                      : __ldcg(a.lse_acc + static_cast<size_t>(bal_slot(pa + q, jb.t, nb, U, P)) * kMlaHeads + head);
-          float M = -INFINITY;
-          for (int q = 0; q < npieces; ++q) M = fmaxf(M, coef[q * 64 + head]);
-          float wsum = 0.f, inv_den = 0.f;
-          if (M != -INFINITY) {
-            for (int q = 0; q < npieces; ++q) {
-              const float l = coef[q * 64 + head];
-              const float w = l == -INFINITY ? 0.f : exp2f(l - M);
-              coef[q * 64 + head] = w;
-              wsum += w;
-            }
-            float den = wsum;
-            if (a.sink != nullptr) den += exp2f(a.sink[head] * kLog2e - M);
-            inv_den = 1.f / den;
-          }
-          for (int q = 0; q < npieces; ++q) coef[q * 64 + head] = M == -INFINITY ? 0.f : coef[q * 64 + head] * inv_den;
-          if (a.lse_out != nullptr)
-            a.lse_out[static_cast<size_t>(jb.t) * kMlaHeads + head] = M == -INFINITY ? -INFINITY : M + log2f(wsum);
-        }
-        named_bar_sync(1, 128);
-        if (all_tiles && !wait_stage()) {   // (no named barrier follows on this path)
-          bad = 1;
-          break;
-        }
-      }
-
-
       // O^T tile q holds dims 128q .. 128q+127 in its lanes and the 64 heads in
       // its columns: this thread handles dim d of every head; for each head the
-      // warp's 32 lanes touch 32 consecutive dims. A balanced piece's partial is
-      // kept in this same order (O^T, [512 dims][64 heads]), so the piece that
-      // merges it reads each thread's 64 values as 16-byte loads.
-      const float* coef = reinterpret_cast<const float*>(smem + kOffPlo);
+      // warp's 32 lanes touch 32 consecutive dims.
 #pragma unroll 1
       for (int q = jb.q0; q < jb.q0 + jb.nq; ++q) {
         const int dl = 32 * sp + lane;   // dim within the tile
         const int d = 128 * q + dl;
-        float v[64];
         if (a.sched == 0) {   // (one job per CTA) tile q of O^T is complete
           if (!bad) bounded(bar(B_OT0 + q), 0, W_SM_PV_EPI);
           tc_fence_after();
         }
-        if (!merge) {
+        float v[64];
+        {
           uint32_t o[64];
           tmem_ld_32x32b_x64(tmem + lane_base + 64 * q, o);
           tmem_wait_ld_x64(o);
@@ -1066,46 +933,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[c + 2] = __uint_as_float(o[c + 2]) * fv.z;
             v[c + 3] = __uint_as_float(o[c + 3]) * fv.w;
           }
-        } else {
-          // sum over the pieces, in token order, of w_q / den * O_q; the own
-          // piece enters as O * (1/l), re-read from TMEM at its turn
-          // (a failed wait only marks this warp bad: every warp still reaches the
-          // named barrier at the end of the tile)
-          if (staged && !all_tiles && !wait_stage()) bad = 1;
-          int oi = 0;   // index of the piece among the other pieces
-#pragma unroll
-          for (int c = 0; c < 64; ++c) v[c] = 0.f;
-#pragma unroll 1
-          for (int pq = 0; pq < npieces; ++pq) {
-            const float* cf = coef + pq * 64;
-            if (pa + pq == static_cast<int>(blockIdx.x)) {
-              uint32_t ow[64];
-              tmem_ld_32x32b_x64(tmem + lane_base + 64 * q, ow);
-              tmem_wait_ld_x64(ow);
-#pragma unroll
-              for (int c = 0; c < 64; ++c) v[c] = fmaf(cf[c], __uint_as_float(ow[c]) * hs[c], v[c]);
-            } else {
-              float4 t4[16];
-              if (staged) {
-                const float4* sl = reinterpret_cast<const float4*>(smem + (all_tiles ? q : oi) * 32768) + dl;
-#pragma unroll
-                for (int k = 0; k < 16; ++k) t4[k] = sl[k * 128];
-              } else {
-                const float4* src = reinterpret_cast<const float4*>(
-                    a.o_acc + static_cast<size_t>(bal_slot(pa + pq, jb.t, nb, U, P)) * kMlaHeads * kMlaDv) + q * 2048 + dl;
-#pragma unroll
-                for (int k = 0; k < 16; ++k) t4[k] = __ldcg(src + k * 128);
-              }
-              ++oi;
-#pragma unroll
-              for (int k = 0; k < 16; ++k) {
-                v[4 * k] = fmaf(cf[4 * k], t4[k].x, v[4 * k]);
-                v[4 * k + 1] = fmaf(cf[4 * k + 1], t4[k].y, v[4 * k + 1]);
-                v[4 * k + 2] = fmaf(cf[4 * k + 2], t4[k].z, v[4 * k + 2]);
-                v[4 * k + 3] = fmaf(cf[4 * k + 3], t4[k].w, v[4 * k + 3]);
-              }
-            }
-          }
         }
         if (q == jb.q0 + jb.nq - 1) {
           // this warp's last read of O^T: the next job's first PV may overwrite it
@@ -1113,17 +940,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(B_OFREE));
         }
-        if (staged && !all_tiles) {
-          named_bar_sync(1, 128);   // the slots are read: the next tile's copies may land
-          if (tid == 0 && q < 3) issue_stage(q + 1, 1);
-        }
-        if (to_final) {
+        if (jb.kind == J_FINAL) {
           amax_l = fmaxf(amax_l, store_final(a, jb.t, d - lane, lane, v));
-        } else if (jb.kind == J_PIECE) {
-          // [tile][k][dim in tile][4 heads]: a warp writes 512 contiguous bytes
-          float4* st = reinterpret_cast<float4*>(a.o_acc + jb.out_row * kMlaDv) + q * 2048 + dl;
-#pragma unroll
-          for (int k = 0; k < 16; ++k) st[k * 128] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
         } else {
           float* st = a.o_acc + jb.out_row * kMlaDv + d;
 #pragma unroll
@@ -1131,27 +949,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (bad) break;
-      if (jb.kind == J_PIECE && !merge) {
-        if (j + 1 < njobs) {
-          // published during the next step, once the stores have drained
-          pending = jb.slot + 1;
-        } else {
-          // publish this piece: every thread's stores, then the ready flag
-          __threadfence();
-          named_bar_sync(1, 128);
-          if (tid == 0) st_release_gpu(a.ready + jb.slot, 1u);
-        }
-      }
     }
     if (a.amax != nullptr && !bad) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) amax_l = fmaxf(amax_l, __shfl_xor_sync(0xffffffffu, amax_l, o));
       if (lane == 0 && amax_l > 0.f) atomicMax(reinterpret_cast<int*>(a.amax), __float_as_int(amax_l));
     }
-    // no bulk copy of a merge may still be landing in shared memory when the CTA
-    // exits (one is in flight at most; it has landed unless the CTA is aborting)
-    if (tid == 0 && nmrg_issued > 0 && !wait_drain(bar(B_MRG), (nmrg_issued - 1) & 1, a.drain_limit_ns))
-      atomicCAS(&a.status[1], 0u, W_DRAIN_MRG);
   }
 
   // ---- teardown: every role reaches this point, TMEM is freed by its owner --

@@ -238,14 +238,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(bar(B_QFULL), kQBytes);
       tma_load_3d(sbase + kOffQ, &tm_q, 0, g * group, q0, bar(B_QFULL));
       int last[kStages] = {-1, -1, -1};
-      bool ok = true;
 #pragma unroll 1
       for (int t = 0; t < nt; ++t) {
         const int st = t % kStages;
-        if (t >= kStages && !wait_bounded(bar(B_SEMPTY0 + st), ((t / kStages) - 1) & 1, wc, W_PROD)) {
-          ok = false;
-          break;
-        }
+        if (t >= kStages && !wait_bounded(bar(B_SEMPTY0 + st), ((t / kStages) - 1) & 1, wc, W_PROD)) break;
         const uint32_t dst = sbase + kOffStage + st * kStageBytes;
         mbar_arrive_expect_tx(bar(B_SFULL_STAGE0 + st), kStageBytes);
         const int key = k0 + (tile0 + t) * kTile;
@@ -256,7 +252,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Nothing this thread started may still be writing shared memory when the
       // CTA exits: wait for the last load of every stage and for Q (all landed
       // already, unless the CTA is aborting).
-      (void)ok;
       for (int st = 0; st < kStages; ++st)
         if (last[st] >= 0 && !wait_drain(bar(B_SFULL_STAGE0 + st), (last[st] / kStages) & 1, a.drain_limit_ns))
           atomicCAS(&a.status[1], 0u, W_DRAIN_TMA2);

@@ -66,6 +66,27 @@ def test_workspace_matches_page(S, s_q):
     assert p.workspace_bytes >= p.lse_acc_offset + p.lse_acc_bytes and p.workspace_bytes % 256 == 0
 
 
+def balanced_slots(s_q_max, nb, sms):
+    """The most pieces one token is cut into by the balanced schedule over every s_q up
+    to s_q_max where it applies (the blocks of all tokens cut into P near-equal ranges,
+    the first U mod P one block longer), restated from the header."""
+    most = 1
+    for s in range(1, s_q_max + 1):
+        U = s * nb
+        per = -(-U // sms)
+        if per < 2:
+            continue
+        if per > nb:
+            return max(most, 2)
+        P = -(-U // per)
+        base, rem = divmod(U, P)
+        big = rem * (base + 1)
+        cta = lambda u: u // (base + 1) if u < big else rem + (u - big) // base
+        for t in range(s):
+            most = max(most, cta((t + 1) * nb - 1) - cta(t * nb) + 1)
+    return most
+
+
 def test_plan_is_deterministic_and_follows_rule():
     for sms in [148, 152, 160, 188]:
         for s_q in [1, 2, 4, 6, 8, 16, 32, 96, 384]:
@@ -83,22 +104,21 @@ def test_plan_is_deterministic_and_follows_rule():
                 assert eff(S) == best
                 assert all(eff(c) > best for c in range(1, S))
                 # uniform workspace (0 for one split), and with the automatic
-                # choice also the balanced schedule's partial slots, counters and flags
+                # choice also the balanced schedule's partial slots
                 ru = lambda x: -(-x // 256) * 256
                 uni = 0 if S == 1 else ru(ru(S * s_q * 64 * 512 * 4) + S * s_q * 64 * 4)
                 per = -(-(s_q * nblk) // sms)
                 mk_uniform = -(-(s_q * S) // sms) * -(-nblk // S)
-                applies = per >= 2 and -(-nblk // per) + 1 <= 32
+                applies = per >= 2
                 enabled = applies and per + 5 < mk_uniform
                 C = min(sms, s_q * nblk) if enabled else 0
-                # partials [2C][64][512] then LSEs [2C][64]; counters [s_q] and
-                # flags [2C] at the very end, past both schedules' partials
-                partials = ru(ru(2 * C * 64 * 512 * 4) + 2 * C * 64 * 4)
-                flags = ru((s_q + 2 * C) * 4)
+                # one partial slot per piece of the most cut token, split layout
+                slots = balanced_slots(s_q, nblk, sms)
+                partials = ru(ru(slots * s_q * 64 * 512 * 4) + slots * s_q * 64 * 4)
                 assert p1.balanced_ctas == C
                 # CTAs per (token, split) job: 4, 2 or 1, whatever still fits the SMs
                 assert p1.dim_groups == next(d for d in (4, 2, 1) if s_q * S * d <= sms or d == 1)
-                assert p1.workspace_bytes == (max(uni, partials) + flags if enabled else uni)
+                assert p1.workspace_bytes == (max(uni, partials) if enabled else uni)
                 pf = b.mla_decode_plan(s_q, topk, num_sms=sms, force_splits=S)
                 assert pf.balanced_ctas == 0 and (pf.workspace_bytes == 0) == (S == 1)
                 pb = b.mla_decode_plan(s_q, topk, num_sms=sms, force_splits=b.MLA_FORCE_BALANCED)

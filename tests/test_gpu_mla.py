@@ -407,8 +407,8 @@ def test_balanced_schedule_matches_oracle(s_q, topk, num_sms, with_sink):
 
 @pytest.mark.parametrize("out_dtype", ["bf16", "e4m3"])
 def test_balanced_schedule_casts_and_amax(out_dtype):
-    """Whole tokens and merged cut tokens are cast by the kernel; the amax is the
-    max over both."""
+    """Whole tokens are cast by the decode kernel and cut tokens by the combine;
+    the amax is the max over both."""
     inp = wl.mla_inputs(5, 32768, 640, seed=41, v_mean=1.0, with_sink=True)
     O, L = oracle_mla(inp)
     r = run_mla(inp, b.MLA_FORCE_BALANCED, out_dtype=out_dtype, inv_scale=64.0, with_amax=True,
@@ -420,7 +420,7 @@ def test_balanced_schedule_casts_and_amax(out_dtype):
 
 def test_balanced_schedule_padding_and_empty_pieces():
     """Padded and out-of-range indices; a piece whose rows are all masked is an
-    empty partial (LSE = -inf) and drops out of the merge; a token with no valid
+    empty partial (LSE = -inf) and drops out of the combine; a token with no valid
     row at all is O = 0, LSE = -inf."""
     inp = wl.mla_inputs(4, 32768, 640, seed=43)
     idx = inp.idx.clone()
@@ -436,17 +436,15 @@ def test_balanced_schedule_padding_and_empty_pieces():
 
 
 def test_balanced_schedule_repeated_calls():
-    """Two calls in a row on one workspace, initialised once: each call leaves the
-    per-token counters and ready flags at the end of the workspace at zero again,
-    so the second call gives the same, correct result."""
+    """Two calls in a row on one workspace that starts out filled with garbage (no
+    clearing): every partial slot a call reads was written by the same call, so both
+    calls give the same, correct result."""
     inp = wl.mla_inputs(3, 32768, 640, seed=47, with_sink=True)
     O, L = oracle_mla(inp)
     dev = torch.device("cuda")
     plan = b.mla_decode_plan(3, 640, num_sms=4, force_splits=b.MLA_FORCE_BALANCED)
     assert plan.balanced_ctas > 0
     ws = torch.full((plan.workspace_bytes,), 0xA5, dtype=torch.uint8, device=dev)
-    b.mla_workspace_init(plan, ws)
-    flag_bytes = -(-((3 + 2 * plan.balanced_ctas) * 4) // 256) * 256
     outs = []
     for _ in range(2):
         out = torch.empty(3, 64, 512, dtype=torch.float32, device=dev)
@@ -455,7 +453,6 @@ def test_balanced_schedule_repeated_calls():
                             inp.sink.to(dev), "f32", 1.0, out, lse, None, ws)
         torch.cuda.synchronize()
         check_status()
-        assert int(ws[plan.workspace_bytes - flag_bytes:].count_nonzero()) == 0
         outs.append((out.cpu(), lse.cpu()))
     for out, lse in outs:
         assert_o_close(out.numpy(), O)

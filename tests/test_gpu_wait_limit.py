@@ -1,16 +1,15 @@
 """The decode kernels' bounded waits, made to run out on the real kernels.
 
 Every pipeline wait of the sparse-MLA decode kernel (uniform schedule with the
-direct epilogue or split partials, and the balanced schedule with its in-kernel
-merge) and of the dense FP8 kernel gives up after a time limit, records
+direct epilogue or split partials, and the balanced schedule whose cut tokens
+leave partials for the combine) and of the dense FP8 kernel gives up after a time limit, records
 MLA_STATUS_TIMEOUT and the site of the wait in the status word, and aborts its
 CTA: the other roles stop at their next wait, the CTA waits for its own copies
 and MMAs in flight, frees its tensor memory and exits. mla_set_wait_limit_ns
 shortens that limit to 200 ns here, far below the latency of any row or tile
 load, so real waits run out (no flag is withheld and nothing faults). The
-test then checks the status, restores the limit, clears a balanced workspace
-again, and requires the next ordinary call on the same context to match the
-oracle.
+test then checks the status, restores the limit, and requires the next
+ordinary call on the same context to match the oracle.
 """
 import numpy as np
 import pytest
@@ -64,8 +63,6 @@ def test_mla_waits_run_out_then_the_next_call_is_correct(kind, S, num_sms):
     _mla_call(inp, plan, wsp, dev)
     _expect_timeout()
     b.mla_set_wait_limit_ns(0)
-    if plan.workspace_bytes:
-        b.mla_workspace_init(plan, ws)     # a timed-out balanced call may leave counters set
     out, lse = _mla_call(inp, plan, wsp, dev)
     torch.cuda.synchronize()
     check_status()

@@ -28,7 +28,7 @@ def _regular(inp, S, dev):
     plan = b.mla_decode_plan(inp.s_q, inp.topk, force_splits=S)
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev) if plan.workspace_bytes else None
     if ws is not None:
-        b.mla_workspace_init(plan, ws)    # the balanced schedule's counters start at zero
+        b.mla_workspace_init(plan, ws)
     out = torch.empty(inp.s_q, 64, 512, dtype=torch.float32, device=dev)
     lse = torch.empty(inp.s_q, 64, dtype=torch.float32, device=dev)
     b.mla_sparse_decode(plan, inp.s_q, inp.q.to(dev), inp.kv.to(dev), inp.n_kv, inp.idx.to(dev), inp.sm_scale,
