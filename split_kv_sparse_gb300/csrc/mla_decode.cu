@@ -506,29 +506,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                           kIdescQK);
         }
       };
-      // PV(g) for O^T tile j (dims 128 j .. 128 j + 127) with P_hi (part 0) or P_lo
-      // (part 1): K = the 64 rows in 4 steps of 16 (2048 B of the MN-major V^T, 32
-      // B of the K-major P^T each); `fresh` starts a new O^T (first step of a job).
-      auto pv_tile = [&](int g, int part, int j, bool fresh) {
-        const uint32_t av = w_v0 + (g & 1) * kHalfStep + j * ((2 * kSlotBytes) >> 4);
-        const uint32_t bp = part ? w_plo : w_phi0 + (g & 1) * kHalfStep;
-        const uint32_t d = tmem + 64 * j;
-        if (fresh && part == 0) mma_f16_wc<0>(d, av, bp, w_hi, kIdescPV);
-        else mma_f16_wc<1>(d, av, bp, w_hi, kIdescPV);
+      // This CTA's O^T tiles: tq0 .. tq0 + nq - 1 (all four unless the job's dims
+      // are spread over several CTAs).
+      const int tq0 = j0.q0;
+      const uint32_t v_q0 = w_v0 + static_cast<uint32_t>(tq0) * ((2 * kSlotBytes) >> 4);
+      const uint32_t d_q0 = tmem + 64u * static_cast<uint32_t>(tq0);
+      // PV(g) for the CTA's tile J (dims 128 (tq0 + J) .. + 127) with P_hi (part 0)
+      // or P_lo (part 1): K = the 64 rows in 4 steps of 16 (2048 B of the MN-major
+      // V^T, 32 B of the K-major P^T each). acc0 = 0 starts a new O^T (first step
+      // of a job): it is the first MMA's accumulate predicate, not a branch.
+      // Every run of MMAs is straight-line code (J is a constant once the callers'
+      // loops are unrolled; conditional commits are predicated instructions): a
+      // branch between two MMAs measured about as costly as another MMA.
+      auto pv_tile = [&](int g, auto part, int J, uint32_t acc0) {
+        constexpr int kPart = decltype(part)::value;
+        const uint32_t av = v_q0 + (g & 1) * kHalfStep + J * ((2 * kSlotBytes) >> 4);
+        const uint32_t bp = kPart ? w_plo : w_phi0 + (g & 1) * kHalfStep;
+        const uint32_t d = d_q0 + 64 * J;
+        mma_f16_w(d, av, bp, w_hi, kIdescPV, kPart ? 1u : acc0);
         mma_f16_wc<1>(d, av + (2048 >> 4), bp + 2, w_hi, kIdescPV);
         mma_f16_wc<1>(d, av + (4096 >> 4), bp + 4, w_hi, kIdescPV);
         mma_f16_wc<1>(d, av + (6144 >> 4), bp + 6, w_hi, kIdescPV);
       };
-      // tiles j0 .. j1-1 of one part (the 4 tiles unrolled, each skipped unless in range)
-      auto pv_tiles = [&](int g, int part, int j0, int j1, bool fresh) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (j >= j0 && j < j1) pv_tile(g, part, j, fresh);
-      };
-      // This CTA's O^T tiles: tq0 .. tq1-1 (all four unless the job's dims are
-      // spread over several CTAs); those below tqa read chunk group A.
-      const int tq0 = j0.q0, tq1 = j0.q0 + j0.nq;
-      const int tqa = min(max(tq0, kGroupSplit / 2), tq1);
+      constexpr std::integral_constant<int, 0> kHi{};
+      constexpr std::integral_constant<int, 1> kLo{};
       bool ok = true;
       auto wait = [&](uint32_t b, uint32_t ph, uint32_t site) {
         if (ok && !wait_bounded(b, ph, wc, site)) ok = false;
@@ -554,42 +555,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (last_of_job) mma_commit(bar(B_QFREE));   // the job's QKs are all issued
         return true;
       };
-      // PV(g) with the release of its chunk groups: tile-major (P_hi and P_lo of a
-      // tile together, so group A frees after the first two tiles) when P_lo is
-      // published already, else all P_hi tiles first (P_lo's buffer is still being
-      // read by PV(g - 1) when PV(g) is issued right behind it).
-      // On the job's last step each O^T tile's completion is signalled on its own
-      // barrier (B_OT0 + j), so the epilogue reads a tile while the MMAs of the
-      // next ones still run.
-      auto issue_pv = [&](int g, bool first, bool tile_major, bool last) {
+      // PV(g) over the CTA's kNq tiles with the release of its chunk groups:
+      // tile-major (P_hi and P_lo of a tile together, so group A frees after the
+      // first two tiles) when P_lo is published already, else all P_hi tiles
+      // first (P_lo's buffer is still being read by PV(g - 1) when PV(g) is
+      // issued right behind it). Group A (chunks 0-3) is read by tiles 0 and 1
+      // only: it is released after the last of those the CTA computes, or before
+      // the run when it computes neither. On the job's last step each O^T tile's
+      // completion is signalled on its own barrier (B_OT0 + tile), so the
+      // epilogue reads a tile while the MMAs of the next ones still run.
+      auto issue_pv = [&](int g, bool first, auto tile_major, auto nq, bool last) {
+        constexpr bool kTileMajor = decltype(tile_major)::value;
+        constexpr int kNq = decltype(nq)::value;
+        constexpr int kAAfter = kNq == 4 ? 1 : kNq - 1;
         const int h = g & 1;
+        const uint32_t acc0 = first ? 0u : 1u, lastu = last ? 1u : 0u;
+        const uint32_t a_lead = tq0 >= 2 ? 1u : 0u;
         if (!wait(bar(B_PHI0 + h), (g >> 1) & 1, W_MMA_STALL)) return false;
-        if (tile_major && !wait(bar(B_PLO0 + h), (g >> 1) & 1, W_MMA_STALL)) return false;
+        if (kTileMajor && !wait(bar(B_PLO0 + h), (g >> 1) & 1, W_MMA_STALL)) return false;
         tc_fence_after();
-        if (tile_major) {
+        mma_commit_if(bar(B_EMPTYA0 + h), a_lead);
+        if constexpr (kTileMajor) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (j >= tq0 && j < tq1) {
-              pv_tile(g, 0, j, first);
-              pv_tile(g, 1, j, first);
-              if (last) mma_commit(bar(B_OT0 + j));
-              if (j + 1 == tqa) mma_commit(bar(B_EMPTYA0 + h));   // after the last tile that reads group A
-            }
+          for (int J = 0; J < kNq; ++J) {
+            pv_tile(g, kHi, J, acc0);
+            pv_tile(g, kLo, J, acc0);
+            mma_commit_if(bar(B_OT0 + tq0 + J), lastu);
+            if (J == kAAfter) mma_commit_if(bar(B_EMPTYA0 + h), a_lead ^ 1u);
           }
-          if (tqa == tq0) mma_commit(bar(B_EMPTYA0 + h));          // no tile of this CTA reads group A
         } else {
-          pv_tiles(g, 0, tq0, tq1, first);
+#pragma unroll
+          for (int J = 0; J < kNq; ++J) pv_tile(g, kHi, J, acc0);
           if (!wait(bar(B_PLO0 + h), (g >> 1) & 1, W_MMA_STALL)) return false;
           tc_fence_after();
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (j >= tq0 && j < tq1) {
-              pv_tile(g, 1, j, false);
-              if (last) mma_commit(bar(B_OT0 + j));
-              if (j + 1 == tqa) mma_commit(bar(B_EMPTYA0 + h));
-            }
+          for (int J = 0; J < kNq; ++J) {
+            pv_tile(g, kLo, J, 1u);
+            mma_commit_if(bar(B_OT0 + tq0 + J), lastu);
+            if (J == kAAfter) mma_commit_if(bar(B_EMPTYA0 + h), a_lead ^ 1u);
           }
-          if (tqa == tq0) mma_commit(bar(B_EMPTYA0 + h));
         }
         mma_commit(bar(B_EMPTYB0 + h));   // the half is free for the rows of step g + 2
         mma_commit(bar(B_PVDONE));
@@ -605,12 +609,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // softmax of g, PV(g) that of g+1; the chunk groups of step g's half are
         // refilled with the rows of g+2 while PV(g+1) and QK(g+2) run.
         const int n = j0.nsteps;
-        for (int g = 0; g < n && ok; g += 2) {
-          if (!issue_qk(g, g == 0, 0, g == n - 1)) break;
-          if (g + 1 < n && !issue_qk(g + 1, false, 0, g + 1 == n - 1)) break;
-          if (!issue_pv(g, g == 0, true, g == n - 1)) break;
-          if (g + 1 < n && !issue_pv(g + 1, false, false, g + 1 == n - 1)) break;
-        }
+        auto run = [&](auto nq) {
+          for (int g = 0; g < n && ok; g += 2) {
+            if (!issue_qk(g, g == 0, 0, g == n - 1)) break;
+            if (g + 1 < n && !issue_qk(g + 1, false, 0, g + 1 == n - 1)) break;
+            if (!issue_pv(g, g == 0, std::true_type{}, nq, g == n - 1)) break;
+            if (g + 1 < n && !issue_pv(g + 1, false, std::false_type{}, nq, g + 1 == n - 1)) break;
+          }
+        };
+        if (j0.nq == 4) run(std::integral_constant<int, 4>{});
+        else if (j0.nq == 2) run(std::integral_constant<int, 2>{});
+        else run(std::integral_constant<int, 1>{});
       } else {
         int total = 0;
 #pragma unroll 1
@@ -638,7 +647,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool progress = false;
           if (c_lo && ready(bar(B_PLO0 + (npl & 1)), (npl >> 1) & 1)) {
             tc_fence_after();
-            pv_tiles(npl, 1, tq0, tq1, false);
+#pragma unroll
+            for (int J = 0; J < 4; ++J) pv_tile(npl, kLo, J, 1u);
             mma_commit(bar(B_EMPTYA0 + (npl & 1)));
             mma_commit(bar(B_EMPTYB0 + (npl & 1)));
             mma_commit(bar(B_PVDONE));
@@ -647,7 +657,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else if (c_hi && ready(bar(B_PHI0 + (nph & 1)), (nph >> 1) & 1) &&
                      (hk > 0 || hj == 0 || ready(bar(B_OFREE), (hj - 1) & 1))) {
             tc_fence_after();
-            pv_tiles(nph, 0, tq0, tq1, hk == 0);
+            const uint32_t acc0 = hk == 0 ? 0u : 1u;
+#pragma unroll
+            for (int J = 0; J < 4; ++J) pv_tile(nph, kHi, J, acc0);
             ++nph;
             if (++hk == hn) {
               hk = 0;

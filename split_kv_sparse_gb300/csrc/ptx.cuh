@@ -322,6 +322,19 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
+// The same, issued only when `cond` is non-zero: a predicated instruction, not a
+// branch, so a run of MMAs around it stays one straight stream.
+__device__ __forceinline__ void mma_commit_if(uint32_t bar, uint32_t cond) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred p;\n"
+      "  setp.ne.b32 p, %1, 0;\n"
+      "  @p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
+      "}\n" ::"r"(bar),
+      "r"(cond)
+      : "memory");
+}
+
 #include "tmem_ldst.inc"
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand.
