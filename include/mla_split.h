@@ -145,13 +145,13 @@ typedef struct {
  * the combine (measured on GB300, topk 640: s_q = 10 takes 5 splits x 2 dim
  * groups, 21.6 us, where 10 splits x 1 took 25.3 us).
  * dim_groups is the largest of 4, 2, 1 with s_q_max * S * dim_groups <= num_sms.
- * With force_splits == 0 the plan also enables the balanced schedule for the
- * one-shot call when it is expected to beat that grid at s_q_max: with per =
- * ceil(s_q_max * num_blocks / num_sms), when 2 <= per and per + 5 <
- * ceil(s_q_max * S / num_sms) * ceil(num_blocks / S) (the most blocks any SM walks
- * under the grid; 5 blocks stands for the schedule's cost of job boundaries and of
- * combining the pieces). force_splits == MLA_FORCE_BALANCED keeps the automatic S
- * and enables the balanced schedule whenever 2 <= per. Enabling it sets
+ * The balanced schedule is never chosen automatically: measured on GB300 (topk
+ * 640, back-to-back calls) the uniform grid beat it at every s_q from 96 to 384,
+ * also where the grid leaves a wave half empty (s_q = 200: 61.8 us against 87.9
+ * us), because the fp32 partials of the cut tokens, their combine and each CTA's
+ * job boundaries cost more than the blocks it saves. force_splits ==
+ * MLA_FORCE_BALANCED keeps the automatic S and enables the balanced schedule
+ * whenever 2 <= per = ceil(s_q_max * num_blocks / num_sms); enabling it sets
  * balanced_ctas = min(num_sms, s_q_max * num_blocks) and sizes the workspace for
  * both schedules: the larger of the two partial areas. With force_splits > 0 the
  * one-shot call runs the (token, split) jobs.

@@ -136,14 +136,6 @@ int balanced_slots(int s_q_max, int nb, int num_sms) {
   }
   return most;
 }
-// Blocks the busiest SM walks under the uniform (token, split) grid.
-int64_t uniform_makespan(int64_t s_q, int nb, int S, int num_sms) {
-  return (s_q * S + num_sms - 1) / num_sms * ((nb + S - 1) / S);
-}
-// What the balanced schedule costs beyond its blocks, in 64-row block times: a
-// CTA's job boundary (the next token's Q, and its first PV waiting for the
-// previous job's epilogue) and the combine of the cut tokens' pieces.
-constexpr int64_t kBalancedOverheadBlocks = 5;
 // The most splits the dense planner's per-sequence rule gives one sequence.
 constexpr int kDenseMaxAdaptiveSplits = 16;
 // CTAs per (token, split) job: the largest of 4, 2, 1 that still fits `jobs`
@@ -280,8 +272,12 @@ int mla_decode_plan(int s_q_max, int h_q, int d_qk, int d_v, int topk, int num_s
     out->workspace_bytes = round_up(out->lse_acc_offset + out->lse_acc_bytes, 256);
   }
   const int64_t per = balanced_per(s_q_max, nblk, num_sms);
-  if (force_splits == 0 && per > 0 &&
-      (want_balanced || per + kBalancedOverheadBlocks < uniform_makespan(s_q_max, nblk, S, num_sms))) {
+  // The balanced schedule only on request: measured on GB300 (topk 640, back-to-back
+  // calls), the uniform grid beat it at every s_q from 96 to 384, even where the
+  // grid leaves a wave half empty (s_q = 200: 61.8 us against 87.9 us), since the
+  // fp32 partials of the cut tokens, their combine and each CTA's job boundaries
+  // cost more than the blocks it saves.
+  if (want_balanced && per > 0) {
     // the one-shot call spreads all tokens' blocks over at most num_sms CTAs; its
     // workspace holds a partial slot per piece of the most cut token
     const int64_t units = static_cast<int64_t>(s_q_max) * nblk;
@@ -355,6 +351,7 @@ int mla_combine_impl(const mla_plan_t* plan, int s_q, const void* workspace, con
   c.inv_scale = out_inv_scale;
   c.lse_out = lse_out;
   c.amax = amax_out;
+  c.num_sms = dev->num_sms;
   return cuda_status(skv::launch_combine(c, zero_amax, /*pdl=*/true, static_cast<cudaStream_t>(stream)));
 }
 
@@ -428,6 +425,7 @@ int mla_decode_balanced(const mla_plan_t* plan, int s_q, const void* q, const vo
   c.inv_scale = out_inv_scale;
   c.lse_out = lse_out;
   c.amax = amax_out;
+  c.num_sms = dev->num_sms;
   c.bal_nb = nb;
   c.bal_units = static_cast<int>(U);
   c.bal_ctas = P;
@@ -706,6 +704,7 @@ int sdpa_combine_impl(const sdpa_plan_t* plan, int total_q, const void* workspac
   c.inv_scale = out_inv_scale;
   c.lse_out = lse_out;
   c.amax = amax_out;
+  c.num_sms = dev->num_sms;
   return cuda_status(skv::launch_combine(c, zero_amax, /*pdl=*/true, static_cast<cudaStream_t>(stream)));
 }
 

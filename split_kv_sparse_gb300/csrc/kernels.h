@@ -62,10 +62,6 @@ __host__ __device__ inline int bal_cta_of(int u, int U, int P) {
   const int big = rem * (base + 1);
   return u < big ? u / (base + 1) : rem + (u - big) / base;
 }
-// Partial slot of token t in CTA p: 2p for the CTA's first job, 2p + 1 for its last.
-__host__ __device__ inline int bal_slot(int p, int t, int nb, int U, int P) {
-  return 2 * p + (t == bal_begin(p, U, P) / nb ? 0 : 1);
-}
 
 // Dynamic shared memory the MLA decode kernel needs.
 int mla_decode_smem_bytes();
@@ -96,6 +92,7 @@ struct CombineArgs {
   // blocks of all tokens, bal_units of them, cut into bal_ctas ranges); a token in
   // one range was finished by the decode kernel and is left alone.
   int bal_nb, bal_units, bal_ctas;
+  int num_sms;          // SMs of the device (caps the grid; 0: one CTA per 8 items)
 };
 // zero_amax: clear *amax first (a memset on the stream); pdl: launch as a
 // programmatic dependent of the preceding kernel on the stream.

@@ -22,10 +22,14 @@
 //             piece of a token cut by range boundaries is a partial in the split
 //             layout, slot = the piece's place among its token's pieces, and the
 //             combine folds them by the log-sum-exp rule ("The Split-K Dispatch",
-//             "The LSE Combine Strategy").
+//             "The LSE Combine Strategy"). Only on request: measured slower
+//             than the uniform grid at every s_q tried (the planner's notes).
+// The kernel is compiled once per schedule, so the uniform one carries none of
+// the job switching.
 //
 // Layout of the work (256 threads, 64 gathered rows per step; the steps of all
-// of a CTA's jobs form one pipeline over a ring of two 64-row halves):
+// of a CTA's jobs form one sequence, one pipeline over a ring of two 64-row
+// halves; the row gathers and the MMA issue run on across job boundaries):
 //   warps 0-1  row gathers: warp w copies rows 32w..32w+31 of the step; lane i
 //              takes 16-byte piece i mod 8 of every 64-dim chunk of rows
 //              32w + 4m + i/8 (m = 0..7), so one warp instruction copies four
@@ -51,7 +55,11 @@
 //              with the other warps, through a per-step barrier that is arrived
 //              on early and waited on late. P_hi is published before P_lo, whose
 //              one buffer must first be released by the previous PV. At the end
-//              of each job: the epilogue, straight from TMEM to global memory.
+//              of each job: the epilogue, straight from TMEM to global memory;
+//              for a job followed by another (balanced schedule) it runs after
+//              the next job's first softmax step, while that step's PV writes
+//              its O^T tiles 0 and 1 to a second place (tile_col) and waits for
+//              the epilogue to have read tiles 2 and 3.
 //
 // Precision: p = 2^(x - m_ref) is stored as P_hi = p truncated to bf16 and
 // P_lo = bf16(p - P_hi); the PV product uses both, so P enters O with ~2^-15
@@ -89,8 +97,8 @@ constexpr int kOffBars = kOffPlo + kHalfBytes;      // 229376
 constexpr int kOffMisc = kOffBars + 256;            // [0] tmem base, [1] abort flag,
                                                     // [4..11] rescale masks [2][4], [12..15] failure flags
 constexpr int kOffAlpha = kOffMisc + 128;           // float[2][64] rescale factors by step parity
-constexpr int kOffHead = kOffAlpha + 512;           // float[2][64] per-head epilogue scalars
-constexpr int kSmemBytes = kOffHead + 512;          // 230784
+constexpr int kOffHead = kOffAlpha + 512;           // float[2][2][64] per-head epilogue scalars by job parity
+constexpr int kSmemBytes = kOffHead + 1024;         // 231296
 
 // The ring half of each step is filled and released in two chunk groups: A =
 // column chunks 0-3 (the V dims of O^T tiles 0 and 1) and B = chunks 4-8 (tiles
@@ -99,14 +107,15 @@ constexpr int kSmemBytes = kOffHead + 512;          // 230784
 // step g + 2 start landing while PV(g) still runs.
 enum {
   B_QFULL = 0, B_FULLA0, B_FULLA1, B_FULLB0, B_FULLB1, B_EMPTYA0, B_EMPTYA1, B_EMPTYB0, B_EMPTYB1,
-  B_SFULL0, B_SFULL1, B_PHI0, B_PHI1, B_PLO0, B_PLO1, B_PVDONE, B_DRAIN, B_XCH0, B_XCH1, B_OFREE,
-  B_QFREE, B_OT0, B_OT1, B_OT2, B_OT3, kNumBars
+  B_SFULL0, B_SFULL1, B_PHI0, B_PHI1, B_PLO0, B_PLO1, B_PVDONE, B_DRAIN, B_XCH0, B_XCH1, B_OFREE2,
+  B_OFREE3, B_QFREE, B_OT0, B_OT1, B_OT2, B_OT3, kNumBars
 };
 constexpr int kGroupSplit = 4;                      // chunks [0, 4) form group A, [4, 9) group B
 static_assert(kNumBars * 8 <= 256, "barrier area");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 256;                    // S buffers at columns 256 and 320
+constexpr uint32_t kTmemAlt = 384;                  // tiles 0 and 1 of O^T for odd jobs: columns 384..511
 constexpr float kRescaleThreshold = 8.0f;           // p = 2^(x - m_ref) <= 256 between rescales
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -146,16 +155,18 @@ struct Job {
   size_t out_row;
 };
 
+template <int kSched>
 __device__ __forceinline__ int num_jobs(const MlaArgs& a) {
-  if (a.sched == 0) return 1;
+  if (kSched == 0) return 1;
   const int U = a.s_q * a.num_blocks, P = a.num_ctas, p = blockIdx.x;
   const int u0 = bal_begin(p, U, P), u1 = bal_begin(p + 1, U, P);
   return (u1 - 1) / a.num_blocks - u0 / a.num_blocks + 1;
 }
 
+template <int kSched>
 __device__ __forceinline__ Job job_at(const MlaArgs& a, int j) {
   Job r;
-  if (a.sched == 0) {
+  if (kSched == 0) {
     const int S = a.num_splits, D = a.dim_groups;
     const int job = static_cast<int>(blockIdx.x) / D, dg = static_cast<int>(blockIdx.x) - job * D;
     const int t = job / S, s = job - t * S;
@@ -188,6 +199,45 @@ __device__ __forceinline__ Job job_at(const MlaArgs& a, int j) {
                                   : (static_cast<size_t>(r.slot) * a.s_q + t) * kMlaHeads;
   }
   return r;
+}
+
+// The steps of a CTA, in order over all of its jobs: step g gathers top-k
+// entries [r0, r1) of token t and belongs to job `job` (the CTA's job index),
+// of which it may be the first and/or the last step.
+struct Step {
+  int t, r0, r1, job;
+  bool first, last;
+};
+
+template <int kSched>
+__device__ __forceinline__ Step step_at(const MlaArgs& a, const Job& j0, int u0, int total, int g) {
+  Step s;
+  if (kSched == 0) {
+    s.t = j0.t;
+    s.r0 = j0.row0 + kMlaBlockRows * g;
+    s.r1 = min(s.r0 + kMlaBlockRows, j0.row1);
+    s.job = 0;
+    s.first = g == 0;
+    s.last = g == total - 1;
+  } else {
+    const int nb = a.num_blocks, u = u0 + g;
+    s.t = u / nb;
+    const int b = u - s.t * nb;
+    s.r0 = b * kMlaBlockRows;
+    s.r1 = min(s.r0 + kMlaBlockRows, a.topk);
+    s.job = s.t - u0 / nb;
+    s.first = g == 0 || b == 0;
+    s.last = g == total - 1 || b == nb - 1;
+  }
+  return s;
+}
+
+// TMEM column of O^T tile q for the CTA's job jj: tiles 0 and 1 alternate
+// between columns 0..127 and 384..511 by job parity, so a job's first PV can
+// write them while the epilogue of the job before still reads that job's
+// tiles (which it takes in the order 2, 3, 0, 1).
+__device__ __forceinline__ uint32_t tile_col(int q, int jj) {
+  return 64u * static_cast<uint32_t>(q) + ((q < 2 && (jj & 1)) ? kTmemAlt : 0u);
 }
 
 // 4x4 transpose of 32-bit words across the four lanes whose lane bits `b` and
@@ -281,6 +331,9 @@ __device__ __forceinline__ float store_final(const MlaArgs& a, int t, int d0, in
   return m;
 }
 
+// kSched: 0 = uniform (one job per CTA), 1 = balanced (a run of jobs per CTA);
+// one instance per schedule keeps the uniform one free of the job switching.
+template <int kSched>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const MlaArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -288,9 +341,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- jobs: the same decode in every role ---------------------------------
-  const int njobs = num_jobs(a);
-  const Job j0 = job_at(a, 0);
+  // ---- jobs and steps: the same decode in every role -----------------------
+  const int njobs = num_jobs<kSched>(a);
+  const Job j0 = job_at<kSched>(a, 0);
+  int u0 = 0, total = j0.nsteps;   // the CTA's first 64-row block (balanced) and its step count
+  if (kSched != 0) {
+    const int U = a.s_q * a.num_blocks;
+    u0 = bal_begin(blockIdx.x, U, a.num_ctas);
+    total = bal_begin(blockIdx.x + 1, U, a.num_ctas) - u0;
+  }
 
   if (j0.nsteps == 0) {
     // A split with no block of its own (uniform schedule only): O = 0 over this
@@ -318,13 +377,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile uint32_t* xch = reinterpret_cast<volatile uint32_t*>(misc + 4);   // [2][4] rescale masks
   volatile int* fin = reinterpret_cast<volatile int*>(misc + 12);             // [4] per-warp failure flags
   float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
-  float* hs = reinterpret_cast<float*>(smem + kOffHead);                       // [2][64] per-head scalars
+  float* hs = reinterpret_cast<float*>(smem + kOffHead);   // [job parity][2][64] per-head scalars
   const WaitCtx wc{a.wait_limit_ns, a.status, abort_flag};
 
   // The first row indices: fetched before the set-up barrier so the global
   // memory latency overlaps TMEM allocation and barrier initialisation. A
-  // loader lane takes rows 32w + lane/2 and 32w + 16 + lane/2 of step 0; a
-  // softmax lane takes rows lane and lane + 32.
+  // loader lane takes row 32w + lane of step 0; a softmax lane takes rows lane
+  // and lane + 32.
   int pre0 = -1, pre1 = -1;
   {
     const int32_t* idx0 = a.idx + static_cast<size_t>(j0.t) * a.topk;
@@ -355,7 +414,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_DRAIN), 1);
     mbar_init(bar(B_XCH0), 4);
     mbar_init(bar(B_XCH1), 4);
-    mbar_init(bar(B_OFREE), 4);            // the epilogue's last TMEM read of O^T, per softmax warp
+    mbar_init(bar(B_OFREE2), 4);           // a job's O^T tile 2 read by the epilogue, per softmax warp
+    mbar_init(bar(B_OFREE3), 4);           // and its tile 3
     mbar_init(bar(B_QFREE), 1);            // a job's last QK has completed: its Q buffer is free
     for (int i = 0; i < 4; ++i) mbar_init(bar(B_OT0 + i), 1);   // O^T tile i of a job is complete
     *abort_flag = 0;
@@ -369,80 +429,75 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  // A programmatic dependent (the combine of the uniform schedule) may begin
-  // launching now; it waits for this whole grid before it reads any partial.
+  // A programmatic dependent (the combine) may begin launching now; it waits
+  // for this whole grid before it reads any partial.
   grid_launch_dependents();
 
   if (warp < 2) {
     // ====================================================== row gathers ===
     const int pc = lane & 7;                       // this lane's 16-byte piece of a chunk
     const int ro = lane >> 3;                      // and its row within each group of 4
-    int g = 0;
-    bool stop = false;
-    int ixl = pre0;                                // index of row 32w + lane of the step
-#pragma unroll 1
-    for (int j = 0; j < njobs && !stop; ++j) {
-      const Job jb = (j == 0) ? j0 : job_at(a, j);
-      const int32_t* idx_t = a.idx + static_cast<size_t>(jb.t) * a.topk;
-      auto fetch = [&](int k) -> int {
-        const int r = jb.row0 + kMlaBlockRows * k + 32 * warp + lane;
-        return r < jb.row1 ? __ldg(idx_t + r) : -1;
-      };
-      if (j > 0) ixl = fetch(0);
-      // Rows two steps ahead are requested into L2 as soon as their index is
-      // known: with two ring halves a step's rows are copied only once the step
-      // two before has finished with its half, so without this their DRAM
-      // latency would sit on the loop's critical chain. One prefetch per
-      // 128-byte line from the load/store path (a bulk prefetch per row goes
-      // through the copy engine, which takes the requests one at a time).
-      int n1 = fetch(1), n2 = fetch(2);            // indices of steps k+1 and k+2
-      auto prefetch_row = [&](int ix) {
-        if (ix >= 0 && ix < a.n_kv) {
-          const uint8_t* r = a.kv + static_cast<size_t>(ix) * kRowBytes;
+    // index of row 32w + lane of step g (any job of the CTA), -1 past the rows
+    auto fetch = [&](int g) -> int {
+      if (g >= total) return -1;
+      const Step s = step_at<kSched>(a, j0, u0, total, g);
+      const int r = s.r0 + 32 * warp + lane;
+      return r < s.r1 ? __ldg(a.idx + static_cast<size_t>(s.t) * a.topk + r) : -1;
+    };
+    // Rows two steps ahead are requested into L2 as soon as their index is
+    // known: with two ring halves a step's rows are copied only once the step
+    // two before has finished with its half, so without this their DRAM
+    // latency would sit on the loop's critical chain. One prefetch per
+    // 128-byte line from the load/store path (a bulk prefetch per row goes
+    // through the copy engine, which takes the requests one at a time). The
+    // steps run on across the CTA's jobs, so the next job's rows are requested
+    // while the current one ends.
+    auto prefetch_row = [&](int ix) {
+      if (ix >= 0 && ix < a.n_kv) {
+        const uint8_t* r = a.kv + static_cast<size_t>(ix) * kRowBytes;
 #pragma unroll
-          for (int c = 0; c < kChunks; ++c) prefetch_l2_line(r + 128 * c);
-        }
-      };
-      // one chunk group of the step's 64 rows: wait until the MMAs of step g - 2
-      // are done with it, copy, and arrive on its FULL barrier when the copies land
-      auto copy_group = [&](auto grp, int g, int h) -> bool {
-        constexpr int G = decltype(grp)::value;
-        if (g >= 2) {
-          int ok = 1;
-          if (lane == 0) ok = wait_bounded(bar((G == 0 ? B_EMPTYA0 : B_EMPTYB0) + h), ((g >> 1) - 1) & 1, wc,
-                                           W_PROD_EMPTY);
-          if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
-        }
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const int rl = 4 * m + ro;                   // row within the warp's 32
-          const int row = 32 * warp + rl;
-          const int ix = __shfl_sync(0xffffffffu, ixl, rl);
-          const bool valid = ix >= 0 && ix < a.n_kv;
-          const uint8_t* src = a.kv + static_cast<size_t>(valid ? ix : 0) * kRowBytes + pc * 16;
-          const uint32_t dst = sbase + kOffRing + h * kHalfBytes + static_cast<uint32_t>(sw128(row, pc));
-          if constexpr (G == 0) copy_row_chunks<0, kGroupSplit>(dst, src, valid ? 16u : 0u);
-          else copy_row_chunks<kGroupSplit, kChunks>(dst, src, valid ? 16u : 0u);
-        }
-        cp_async_arrive_noinc(bar((G == 0 ? B_FULLA0 : B_FULLB0) + h));
-        return true;
-      };
-#pragma unroll 1
-      for (int k = 0; k < jb.nsteps; ++k, ++g) {
-        const int h = g & 1;
-        if (!copy_group(std::integral_constant<int, 0>{}, g, h) ||
-            !copy_group(std::integral_constant<int, 1>{}, g, h)) {
-          stop = true;
-          break;
-        }
-        // (Deferring the first prefetches until the first two steps' copies are on
-        // their way measured slower, at s_q = 1 and 96 alike.)
-        if (k == 0) prefetch_row(n1);
-        prefetch_row(n2);
-        ixl = n1;
-        n1 = n2;
-        n2 = fetch(k + 3);                         // arrives while this step is computed
+        for (int c = 0; c < kChunks; ++c) prefetch_l2_line(r + 128 * c);
       }
+    };
+    int ixl = pre0;                                // index of row 32w + lane of the step
+    int n1 = fetch(1), n2 = fetch(2);              // indices of steps g+1 and g+2
+    // one chunk group of the step's 64 rows: wait until the MMAs of step g - 2
+    // are done with it, copy, and arrive on its FULL barrier when the copies land
+    auto copy_group = [&](auto grp, int g, int h) -> bool {
+      constexpr int G = decltype(grp)::value;
+      if (g >= 2) {
+        int ok = 1;
+        if (lane == 0) ok = wait_bounded(bar((G == 0 ? B_EMPTYA0 : B_EMPTYB0) + h), ((g >> 1) - 1) & 1, wc,
+                                         W_PROD_EMPTY);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+      }
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int rl = 4 * m + ro;                   // row within the warp's 32
+        const int row = 32 * warp + rl;
+        const int ix = __shfl_sync(0xffffffffu, ixl, rl);
+        const bool valid = ix >= 0 && ix < a.n_kv;
+        const uint8_t* src = a.kv + static_cast<size_t>(valid ? ix : 0) * kRowBytes + pc * 16;
+        const uint32_t dst = sbase + kOffRing + h * kHalfBytes + static_cast<uint32_t>(sw128(row, pc));
+        if constexpr (G == 0) copy_row_chunks<0, kGroupSplit>(dst, src, valid ? 16u : 0u);
+        else copy_row_chunks<kGroupSplit, kChunks>(dst, src, valid ? 16u : 0u);
+      }
+      cp_async_arrive_noinc(bar((G == 0 ? B_FULLA0 : B_FULLB0) + h));
+      return true;
+    };
+#pragma unroll 1
+    for (int g = 0; g < total; ++g) {
+      const int h = g & 1;
+      if (!copy_group(std::integral_constant<int, 0>{}, g, h) ||
+          !copy_group(std::integral_constant<int, 1>{}, g, h))
+        break;
+      // (Deferring the first prefetches until the first two steps' copies are on
+      // their way measured slower, at s_q = 1 and 96 alike.)
+      if (g == 0) prefetch_row(n1);
+      prefetch_row(n2);
+      ixl = n1;
+      n1 = n2;
+      n2 = fetch(g + 3);                           // arrives while this step is computed
     }
     cp_async_wait_all();   // nothing of this thread is still landing when the CTA exits
   } else if (warp == 2) {
@@ -452,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
 #pragma unroll 1
       for (int j = 0; j < njobs; ++j) {
-        const Job jb = (j == 0) ? j0 : job_at(a, j);
+        const Job jb = (j == 0) ? j0 : job_at<kSched>(a, j);
         // the buffer is free once the previous job's last QK has completed; that
         // barrier has one phase per job, waited in order
         if (j > 0 && !wait_bounded(bar(B_QFREE), (j - 1) & 1, wc, W_PROD_Q)) break;
@@ -461,6 +516,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kChunks; ++c)
           tma_load_2d(sbase + kOffQ + c * kQChunkBytes, &tm_q, 64 * c, kMlaHeads * jb.t, bar(B_QFULL));
         ++issued;
+        // the next job's Q is requested into L2 now, so its load (once this job's
+        // QKs are done) does not wait for DRAM
+        if (j + 1 < njobs) {
+          const int tn = job_at<kSched>(a, j + 1).t;
+#pragma unroll 1
+          for (int c = 0; c < kChunks; ++c) tma_prefetch_2d(&tm_q, 64 * c, kMlaHeads * tn);
+        }
       }
       // Nothing this thread started may still be writing shared memory when the
       // CTA exits: wait for the last Q load (each load is issued only after the
@@ -515,14 +577,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // or P_lo (part 1): K = the 64 rows in 4 steps of 16 (2048 B of the MN-major
       // V^T, 32 B of the K-major P^T each). acc0 = 0 starts a new O^T (first step
       // of a job): it is the first MMA's accumulate predicate, not a branch.
+      // `par` moves tiles 0 and 1 of an odd job to their second place (tile_col).
       // Every run of MMAs is straight-line code (J is a constant once the callers'
       // loops are unrolled; conditional commits are predicated instructions): a
       // branch between two MMAs measured about as costly as another MMA.
-      auto pv_tile = [&](int g, auto part, int J, uint32_t acc0) {
+      auto pv_tile = [&](int g, auto part, int J, uint32_t acc0, uint32_t par) {
         constexpr int kPart = decltype(part)::value;
         const uint32_t av = v_q0 + (g & 1) * kHalfStep + J * ((2 * kSlotBytes) >> 4);
         const uint32_t bp = kPart ? w_plo : w_phi0 + (g & 1) * kHalfStep;
-        const uint32_t d = d_q0 + 64 * J;
+        const uint32_t d = d_q0 + 64 * J + (J < 2 ? par : 0u);
         mma_f16_w(d, av, bp, w_hi, kIdescPV, kPart ? 1u : acc0);
         mma_f16_wc<1>(d, av + (2048 >> 4), bp + 2, w_hi, kIdescPV);
         mma_f16_wc<1>(d, av + (4096 >> 4), bp + 4, w_hi, kIdescPV);
@@ -541,18 +604,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_after();
       };
-      // QK(g) in its two chunk groups, each after its rows have landed
-      auto issue_qk = [&](int g, bool first_of_job, int qphase, bool last_of_job) {
+      // QK(g) in its two chunk groups, each after its rows have landed; the first
+      // step of a job also waits for the job's Q, the last one releases it.
+      auto issue_qk = [&](int g, const Step& st) {
         const int h = g & 1;
         if (!wait(bar(B_FULLA0 + h), (g >> 1) & 1, W_MMA_STALL)) return false;
-        if (first_of_job && !wait(bar(B_QFULL), qphase & 1, W_MMA_Q)) return false;
+        if (st.first && !wait(bar(B_QFULL), st.job & 1, W_MMA_Q)) return false;
         rows_visible();
         qk_chunks(g, std::integral_constant<int, 0>{}, std::integral_constant<int, kGroupSplit>{});
         if (!wait(bar(B_FULLB0 + h), (g >> 1) & 1, W_MMA_STALL)) return false;
         rows_visible();
         qk_chunks(g, std::integral_constant<int, kGroupSplit>{}, std::integral_constant<int, kChunks>{});
         mma_commit(bar(B_SFULL0 + h));
-        if (last_of_job) mma_commit(bar(B_QFREE));   // the job's QKs are all issued
+        if (st.last) mma_commit(bar(B_QFREE));   // the job's QKs are all issued
         return true;
       };
       // PV(g) over the CTA's kNq tiles with the release of its chunk groups:
@@ -563,14 +627,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       // only: it is released after the last of those the CTA computes, or before
       // the run when it computes neither. On the job's last step each O^T tile's
       // completion is signalled on its own barrier (B_OT0 + tile), so the
-      // epilogue reads a tile while the MMAs of the next ones still run.
-      auto issue_pv = [&](int g, bool first, auto tile_major, auto nq, bool last) {
+      // epilogue reads a tile while the MMAs of the next ones still run. The
+      // first step of a job after the first (kBoundary) writes tiles 2 and 3 only
+      // once the epilogue of the job before has read them.
+      auto issue_pv = [&](int g, const Step& st, auto tile_major, auto nq, auto boundary) {
         constexpr bool kTileMajor = decltype(tile_major)::value;
+        constexpr bool kBoundary = decltype(boundary)::value;
         constexpr int kNq = decltype(nq)::value;
         constexpr int kAAfter = kNq == 4 ? 1 : kNq - 1;
         const int h = g & 1;
-        const uint32_t acc0 = first ? 0u : 1u, lastu = last ? 1u : 0u;
+        const uint32_t acc0 = st.first ? 0u : 1u, lastu = st.last ? 1u : 0u;
+        const uint32_t par = (st.job & 1) ? kTmemAlt : 0u;
         const uint32_t a_lead = tq0 >= 2 ? 1u : 0u;
+        auto tile_free = [&](int J) {   // (kBoundary only) tile J of the previous job has been read
+          if (!wait(bar(J == 2 ? B_OFREE2 : B_OFREE3), (st.job - 1) & 1, W_MMA_STALL)) return false;
+          tc_fence_after();
+          return true;
+        };
         if (!wait(bar(B_PHI0 + h), (g >> 1) & 1, W_MMA_STALL)) return false;
         if (kTileMajor && !wait(bar(B_PLO0 + h), (g >> 1) & 1, W_MMA_STALL)) return false;
         tc_fence_after();
@@ -578,19 +651,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kTileMajor) {
 #pragma unroll
           for (int J = 0; J < kNq; ++J) {
-            pv_tile(g, kHi, J, acc0);
-            pv_tile(g, kLo, J, acc0);
+            if (kBoundary && J >= 2 && !tile_free(J)) return false;
+            pv_tile(g, kHi, J, acc0, par);
+            pv_tile(g, kLo, J, acc0, par);
             mma_commit_if(bar(B_OT0 + tq0 + J), lastu);
             if (J == kAAfter) mma_commit_if(bar(B_EMPTYA0 + h), a_lead ^ 1u);
           }
         } else {
 #pragma unroll
-          for (int J = 0; J < kNq; ++J) pv_tile(g, kHi, J, acc0);
+          for (int J = 0; J < kNq; ++J) {
+            if (kBoundary && J >= 2 && !tile_free(J)) return false;
+            pv_tile(g, kHi, J, acc0, par);
+          }
           if (!wait(bar(B_PLO0 + h), (g >> 1) & 1, W_MMA_STALL)) return false;
           tc_fence_after();
 #pragma unroll
           for (int J = 0; J < kNq; ++J) {
-            pv_tile(g, kLo, J, 1u);
+            pv_tile(g, kLo, J, 1u, par);
             mma_commit_if(bar(B_OT0 + tq0 + J), lastu);
             if (J == kAAfter) mma_commit_if(bar(B_EMPTYA0 + h), a_lead ^ 1u);
           }
@@ -599,103 +676,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(B_PVDONE));
         return true;
       };
-      if (a.sched == 0) {
-        // Uniform schedule, one job: a fixed order by pairs of steps,
-        //   QK(g) QK(g+1) PV(g) PV(g+1),
-        // each group issued after its own bounded waits. Every wait's producer was
-        // issued earlier in this order (the rows of g+1 come after PV(g-1) freed
-        // its half, P_lo(g) after PV(g-1) is done, S(g)'s buffer is free once
-        // PV(g-2) is issued), so the order cannot deadlock. QK(g+1) covers the
-        // softmax of g, PV(g) that of g+1; the chunk groups of step g's half are
-        // refilled with the rows of g+2 while PV(g+1) and QK(g+2) run.
-        const int n = j0.nsteps;
-        auto run = [&](auto nq) {
-          for (int g = 0; g < n && ok; g += 2) {
-            if (!issue_qk(g, g == 0, 0, g == n - 1)) break;
-            if (g + 1 < n && !issue_qk(g + 1, false, 0, g + 1 == n - 1)) break;
-            if (!issue_pv(g, g == 0, std::true_type{}, nq, g == n - 1)) break;
-            if (g + 1 < n && !issue_pv(g + 1, false, std::false_type{}, nq, g + 1 == n - 1)) break;
+      // A fixed order by pairs of steps over all of the CTA's jobs,
+      //   QK(g) QK(g+1) PV(g) PV(g+1),
+      // each group issued after its own bounded waits. Every wait's producer was
+      // issued earlier in this order (the rows of g+1 come after PV(g-1) freed
+      // its half, P_lo(g) after PV(g-1) is done, S(g)'s buffer is free once
+      // PV(g-2) is issued, a job's Q after the previous job's last QK, the
+      // previous job's O^T tiles are read once PV of its last step is done), so
+      // the order cannot deadlock. QK(g+1) covers the softmax of g, PV(g) that of
+      // g+1; the chunk groups of step g's half are refilled with the rows of g+2
+      // while PV(g+1) and QK(g+2) run.
+      auto run = [&](auto nq) {
+        constexpr int kNq = decltype(nq)::value;
+        auto pv = [&](int g, const Step& st, auto tm) {
+          if constexpr (kNq == 4 && kSched != 0) {
+            if (st.first && st.job > 0) return issue_pv(g, st, tm, nq, std::true_type{});
           }
+          return issue_pv(g, st, tm, nq, std::false_type{});
         };
-        if (j0.nq == 4) run(std::integral_constant<int, 4>{});
-        else if (j0.nq == 2) run(std::integral_constant<int, 2>{});
-        else run(std::integral_constant<int, 1>{});
-      } else {
-        int total = 0;
 #pragma unroll 1
-        for (int j = 0; j < njobs; ++j) total += (j == 0) ? j0.nsteps : job_at(a, j).nsteps;
-        // Issue order, highest priority first:
-        //   PV_lo(g)  once softmax(g) has written P_lo; its completion frees the
-        //             half for the loads of step g+2 (the loop's critical chain);
-        //   PV_hi(g)  once softmax(g) has written P_hi (the first step of a job
-        //             also waits for the previous job's epilogue to read O^T);
-        //   QK(g)     once its rows (and, first in a job, its Q)
-        //             have landed and its S buffer is free: softmax(g-2) published
-        //             P_hi, i.e. PV_hi(g-2) was issued.
-        // tcgen05 runs the MMAs in issue order. The thread polls the barriers
-        // without blocking (test_wait; measured a little faster here than
-        // letting try_wait suspend the thread).
-        int nqk = 0, nph = 0, npl = 0;
-        int qj = 0, qk = 0, qn = j0.nsteps;   // QK cursor: job, step within it, its steps
-        int hj = 0, hk = 0, hn = j0.nsteps;   // PV_hi cursor
-        uint64_t t_idle = 0;
-        while (ok && npl < total) {
-          const bool c_lo = npl < nph;
-          const bool c_hi = nph < nqk;
-          const bool c_qk = nqk < total && nqk <= nph + 1;
-          auto ready = [&](uint32_t b, uint32_t ph) { return mbar_test_wait(b, ph); };
-          bool progress = false;
-          if (c_lo && ready(bar(B_PLO0 + (npl & 1)), (npl >> 1) & 1)) {
-            tc_fence_after();
-#pragma unroll
-            for (int J = 0; J < 4; ++J) pv_tile(npl, kLo, J, 1u);
-            mma_commit(bar(B_EMPTYA0 + (npl & 1)));
-            mma_commit(bar(B_EMPTYB0 + (npl & 1)));
-            mma_commit(bar(B_PVDONE));
-            ++npl;
-            progress = true;
-          } else if (c_hi && ready(bar(B_PHI0 + (nph & 1)), (nph >> 1) & 1) &&
-                     (hk > 0 || hj == 0 || ready(bar(B_OFREE), (hj - 1) & 1))) {
-            tc_fence_after();
-            const uint32_t acc0 = hk == 0 ? 0u : 1u;
-#pragma unroll
-            for (int J = 0; J < 4; ++J) pv_tile(nph, kHi, J, acc0);
-            ++nph;
-            if (++hk == hn) {
-              hk = 0;
-              if (++hj < njobs) hn = job_at(a, hj).nsteps;
-            }
-            progress = true;
-          } else if (c_qk && ready(bar(B_FULLA0 + (nqk & 1)), (nqk >> 1) & 1) &&
-                     ready(bar(B_FULLB0 + (nqk & 1)), (nqk >> 1) & 1) &&
-                     (qk > 0 || ready(bar(B_QFULL), qj & 1))) {
-            rows_visible();
-            qk_chunks(nqk, std::integral_constant<int, 0>{}, std::integral_constant<int, kChunks>{});
-            mma_commit(bar(B_SFULL0 + (nqk & 1)));
-            ++nqk;
-            if (++qk == qn) {
-              mma_commit(bar(B_QFREE));   // the job's QKs are all issued
-              qk = 0;
-              if (++qj < njobs) qn = job_at(a, qj).nsteps;
-            }
-            progress = true;
-          }
-          if (progress) {
-            t_idle = 0;
-          } else {
-            const uint64_t now = globaltimer_ns();
-            if (*abort_flag) {
-              ok = false;
-            } else if (t_idle == 0) {
-              t_idle = now;
-            } else if (now - t_idle > a.wait_limit_ns) {
-              *abort_flag = 1;
-              atomicOr(&a.status[0], 1u);
-              atomicCAS(&a.status[1], 0u, W_MMA_STALL);
-              ok = false;
-            }
-          }
+        for (int g = 0; g < total && ok; g += 2) {
+          const bool two = g + 1 < total;
+          const Step s0 = step_at<kSched>(a, j0, u0, total, g);
+          const Step s1 = two ? step_at<kSched>(a, j0, u0, total, g + 1) : s0;
+          if (!issue_qk(g, s0)) break;
+          if (two && !issue_qk(g + 1, s1)) break;
+          if (!pv(g, s0, std::true_type{})) break;
+          if (two && !pv(g + 1, s1, std::false_type{})) break;
         }
+      };
+      if (kSched != 0 || j0.nq == 4) run(std::integral_constant<int, 4>{});   // (balanced: always 4)
+      else if constexpr (kSched == 0) {
+        if (j0.nq == 2) run(std::integral_constant<int, 2>{});
+        else run(std::integral_constant<int, 1>{});
       }
       if (!ok) {
         // no MMA may still be reading shared memory or writing TMEM when the CTA exits
@@ -711,7 +724,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rb = (lane >> 4) * 32;          // and its 32 rows rb..rb+31 of every step
     int bad = 0;               // a bounded wait of this warp ran out
     float amax_l = 0.f;        // max |O| over the final rows this thread wrote
-    int g = 0;                 // step index over all of this CTA's jobs
     auto bounded = [&](uint32_t b, uint32_t ph, uint32_t site) {
       int w = 1;
       if (lane == 0) w = wait_bounded(b, ph, wc, site);
@@ -720,248 +732,276 @@ __global__ void __launch_bounds__(kThreads, 1)
       return w != 0;
     };
 
-#pragma unroll 1
-    for (int j = 0; j < njobs && !bad; ++j) {
-      const Job jb = (j == 0) ? j0 : job_at(a, j);
-      const int32_t* idx_t = a.idx + static_cast<size_t>(jb.t) * a.topk;
-      float m_run = -INFINITY;   // reference max of the head (log2 units), shared by its two lanes
-      float lsum = 0.f;          // fp32 softmax denominator over this thread's rows
-      int ia = pre0, ib = pre1;  // indices of rows lane and lane + 32 of the step
-      if (j > 0) {
-        const int r = jb.row0 + lane;
-        ia = r < jb.row1 ? __ldg(idx_t + r) : -1;
-        ib = r + 32 < jb.row1 ? __ldg(idx_t + r + 32) : -1;
-      }
-
-#pragma unroll 1
-      for (int k = 0; k < jb.nsteps; ++k, ++g) {
-        const int h = g & 1;
-        // which of this thread's 32 rows hold a valid index
-        const uint32_t vlo = __ballot_sync(0xffffffffu, ia >= 0 && ia < a.n_kv);
-        const uint32_t vhi = __ballot_sync(0xffffffffu, ib >= 0 && ib < a.n_kv);
-        const uint32_t vm = rb ? vhi : vlo;
-        if (k + 1 < jb.nsteps) {   // the next step's indices, in flight during this step
-          const int rn = jb.row0 + kMlaBlockRows * (k + 1) + lane;
-          ia = rn < jb.row1 ? __ldg(idx_t + rn) : -1;
-          ib = rn + 32 < jb.row1 ? __ldg(idx_t + rn + 32) : -1;
-        }
-
-        const bool w = bounded(bar(B_SFULL0 + h), (g >> 1) & 1, W_SM_S);
-        tc_fence_after();
-        float x[32];
-        float mx = -INFINITY;
-        if (w) {
-          uint32_t raw[32];
-          tmem_ld_16x32bx2_x32_h32(tmem + lane_base + kTmemS + 64 * h, raw);
-          tmem_wait_ld_x32(raw);
-          if (vm == 0xffffffffu) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              x[i] = __uint_as_float(raw[i]) * a.scale_log2;
-              mx = fmaxf(mx, x[i]);
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              x[i] = ((vm >> i) & 1u) ? __uint_as_float(raw[i]) * a.scale_log2 : -INFINITY;
-              mx = fmaxf(mx, x[i]);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) x[i] = -INFINITY;
-        }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));   // over the step's 64 rows
-
-        // Lazy rescale: move the reference max only when a score exceeds it by
-        // more than the threshold (always on the first valid row of a head). Both
-        // lanes of the head see the same mx and take the same decision.
-        const bool need = mx > m_run + kRescaleThreshold;
-        if (need) {
-          const float al = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - mx);
-          lsum *= al;
-          m_run = mx;
-          if (lane < 16) alpha_s[h * 64 + head] = al;
-        }
-        const uint32_t rmask = __ballot_sync(0xffffffffu, need) & 0xffffu;
-        __syncwarp();
-        if (lane == 0) {
-          xch[h * 4 + sp] = rmask | (bad ? 0x10000u : 0u);
-          mbar_arrive(bar(B_XCH0 + h));      // release: the mask and the factors above
-        }
-
-        // p = 2^(x - m_ref); a masked row gives 0
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = (x[i] == -INFINITY) ? 0.f : ex2_approx(x[i] - m_run);
-        {
-          float ts[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) ts[i] = x[i] + x[i + 16];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) ts[i] += ts[i + 8];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) ts[i] += ts[i + 4];
-          lsum += (ts[0] + ts[2]) + (ts[1] + ts[3]);
-        }
-        // P_hi = p with its mantissa cut to bf16 (exact bit truncation, no
-        // conversion); P_lo = bf16(p - P_hi), two rows per packed conversion.
-        // |P_lo| < 2^-7 p, so P_hi + P_lo matches p to 2^-15.
-        uint32_t hi[16], lo[16];
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const uint32_t b0 = __float_as_uint(x[i]) & 0xFFFF0000u;
-          const uint32_t b1 = __float_as_uint(x[i + 1]) & 0xFFFF0000u;
-          const __nv_bfloat162 lo2 =
-              __floats2bfloat162_rn(x[i] - __uint_as_float(b0), x[i + 1] - __uint_as_float(b1));
-          hi[i / 2] = (b0 >> 16) | b1;
-          lo[i / 2] = *reinterpret_cast<const uint32_t*>(&lo2);
-        }
-
-        // The other warps' rescale masks for this step.
-        const bool wx = bounded(bar(B_XCH0 + h), (g >> 1) & 1, W_SM_X);
-        const uint32_t x0 = xch[h * 4 + 0], x1 = xch[h * 4 + 1], x2 = xch[h * 4 + 2], x3 = xch[h * 4 + 3];
-        if (((x0 | x1 | x2 | x3) & 0x10000u) || !wx) {
-          bad = 1;
-          break;   // every softmax warp sees the same masks and leaves together
-        }
-        const uint64_t resc = static_cast<uint64_t>(x0) | (static_cast<uint64_t>(x1) << 16) |
-                              (static_cast<uint64_t>(x2) << 32) | (static_cast<uint64_t>(x3) << 48);
-        // P^T as a K-major operand: N = heads, K = rows; the 64 rows of one head
-        // are one 128-byte line of the swizzled tile, this thread's 32 rows are
-        // its pieces rb/8 .. rb/8+3.
-        uint8_t* p_hi = smem + kOffRing + 8 * kSlotBytes + h * kHalfBytes;
-        uint8_t* p_lo = smem + kOffPlo;
-        auto store_p = [&](uint8_t* dst, const uint32_t (&v)[16]) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(dst + sw128(head, (rb >> 3) + q)) =
-                make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        };
-        auto publish = [&](int b) {   // generic-proxy stores -> the tensor core's reads
-          fence_proxy_async_smem();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(b));
-        };
-        if (resc == 0 || k == 0) {
-          // O^T needs no rescale before PV_hi(g) (or holds nothing of this job
-          // yet): publish P_hi now; P_lo's buffer is free once PV(g-1) is done.
-          store_p(p_hi, hi);
-          publish(B_PHI0 + h);
-          if (g >= 1) {
-            bounded(bar(B_PVDONE), (g - 1) & 1, W_SM_PV);
-            tc_fence_after();
-          }
-          store_p(p_lo, lo);
-          publish(B_PLO0 + h);
-        } else {
-          // O^T holds PV of this job's earlier steps: once PV(g-1) is done, scale
-          // the columns of the rescaled heads in the 32 dims (TMEM lanes) of each
-          // tile this warp can reach, then publish both halves of P.
-          bounded(bar(B_PVDONE), (g - 1) & 1, W_SM_PV);
-          tc_fence_after();
-          if (!bad) {
-#pragma unroll 1
-            for (int q = 2 * jb.q0; q < 2 * (jb.q0 + jb.nq); ++q) {   // own O^T tiles x 2 halves of 32 heads
-              const int c0 = 32 * (q & 1);
-              if (((resc >> c0) & 0xffffffffull) == 0) continue;
-              uint32_t o[32];
-              float al[32];
-#pragma unroll
-              for (int i = 0; i < 32; ++i) al[i] = ((resc >> (c0 + i)) & 1ull) ? alpha_s[h * 64 + c0 + i] : 1.f;
-              const uint32_t col = 64 * (q >> 1) + c0;
-              tmem_ld_32x32b_x32(tmem + lane_base + col, o);
-              tmem_wait_ld_x32(o);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * al[i]);
-              tmem_st_32x32b_x32(tmem + lane_base + col, o);
-            }
-            tmem_wait_st();
-          }
-          store_p(p_hi, hi);
-          store_p(p_lo, lo);
-          fence_proxy_async_smem();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(bar(B_PHI0 + h));
-            mbar_arrive(bar(B_PLO0 + h));
-          }
-        }
-      }
-
-      // ---- epilogue of job j ------------------------------------------------
-      // Every softmax warp reaches each named barrier below (a failed wait only
-      // ends the job loop after the exchange that follows it), so none can wait
-      // there forever. Per-head scalars hs[0..1][64]: 1/denominator and the job's
-      // own LSE.
+    // The end of job jj: the softmax denominator and the job's own LSE per head
+    // into hs[jj & 1] (1/denominator, LSE), and the LSE to global memory.
+    auto finalize = [&](const Job& J, int jj, float m_run, float lsum) {
       lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);
-      if (!bad && a.sched != 0) {
-        bounded(bar(B_PVDONE), (g - 1) & 1, W_SM_PV_EPI);   // O^T is complete
-        tc_fence_after();
-      }
       const float lse_own = lsum > 0.f ? m_run + log2f(lsum) : -INFINITY;
       if (lane < 16) {
         float den = lsum;
-        if (jb.kind == J_FINAL && a.sink != nullptr && lsum > 0.f) den += exp2f(a.sink[head] * kLog2e - m_run);
-        hs[head] = lsum > 0.f ? 1.f / den : 0.f;
-        hs[64 + head] = lse_own;
-        if (!bad && jb.q0 == 0) {   // (every CTA of a job has the same LSE)
-          if (jb.kind == J_FINAL) {
-            if (a.lse_out != nullptr) a.lse_out[jb.out_row + head] = lse_own;
+        if (J.kind == J_FINAL && a.sink != nullptr && lsum > 0.f) den += exp2f(a.sink[head] * kLog2e - m_run);
+        float* hj = hs + (jj & 1) * 128;
+        hj[head] = lsum > 0.f ? 1.f / den : 0.f;
+        hj[64 + head] = lse_own;
+        if (!bad && J.q0 == 0) {   // (every CTA of a job has the same LSE)
+          if (J.kind == J_FINAL) {
+            if (a.lse_out != nullptr) a.lse_out[J.out_row + head] = lse_own;
           } else {
-            a.lse_acc[jb.out_row + head] = lse_own;
+            a.lse_acc[J.out_row + head] = lse_own;
           }
         }
       }
-      if (lane == 0) fin[sp] = bad;
-      named_bar_sync(1, 128);
-      if (fin[0] | fin[1] | fin[2] | fin[3]) {
-        bad = 1;
-        break;   // every softmax warp leaves together
-      }
-      // O^T tile q holds dims 128q .. 128q+127 in its lanes and the 64 heads in
-      // its columns: this thread handles dim d of every head; for each head the
-      // warp's 32 lanes touch 32 consecutive dims.
+    };
+    // The epilogue of job J (the CTA's job jj), straight from TMEM to global
+    // memory. O^T tile q holds dims 128q .. 128q+127 in its lanes and the 64
+    // heads in its columns: this thread handles dim d of every head; for each
+    // head the warp's 32 lanes touch 32 consecutive dims. `deferred` (balanced
+    // schedule): the next job has started, and its first PV waits for tiles 2
+    // and 3 (taken first, each released right after its read); tiles 0 and 1 of
+    // the next job have their own place.
+    auto epilogue = [&](const Job& J, int jj, bool deferred) {
+      const float* hj = hs + (jj & 1) * 128;
 #pragma unroll 1
-      for (int q = jb.q0; q < jb.q0 + jb.nq; ++q) {
-        const int dl = 32 * sp + lane;   // dim within the tile
-        const int d = 128 * q + dl;
-        if (a.sched == 0) {   // (one job per CTA) tile q of O^T is complete
-          if (!bad) bounded(bar(B_OT0 + q), 0, W_SM_PV_EPI);
-          tc_fence_after();
-        }
+      for (int i = 0; i < J.nq; ++i) {
+        const int q = deferred ? ((i + 2) & 3) : J.q0 + i;
+        const int d = 128 * q + 32 * sp + lane;
+        // Deferred, tiles 0 and 1 are not waited for: the commits of tiles 2 and
+        // 3, waited first, track every earlier MMA of the job; and the next
+        // job's first PV, free to write its own tiles 0 and 1, may already have
+        // completed their barriers' next phase (a one-step job), which a wait
+        // on this job's phase would then take for the one after.
+        if (!bad && (!deferred || q >= 2)) bounded(bar(B_OT0 + q), jj & 1, W_SM_PV_EPI);
+        tc_fence_after();
         float v[64];
         {
           uint32_t o[64];
-          tmem_ld_32x32b_x64(tmem + lane_base + 64 * q, o);
+          tmem_ld_32x32b_x64(tmem + lane_base + tile_col(q, jj), o);
           tmem_wait_ld_x64(o);
           // the per-head factor read into registers before any store below
 #pragma unroll
           for (int c = 0; c < 64; c += 4) {
-            const float4 fv = *reinterpret_cast<const float4*>(hs + c);
+            const float4 fv = *reinterpret_cast<const float4*>(hj + c);
             v[c] = __uint_as_float(o[c]) * fv.x;
             v[c + 1] = __uint_as_float(o[c + 1]) * fv.y;
             v[c + 2] = __uint_as_float(o[c + 2]) * fv.z;
             v[c + 3] = __uint_as_float(o[c + 3]) * fv.w;
           }
         }
-        if (q == jb.q0 + jb.nq - 1) {
-          // this warp's last read of O^T: the next job's first PV may overwrite it
+        if (kSched != 0 && q >= 2) {
+          // this warp's read of the tile is done: the next job's first PV may write it
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_OFREE));
+          if (lane == 0) mbar_arrive(bar(q == 2 ? B_OFREE2 : B_OFREE3));
         }
-        if (jb.kind == J_FINAL) {
-          amax_l = fmaxf(amax_l, store_final(a, jb.t, d - lane, lane, v));
+        if (J.kind == J_FINAL) {
+          amax_l = fmaxf(amax_l, store_final(a, J.t, d - lane, lane, v));
         } else {
-          float* st = a.o_acc + jb.out_row * kMlaDv + d;
+          float* st = a.o_acc + J.out_row * kMlaDv + d;
 #pragma unroll
           for (int c = 0; c < 64; ++c) st[c * kMlaDv] = v[c];
         }
       }
-      if (bad) break;
+    };
+
+    Job jb = j0;               // the job of the current step
+    int job = 0;
+    Job jp = j0;               // a finished job whose epilogue is still to run
+    int pend = -1;
+    float m_run = -INFINITY;   // reference max of the head (log2 units), shared by its two lanes
+    float lsum = 0.f;          // fp32 softmax denominator over this thread's rows
+    int ia = pre0, ib = pre1;  // indices of rows lane and lane + 32 of the step
+    int g = 0;
+#pragma unroll 1
+    for (; g < total && !bad; ++g) {
+      const int h = g & 1;
+      const Step st = step_at<kSched>(a, j0, u0, total, g);
+      if (st.first && g > 0) {
+        job = st.job;
+        jb = job_at<kSched>(a, job);
+        m_run = -INFINITY;
+        lsum = 0.f;
+      }
+      // which of this thread's 32 rows hold a valid index
+      const uint32_t vlo = __ballot_sync(0xffffffffu, ia >= 0 && ia < a.n_kv);
+      const uint32_t vhi = __ballot_sync(0xffffffffu, ib >= 0 && ib < a.n_kv);
+      const uint32_t vm = rb ? vhi : vlo;
+      if (g + 1 < total) {   // the next step's indices, in flight during this step
+        const Step sn = step_at<kSched>(a, j0, u0, total, g + 1);
+        const int32_t* idx_n = a.idx + static_cast<size_t>(sn.t) * a.topk;
+        const int rn = sn.r0 + lane;
+        ia = rn < sn.r1 ? __ldg(idx_n + rn) : -1;
+        ib = rn + 32 < sn.r1 ? __ldg(idx_n + rn + 32) : -1;
+      }
+
+      const bool w = bounded(bar(B_SFULL0 + h), (g >> 1) & 1, W_SM_S);
+      tc_fence_after();
+      float x[32];
+      float mx = -INFINITY;
+      if (w) {
+        uint32_t raw[32];
+        tmem_ld_16x32bx2_x32_h32(tmem + lane_base + kTmemS + 64 * h, raw);
+        tmem_wait_ld_x32(raw);
+        if (vm == 0xffffffffu) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            x[i] = __uint_as_float(raw[i]) * a.scale_log2;
+            mx = fmaxf(mx, x[i]);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            x[i] = ((vm >> i) & 1u) ? __uint_as_float(raw[i]) * a.scale_log2 : -INFINITY;
+            mx = fmaxf(mx, x[i]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = -INFINITY;
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));   // over the step's 64 rows
+
+      // Lazy rescale: move the reference max only when a score exceeds it by
+      // more than the threshold (always on the first valid row of a head). Both
+      // lanes of the head see the same mx and take the same decision.
+      const bool need = mx > m_run + kRescaleThreshold;
+      if (need) {
+        const float al = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - mx);
+        lsum *= al;
+        m_run = mx;
+        if (lane < 16) alpha_s[h * 64 + head] = al;
+      }
+      const uint32_t rmask = __ballot_sync(0xffffffffu, need) & 0xffffu;
+      __syncwarp();
+      if (lane == 0) {
+        xch[h * 4 + sp] = rmask | (bad ? 0x10000u : 0u);
+        mbar_arrive(bar(B_XCH0 + h));      // release: the mask and the factors above
+      }
+
+      // p = 2^(x - m_ref); a masked row gives 0
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = (x[i] == -INFINITY) ? 0.f : ex2_approx(x[i] - m_run);
+      {
+        float ts[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ts[i] = x[i] + x[i + 16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ts[i] += ts[i + 8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ts[i] += ts[i + 4];
+        lsum += (ts[0] + ts[2]) + (ts[1] + ts[3]);
+      }
+      // P_hi = p with its mantissa cut to bf16 (exact bit truncation, no
+      // conversion); P_lo = bf16(p - P_hi), two rows per packed conversion.
+      // |P_lo| < 2^-7 p, so P_hi + P_lo matches p to 2^-15.
+      uint32_t hi[16], lo[16];
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        const uint32_t b0 = __float_as_uint(x[i]) & 0xFFFF0000u;
+        const uint32_t b1 = __float_as_uint(x[i + 1]) & 0xFFFF0000u;
+        const __nv_bfloat162 lo2 =
+            __floats2bfloat162_rn(x[i] - __uint_as_float(b0), x[i + 1] - __uint_as_float(b1));
+        hi[i / 2] = (b0 >> 16) | b1;
+        lo[i / 2] = *reinterpret_cast<const uint32_t*>(&lo2);
+      }
+
+      // The other warps' rescale masks for this step.
+      const bool wx = bounded(bar(B_XCH0 + h), (g >> 1) & 1, W_SM_X);
+      const uint32_t x0 = xch[h * 4 + 0], x1 = xch[h * 4 + 1], x2 = xch[h * 4 + 2], x3 = xch[h * 4 + 3];
+      if (((x0 | x1 | x2 | x3) & 0x10000u) || !wx) {
+        bad = 1;
+        break;   // every softmax warp sees the same masks and leaves together
+      }
+      const uint64_t resc = static_cast<uint64_t>(x0) | (static_cast<uint64_t>(x1) << 16) |
+                            (static_cast<uint64_t>(x2) << 32) | (static_cast<uint64_t>(x3) << 48);
+      // P^T as a K-major operand: N = heads, K = rows; the 64 rows of one head
+      // are one 128-byte line of the swizzled tile, this thread's 32 rows are
+      // its pieces rb/8 .. rb/8+3.
+      uint8_t* p_hi = smem + kOffRing + 8 * kSlotBytes + h * kHalfBytes;
+      uint8_t* p_lo = smem + kOffPlo;
+      auto store_p = [&](uint8_t* dst, const uint32_t (&v)[16]) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(dst + sw128(head, (rb >> 3) + q)) =
+              make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      };
+      auto publish = [&](int b) {   // generic-proxy stores -> the tensor core's reads
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(b));
+      };
+      if (resc == 0 || st.first) {
+        // O^T needs no rescale before PV_hi(g) (or holds nothing of this job
+        // yet): publish P_hi now; P_lo's buffer is free once PV(g-1) is done.
+        store_p(p_hi, hi);
+        publish(B_PHI0 + h);
+        if (g >= 1) {
+          bounded(bar(B_PVDONE), (g - 1) & 1, W_SM_PV);
+          tc_fence_after();
+        }
+        store_p(p_lo, lo);
+        publish(B_PLO0 + h);
+      } else {
+        // O^T holds PV of this job's earlier steps: once PV(g-1) is done, scale
+        // the columns of the rescaled heads in the 32 dims (TMEM lanes) of each
+        // tile this warp can reach, then publish both halves of P.
+        bounded(bar(B_PVDONE), (g - 1) & 1, W_SM_PV);
+        tc_fence_after();
+        if (!bad) {
+#pragma unroll 1
+          for (int q = 2 * jb.q0; q < 2 * (jb.q0 + jb.nq); ++q) {   // own O^T tiles x 2 halves of 32 heads
+            const int c0 = 32 * (q & 1);
+            if (((resc >> c0) & 0xffffffffull) == 0) continue;
+            uint32_t o[32];
+            float al[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) al[i] = ((resc >> (c0 + i)) & 1ull) ? alpha_s[h * 64 + c0 + i] : 1.f;
+            const uint32_t col = tile_col(q >> 1, job) + c0;
+            tmem_ld_32x32b_x32(tmem + lane_base + col, o);
+            tmem_wait_ld_x32(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * al[i]);
+            tmem_st_32x32b_x32(tmem + lane_base + col, o);
+          }
+          tmem_wait_st();
+        }
+        store_p(p_hi, hi);
+        store_p(p_lo, lo);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(B_PHI0 + h));
+          mbar_arrive(bar(B_PLO0 + h));
+        }
+      }
+
+      // The previous job's epilogue, now that this (its successor's first) step
+      // is published: the issuer computes this job's first PV meanwhile.
+      if (kSched != 0) {
+        if (pend >= 0) {
+          epilogue(jp, pend, true);
+          pend = -1;
+        }
+        if (st.last) {
+          finalize(jb, job, m_run, lsum);
+          if (g + 1 < total) {
+            jp = jb;
+            pend = job;
+          }
+        }
+      }
     }
+
+    if (kSched == 0 && !bad) finalize(jb, job, m_run, lsum);   // (the one job of the uniform schedule)
+    // ---- epilogue of the last job -------------------------------------------
+    // Every softmax warp reaches this named barrier (a failed wait only ends the
+    // step loop after the exchange that follows it), so none can wait there
+    // forever; it also makes every warp's per-head scalars visible.
+    if (lane == 0) fin[sp] = bad;
+    named_bar_sync(1, 128);
+    if (fin[0] | fin[1] | fin[2] | fin[3]) bad = 1;
+    if (!bad) epilogue(jb, job, false);
     if (a.amax != nullptr && !bad) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) amax_l = fmaxf(amax_l, __shfl_xor_sync(0xffffffffu, amax_l, o));
@@ -984,7 +1024,10 @@ int mla_decode_smem_bytes() { return kSmemBytes; }
 
 cudaError_t prepare_mla_kernels() {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  return cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  const cudaError_t e =
+      cudaFuncSetAttribute(mla_decode_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(mla_decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
 }
 
 cudaError_t launch_mla_decode(const CUtensorMap& tm_q, const MlaArgs& a, cudaStream_t stream) {
@@ -992,7 +1035,8 @@ cudaError_t launch_mla_decode(const CUtensorMap& tm_q, const MlaArgs& a, cudaStr
   const dim3 grid(a.sched == 0 ? static_cast<unsigned>(a.s_q) * static_cast<unsigned>(a.num_splits) *
                                      static_cast<unsigned>(a.dim_groups)
                                : static_cast<unsigned>(a.num_ctas));
-  mla_decode_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, a);
+  if (a.sched == 0) mla_decode_kernel<0><<<grid, kThreads, kSmemBytes, stream>>>(tm_q, a);
+  else mla_decode_kernel<1><<<grid, kThreads, kSmemBytes, stream>>>(tm_q, a);
   return cudaGetLastError();
 }
 
