@@ -38,6 +38,7 @@ H_Q, D_QK, D_V = 64, 576, 512
 INV_SCALE = 64.0
 SWEEP_SQ = (1, 6, 16, 96, 384)
 SWEEP_S = (1, 2, 4, 8, 16)
+BF16_PARTIALS_SQ, BF16_PARTIALS_S = 16, (8, 0)   # sweep points also run with bf16 partials
 FLUSH_BYTES = 256 << 20
 
 
@@ -47,17 +48,18 @@ def workload_name(s_q: int) -> str:
             f"Q bf16 ~N(0,1), sm_scale 1/sqrt(576), no sink, FP8 e4m3 output (inv_scale {INV_SCALE:g})")
 
 
-def algorithmic_bytes(s_q: int, S: int, part: str = "call") -> int:
+def algorithmic_bytes(s_q: int, S: int, part: str = "call", partial_bytes: int = 4) -> int:
     """Bytes the split method must move (gathered rows counted per token).
 
     per token: Q 64*576*2 + idx topk*4 + rows topk*1152 (+ FP8 output 64*512 + LSE 64*4 when
     the output is written); S > 1 adds the fp32 partial O + LSE, written by the split
     kernel and read by the combine: S*(64*512*4 + 64*4) each way.
     part: "call" (whole call), "split" (the split or direct kernel alone).
+    partial_bytes: 4 for fp32 O partials, 2 for bf16 ones (the LSE partials stay fp32).
     """
     per_tok_in = H_Q * D_QK * 2 + TOPK * 4 + TOPK * D_QK * 2
     out = H_Q * D_V * 1 + H_Q * 4
-    partial = S * (H_Q * D_V * 4 + H_Q * 4)
+    partial = S * (H_Q * D_V * partial_bytes + H_Q * 4)
     if S == 1:
         return s_q * (per_tok_in + out)
     if part == "split":
@@ -201,13 +203,15 @@ class Case:
     `layers` caches (views of one allocation) and per-layer queries / indices whose
     total exceeds L2 several times, back to back in one CUDA graph."""
 
-    def __init__(self, b, torch, kv_all, qs, idxs, sm_scale, S):
+    def __init__(self, b, torch, kv_all, qs, idxs, sm_scale, S, bf16_partials=False):
         self.b, self.torch = b, torch
         self.layers = len(qs)
         self.s_q = qs[0].shape[0]
         self.kv_all, self.qs, self.idxs, self.sm_scale = kv_all, qs, idxs, sm_scale
         dev = kv_all.device
         self.plan = b.mla_decode_plan(self.s_q, TOPK, force_splits=S) if S else b.mla_decode_plan(self.s_q, TOPK)
+        if bf16_partials:
+            b.mla_plan_set_partials_bf16(self.plan)
         self.S = self.plan.num_splits
         # the automatic plan's one-shot call runs the balanced schedule (one kernel)
         # when the planner enabled it and this s_q leaves >= 2 blocks per CTA
@@ -515,12 +519,27 @@ def run_gpu(args):
                 ks = c.time("kernel", steps, c.layers)
                 cb = point_bytes(s_q, c.S, c.balanced, c.plan.num_sms)
                 sweep.append({"s_q": s_q, "num_splits": {0: "planner", -1: "balanced"}.get(S, S),
-                              "planner": S == 0, "layers": c.layers, "steps": steps,
+                              "planner": S == 0, "partials": "fp32", "layers": c.layers, "steps": steps,
                               "schedule": c.schedule(), "us_per_call": round(us, 2),
                               "split_kernel_us": round(ks, 2), "alg_bytes": cb,
                               "gb_s": round(cb / (us * 1e-6) / 1e9, 1),
                               "frac_of_peak": round(cb / (us * 1e-6) / 1e9 / peak, 4)})
                 del c
+            if s_q == BF16_PARTIALS_SQ:
+                # the opt-in bf16 partials, where the partials outweigh the inputs
+                for S in BF16_PARTIALS_S:
+                    c = Case(b, torch, kv_all, qs, idxs, base.sm_scale, S, bf16_partials=True)
+                    steps = max(args.sweep_steps, c.layers)
+                    us = c.time("call", steps, c.layers)
+                    ks = c.time("kernel", steps, c.layers)
+                    cb = algorithmic_bytes(s_q, c.S, "call", partial_bytes=2)
+                    sweep.append({"s_q": s_q, "num_splits": S if S else "planner", "planner": S == 0,
+                                  "partials": "bf16", "layers": c.layers, "steps": steps,
+                                  "schedule": c.schedule(), "us_per_call": round(us, 2),
+                                  "split_kernel_us": round(ks, 2), "alg_bytes": cb,
+                                  "gb_s": round(cb / (us * 1e-6) / 1e9, 1),
+                                  "frac_of_peak": round(cb / (us * 1e-6) / 1e9 / peak, 4)})
+                    del c
             del qs, idxs
         torch.cuda.synchronize()
         # the dense FP8 GQA variant (same partial / LSE protocol), forced split

@@ -85,7 +85,8 @@ extern "C" {
 /* A plan: every size and offset the split and combine calls need, computed once
  * per s_q bucket on the host ("The Split-K Dispatch", "CUDA Graph Safety").
  * Workspace layout (one caller-owned device buffer, 256-byte aligned):
- *   [0, o_acc_bytes)                       fp32 O partials, split-major
+ *   [0, o_acc_bytes)                       fp32 (or bf16, see partial_bf16) O
+ *                                          partials, split-major
  *                                          [num_splits][s_q][h_q][d_v]
  *   [lse_acc_offset, + lse_acc_bytes)      fp32 log2 LSE partials
  *                                          [num_splits][s_q][h_q]
@@ -107,7 +108,10 @@ typedef struct {
                            job's scores and softmax and 512/dim_groups of its output
                            dims, so PV and the output stores of one job spread over
                            dim_groups SMs (used when s_q_max * num_splits leaves SMs idle) */
-  uint64_t o_acc_bytes;     /* num_splits * s_q_max * h_q * d_v * 4                */
+  int32_t partial_bf16; /* 0 (default): O partials in fp32; 1: in bf16 (set with
+                           mla_plan_set_partials_bf16; LSE partials stay fp32)     */
+  uint64_t o_acc_bytes;     /* num_splits * s_q_max * h_q * d_v * (4, or 2 with bf16
+                               partials)                                           */
   uint64_t lse_acc_offset;  /* o_acc_bytes rounded up to 256                       */
   uint64_t lse_acc_bytes;   /* num_splits * s_q_max * h_q * 4                      */
   uint64_t workspace_bytes; /* what every call on this plan needs; 0 when num_splits == 1
@@ -143,7 +147,12 @@ typedef struct {
  * max(2, ceil(num_blocks / S)): a split of two 64-row blocks costs about what a
  * split of one does, and fewer splits leave SMs to dim groups and partials to
  * the combine (measured on GB300, topk 640: s_q = 10 takes 5 splits x 2 dim
- * groups, 21.6 us, where 10 splits x 1 took 25.3 us).
+ * groups, 21.6 us, where 10 splits x 1 took 25.3 us); except that, when that S
+ * is above 1, S = num_blocks (one block per split) when num_blocks is within
+ * that bound and s_q_max *
+ * num_blocks * 4 <= num_sms, i.e. every one-block split still gets 4 dim groups
+ * (measured on GB300, topk 640: s_q = 1, 2, 3 take 9.2, 9.4, 9.8 us with 10
+ * splits against 10.1, 10.2, 10.5 us with 5).
  * dim_groups is the largest of 4, 2, 1 with s_q_max * S * dim_groups <= num_sms.
  * The balanced schedule is never chosen automatically: measured on GB300 (topk
  * 640, back-to-back calls) the uniform grid beat it at every s_q from 96 to 384,
@@ -159,6 +168,22 @@ typedef struct {
  *         MLA_ERR_INVALID_ARG for s_q_max < 1, topk < 1, out == NULL, or bad split counts. */
 MLA_API int mla_decode_plan(int s_q_max, int h_q, int d_qk, int d_v, int topk,
                     int num_sms, int max_splits, int force_splits, mla_plan_t* out);
+
+/* Switches a plan's O partials to bf16 (enable = 1) or back to fp32 (enable = 0),
+ * and recomputes o_acc_bytes, lse_acc_offset, lse_acc_bytes and workspace_bytes
+ * for it; every later call on the plan (split pass, combine, one-shot call, also
+ * the balanced schedule) stores and reads the partials in that type. The pages
+ * name bf16 partials as the way to halve the partial traffic that regressed the
+ * 16-token lane ("The Split-K Dispatch", "Numerical Precision Tradeoffs";
+ * FlashMLA PR #25, "Measured"). fp32 stays the default because bf16 partials do
+ * not keep the identical-code floor of the FP8 output: every e4m3 code stays
+ * within one step of the oracle's and O within 2e-3 norm-wise per row, but with
+ * non-cancelling V (mean 1.0) fewer than 99 % of the codes equal the oracle's
+ * (98.8 % in the oracle's own simulation at s_q = 16, 2 splits). The LSE is
+ * unchanged (fp32 partials). Errors: MLA_ERR_INVALID_ARG for plan == NULL,
+ * enable not 0 or 1, or a plan not made by mla_decode_plan. This entry point has
+ * no counterpart in the pages. */
+MLA_API int mla_plan_set_partials_bf16(mla_plan_t* plan, int enable);
 
 /* Zeroes all plan->workspace_bytes of `workspace` on `stream`. No schedule needs
  * its workspace to start at zero (every partial slot a call reads was written by

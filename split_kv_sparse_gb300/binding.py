@@ -30,7 +30,7 @@ EXPORTS = [
     "mla_sparse_decode", "mla_sparse_decode_host", "sdpa_fp8_decode_plan", "sdpa_fp8_decode_split",
     "sdpa_split_combine", "sdpa_fp8_decode_direct", "sdpa_fp8_decode", "mla_get_status",
     "mla_selftest_wait_timeout", "mla_status_string", "mla_abi_version", "mla_sparse_decode_noalloc",
-    "mla_workspace_init", "mla_set_wait_limit_ns",
+    "mla_workspace_init", "mla_set_wait_limit_ns", "mla_plan_set_partials_bf16",
 ]
 
 
@@ -45,7 +45,7 @@ class MlaPlan(ctypes.Structure):
                 ("d_v", ctypes.c_int32), ("topk", ctypes.c_int32), ("block_rows", ctypes.c_int32),
                 ("num_blocks", ctypes.c_int32), ("num_splits", ctypes.c_int32), ("num_sms", ctypes.c_int32),
                 ("balanced_ctas", ctypes.c_int32), ("dim_groups", ctypes.c_int32),
-                ("o_acc_bytes", ctypes.c_uint64),
+                ("partial_bf16", ctypes.c_int32), ("o_acc_bytes", ctypes.c_uint64),
                 ("lse_acc_offset", ctypes.c_uint64), ("lse_acc_bytes", ctypes.c_uint64),
                 ("workspace_bytes", ctypes.c_uint64)]
 
@@ -88,6 +88,7 @@ _SIGS = {
     "mla_sparse_decode_noalloc": [_I, _I, _P, _P, _I64, _P, _F, _P, _I, _I, _F, _P, _P, _P, _P],
     "mla_workspace_init": [ctypes.POINTER(MlaPlan), _P, _P],
     "mla_set_wait_limit_ns": [_U64],
+    "mla_plan_set_partials_bf16": [ctypes.POINTER(MlaPlan), _I],
 }
 
 
@@ -143,6 +144,13 @@ def mla_decode_plan(s_q_max: int, topk: int, *, h_q: int = 64, d_qk: int = 576, 
     plan = MlaPlan()
     _check(lib().mla_decode_plan(s_q_max, h_q, d_qk, d_v, topk, num_sms, max_splits, force_splits,
                                  ctypes.byref(plan)), "mla_decode_plan")
+    return plan
+
+
+def mla_plan_set_partials_bf16(plan: MlaPlan, enable: bool = True) -> MlaPlan:
+    """Switches the plan's O partials to bf16 (or back to fp32) in place; returns the plan."""
+    _check(lib().mla_plan_set_partials_bf16(ctypes.byref(plan), enable if isinstance(enable, int) else int(enable)),
+           "mla_plan_set_partials_bf16")
     return plan
 
 

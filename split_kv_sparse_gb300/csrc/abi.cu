@@ -98,8 +98,8 @@ uint64_t round_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
 // Workspace of the (token, split) schedule: fp32 O partials [S][s_q][64][512],
 // then fp32 LSE partials [S][s_q][64] at the next 256-byte boundary.
-uint64_t split_workspace_bytes(int S, int s_q) {
-  const uint64_t o = static_cast<uint64_t>(S) * s_q * kMlaHeads * kMlaDv * 4ull;
+uint64_t split_workspace_bytes(int S, int s_q, int o_elem_bytes = 4) {
+  const uint64_t o = static_cast<uint64_t>(S) * s_q * kMlaHeads * kMlaDv * static_cast<uint64_t>(o_elem_bytes);
   return round_up(round_up(o, 256) + static_cast<uint64_t>(S) * s_q * kMlaHeads * 4ull, 256);
 }
 
@@ -144,6 +144,24 @@ int dim_groups_for(int64_t jobs, int num_sms) {
   for (int d = 4; d > 1; d /= 2)
     if (jobs * d <= num_sms) return d;
   return 1;
+}
+
+// The workspace of a plan from its split count, schedule and partial type: the
+// split layout ([S][s_q_max][64][512] O partials of 4 or 2 bytes, then
+// [S][s_q_max][64] fp32 LSE partials at the next 256-byte boundary), large
+// enough for the balanced schedule's slots when that schedule is enabled.
+void plan_workspace(mla_plan_t* p) {
+  const int esz = p->partial_bf16 ? 2 : 4;
+  p->o_acc_bytes = p->lse_acc_offset = p->lse_acc_bytes = p->workspace_bytes = 0;
+  if (p->num_splits > 1) {
+    p->o_acc_bytes = static_cast<uint64_t>(p->num_splits) * p->s_q_max * p->h_q * p->d_v * static_cast<uint64_t>(esz);
+    p->lse_acc_offset = round_up(p->o_acc_bytes, 256);
+    p->lse_acc_bytes = static_cast<uint64_t>(p->num_splits) * p->s_q_max * p->h_q * 4ull;
+    p->workspace_bytes = round_up(p->lse_acc_offset + p->lse_acc_bytes, 256);
+  }
+  if (p->balanced_ctas > 0)
+    p->workspace_bytes = std::max<uint64_t>(
+        p->workspace_bytes, split_workspace_bytes(balanced_slots(p->s_q_max, p->num_blocks, p->num_sms), p->s_q_max, esz));
 }
 
 int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
@@ -253,6 +271,10 @@ int mla_decode_plan(int s_q_max, int h_q, int d_qk, int d_v, int topk, int num_s
         S = c;
         break;
       }
+    // Except when every one-block split still gets 4 dim groups: then a split of
+    // one block is quicker than one of two (measured on GB300, topk 640, s_q = 1,
+    // 2, 3: 9.2, 9.4, 9.8 us with 10 splits against 10.1, 10.2, 10.5 with 5).
+    if (S > 1 && nblk <= smax && static_cast<int64_t>(s_q_max) * nblk * 4 <= num_sms) S = nblk;
   }
   if (static_cast<int64_t>(s_q_max) * S > 0x7FFFFFFFll) return MLA_ERR_INVALID_ARG;
   out->s_q_max = s_q_max;
@@ -265,12 +287,6 @@ int mla_decode_plan(int s_q_max, int h_q, int d_qk, int d_v, int topk, int num_s
   out->num_splits = S;
   out->num_sms = num_sms;
   out->dim_groups = dim_groups_for(static_cast<int64_t>(s_q_max) * S, num_sms);
-  if (S > 1) {
-    out->o_acc_bytes = static_cast<uint64_t>(S) * s_q_max * h_q * d_v * 4ull;
-    out->lse_acc_offset = round_up(out->o_acc_bytes, 256);
-    out->lse_acc_bytes = static_cast<uint64_t>(S) * s_q_max * h_q * 4ull;
-    out->workspace_bytes = round_up(out->lse_acc_offset + out->lse_acc_bytes, 256);
-  }
   const int64_t per = balanced_per(s_q_max, nblk, num_sms);
   // The balanced schedule only on request: measured on GB300 (topk 640, back-to-back
   // calls), the uniform grid beat it at every s_q from 96 to 384, even where the
@@ -282,9 +298,16 @@ int mla_decode_plan(int s_q_max, int h_q, int d_qk, int d_v, int topk, int num_s
     // workspace holds a partial slot per piece of the most cut token
     const int64_t units = static_cast<int64_t>(s_q_max) * nblk;
     out->balanced_ctas = static_cast<int32_t>(std::min<int64_t>(units, num_sms));
-    out->workspace_bytes =
-        std::max<uint64_t>(out->workspace_bytes, split_workspace_bytes(balanced_slots(s_q_max, nblk, num_sms), s_q_max));
   }
+  plan_workspace(out);
+  return MLA_OK;
+}
+
+int mla_plan_set_partials_bf16(mla_plan_t* plan, int enable) {
+  if (plan == nullptr || (enable != 0 && enable != 1)) return MLA_ERR_INVALID_ARG;
+  if (plan->h_q != kMlaHeads || plan->d_v != kMlaDv || plan->num_blocks < 1) return MLA_ERR_INVALID_ARG;
+  plan->partial_bf16 = enable;
+  plan_workspace(plan);
   return MLA_OK;
 }
 
@@ -314,6 +337,7 @@ int mla_sparse_decode_split(const mla_plan_t* plan, int s_q, const void* q, cons
   a.scale_log2 = sm_scale * 1.4426950408889634f;
   a.o_acc = static_cast<float*>(workspace);
   a.lse_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan->lse_acc_offset);
+  a.partial_bf16 = plan->partial_bf16;
   a.status = dev->status;
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.drain_limit_ns = kWaitLimitNs;
@@ -342,6 +366,7 @@ int mla_combine_impl(const mla_plan_t* plan, int s_q, const void* workspace, con
   c.o_acc = static_cast<const float*>(workspace);
   c.lse_acc = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + plan->lse_acc_offset);
   c.num_splits = plan->num_splits;
+  c.partial_bf16 = plan->partial_bf16;
   c.rows = s_q * kMlaHeads;
   c.heads = kMlaHeads;
   c.d = kMlaDv;
@@ -374,9 +399,10 @@ int mla_decode_balanced(const mla_plan_t* plan, int s_q, const void* q, const vo
   const int P = balanced_ctas(s_q, nb, plan->num_sms);
   if (P > plan->balanced_ctas) return MLA_ERR_WORKSPACE;
   const int slots = balanced_slots(plan->s_q_max, nb, plan->num_sms);
-  const uint64_t o_bytes = static_cast<uint64_t>(slots) * plan->s_q_max * kMlaHeads * kMlaDv * 4ull;
+  const int esz = plan->partial_bf16 ? 2 : 4;
+  const uint64_t o_bytes = static_cast<uint64_t>(slots) * plan->s_q_max * kMlaHeads * kMlaDv * static_cast<uint64_t>(esz);
   if (workspace == nullptr || !aligned(workspace, 256) ||
-      plan->workspace_bytes < split_workspace_bytes(slots, plan->s_q_max))
+      plan->workspace_bytes < split_workspace_bytes(slots, plan->s_q_max, esz))
     return MLA_ERR_WORKSPACE;
   DeviceState* dev = nullptr;
   if ((st = device_state(&dev)) != MLA_OK) return st;
@@ -402,6 +428,7 @@ int mla_decode_balanced(const mla_plan_t* plan, int s_q, const void* q, const vo
   a.scale_log2 = sm_scale * 1.4426950408889634f;
   a.o_acc = reinterpret_cast<float*>(ws);
   a.lse_acc = reinterpret_cast<float*>(ws + round_up(o_bytes, 256));
+  a.partial_bf16 = plan->partial_bf16;
   a.out = out;
   a.out_dtype = out_dtype;
   a.inv_scale = out_inv_scale;
@@ -415,6 +442,7 @@ int mla_decode_balanced(const mla_plan_t* plan, int s_q, const void* q, const vo
   skv::CombineArgs c{};
   c.o_acc = a.o_acc;
   c.lse_acc = a.lse_acc;
+  c.partial_bf16 = a.partial_bf16;
   c.num_splits = slots;
   c.rows = s_q * kMlaHeads;
   c.heads = kMlaHeads;

@@ -37,7 +37,21 @@ __device__ __forceinline__ float warp_sum(float v) {
 // kBatch: splits' slices in flight at a time. 8 keeps a thread within 64
 // registers, so 32 warps fit an SM and a few thousand rows run in one wave; 16
 // (more registers) serves combines over more than 8 splits.
-template <int D, int kBatch>
+// A lane's four consecutive values of split s's slice: one 16-byte load of
+// fp32 partials, or one 8-byte load of bf16 partials widened exactly.
+template <bool kBf16>
+__device__ __forceinline__ float4 load_slice(const float* o_acc, size_t off, int lane) {
+  if constexpr (kBf16) {
+    const uint2 w = __ldcs(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(o_acc) + off) + lane);
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+  } else {
+    return __ldcs(reinterpret_cast<const float4*>(o_acc + off) + lane);
+  }
+}
+
+template <int D, int kBatch, bool kBf16>
 __global__ void __launch_bounds__(kWarps * 32, kBatch == 8 ? 4 : 1) combine_kernel(const CombineArgs a) {
   constexpr int kSlices = D / 128;   // 128 floats = one float4 per lane
   const int warp = threadIdx.x >> 5;
@@ -60,16 +74,15 @@ __global__ void __launch_bounds__(kWarps * 32, kBatch == 8 ? 4 : 1) combine_kern
       S = bal_cta_of((t + 1) * a.bal_nb - 1, a.bal_units, a.bal_ctas) - pa + 1;
       if (S == 1) continue;      // a whole token: the decode kernel wrote its final rows
     }
-    auto src_of = [&](int s) {
-      return reinterpret_cast<const float4*>(a.o_acc + (static_cast<size_t>(s) * rows + row) * D + slice * 128) +
-             lane;
+    auto load = [&](int s) {
+      return load_slice<kBf16>(a.o_acc, (static_cast<size_t>(s) * rows + row) * D + slice * 128, lane);
     };
     // The first kBatch splits' slices are requested together with the LSEs, before
     // the weights are known (one memory round trip for S <= kBatch); a split whose
     // weight turns out 0 (empty) is then skipped, whatever its slice holds.
     float4 x[kBatch];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) x[u] = u < S ? __ldcs(src_of(u)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < kBatch; ++u) x[u] = u < S ? load(u) : make_float4(0.f, 0.f, 0.f, 0.f);
     const float l0 = lane < S ? a.lse_acc[static_cast<size_t>(lane) * rows + row] : -INFINITY;
     const float l1 = lane + 32 < S ? a.lse_acc[static_cast<size_t>(lane + 32) * rows + row] : -INFINITY;
     const float M = warp_max(fmaxf(l0, l1));
@@ -98,7 +111,7 @@ __global__ void __launch_bounds__(kWarps * 32, kBatch == 8 ? 4 : 1) combine_kern
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
         ws[u] = s0 + u < S ? weight(s0 + u) : 0.f;
-        x[u] = ws[u] != 0.f ? __ldcs(src_of(s0 + u)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        x[u] = ws[u] != 0.f ? load(s0 + u) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) fold(ws[u], x[u]);
@@ -162,8 +175,11 @@ cudaError_t launch_combine(const CombineArgs& a, bool zero_amax, bool pdl, cudaS
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (a.d == 512) return cudaLaunchKernelEx(&cfg, wide ? combine_kernel<512, 16> : combine_kernel<512, 8>, a);
-  if (a.d == 128) return cudaLaunchKernelEx(&cfg, wide ? combine_kernel<128, 16> : combine_kernel<128, 8>, a);
+  if (a.d == 512 && a.partial_bf16)
+    return cudaLaunchKernelEx(&cfg, wide ? combine_kernel<512, 16, true> : combine_kernel<512, 8, true>, a);
+  if (a.d == 512) return cudaLaunchKernelEx(&cfg, wide ? combine_kernel<512, 16, false> : combine_kernel<512, 8, false>, a);
+  if (a.d == 128 && !a.partial_bf16)
+    return cudaLaunchKernelEx(&cfg, wide ? combine_kernel<128, 16, false> : combine_kernel<128, 8, false>, a);
   return cudaErrorInvalidValue;
 }
 

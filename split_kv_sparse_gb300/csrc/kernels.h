@@ -35,8 +35,9 @@ struct MlaArgs {
   // Partial workspace: [slot][s_q][64][512] and [slot][s_q][64]. Uniform: slot =
   // the split. Balanced: slot = a piece's place among the pieces of its token
   // (a token cut by range boundaries); whole tokens write their final rows.
-  float* o_acc;
+  float* o_acc;         // fp32, or bf16 values when partial_bf16
   float* lse_acc;
+  int partial_bf16;     // O partials stored as bf16 (LSE partials stay fp32)
   // direct path: final output
   void* out;            // [s_q][64][512] of out_dtype
   int out_dtype;
@@ -75,8 +76,9 @@ cudaError_t launch_mla_decode(const CUtensorMap& tm_q, const MlaArgs& a, cudaStr
 
 // Log-sum-exp combine over `rows` output rows of width d (512 or 128).
 struct CombineArgs {
-  const float* o_acc;   // [S][rows][d]
+  const float* o_acc;   // [S][rows][d], fp32 or (partial_bf16) bf16 values
   const float* lse_acc; // [S][rows]
+  int partial_bf16;
   int num_splits;
   int rows;             // tokens * heads
   int heads;            // head index = row % heads (for the sink)

@@ -266,16 +266,19 @@ __device__ __forceinline__ void transpose4_words(uint32_t (&m)[4], int lane, int
 // instruction covers 128 contiguous bytes of one head). bf16 and e4m3 codes are
 // first moved across lanes so that each lane holds 16 contiguous bytes of one
 // head row, stored with one 16-byte store per head and half-row group.
-__device__ __forceinline__ float store_final(const MlaArgs& a, int t, int d0, int lane, const float (&v)[64]) {
+// `rows`: the token's [64 heads][512] rows of element type `dtype` (0 fp32, 1
+// bf16, 2 e4m3 scaled by inv_scale).
+__device__ __forceinline__ float store_rows(void* rows, int dtype, float inv_scale, int d0, int lane,
+                                            const float (&v)[64]) {
   float m = 0.f;
 #pragma unroll
   for (int c = 0; c < 64; ++c) m = fmaxf(m, fabsf(v[c]));
-  const size_t row0 = static_cast<size_t>(t) * kMlaHeads * kMlaDv + d0;   // head 0, dim d0
-  if (a.out_dtype == 0) {
-    float* st = static_cast<float*>(a.out) + row0 + lane;
+  const size_t row0 = static_cast<size_t>(d0);   // head 0, dim d0
+  if (dtype == 0) {
+    float* st = static_cast<float*>(rows) + row0 + lane;
 #pragma unroll
     for (int c = 0; c < 64; ++c) st[c * kMlaDv] = v[c];
-  } else if (a.out_dtype == 1) {
+  } else if (dtype == 1) {
     // w[k]: heads 2k, 2k+1 at dim d0 + lane. Lane pairs swap halves, so lane
     // 2i+j holds head 2k+j at dims 2i, 2i+1; then the four lanes 8h+2i'+j
     // (i' = 0..3) transpose groups of four words, so lane 8h+2i'+j holds, for k
@@ -296,7 +299,7 @@ __device__ __forceinline__ float store_final(const MlaArgs& a, int t, int d0, in
       transpose4_words(w, lane, 2);
       const int ip = (lane >> 1) & 3, j = lane & 1, hq = lane >> 3;
       const int head = 2 * (4 * G + ip) + j;
-      __nv_bfloat16* st = static_cast<__nv_bfloat16*>(a.out) + row0 + static_cast<size_t>(head) * kMlaDv + 8 * hq;
+      __nv_bfloat16* st = static_cast<__nv_bfloat16*>(rows) + row0 + static_cast<size_t>(head) * kMlaDv + 8 * hq;
       *reinterpret_cast<uint4*>(st) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   } else {
@@ -313,10 +316,10 @@ __device__ __forceinline__ float store_final(const MlaArgs& a, int t, int d0, in
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int k = 4 * G + r;
-        const uint32_t c01 = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * k] * a.inv_scale, v[4 * k + 1] * a.inv_scale),
+        const uint32_t c01 = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * k] * inv_scale, v[4 * k + 1] * inv_scale),
                                                       __NV_SATFINITE, __NV_E4M3);
         const uint32_t c23 = __nv_cvt_float2_to_fp8x2(
-            make_float2(v[4 * k + 2] * a.inv_scale, v[4 * k + 3] * a.inv_scale), __NV_SATFINITE, __NV_E4M3);
+            make_float2(v[4 * k + 2] * inv_scale, v[4 * k + 3] * inv_scale), __NV_SATFINITE, __NV_E4M3);
         uint32_t x = (c01 & 0xFFFFu) | (c23 << 16);
         x = __byte_perm(x, __shfl_xor_sync(0xffffffffu, x, 2), sel1);
         w[r] = __byte_perm(x, __shfl_xor_sync(0xffffffffu, x, 1), sel2);
@@ -324,11 +327,18 @@ __device__ __forceinline__ float store_final(const MlaArgs& a, int t, int d0, in
       transpose4_words(w, lane, 4);
       const int ip = (lane >> 2) & 3, hq = lane >> 4;
       const int head = 4 * (4 * G + ip) + j;
-      uint8_t* st = static_cast<uint8_t*>(a.out) + row0 + static_cast<size_t>(head) * kMlaDv + 16 * hq;
+      uint8_t* st = static_cast<uint8_t*>(rows) + row0 + static_cast<size_t>(head) * kMlaDv + 16 * hq;
       *reinterpret_cast<uint4*>(st) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
   return m;
+}
+
+// Final rows of token t (the call's output, its dtype and scale).
+__device__ __forceinline__ float store_final(const MlaArgs& a, int t, int d0, int lane, const float (&v)[64]) {
+  const size_t esz = a.out_dtype == 0 ? 4 : (a.out_dtype == 1 ? 2 : 1);
+  return store_rows(static_cast<uint8_t*>(a.out) + static_cast<size_t>(t) * kMlaHeads * kMlaDv * esz, a.out_dtype,
+                    a.inv_scale, d0, lane, v);
 }
 
 // kSched: 0 = uniform (one job per CTA), 1 = balanced (a run of jobs per CTA);
@@ -355,11 +365,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A split with no block of its own (uniform schedule only): O = 0 over this
     // CTA's dims, LSE = -inf (written by the CTA of the first dims).
     grid_launch_dependents();
-    float4* o = reinterpret_cast<float4*>(a.o_acc + j0.out_row * kMlaDv);
-    const int per_head = 32 * j0.nq;   // float4s of one head row this CTA owns
-    for (int i = threadIdx.x; i < kMlaHeads * per_head; i += kThreads) {
-      const int h = i / per_head;
-      o[h * (kMlaDv / 4) + 32 * j0.q0 + (i - h * per_head)] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int per_head = 32 * j0.nq;   // groups of 4 values of one head row this CTA owns
+    if (a.partial_bf16) {
+      uint2* o = reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.o_acc) + j0.out_row * kMlaDv);
+      for (int i = threadIdx.x; i < kMlaHeads * per_head; i += kThreads) {
+        const int h = i / per_head;
+        o[h * (kMlaDv / 4) + 32 * j0.q0 + (i - h * per_head)] = make_uint2(0u, 0u);
+      }
+    } else {
+      float4* o = reinterpret_cast<float4*>(a.o_acc + j0.out_row * kMlaDv);
+      for (int i = threadIdx.x; i < kMlaHeads * per_head; i += kThreads) {
+        const int h = i / per_head;
+        o[h * (kMlaDv / 4) + 32 * j0.q0 + (i - h * per_head)] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
     if (j0.q0 == 0 && threadIdx.x < kMlaHeads) a.lse_acc[j0.out_row + threadIdx.x] = -INFINITY;
     return;
@@ -795,6 +813,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (J.kind == J_FINAL) {
           amax_l = fmaxf(amax_l, store_final(a, J.t, d - lane, lane, v));
+        } else if (a.partial_bf16) {
+          // bf16 partials: the rows of the final bf16 output's layout, at the slot
+          store_rows(reinterpret_cast<__nv_bfloat16*>(a.o_acc) + J.out_row * kMlaDv, 1, 1.f, d - lane, lane, v);
         } else {
           float* st = a.o_acc + J.out_row * kMlaDv + d;
 #pragma unroll

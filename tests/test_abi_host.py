@@ -101,8 +101,12 @@ def test_plan_is_deterministic_and_follows_rule():
                 smax = max(1, min(sms // s_q, nblk, 64))
                 eff = lambda c: max(2, -(-nblk // c))   # one- and two-block splits count alike
                 best = eff(smax)
-                assert eff(S) == best
-                assert all(eff(c) > best for c in range(1, S))
+                S2 = next(c for c in range(1, smax + 1) if eff(c) == best)
+                # ... unless every one-block split still gets 4 dim groups
+                if S2 > 1 and nblk <= smax and s_q * nblk * 4 <= sms:
+                    assert S == nblk
+                else:
+                    assert S == S2
                 # uniform workspace (0 for one split), and with the automatic
                 # choice also the balanced schedule's partial slots
                 ru = lambda x: -(-x // 256) * 256
@@ -126,8 +130,10 @@ def test_plan_is_deterministic_and_follows_rule():
 
 
 def test_plan_examples():
-    assert b.mla_decode_plan(1, 640, num_sms=152).num_splits == 5      # 2 blocks each
-    assert b.mla_decode_plan(1, 640, num_sms=152).dim_groups == 4      # 20 CTAs
+    assert b.mla_decode_plan(1, 640, num_sms=152).num_splits == 10     # 1 block each (4 dim groups fit)
+    assert b.mla_decode_plan(1, 640, num_sms=152).dim_groups == 4      # 40 CTAs
+    assert b.mla_decode_plan(3, 640, num_sms=152).num_splits == 10     # 120 CTAs
+    assert b.mla_decode_plan(4, 640, num_sms=152).num_splits == 5      # 160 would not fit: 2 blocks each
     assert b.mla_decode_plan(6, 640, num_sms=152).dim_groups == 4      # 5 splits, 120 CTAs
     assert b.mla_decode_plan(10, 640, num_sms=152).dim_groups == 2     # 5 splits, 100 CTAs
     assert b.mla_decode_plan(16, 640, num_sms=152).dim_groups == 1     # 5 splits, 80 CTAs
@@ -299,3 +305,38 @@ def test_balanced_schedule_choice_examples():
     assert b.mla_decode_plan(1, 640, num_sms=152).balanced_ctas == 0
     assert b.mla_decode_plan(16, 640, num_sms=152).balanced_ctas == 0
     assert b.mla_decode_plan(96, 640, num_sms=152, force_splits=1).balanced_ctas == 0
+
+
+def test_bf16_partials_setter_recomputes_the_workspace():
+    ru = lambda x: -(-x // 256) * 256
+    p = b.mla_decode_plan(16, 640, num_sms=152, force_splits=8)
+    assert p.partial_bf16 == 0
+    assert p.o_acc_bytes == 8 * 16 * 64 * 512 * 4
+    b.mla_plan_set_partials_bf16(p)
+    assert p.partial_bf16 == 1
+    assert p.o_acc_bytes == 8 * 16 * 64 * 512 * 2
+    assert p.lse_acc_offset == ru(p.o_acc_bytes)
+    assert p.lse_acc_bytes == 8 * 16 * 64 * 4
+    assert p.workspace_bytes == ru(p.lse_acc_offset + p.lse_acc_bytes)
+    b.mla_plan_set_partials_bf16(p, False)
+    assert bytes(p) == bytes(b.mla_decode_plan(16, 640, num_sms=152, force_splits=8))
+    # one split: still no workspace; balanced: the slots' area in bf16
+    p1 = b.mla_plan_set_partials_bf16(b.mla_decode_plan(96, 640, num_sms=152))
+    assert p1.num_splits == 1 and p1.workspace_bytes == 0
+    pb = b.mla_decode_plan(96, 640, num_sms=152, force_splits=-1)
+    slots = balanced_slots(96, 10, 152)
+    b.mla_plan_set_partials_bf16(pb)
+    assert pb.workspace_bytes == ru(ru(slots * 96 * 64 * 512 * 2) + slots * 96 * 64 * 4)
+
+
+def test_bf16_partials_setter_errors():
+    invalid_arg = 1
+    p = b.mla_decode_plan(16, 640, num_sms=152)
+    before = bytes(p)
+    with pytest.raises(b.SplitKVError) as e:
+        b.mla_plan_set_partials_bf16(p, 2)
+    assert e.value.status == invalid_arg
+    assert bytes(p) == before                      # refused: the plan is left as it was
+    assert b.lib().mla_plan_set_partials_bf16(None, 1) == invalid_arg
+    q = b.MlaPlan()   # not made by mla_decode_plan
+    assert b.lib().mla_plan_set_partials_bf16(ctypes.byref(q), 1) == invalid_arg
