@@ -29,18 +29,24 @@
 namespace skv {
 namespace {
 
-// Four e4m3 codes (bytes 0..3 of w) to four f16 values, exactly (every e4m3
-// value is an f16 value): bytes 0, 1 -> lo, bytes 2, 3 -> hi, low half first.
-__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  asm("{\n"
-      "  .reg .b16 a, b;\n"
-      "  mov.b32 {a, b}, %2;\n"
-      "  cvt.rn.f16x2.e4m3x2 %0, a;\n"
-      "  cvt.rn.f16x2.e4m3x2 %1, b;\n"
-      "}\n"
-      : "=r"(lo), "=r"(hi)
-      : "r"(w));
+// Four e4m3 codes (bytes 0..3 of w) to four f16 values equal to the codes'
+// values times 2^-8, exactly, with integer operations only (the conversion unit
+// is left to the softmax's exponentials): bytes 0, 1 -> lo, bytes 2, 3 -> hi,
+// low half first. An e4m3 byte s.eeee.mmm is 2^(e-7) * 1.mmm (e > 0) or
+// 2^-6 * 0.mmm (e = 0); placed as s.0eeee.mmm0000000 in an f16 it reads
+// 2^(e-15) * 1.mmm or 2^-14 * 0.mmm: the same value times 2^-8, subnormals
+// included. (The one NaN code pair, s.1111.111, reads as +-480 * 2^-8.) Each
+// byte goes to the low byte of its 16-bit half; then the 7 value bits move up
+// by 7 and the sign bit by 8 (added to itself once, it carries one place up).
+__device__ __forceinline__ uint32_t e4m3x2_bits_to_f16x2(uint32_t x) {   // x = [0 b1 0 b0]
+  return (x + (x & 0x00800080u)) << 7;
 }
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  lo = e4m3x2_bits_to_f16x2(__byte_perm(w, 0u, 0x4140));
+  hi = e4m3x2_bits_to_f16x2(__byte_perm(w, 0u, 0x4342));
+}
+// The converted V is the e4m3 value times 2^-8: the epilogue's scale takes 2^8.
+constexpr float kV16Scale = 256.0f;
 
 constexpr int kThreads = 320;
 constexpr int kConverters = 4;             // warps 6-9: one key row of the V tile per thread
@@ -507,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float lse = -INFINITY, inv = 0.f;
       if (lsum > 0.f) {
         lse = m_run + log2f(lsum);
-        inv = dv / lsum;
+        inv = dv * kV16Scale / lsum;
       }
       inv_s[row] = inv;
       if (!bad) {
