@@ -365,6 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A split with no block of its own (uniform schedule only): O = 0 over this
     // CTA's dims, LSE = -inf (written by the CTA of the first dims).
     grid_launch_dependents();
+    grid_dependency_wait();   // the preceding kernel may still read this workspace
     const int per_head = 32 * j0.nq;   // groups of 4 values of one head row this CTA owns
     if (a.partial_bf16) {
       uint2* o = reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.o_acc) + j0.out_row * kMlaDv);
@@ -398,24 +399,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* hs = reinterpret_cast<float*>(smem + kOffHead);   // [job parity][2][64] per-head scalars
   const WaitCtx wc{a.wait_limit_ns, a.status, abort_flag};
 
-  // The first row indices: fetched before the set-up barrier so the global
-  // memory latency overlaps TMEM allocation and barrier initialisation. A
-  // loader lane takes row 32w + lane of step 0; a softmax lane takes rows lane
-  // and lane + 32.
-  int pre0 = -1, pre1 = -1;
-  {
-    const int32_t* idx0 = a.idx + static_cast<size_t>(j0.t) * a.topk;
-    int r = -1, r2 = -1;
-    if (warp < 2) {
-      r = j0.row0 + 32 * warp + lane;
-    } else if (warp >= 4) {
-      r = j0.row0 + lane;
-      r2 = r + 32;
-    }
-    if (r >= 0 && r < j0.row1) pre0 = __ldg(idx0 + r);
-    if (r2 >= 0 && r2 < j0.row1) pre1 = __ldg(idx0 + r2);
-  }
-
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
     for (int i = 0; i < 4; ++i) {
@@ -447,9 +430,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  // A programmatic dependent (the combine) may begin launching now; it waits
-  // for this whole grid before it reads any partial.
+  // A programmatic dependent (the combine, or the next call) may begin
+  // launching now; it waits for this whole grid before it touches memory.
   grid_launch_dependents();
+  // This grid may itself have started early, behind the preceding kernel on the
+  // stream: everything above touched only this CTA's own resources; from here
+  // on it reads its inputs and writes its outputs, so that kernel must be done.
+  grid_dependency_wait();
+
+  // The first row indices: a loader lane takes row 32w + lane of step 0; a
+  // softmax lane takes rows lane and lane + 32.
+  int pre0 = -1, pre1 = -1;
+  {
+    const int32_t* idx0 = a.idx + static_cast<size_t>(j0.t) * a.topk;
+    int r = -1, r2 = -1;
+    if (warp < 2) {
+      r = j0.row0 + 32 * warp + lane;
+    } else if (warp >= 4) {
+      r = j0.row0 + lane;
+      r2 = r + 32;
+    }
+    if (r >= 0 && r < j0.row1) pre0 = __ldg(idx0 + r);
+    if (r2 >= 0 && r2 < j0.row1) pre1 = __ldg(idx0 + r2);
+  }
 
   if (warp < 2) {
     // ====================================================== row gathers ===
@@ -1056,9 +1059,20 @@ cudaError_t launch_mla_decode(const CUtensorMap& tm_q, const MlaArgs& a, cudaStr
   const dim3 grid(a.sched == 0 ? static_cast<unsigned>(a.s_q) * static_cast<unsigned>(a.num_splits) *
                                      static_cast<unsigned>(a.dim_groups)
                                : static_cast<unsigned>(a.num_ctas));
-  if (a.sched == 0) mla_decode_kernel<0><<<grid, kThreads, kSmemBytes, stream>>>(tm_q, a);
-  else mla_decode_kernel<1><<<grid, kThreads, kSmemBytes, stream>>>(tm_q, a);
-  return cudaGetLastError();
+  // launched as a programmatic dependent of the preceding kernel on the stream:
+  // its CTAs may become resident and set up while that kernel finishes
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (a.sched == 0) return cudaLaunchKernelEx(&cfg, mla_decode_kernel<0>, tm_q, a);
+  return cudaLaunchKernelEx(&cfg, mla_decode_kernel<1>, tm_q, a);
 }
 
 // ---- bounded-wait self test ---------------------------------------------------

@@ -96,6 +96,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // Launched as a programmatic dependent: the CTA may be resident before the
+  // preceding kernel on the stream is done, and the job decode below already
+  // reads inputs (the sequence lengths), so it waits first.
+  grid_dependency_wait();
 
   // ---- job decode (shared by every role) ------------------------------------
   const int S = a.num_splits;   // splits per sequence (adaptive: the most any sequence gets)
@@ -592,7 +596,18 @@ cudaError_t launch_sdpa_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
   const long long one = static_cast<long long>(a.batch) * a.h_kv;
   const long long bound = a.adaptive ? (one > a.num_sms ? one : static_cast<long long>(a.num_sms)) : all;
   const dim3 grid(static_cast<unsigned>(bound < all ? bound : all));
-  sdpa_decode_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, a, direct ? 1 : 0);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, sdpa_decode_kernel, tm_q, tm_k, tm_v, a, direct ? 1 : 0);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
