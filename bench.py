@@ -545,7 +545,7 @@ def run_gpu(args):
         # the dense FP8 GQA variant (same partial / LSE protocol), forced split
         # counts and the planner's choice
         dinp = wl.sdpa_inputs(8, 32, 8, 128, seed=0)
-        for S in list(SWEEP_S) + [0]:
+        for S in (args.dense_splits if args.dense_splits is not None else list(SWEEP_S) + [0]):
             c = DenseCase(b, torch, dinp, S)
             steps = max(args.sweep_steps, c.layers)
             us = c.time("call", steps, c.layers)
@@ -637,7 +637,7 @@ def known_traffic(s_q, S):
     except OSError:
         return None
     table = {   # (source hash, s_q, S) -> dram bytes per launch
-        ("5fd6d0fb3f19d7c4", 96, 1): 55_383_296,
+        ("09f9d5d92a7ac9c3", 96, 1): 55_390_464,
     }
     return table.get((h, s_q, S))
 
@@ -722,6 +722,8 @@ def main():
     ap.add_argument("--sweep-steps", type=int, default=50)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-mla-sweep", action="store_true", help="run only the dense part of the sweep")
+    ap.add_argument("--dense-splits", type=int, nargs="*", default=None,
+                    help="the dense sweep's split counts (0 = the planner's choice); default 1 2 4 8 16 0")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--_cpu-worker", action="store_true", help=argparse.SUPPRESS)

@@ -340,3 +340,11 @@ def test_bf16_partials_setter_errors():
     assert b.lib().mla_plan_set_partials_bf16(None, 1) == invalid_arg
     q = b.MlaPlan()   # not made by mla_decode_plan
     assert b.lib().mla_plan_set_partials_bf16(ctypes.byref(q), 1) == invalid_arg
+
+
+def test_package_reexports_every_entry_point():
+    import split_kv_sparse_gb300 as pkg
+    for name in b.EXPORTS:
+        if name == "mla_status_string":
+            continue      # wrapped as status_string
+        assert hasattr(pkg, name), name
