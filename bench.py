@@ -5,11 +5,13 @@ FlashMLA PR #25 workload (h_q = 64, d_qk = 576, d_v = 512, topk = 128 + 512,
 one bf16 latent KV cache of 131072 rows, FP8 e4m3 output with a per-tensor scale).
 
 One "step" is one decode call through mla_sparse_decode: the split kernel plus
-the combine, the direct-epilogue kernel when the plan picks one split, or the
-balanced kernel, replayed as a CUDA graph with inputs resident in HBM; L2 is
-flushed (256 MiB write, untimed) before every timed call and each call is timed
-with CUDA events on its stream. The line also carries an s_q x num_splits sweep
-and the dense FP8 GQA variant's sweep (the same partial / LSE protocol).
+the combine, or the direct-epilogue kernel when the plan picks one split, with
+inputs resident in HBM. The K timed steps are K consecutive calls rotating over
+per-layer KV caches and query / index sets whose reads exceed L2 several times
+(as the layers of a model do), replayed as CUDA graphs and bracketed by one pair
+of CUDA events on the launching stream. The line also carries an s_q x
+num_splits sweep (with the balanced schedule and bf16 partials where they
+apply) and the dense FP8 GQA variant's sweep (the same partial / LSE protocol).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--s-q 96] [--impl ours|reference]
 
