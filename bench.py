@@ -189,10 +189,16 @@ def unique_bytes(s_q: int) -> int:
     return s_q * (H_Q * D_QK * 2 + TOPK * 4 + TOPK * D_QK * 2)
 
 
+LAYERS_OVERRIDE = 0
+
+
 def layers_for(s_q: int, l2_bytes: int) -> int:
     """How many per-layer caches (and query/index sets) a timed run rotates through so
     that what one call reads has left L2 by the time the same layer comes round again:
-    at least 3x L2 of other calls' reads, at least 4 layers, at most MAX_LAYERS."""
+    at least 3x L2 of other calls' reads, at least 4 layers, at most MAX_LAYERS (or the
+    --layers count when given)."""
+    if LAYERS_OVERRIDE > 0:
+        return LAYERS_OVERRIDE
     return max(4, min(MAX_LAYERS, -(-3 * l2_bytes // unique_bytes(s_q))))
 
 
@@ -255,7 +261,9 @@ class Case:
         if self.balanced:
             return (f"balanced: {self.P} CTAs x <= {self.per} blocks of 64 rows; "
                     f"{self.cut} of {self.s_q} tokens cut into {self.pieces} pieces, folded by the combine")
-        return f"uniform: {self.S} split(s) per token, {self.s_q * self.S} CTAs"
+        D = self.plan.dim_groups
+        return (f"uniform: {self.S} split(s) per token x {D} dim group(s), {self.s_q * self.S * D} CTAs"
+                + (", bf16 partials" if self.plan.partial_bf16 else ""))
 
     def _capture(self, fn):
         torch = self.torch
@@ -431,6 +439,8 @@ def run_gpu(args):
     # timed rotation (views of one allocation), and per-layer queries / indices per s_q
     l2_bytes = int(getattr(torch.cuda.get_device_properties(local), "L2_cache_size", 0) or L2_FALLBACK)
     s_q_list = [args.s_q] + ([] if (args.no_sweep or args.no_mla_sweep) else [s for s in SWEEP_SQ if s != args.s_q])
+    global LAYERS_OVERRIDE
+    LAYERS_OVERRIDE = args.layers   # a fixed rotation (a small device footprint, e.g. for a profiler capture)
     n_layers_max = max(layers_for(s, l2_bytes) for s in s_q_list)
     base = wl.mla_inputs(1, N_KV, TOPK, seed=0)
     kv_all = torch.empty(n_layers_max, N_KV, D_QK, dtype=torch.bfloat16, device=dev)
@@ -727,6 +737,8 @@ def main():
     ap.add_argument("--dense-splits", type=int, nargs="*", default=None,
                     help="the dense sweep's split counts (0 = the planner's choice); default 1 2 4 8 16 0")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="per-layer caches the timed calls rotate over (0: enough to exceed L2 3x)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--_cpu-worker", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
