@@ -5,16 +5,16 @@
 // into split-major slots (or, unsplit, a direct bf16/fp32/e4m3 epilogue that
 // also computes the amax).
 //
-// One CTA per job (sequence b, KV head g, split s), 320 threads:
+// One CTA per job (sequence b, KV head g, split s), 448 threads:
 //   warp 0     TMA: the job's Q rows once (the group's h_q/h_kv heads of up to
 //              64/group tokens = 64 rows x 128 B), then per tile K and V
 //              (128 keys x 128 B each, e4m3) into a 3-stage ring.
 //   warp 1     tcgen05 issue:  S[64 rows x 128 keys] = Q . K^T     (kind::f8f6f4, K=128)
 //                              O^T[128 d x 64 rows] += V^T . P^T   (kind::f16, f16 operands)
-//   warps 2-5  softmax over the keys of each query row (S = Q.K^T, M=64: a row
-//              per lane pair, the tile's keys in its columns), lazy rescale of O^T,
-//              P^T in f16, then the epilogue.
-//   warps 6-9  convert each V tile from e4m3 to f16 (exact) into the
+//   warps 2-9  softmax over the keys of each query row (S = Q.K^T, M=64: two
+//              warps per TMEM sub-partition, each with 64 of the tile's 128 keys,
+//              32 per thread), lazy rescale of O^T, P^T in f16, then the epilogue.
+//   warps 10-13 convert each V tile from e4m3 to f16 (exact) into the
 //              MN-major 128-byte-swizzled layout the PV MMA reads.
 // The QK product of e4m3 codes is exact in fp32; descales multiply the scores
 // (dq*dk*sm_scale) and the output (dv).
@@ -48,8 +48,10 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32
 // The converted V is the e4m3 value times 2^-8: the epilogue's scale takes 2^8.
 constexpr float kV16Scale = 256.0f;
 
-constexpr int kThreads = 320;
-constexpr int kConverters = 4;             // warps 6-9: one key row of the V tile per thread
+constexpr int kThreads = 448;
+constexpr int kSoftmaxWarps = 8;           // warps 2-9: two per TMEM sub-partition
+constexpr int kConverters = 4;             // warps 10-13: one key row of the V tile per thread
+constexpr int kFirstConverter = 2 + kSoftmaxWarps;
 constexpr int kD = 128;
 constexpr int kTile = 128;                 // keys per tile (split unit)
 constexpr int kRows = 64;                  // query rows per job (tokens x group heads)
@@ -68,7 +70,9 @@ constexpr int kOffBars = kOffQ + kQBytes;                    // 204800
 constexpr int kOffMisc = kOffBars + 256;
 constexpr int kOffAlpha = kOffMisc + 128;                    // float[2][64] rescale factors by tile parity
 constexpr int kOffInv = kOffAlpha + 512;                     // float[64] dv / l per row
-constexpr int kSmemUsed = kOffInv + 256;
+constexpr int kOffHalf = kOffInv + 256;                      // float[2][2][64] per-row maxima of each key half
+                                                             // by tile parity, then float[2][64] row sums
+constexpr int kSmemUsed = kOffHalf + 1536;
 constexpr int kSmemBytes = kSmemUsed + 1024;
 
 enum {
@@ -219,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_SREADY0 + i), 1);
-      mbar_init(bar(B_PFULL0 + i), 4);
+      mbar_init(bar(B_PFULL0 + i), kSoftmaxWarps);
       mbar_init(bar(B_V16FULL0 + i), kConverters);
       mbar_init(bar(B_V16EMPTY0 + i), 1);
     }
@@ -325,9 +329,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_drain(bar(B_DRAIN), 0, a.drain_limit_ns)) atomicCAS(&a.status[1], 0u, W_DRAIN_MMA2);
       }
     }
-  } else if (warp >= 6) {
+  } else if (warp >= kFirstConverter) {
     // ==================================================== V e4m3 -> f16 ===
-    const int key = threadIdx.x - 192;      // 0..127: this thread's key row of each tile
+    const int key = threadIdx.x - 32 * kFirstConverter;   // 0..127: this thread's key row of each tile
     const int r8 = key & 7;
 #pragma unroll 1
     for (int t = 0; t < nt; ++t) {
@@ -370,157 +374,185 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============================================== softmax + epilogue ====
     // S = Q.K^T is an M=64 accumulator: row r (token r / group, head r % group)
     // sits in lane r % 16 of sub-partition r / 16, the tile's 128 keys in its
-    // columns. Lanes i and i + 16 of a warp hold row 16 sp + i: keys 0-63 and
-    // 64-127 (tcgen05.ld 16x32bx2), so a row's max and sum take one shuffle.
-    const int sp = warp & 3;
-    const int wi = warp - 2;
+    // columns. Two warps share each sub-partition and split the keys: warp
+    // (sub-partition sp, half hf) takes keys 64 hf .. 64 hf + 63 of the tile,
+    // its lanes i and i + 16 keys +0..31 and +32..63 of row 16 sp + i
+    // (tcgen05.ld 16x32bx2), so a thread walks 32 keys per tile. Both warps of a
+    // row keep its reference max; it moves only when a score exceeds it by the
+    // threshold. P is computed with the current reference first and recomputed
+    // for a warp with a row whose reference moves (rare: the first visible keys,
+    // a large new score), once the two halves' maxima have been exchanged.
+    const int si = warp - 2;                        // 0..7
+    const int sp = warp & 3;                        // TMEM sub-partition
+    const int hf = si >> 2;                         // key half of the tile
     const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
     const int row = 16 * sp + (lane & 15);
-    const int kh = lane >> 4;                       // key half of the tile
+    const int kq = lane >> 4;                       // 32-key quarter within the half
+    const int partner = si ^ 4;                     // the other warp of this sub-partition
     const bool live = row < R;
     // last key (sequence-relative) this row may see inside this split: bottom-right causal
     const int lim_r = live ? min(key_end - 1, kvlen - sq + row / group) : -1;
     const float sc = dq * dk * a.scale_log2;
-    float m_run = -INFINITY;   // the row's reference max (log2 units), shared by its two lanes
+    float* hmax = reinterpret_cast<float*>(smem + kOffHalf);   // [2 tile parity][2 half][64 rows]
+    float* hsum = hmax + 256;                                     // [2 half][64 rows]
+    float m_run = -INFINITY;   // the row's reference max (log2 units), kept by its four lanes
     float lsum = 0.f;          // fp32 softmax denominator over this thread's keys
     int bad = 0;
+    // this thread's 32 scores of tile t (S buffer t & 1), scaled to log2 units,
+    // -inf where not visible; returns their max
+    auto load_scores = [&](int t, bool w, float (&x)[32]) -> float {
+      uint32_t raw[32];
+      tmem_ld_16x32bx2_x32_h32(tmem + lane_base + kTmemS + 128 * (t & 1) + 64 * hf, raw);
+      tmem_wait_ld_x32(raw);
+      const int key0 = (tile0 + t) * kTile + 64 * hf + 32 * kq;   // sequence-relative
+      float mx = -INFINITY;
+      if (w && key0 + 31 <= lim_r) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          x[i] = __uint_as_float(raw[i]) * sc;
+          mx = fmaxf(mx, x[i]);
+        }
+      } else if (w) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          x[i] = key0 + i <= lim_r ? __uint_as_float(raw[i]) * sc : -INFINITY;
+          mx = fmaxf(mx, x[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = -INFINITY;
+      }
+      return mx;
+    };
+    // p = 2^(x - m_ref) (0 where not visible) as f16 into P (the K-major B operand
+    // of PV: N = rows, K = keys; the row's 64 keys of this half are one 128-byte
+    // line of swizzle atom hf, this thread's 32 keys its pieces 4 kq .. 4 kq + 3;
+    // rows past R are never read back: not stored); returns the sum of p
+    auto exp_store = [&](int t, const float (&x)[32]) -> float {
+      uint32_t h[16];
+      float ps[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float p0 = x[2 * i] == -INFINITY ? 0.f : ex2_approx(x[2 * i] - m_run);
+        const float p1 = x[2 * i + 1] == -INFINITY ? 0.f : ex2_approx(x[2 * i + 1] - m_run);
+        ps[i] = p0 + p1;
+        const __half2 ph = __floats2half2_rn(p0, p1);
+        h[i] = *reinterpret_cast<const uint32_t*>(&ph);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ps[i] += ps[i + 8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ps[i] += ps[i + 4];
+      if (live) {
+        uint8_t* pt = smem + kOffP + (t & 1) * kPBytes + hf * 8192 + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4*>(pt + (((4 * kq + c) ^ (row & 7)) << 4)) =
+              make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+      }
+      return (ps[0] + ps[2]) + (ps[1] + ps[3]);
+    };
+    // the other warps' per-tile words: bits 0-15 rows of the writer's sub-partition
+    // whose reference moves in its half, bit 16 a failed wait
+    auto warp_of = [](int sub, int half) { return ((sub + 2) & 3) + 4 * half; };
 #pragma unroll 1
     for (int t = 0; t < nt; ++t) {
-      const int key0 = (tile0 + t) * kTile + 64 * kh;   // this thread's first key, sequence-relative
       int w = 1;
       if (lane == 0) w = wait_bounded(bar(B_SREADY0 + (t & 1)), (t >> 1) & 1, wc, W_SM_S);
       w = __shfl_sync(0xffffffffu, w, 0);
       if (!w) bad = 1;
       tc_fence_after();
-      float x[64];
-      float mx = -INFINITY;
-      bool all_vis = false;   // x holds raw scores (every key visible) rather than scaled ones
-      {
-        uint32_t raw[64];
-        tmem_ld_16x32bx2_x64_h64(tmem + lane_base + kTmemS + 128 * (t & 1), raw);
-        tmem_wait_ld_x64(raw);
-        if (w && key0 + 63 <= lim_r) {
-          // every key visible: the max of the raw scores (sc > 0), the scale
-          // folded into the exponent below
-          float mr = __uint_as_float(raw[0]);
-#pragma unroll
-          for (int i = 1; i < 64; ++i) mr = fmaxf(mr, __uint_as_float(raw[i]));
-#pragma unroll
-          for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(raw[i]);
-          mx = mr * sc;
-          all_vis = true;
-        } else if (w) {
-#pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            x[i] = key0 + i <= lim_r ? __uint_as_float(raw[i]) * sc : -INFINITY;
-            mx = fmaxf(mx, x[i]);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 64; ++i) x[i] = -INFINITY;
-        }
-      }
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      // Lazy rescale: move the reference only when a score exceeds it by more
-      // than the threshold (always on the row's first visible key). Both lanes
-      // of the row see the same mx and take the same decision.
+      float x[32];
+      float mx = load_scores(t, w != 0, x);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));   // this warp's 64 keys of the row
       const bool need = mx > m_run + kRescaleThreshold;
-      float al = 1.f;
-      if (need) {
-        al = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - mx);
-        lsum *= al;
-        m_run = mx;
-      }
       float* alpha = alpha_s + 64 * (t & 1);
-      if (lane < 16) alpha[row] = al;
+      if (lane < 16) {
+        hmax[(t & 1) * 128 + hf * 64 + row] = mx;
+        if (hf == 0) alpha[row] = 1.f;   // rewritten below for a row whose reference moves
+      }
       const unsigned rmask = __ballot_sync(0xffffffffu, need) & 0xffffu;
-      if (lane == 0) flags[(t & 1) * 4 + wi] = static_cast<int>(rmask) | (bad ? 0x10000 : 0);
-      // p = 2^(x - m_ref); an invisible key gives 0
-      if (all_vis) {
-        const float nm = -m_run;
+      if (lane == 0) flags[(t & 1) * 8 + si] = static_cast<int>(rmask) | (bad ? 0x10000 : 0);
+      float ts = exp_store(t, x);   // with the current reference
+      // every warp's maxima and flags of this tile
+      named_bar_sync(1, 32 * kSoftmaxWarps);
+      int fl[kSoftmaxWarps];
+      int any = 0;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) x[i] = ex2_approx(fmaf(x[i], sc, nm));
-      } else {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) x[i] = (x[i] == -INFINITY) ? 0.f : ex2_approx(x[i] - m_run);
+      for (int k = 0; k < kSoftmaxWarps; ++k) {
+        fl[k] = flags[(t & 1) * 8 + k];
+        any |= fl[k];
       }
-      {
-        float ts[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) ts[i] = x[i] + x[i + 32];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) ts[i] += ts[i + 16];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) ts[i] += ts[i + 8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) ts[i] += ts[i + 4];
-        lsum += (ts[0] + ts[2]) + (ts[1] + ts[3]);
-      }
-      // P (f16) as the K-major B operand of PV: N = rows, K = keys; the row's 64
-      // keys of this half are one 128-byte line of swizzle atom kh, stored as
-      // eight 16-byte pieces (rows past R are never read back: not stored)
-      uint8_t* pt = smem + kOffP + (t & 1) * kPBytes + kh * 8192 + (row >> 3) * 1024 + (row & 7) * 128;
-      if (live) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t h4[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const __half2 ph = __floats2half2_rn(x[8 * c + 2 * j], x[8 * c + 2 * j + 1]);
-            h4[j] = *reinterpret_cast<const uint32_t*>(&ph);
-          }
-          *reinterpret_cast<uint4*>(pt + ((c ^ (row & 7)) << 4)) = make_uint4(h4[0], h4[1], h4[2], h4[3]);
-        }
-      }
-      // the other warps' rescale masks: O^T holds every row in all four warps' lanes
-      named_bar_sync(1, 128);
-      const int f0 = flags[(t & 1) * 4 + 0], f1 = flags[(t & 1) * 4 + 1], f2 = flags[(t & 1) * 4 + 2],
-                f3 = flags[(t & 1) * 4 + 3];
-      if ((f0 | f1 | f2 | f3) & 0x10000) {
+      if (any & 0x10000) {
         bad = 1;
         break;   // every softmax warp sees the same flags and leaves together
       }
-      const uint64_t resc = static_cast<uint64_t>(f0 & 0xffff) | (static_cast<uint64_t>(f1 & 0xffff) << 16) |
-                            (static_cast<uint64_t>(f2 & 0xffff) << 32) | (static_cast<uint64_t>(f3 & 0xffff) << 48);
-      if (resc != 0 && t >= 1) {
-        // O^T must hold PV(t-1) before it is scaled. S^T(t) ready already
-        // implies PV(t-2) is done, so this waits for one phase at most.
+      const unsigned mv = static_cast<unsigned>(fl[si] | fl[partner]) & 0xffffu;   // this warp's rows that move
+      if (mv != 0) {
+        // a row whose reference moves takes the max of both halves; the warp
+        // reloads its scores and redoes P and the tile sum (a row that does not
+        // move gets the same values again)
+        if ((mv >> (lane & 15)) & 1u) {
+          const float nm = fmaxf(hmax[(t & 1) * 128 + row], hmax[(t & 1) * 128 + 64 + row]);
+          const float al = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - nm);
+          lsum *= al;
+          m_run = nm;
+          if (hf == 0 && lane < 16) alpha[row] = al;
+        }
+        load_scores(t, w != 0, x);
+        ts = exp_store(t, x);
+      }
+      lsum += ts;
+      if ((any & 0xffff) != 0 && t >= 1) {
+        // O^T holds PV of earlier tiles: once PV(t-1) is done, scale the columns
+        // (rows) that moved, in this warp's 32 dims (TMEM lanes) and its 32 of the
+        // 64 columns, after every warp has written its factors
+        named_bar_sync(1, 32 * kSoftmaxWarps);
         int wp = 1;
         if (lane == 0) wp = wait_bounded(bar(B_PVDONE), (t - 1) & 1, wc, W_SM_PV);
         if (!__shfl_sync(0xffffffffu, wp, 0)) bad = 1;
         tc_fence_after();
-#pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
-          if (((resc >> (32 * j)) & 0xffffffffull) == 0) continue;
+        // rows 32 hf .. 32 hf + 15 are sub-partition 2 hf's, the next 16 the one after
+        const unsigned m32 = ((static_cast<unsigned>(fl[warp_of(2 * hf, 0)] | fl[warp_of(2 * hf, 1)]) & 0xffffu)) |
+                             ((static_cast<unsigned>(fl[warp_of(2 * hf + 1, 0)] | fl[warp_of(2 * hf + 1, 1)]) &
+                               0xffffu) << 16);
+        if (m32 != 0 && !bad) {
           uint32_t o[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + 32 * j, o);
+          tmem_ld_32x32b_x32(tmem + lane_base + 32 * hf, o);
           tmem_wait_ld_x32(o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha[32 * j + i]);
-          tmem_st_32x32b_x32(tmem + lane_base + 32 * j, o);
+          for (int i = 0; i < 32; ++i)
+            if ((m32 >> i) & 1u) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha[32 * hf + i]);
+          tmem_st_32x32b_x32(tmem + lane_base + 32 * hf, o);
+          tmem_wait_st();
         }
-        tmem_wait_st();
       }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PFULL0 + (t & 1)));
-      // alpha and the flags of this tile's parity are rewritten two tiles on, past
-      // the named barrier of the next tile, which every warp reaches only after
-      // reading them here
+      // alpha, the maxima and the flags of this tile's parity are rewritten two
+      // tiles on, before the first named barrier of that tile, which every warp
+      // reaches only after it has read them here
     }
 
     // ---- epilogue ---------------------------------------------------------
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);   // the row's two key halves
-    if (lane == 0) flags[8 + wi] = bad;
-    if (lane < 16 && live) {
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);   // this warp's 64 keys of the row
+    if (lane == 0) flags[16 + si] = bad;
+    if (lane < 16) hsum[hf * 64 + row] = lsum;
+    named_bar_sync(1, 32 * kSoftmaxWarps);
+    int any_bad = 0;
+#pragma unroll
+    for (int k = 0; k < kSoftmaxWarps; ++k) any_bad |= flags[16 + k];
+    if (hf == 0 && lane < 16 && live) {
+      const float tot = hsum[row] + hsum[64 + row];   // both key halves
       float lse = -INFINITY, inv = 0.f;
-      if (lsum > 0.f) {
-        lse = m_run + log2f(lsum);
-        inv = dv * kV16Scale / lsum;
+      if (tot > 0.f) {
+        lse = m_run + log2f(tot);
+        inv = dv * kV16Scale / tot;
       }
       inv_s[row] = inv;
-      if (!bad) {
+      if (!any_bad) {
         if (direct) {
           if (a.lse_out != nullptr) a.lse_out[out_index(row)] = lse;
         } else {
@@ -528,26 +560,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    named_bar_sync(1, 128);
-    const bool any_bad = flags[8] | flags[9] | flags[10] | flags[11];
+    named_bar_sync(1, 32 * kSoftmaxWarps);
     if (!any_bad) {
       int w = 1;
       if (lane == 0) w = wait_bounded(bar(B_FINAL), 0, wc, W_SM_FINAL);
       w = __shfl_sync(0xffffffffu, w, 0);
       tc_fence_after();
       if (w) {
-        uint32_t o[64];
-        tmem_ld_32x32b_x64(tmem + lane_base, o);
-        tmem_wait_ld_x64(o);
+        // O^T: this thread's dim d (a TMEM lane) of the warp's 32 rows (columns)
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + 32 * hf, o);
+        tmem_wait_ld_x32(o);
         const int d = 32 * sp + lane;
         float amax_l = 0.f;
-        float inv[kRows];   // in registers: no shared-memory reload between the global stores
+        float inv[32];   // in registers: no shared-memory reload between the global stores
 #pragma unroll
-        for (int rho = 0; rho < kRows; ++rho) inv[rho] = inv_s[rho];
+        for (int j = 0; j < 32; ++j) inv[j] = inv_s[32 * hf + j];
 #pragma unroll
-        for (int rho = 0; rho < kRows; ++rho) {
+        for (int j = 0; j < 32; ++j) {
+          const int rho = 32 * hf + j;
           if (rho >= R) continue;
-          const float v = __uint_as_float(o[rho]) * inv[rho];
+          const float v = __uint_as_float(o[j]) * inv[j];
           const size_t oi = out_index(rho) * kD + d;
           if (!direct) {
             a.o_acc[oi] = v;

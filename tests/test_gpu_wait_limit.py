@@ -41,6 +41,14 @@ def _mla_call(inp, plan, ws, dev):
     return out, lse
 
 
+def _flush_l2(dev):
+    """A 256 MiB write: the next call's first loads come from DRAM, so its first
+    waits last far longer than the short limit (inputs just copied to the device
+    can otherwise still sit in L2, and a wait that ends within the first polls
+    never reads the timer)."""
+    torch.empty(256 << 20, dtype=torch.uint8, device=dev).fill_(1)
+
+
 def _expect_timeout():
     st, site = b.mla_get_status()          # synchronises the device first
     assert st & b.MLA_STATUS_TIMEOUT, f"no timeout recorded (status {st:#x})"
@@ -59,6 +67,7 @@ def test_mla_waits_run_out_then_the_next_call_is_correct(kind, S, num_sms):
     if plan.workspace_bytes:
         b.mla_workspace_init(plan, ws)
     wsp = ws if plan.workspace_bytes else None
+    _flush_l2(dev)
     b.mla_set_wait_limit_ns(SHORT_NS)
     _mla_call(inp, plan, wsp, dev)
     _expect_timeout()
@@ -74,9 +83,11 @@ def test_mla_waits_run_out_then_the_next_call_is_correct(kind, S, num_sms):
 @pytest.mark.parametrize("S", [1, 3])
 def test_dense_waits_run_out_then_the_next_call_is_correct(S):
     dev = torch.device("cuda")
-    inp = wl.sdpa_inputs(2, 8, 2, 128, q_per_seq=(1, 3), kv_len=(3000, 4000), seed=501)
+    # long sequences: dozens of tiles per CTA, so some of its waits outlast the
+    # short limit whatever the timer's granularity
+    inp = wl.sdpa_inputs(2, 8, 2, 128, q_per_seq=(1, 3), kv_len=(12000, 16000), seed=501)
     total_q, total_kv = int(inp.cu_seqlens_q[-1]), int(inp.cu_seqlens_kv[-1])
-    plan = b.sdpa_fp8_decode_plan(2, 8, 2, 128, 3, total_q, 4000, force_splits=S)
+    plan = b.sdpa_fp8_decode_plan(2, 8, 2, 128, 3, total_q, 16000, force_splits=S)
     ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
     ds = [torch.tensor([x], dtype=torch.float32, device=dev) for x in (inp.descale_q, inp.descale_k, inp.descale_v)]
     args = (inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), inp.cu_seqlens_q.to(dev), inp.cu_seqlens_kv.to(dev))
@@ -88,6 +99,7 @@ def test_dense_waits_run_out_then_the_next_call_is_correct(S):
                           None, ws if plan.workspace_bytes else None)
         return out, lse
 
+    _flush_l2(dev)
     b.mla_set_wait_limit_ns(SHORT_NS)
     call()
     _expect_timeout()
