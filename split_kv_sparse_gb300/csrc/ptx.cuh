@@ -131,6 +131,23 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Named barrier that also returns the OR of `v` over the participating threads
+// (a reduction in the barrier itself, with no shared-memory traffic).
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n"
+      "  .reg .pred p, q;\n"
+      "  setp.ne.u32 q, %1, 0;\n"
+      "  bar.red.or.pred p, %2, %3, q;\n"
+      "  selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 // ------------------------------------------- programmatic dependent launch --
 
 // Lets the next kernel in the stream (launched with programmatic serialisation)
@@ -320,6 +337,24 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t
       "  tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n"
       "}\n" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// kind::f8f6f4 with each operand descriptor as its two 32-bit words (see
+// mma_f16_w) and a compile-time accumulate flag.
+template <int kAccumulate>
+__device__ __forceinline__ void mma_f8_wc(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t ab_hi,
+                                          uint32_t idesc) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred p;\n"
+      "  .reg .b64 da, db;\n"
+      "  setp.ne.b32 p, %5, 0;\n"
+      "  mov.b64 da, {%1, %3};\n"
+      "  mov.b64 db, {%2, %3};\n"
+      "  tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %4, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(ab_hi), "r"(idesc), "n"(kAccumulate)
       : "memory");
 }
 

@@ -65,8 +65,9 @@ constexpr int kQBytes = kRows * kD;        // 8192
 constexpr int kOffStage = 0;
 constexpr int kOffV16 = kOffStage + kStages * kStageBytes;   // 98304
 constexpr int kOffP = kOffV16 + 2 * kV16Bytes;               // 163840
-constexpr int kOffQ = kOffP + 2 * kPBytes;                   // 196608
-constexpr int kOffBars = kOffQ + kQBytes;                    // 204800
+constexpr int kPBuffers = 3;               // P(t) in buffer t % 3 (see the MMA loop)
+constexpr int kOffQ = kOffP + kPBuffers * kPBytes;           // 212992
+constexpr int kOffBars = kOffQ + kQBytes;                    // 221184
 constexpr int kOffMisc = kOffBars + 256;
 constexpr int kOffAlpha = kOffMisc + 128;                    // float[2][64] rescale factors by tile parity
 constexpr int kOffInv = kOffAlpha + 512;                     // float[64] dv / l per row
@@ -276,28 +277,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescQK = idesc_make(64, 128, 0, false, false);   // e4m3 x e4m3, M=64 rows, N=128 keys
       constexpr uint32_t kIdescPV = idesc_make(128, 64, 0, true, false);    // f16, A MN-major
+      // Operand descriptors as 32-bit words: every operand here is 128-byte
+      // swizzled with a 1024-byte atom stride, so all share one high word, and
+      // another stage, buffer or K step is an add to the low word (start address
+      // >> 4, below 256 KB), a compile-time constant inside a run of MMAs. Each
+      // run is straight-line code; the first PV's accumulate flag is a predicate.
+      const uint32_t w_hi = static_cast<uint32_t>(sdesc_sw128(sbase, 16, 1024) >> 32);
+      const uint32_t w_q = static_cast<uint32_t>(sdesc_sw128(sbase + kOffQ, 16, 1024));
+      const uint32_t w_k0 = static_cast<uint32_t>(sdesc_sw128(sbase + kOffStage, 16, 1024));
+      const uint32_t w_v0 = static_cast<uint32_t>(sdesc_sw128(sbase + kOffV16, 16384, 1024));
+      const uint32_t w_p0 = static_cast<uint32_t>(sdesc_sw128(sbase + kOffP, 16, 1024));
       auto issue_qk = [&](int t) {
-        const uint32_t kt = sbase + kOffStage + (t % kStages) * kStageBytes;
-        const uint32_t d = tmem + kTmemS + 128 * (t & 1);
         // A = Q (64 rows x 128 B), B = the K tile (128 keys x 128 B), both K-major;
         // K = 32 e4m3 codes (32 bytes) per MMA
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_f8(d, sdesc_sw128(sbase + kOffQ + kk * 32, 16, 1024), sdesc_sw128(kt + kk * 32, 16, 1024),
-                 kIdescQK, kk != 0);
+        const uint32_t bk = w_k0 + static_cast<uint32_t>(t % kStages) * (kStageBytes >> 4);
+        const uint32_t d = tmem + kTmemS + 128 * (t & 1);
+        mma_f8_wc<0>(d, w_q, bk, w_hi, kIdescQK);
+        mma_f8_wc<1>(d, w_q + 2, bk + 2, w_hi, kIdescQK);
+        mma_f8_wc<1>(d, w_q + 4, bk + 4, w_hi, kIdescQK);
+        mma_f8_wc<1>(d, w_q + 6, bk + 6, w_hi, kIdescQK);
       };
       auto issue_pv = [&](int t) {
-        const uint32_t v16 = sbase + kOffV16 + (t & 1) * kV16Bytes;
-        const uint32_t pt = sbase + kOffP + (t & 1) * kPBytes;
+        // A = V^T (MN-major f16, 2048 B per 16 keys), B = P^T (K-major f16, 32 B
+        // per 16 keys within each 64-key atom of 8192 B)
+        const uint32_t av = w_v0 + static_cast<uint32_t>(t & 1) * (kV16Bytes >> 4);
+        const uint32_t bp = w_p0 + static_cast<uint32_t>(t % kPBuffers) * (kPBytes >> 4);
+        mma_f16_w(tmem, av, bp, w_hi, kIdescPV, t > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_f16(tmem, sdesc_sw128(v16 + kk * 2048, 16384, 1024),
-                  sdesc_sw128(pt + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), kIdescPV, (t > 0 || kk > 0));
+        for (int kk = 1; kk < 8; ++kk)
+          mma_f16_wc<1>(tmem, av + kk * (2048 >> 4), bp + (kk >> 2) * (8192 >> 4) + (kk & 3) * 2, w_hi, kIdescPV);
       };
-      // Per tile t: QK(t) as soon as its K tile has landed (its S buffer was
-      // read by softmax(t-2), whose P the previous iteration waited for), then
-      // PV(t-1) once softmax(t-1) has written P(t-1). So the scores of tile t
-      // are computed while the softmax of tile t-1 runs.
+      // Iteration u: QK(u) as soon as its K tile has landed and its S buffer is
+      // free (softmax(u-2), the buffer's last reader, has published P(u-2)), then
+      // PV(u-2). The scores of tile u depend only on P(u-2), not on PV(u-2) or
+      // PV(u-1), so they are ready while the softmax still works on tile u-1 (with
+      // PV(t-1) issued before QK(t+1), the softmax waited ~0.3 us for its scores
+      // every tile). PV runs two tiles behind, within its V16 double buffer; P has
+      // three buffers: softmax(u) writes buffer u % 3 once S(u) is ready, and that
+      // buffer's last reader, PV(u-3), was issued before QK(u), so it is done.
       auto pv_step = [&](int u) {
         const bool w = wait_bounded(bar(B_PFULL0 + (u & 1)), (u >> 1) & 1, wc, W_MMA_P) &&
                        wait_bounded(bar(B_V16FULL0 + (u & 1)), (u >> 1) & 1, wc, W_MMA_V);
@@ -311,19 +328,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       bool ok = wait_bounded(bar(B_QFULL), 0, wc, W_MMA_Q);
 #pragma unroll 1
-      for (int t = 0; ok && t < nt; ++t) {
-        ok = wait_bounded(bar(B_SFULL_STAGE0 + t % kStages), (t / kStages) & 1, wc, W_MMA_FULL);
-        if (!ok) break;
-        tc_fence_after();
-        issue_qk(t);
-        mma_commit(bar(B_SREADY0 + (t & 1)));
-        mma_commit(bar(B_SEMPTY0 + t % kStages));
-        if (t >= 1) ok = pv_step(t - 1);
+      for (int u = 0; ok && u < nt + 2; ++u) {
+        if (u < nt) {
+          if (u >= 2 && !(ok = wait_bounded(bar(B_PFULL0 + (u & 1)), ((u - 2) >> 1) & 1, wc, W_MMA_P))) break;
+          if (!(ok = wait_bounded(bar(B_SFULL_STAGE0 + u % kStages), (u / kStages) & 1, wc, W_MMA_FULL))) break;
+          tc_fence_after();
+          issue_qk(u);
+          mma_commit(bar(B_SREADY0 + (u & 1)));
+          mma_commit(bar(B_SEMPTY0 + u % kStages));
+        }
+        if (u >= 2) ok = pv_step(u - 2);
       }
-      if (ok) {
-        ok = pv_step(nt - 1);
-        if (ok) mma_commit(bar(B_FINAL));
-      }
+      if (ok) mma_commit(bar(B_FINAL));
       if (!ok) {
         mma_commit(bar(B_DRAIN));
         if (!wait_drain(bar(B_DRAIN), 0, a.drain_limit_ns)) atomicCAS(&a.status[1], 0u, W_DRAIN_MMA2);
@@ -444,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 4; ++i) ps[i] += ps[i + 4];
       if (live) {
-        uint8_t* pt = smem + kOffP + (t & 1) * kPBytes + hf * 8192 + (row >> 3) * 1024 + (row & 7) * 128;
+        uint8_t* pt = smem + kOffP + (t % kPBuffers) * kPBytes + hf * 8192 + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           *reinterpret_cast<uint4*>(pt + (((4 * kq + c) ^ (row & 7)) << 4)) =
@@ -474,14 +490,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const unsigned rmask = __ballot_sync(0xffffffffu, need) & 0xffffu;
       if (lane == 0) flags[(t & 1) * 8 + si] = static_cast<int>(rmask) | (bad ? 0x10000 : 0);
       float ts = exp_store(t, x);   // with the current reference
-      // every warp's maxima and flags of this tile
-      named_bar_sync(1, 32 * kSoftmaxWarps);
+      // Every warp's maxima and flags of this tile are written; the barrier's own
+      // reduction says whether any row moves or any wait failed. Only then are
+      // the flags read (shared-memory loads right after the barrier wait behind
+      // the tile's stores: about 800 cycles, measured).
+      const bool report = named_bar_or(1, 32 * kSoftmaxWarps, need || bad != 0);
       int fl[kSoftmaxWarps];
       int any = 0;
 #pragma unroll
-      for (int k = 0; k < kSoftmaxWarps; ++k) {
-        fl[k] = flags[(t & 1) * 8 + k];
-        any |= fl[k];
+      for (int k = 0; k < kSoftmaxWarps; ++k) fl[k] = 0;
+      if (report) {
+#pragma unroll
+        for (int k = 0; k < kSoftmaxWarps; ++k) {
+          fl[k] = flags[(t & 1) * 8 + k];
+          any |= fl[k];
+        }
       }
       if (any & 0x10000) {
         bad = 1;
