@@ -66,9 +66,10 @@ __device__ __forceinline__ void tmem_wait_ld_x{n}(uint32_t (&r)[{n}]) {{
 
 def main():
     parts = ["// Inline-PTX wrappers for tcgen05.ld / tcgen05.st (written by gen_tmem_ldst.py).\n"]
-    parts += [ld_32x32b(32), ld_32x32b(64), ld_16x32bx2(32, 32), ld_16x32bx2(16, 32), ld_16x32bx2(64, 64)]
+    parts += [ld_32x32b(16), ld_32x32b(32), ld_32x32b(64), ld_16x32bx2(32, 32), ld_16x32bx2(16, 32),
+              ld_16x32bx2(64, 64)]
     parts += [wait_ld(16), wait_ld(32), wait_ld(64)]
-    parts += [st_32x32b(32), st_32x32b(64)]
+    parts += [st_32x32b(16), st_32x32b(32), st_32x32b(64)]
     out = Path(__file__).with_name("tmem_ldst.inc")
     out.write_text("\n".join(parts))
 

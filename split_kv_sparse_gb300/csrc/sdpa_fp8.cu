@@ -48,10 +48,14 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32
 // The converted V is the e4m3 value times 2^-8: the epilogue's scale takes 2^8.
 constexpr float kV16Scale = 256.0f;
 
-constexpr int kThreads = 448;
-constexpr int kSoftmaxWarps = 8;           // warps 2-9: two per TMEM sub-partition
-constexpr int kConverters = 4;             // warps 10-13: one key row of the V tile per thread
+constexpr int kKeyWarps = 2;              // softmax warps per TMEM sub-partition, splitting a tile's keys
+constexpr int kSoftmaxWarps = 4 * kKeyWarps;   // warps 2 .. 1 + kSoftmaxWarps
+constexpr int kKPT = 64 / kKeyWarps;       // keys of a tile per softmax thread
+constexpr int kCPW = 64 / kKeyWarps;       // O^T columns (query rows) per softmax warp in the epilogue
+constexpr int kConverters = 4;             // the last 4 warps: one key row of the V tile per thread
 constexpr int kFirstConverter = 2 + kSoftmaxWarps;
+constexpr int kThreads = 32 * (kFirstConverter + kConverters);
+static_assert(kKeyWarps == 2 || kKeyWarps == 4, "the TMEM load shapes below");
 constexpr int kD = 128;
 constexpr int kTile = 128;                 // keys per tile (split unit)
 constexpr int kRows = 64;                  // query rows per job (tokens x group heads)
@@ -71,9 +75,11 @@ constexpr int kOffBars = kOffQ + kQBytes;                    // 221184
 constexpr int kOffMisc = kOffBars + 256;
 constexpr int kOffAlpha = kOffMisc + 128;                    // float[2][64] rescale factors by tile parity
 constexpr int kOffInv = kOffAlpha + 512;                     // float[64] dv / l per row
-constexpr int kOffHalf = kOffInv + 256;                      // float[2][2][64] per-row maxima of each key half
-                                                             // by tile parity, then float[2][64] row sums
-constexpr int kSmemUsed = kOffHalf + 1536;
+constexpr int kOffHalf = kOffInv + 256;                      // float[2][kKeyWarps][64] per-row maxima of each
+                                                             // key part by tile parity, then float[kKeyWarps][64]
+                                                             // row sums
+constexpr int kOffFlags = kOffHalf + 3 * kKeyWarps * 256;    // int[2][kSoftmaxWarps] per-tile words, int[kSoftmaxWarps]
+constexpr int kSmemUsed = kOffFlags + 3 * kSoftmaxWarps * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;
 
 enum {
@@ -91,6 +97,33 @@ enum : uint32_t {
   W_PROD = 101, W_MMA_Q, W_MMA_P, W_MMA_V, W_MMA_FULL, W_SM_S, W_SM_FINAL, W_CV_FULL, W_CV_EMPTY,
   W_DRAIN_MMA2, W_DRAIN_TMA2, W_SM_PV
 };
+
+// TMEM moves chosen by the register count (the softmax warps' share of a tile
+// or of O^T depends on how many warps split it).
+template <int N>
+__device__ __forceinline__ void tld_16x32bx2_h32(uint32_t a, uint32_t (&r)[N]) {
+  static_assert(N == 16 || N == 32, "shape");
+  if constexpr (N == 32) tmem_ld_16x32bx2_x32_h32(a, r);
+  else tmem_ld_16x32bx2_x16_h32(a, r);
+}
+template <int N>
+__device__ __forceinline__ void tld_32x32b(uint32_t a, uint32_t (&r)[N]) {
+  static_assert(N == 16 || N == 32, "shape");
+  if constexpr (N == 32) tmem_ld_32x32b_x32(a, r);
+  else tmem_ld_32x32b_x16(a, r);
+}
+template <int N>
+__device__ __forceinline__ void tst_32x32b(uint32_t a, const uint32_t (&r)[N]) {
+  static_assert(N == 16 || N == 32, "shape");
+  if constexpr (N == 32) tmem_st_32x32b_x32(a, r);
+  else tmem_st_32x32b_x16(a, r);
+}
+template <int N>
+__device__ __forceinline__ void twait_ld(uint32_t (&r)[N]) {
+  static_assert(N == 16 || N == 32, "shape");
+  if constexpr (N == 32) tmem_wait_ld_x32(r);
+  else tmem_wait_ld_x16(r);
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     sdpa_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -211,7 +244,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBars + 8 * i; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
-  volatile int* flags = reinterpret_cast<volatile int*>(misc + 4);
   float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
   float* inv_s = reinterpret_cast<float*>(smem + kOffInv);
   const WaitCtx wc{a.wait_limit_ns, a.status, abort_flag};
@@ -390,65 +422,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============================================== softmax + epilogue ====
     // S = Q.K^T is an M=64 accumulator: row r (token r / group, head r % group)
     // sits in lane r % 16 of sub-partition r / 16, the tile's 128 keys in its
-    // columns. Two warps share each sub-partition and split the keys: warp
-    // (sub-partition sp, half hf) takes keys 64 hf .. 64 hf + 63 of the tile,
-    // its lanes i and i + 16 keys +0..31 and +32..63 of row 16 sp + i
-    // (tcgen05.ld 16x32bx2), so a thread walks 32 keys per tile. Both warps of a
-    // row keep its reference max; it moves only when a score exceeds it by the
+    // columns. kKeyWarps warps share each sub-partition and split the keys:
+    // warp kw of sub-partition sp reads columns c0 .. c0 + kKPT - 1 with its
+    // lanes 0-15 and c0 + 32 .. c0 + 32 + kKPT - 1 with lanes 16-31 (tcgen05.ld
+    // 16x32bx2), lane i and i + 16 holding row 16 sp + i. The warps of a row all
+    // keep its reference max; it moves only when a score exceeds it by the
     // threshold. P is computed with the current reference first and recomputed
-    // for a warp with a row whose reference moves (rare: the first visible keys,
-    // a large new score), once the two halves' maxima have been exchanged.
-    const int si = warp - 2;                        // 0..7
+    // by a warp with a row whose reference moves (rare: the first visible keys,
+    // a large new score), once every part's maximum has been exchanged.
+    const int si = warp - 2;                        // 0 .. kSoftmaxWarps - 1
     const int sp = warp & 3;                        // TMEM sub-partition
-    const int hf = si >> 2;                         // key half of the tile
+    const int kw = si >> 2;                         // which part of the keys
+    constexpr int kParts = kKeyWarps / 2;           // parts per 64-key half
+    const int c0 = 64 * (kw / kParts) + kKPT * (kw % kParts);   // first column of lanes 0-15
     const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
     const int row = 16 * sp + (lane & 15);
-    const int kq = lane >> 4;                       // 32-key quarter within the half
-    const int partner = si ^ 4;                     // the other warp of this sub-partition
+    const int kq = lane >> 4;
     const bool live = row < R;
     // last key (sequence-relative) this row may see inside this split: bottom-right causal
     const int lim_r = live ? min(key_end - 1, kvlen - sq + row / group) : -1;
     const float sc = dq * dk * a.scale_log2;
-    float* hmax = reinterpret_cast<float*>(smem + kOffHalf);   // [2 tile parity][2 half][64 rows]
-    float* hsum = hmax + 256;                                     // [2 half][64 rows]
-    float m_run = -INFINITY;   // the row's reference max (log2 units), kept by its four lanes
+    float* hmax = reinterpret_cast<float*>(smem + kOffHalf);   // [2 tile parity][kKeyWarps][64 rows]
+    float* hsum = hmax + 2 * kKeyWarps * 64;                     // [kKeyWarps][64 rows]
+    volatile int* wflags = reinterpret_cast<volatile int*>(smem + kOffFlags);   // [2][kSoftmaxWarps], then bad
+    float m_run = -INFINITY;   // the row's reference max (log2 units), kept by all of its lanes
     float lsum = 0.f;          // fp32 softmax denominator over this thread's keys
     int bad = 0;
-    // this thread's 32 scores of tile t (S buffer t & 1), scaled to log2 units,
+    // this thread's kKPT scores of tile t (S buffer t & 1), scaled to log2 units,
     // -inf where not visible; returns their max
-    auto load_scores = [&](int t, bool w, float (&x)[32]) -> float {
-      uint32_t raw[32];
-      tmem_ld_16x32bx2_x32_h32(tmem + lane_base + kTmemS + 128 * (t & 1) + 64 * hf, raw);
-      tmem_wait_ld_x32(raw);
-      const int key0 = (tile0 + t) * kTile + 64 * hf + 32 * kq;   // sequence-relative
+    auto load_scores = [&](int t, bool w, float (&x)[kKPT]) -> float {
+      uint32_t raw[kKPT];
+      const uint32_t col = tmem + lane_base + kTmemS + 128 * (t & 1) + c0;
+      tld_16x32bx2_h32(col, raw);
+      twait_ld(raw);
+      const int key0 = (tile0 + t) * kTile + c0 + 32 * kq;   // sequence-relative
       float mx = -INFINITY;
-      if (w && key0 + 31 <= lim_r) {
+      if (w && key0 + kKPT - 1 <= lim_r) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < kKPT; ++i) {
           x[i] = __uint_as_float(raw[i]) * sc;
           mx = fmaxf(mx, x[i]);
         }
       } else if (w) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < kKPT; ++i) {
           x[i] = key0 + i <= lim_r ? __uint_as_float(raw[i]) * sc : -INFINITY;
           mx = fmaxf(mx, x[i]);
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = -INFINITY;
+        for (int i = 0; i < kKPT; ++i) x[i] = -INFINITY;
       }
       return mx;
     };
     // p = 2^(x - m_ref) (0 where not visible) as f16 into P (the K-major B operand
-    // of PV: N = rows, K = keys; the row's 64 keys of this half are one 128-byte
-    // line of swizzle atom hf, this thread's 32 keys its pieces 4 kq .. 4 kq + 3;
-    // rows past R are never read back: not stored); returns the sum of p
-    auto exp_store = [&](int t, const float (&x)[32]) -> float {
-      uint32_t h[16];
-      float ps[16];
+    // of PV: N = rows, K = keys; a row's 64 keys of one half are one 128-byte line
+    // of that half's swizzle atom, this thread's keys its 16-byte pieces from
+    // (c0 % 64 + 32 kq) / 8 on; rows past R are never read back: not stored);
+    // returns the sum of p
+    const int p_atom = c0 / 64, p_piece = (c0 % 64 + 32 * kq) / 8;
+    auto exp_store = [&](int t, const float (&x)[kKPT]) -> float {
+      uint32_t h[kKPT / 2];
+      float ps[kKPT / 2];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int i = 0; i < kKPT / 2; ++i) {
         const float p0 = x[2 * i] == -INFINITY ? 0.f : ex2_approx(x[2 * i] - m_run);
         const float p1 = x[2 * i + 1] == -INFINITY ? 0.f : ex2_approx(x[2 * i + 1] - m_run);
         ps[i] = p0 + p1;
@@ -456,21 +493,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         h[i] = *reinterpret_cast<const uint32_t*>(&ph);
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) ps[i] += ps[i + 8];
+      for (int w2 = kKPT / 4; w2 > 0; w2 >>= 1)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) ps[i] += ps[i + 4];
+        for (int i = 0; i < w2; ++i) ps[i] += ps[i + w2];
       if (live) {
-        uint8_t* pt = smem + kOffP + (t % kPBuffers) * kPBytes + hf * 8192 + (row >> 3) * 1024 + (row & 7) * 128;
+        uint8_t* pt = smem + kOffP + (t % kPBuffers) * kPBytes + p_atom * 8192 + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint4*>(pt + (((4 * kq + c) ^ (row & 7)) << 4)) =
+        for (int c = 0; c < kKPT / 8; ++c)
+          *reinterpret_cast<uint4*>(pt + (((p_piece + c) ^ (row & 7)) << 4)) =
               make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
       }
-      return (ps[0] + ps[2]) + (ps[1] + ps[3]);
+      return ps[0];
     };
-    // the other warps' per-tile words: bits 0-15 rows of the writer's sub-partition
-    // whose reference moves in its half, bit 16 a failed wait
-    auto warp_of = [](int sub, int half) { return ((sub + 2) & 3) + 4 * half; };
+    // the per-tile word of warp kk of sub-partition sub
+    auto warp_of = [](int sub, int kk) { return ((sub + 2) & 3) + 4 * kk; };
 #pragma unroll 1
     for (int t = 0; t < nt; ++t) {
       int w = 1;
@@ -478,75 +514,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       w = __shfl_sync(0xffffffffu, w, 0);
       if (!w) bad = 1;
       tc_fence_after();
-      float x[32];
+      float x[kKPT];
       float mx = load_scores(t, w != 0, x);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));   // this warp's 64 keys of the row
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));   // this warp's part of the row
       const bool need = mx > m_run + kRescaleThreshold;
       float* alpha = alpha_s + 64 * (t & 1);
       if (lane < 16) {
-        hmax[(t & 1) * 128 + hf * 64 + row] = mx;
-        if (hf == 0) alpha[row] = 1.f;   // rewritten below for a row whose reference moves
+        hmax[((t & 1) * kKeyWarps + kw) * 64 + row] = mx;
+        if (kw == 0) alpha[row] = 1.f;   // rewritten below for a row whose reference moves
       }
       const unsigned rmask = __ballot_sync(0xffffffffu, need) & 0xffffu;
-      if (lane == 0) flags[(t & 1) * 8 + si] = static_cast<int>(rmask) | (bad ? 0x10000 : 0);
+      if (lane == 0) wflags[(t & 1) * kSoftmaxWarps + si] = static_cast<int>(rmask) | (bad ? 0x10000 : 0);
       float ts = exp_store(t, x);   // with the current reference
-      // Every warp's maxima and flags of this tile are written; the barrier's own
+      // Every warp's maxima and words of this tile are written; the barrier's own
       // reduction says whether any row moves or any wait failed. Only then are
-      // the flags read (shared-memory loads right after the barrier wait behind
-      // the tile's stores: about 800 cycles, measured).
+      // the words read (shared-memory loads right after the barrier wait behind
+      // the tile's stores).
       const bool report = named_bar_or(1, 32 * kSoftmaxWarps, need || bad != 0);
-      int fl[kSoftmaxWarps];
-      int any = 0;
-#pragma unroll
-      for (int k = 0; k < kSoftmaxWarps; ++k) fl[k] = 0;
+      uint64_t moving = 0;   // bit r: the reference of row r moves in this tile
+      bool failed = false;
       if (report) {
 #pragma unroll
-        for (int k = 0; k < kSoftmaxWarps; ++k) {
-          fl[k] = flags[(t & 1) * 8 + k];
-          any |= fl[k];
+        for (int sub = 0; sub < 4; ++sub) {
+          int f = 0;
+#pragma unroll
+          for (int kk = 0; kk < kKeyWarps; ++kk) f |= wflags[(t & 1) * kSoftmaxWarps + warp_of(sub, kk)];
+          failed |= (f & 0x10000) != 0;
+          moving |= static_cast<uint64_t>(f & 0xffff) << (16 * sub);
         }
       }
-      if (any & 0x10000) {
+      if (failed) {
         bad = 1;
-        break;   // every softmax warp sees the same flags and leaves together
+        break;   // every softmax warp sees the same words and leaves together
       }
-      const unsigned mv = static_cast<unsigned>(fl[si] | fl[partner]) & 0xffffu;   // this warp's rows that move
+      const unsigned mv = static_cast<unsigned>(moving >> (16 * sp)) & 0xffffu;   // this warp's rows that move
       if (mv != 0) {
-        // a row whose reference moves takes the max of both halves; the warp
-        // reloads its scores and redoes P and the tile sum (a row that does not
-        // move gets the same values again)
+        // a row whose reference moves takes the max of all of its parts; the
+        // warp reloads its scores and redoes P and the tile sum (a row that does
+        // not move gets the same values again)
         if ((mv >> (lane & 15)) & 1u) {
-          const float nm = fmaxf(hmax[(t & 1) * 128 + row], hmax[(t & 1) * 128 + 64 + row]);
+          float nm = -INFINITY;
+#pragma unroll
+          for (int kk = 0; kk < kKeyWarps; ++kk) nm = fmaxf(nm, hmax[((t & 1) * kKeyWarps + kk) * 64 + row]);
           const float al = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - nm);
           lsum *= al;
           m_run = nm;
-          if (hf == 0 && lane < 16) alpha[row] = al;
+          if (kw == 0 && lane < 16) alpha[row] = al;
         }
         load_scores(t, w != 0, x);
         ts = exp_store(t, x);
       }
       lsum += ts;
-      if ((any & 0xffff) != 0 && t >= 1) {
+      if (moving != 0 && t >= 1) {
         // O^T holds PV of earlier tiles: once PV(t-1) is done, scale the columns
-        // (rows) that moved, in this warp's 32 dims (TMEM lanes) and its 32 of the
-        // 64 columns, after every warp has written its factors
+        // (rows) that moved, in this warp's 32 dims (TMEM lanes) and its kCPW of
+        // the 64 columns, after every warp has written its factors
         named_bar_sync(1, 32 * kSoftmaxWarps);
         int wp = 1;
         if (lane == 0) wp = wait_bounded(bar(B_PVDONE), (t - 1) & 1, wc, W_SM_PV);
         if (!__shfl_sync(0xffffffffu, wp, 0)) bad = 1;
         tc_fence_after();
-        // rows 32 hf .. 32 hf + 15 are sub-partition 2 hf's, the next 16 the one after
-        const unsigned m32 = ((static_cast<unsigned>(fl[warp_of(2 * hf, 0)] | fl[warp_of(2 * hf, 1)]) & 0xffffu)) |
-                             ((static_cast<unsigned>(fl[warp_of(2 * hf + 1, 0)] | fl[warp_of(2 * hf + 1, 1)]) &
-                               0xffffu) << 16);
-        if (m32 != 0 && !bad) {
-          uint32_t o[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + 32 * hf, o);
-          tmem_wait_ld_x32(o);
+        const unsigned mc = static_cast<unsigned>(moving >> (kCPW * kw)) &
+                            static_cast<unsigned>((1ull << kCPW) - 1);
+        if (mc != 0 && !bad) {
+          uint32_t o[kCPW];
+          tld_32x32b(tmem + lane_base + kCPW * kw, o);
+          twait_ld(o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if ((m32 >> i) & 1u) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha[32 * hf + i]);
-          tmem_st_32x32b_x32(tmem + lane_base + 32 * hf, o);
+          for (int i = 0; i < kCPW; ++i)
+            if ((mc >> i) & 1u) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha[kCPW * kw + i]);
+          tst_32x32b(tmem + lane_base + kCPW * kw, o);
           tmem_wait_st();
         }
       }
@@ -554,21 +591,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PFULL0 + (t & 1)));
-      // alpha, the maxima and the flags of this tile's parity are rewritten two
+      // alpha, the maxima and the words of this tile's parity are rewritten two
       // tiles on, before the first named barrier of that tile, which every warp
       // reaches only after it has read them here
     }
 
     // ---- epilogue ---------------------------------------------------------
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);   // this warp's 64 keys of the row
-    if (lane == 0) flags[16 + si] = bad;
-    if (lane < 16) hsum[hf * 64 + row] = lsum;
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);   // this warp's part of the row
+    if (lane == 0) wflags[2 * kSoftmaxWarps + si] = bad;
+    if (lane < 16) hsum[kw * 64 + row] = lsum;
     named_bar_sync(1, 32 * kSoftmaxWarps);
     int any_bad = 0;
 #pragma unroll
-    for (int k = 0; k < kSoftmaxWarps; ++k) any_bad |= flags[16 + k];
-    if (hf == 0 && lane < 16 && live) {
-      const float tot = hsum[row] + hsum[64 + row];   // both key halves
+    for (int k = 0; k < kSoftmaxWarps; ++k) any_bad |= wflags[2 * kSoftmaxWarps + k];
+    if (kw == 0 && lane < 16 && live) {
+      float tot = 0.f;   // every part of the row
+#pragma unroll
+      for (int kk = 0; kk < kKeyWarps; ++kk) tot += hsum[kk * 64 + row];
       float lse = -INFINITY, inv = 0.f;
       if (tot > 0.f) {
         lse = m_run + log2f(tot);
@@ -590,18 +629,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       w = __shfl_sync(0xffffffffu, w, 0);
       tc_fence_after();
       if (w) {
-        // O^T: this thread's dim d (a TMEM lane) of the warp's 32 rows (columns)
-        uint32_t o[32];
-        tmem_ld_32x32b_x32(tmem + lane_base + 32 * hf, o);
-        tmem_wait_ld_x32(o);
+        // O^T: this thread's dim d (a TMEM lane) of the warp's kCPW rows (columns)
+        uint32_t o[kCPW];
+        tld_32x32b(tmem + lane_base + kCPW * kw, o);
+        twait_ld(o);
         const int d = 32 * sp + lane;
         float amax_l = 0.f;
-        float inv[32];   // in registers: no shared-memory reload between the global stores
+        float inv[kCPW];   // in registers: no shared-memory reload between the global stores
 #pragma unroll
-        for (int j = 0; j < 32; ++j) inv[j] = inv_s[32 * hf + j];
+        for (int j = 0; j < kCPW; ++j) inv[j] = inv_s[kCPW * kw + j];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int rho = 32 * hf + j;
+        for (int j = 0; j < kCPW; ++j) {
+          const int rho = kCPW * kw + j;
           if (rho >= R) continue;
           const float v = __uint_as_float(o[j]) * inv[j];
           const size_t oi = out_index(rho) * kD + d;
