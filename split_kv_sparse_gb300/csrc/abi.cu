@@ -733,6 +733,9 @@ int sdpa_combine_impl(const sdpa_plan_t* plan, int total_q, const void* workspac
   c.lse_out = lse_out;
   c.amax = amax_out;
   c.num_sms = dev->num_sms;
+  // per-sequence split counts: the slots past a sequence's own count hold LSE =
+  // -inf and an O that was never written, so nothing is read before its weight
+  c.sparse_splits = plan->adaptive_splits;
   return cuda_status(skv::launch_combine(c, zero_amax, /*pdl=*/true, static_cast<cudaStream_t>(stream)));
 }
 

@@ -80,9 +80,13 @@ __global__ void __launch_bounds__(kWarps * 32, kBatch == 8 ? 4 : 1) combine_kern
     // The first kBatch splits' slices are requested together with the LSEs, before
     // the weights are known (one memory round trip for S <= kBatch); a split whose
     // weight turns out 0 (empty) is then skipped, whatever its slice holds.
+    // (With sparse splits — a plan whose slots are mostly empty for most rows —
+    // the slices are requested only once the weights are known.)
     float4 x[kBatch];
+    if (!a.sparse_splits) {
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) x[u] = u < S ? load(u) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int u = 0; u < kBatch; ++u) x[u] = u < S ? load(u) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     const float l0 = lane < S ? a.lse_acc[static_cast<size_t>(lane) * rows + row] : -INFINITY;
     const float l1 = lane + 32 < S ? a.lse_acc[static_cast<size_t>(lane + 32) * rows + row] : -INFINITY;
     const float M = warp_max(fmaxf(l0, l1));
@@ -91,6 +95,11 @@ __global__ void __launch_bounds__(kWarps * 32, kBatch == 8 ? 4 : 1) combine_kern
     const float w1 = (l1 == -INFINITY) ? 0.f : exp2f(l1 - M);
     const float wsum = warp_sum(w0 + w1);
     auto weight = [&](int s) { return __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31); };
+    if (a.sparse_splits) {
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        x[u] = (u < S && weight(u) != 0.f) ? load(u) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 
     // acc = sum over s, in split order, of w_s * O_s
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);

@@ -95,6 +95,8 @@ struct CombineArgs {
   // one range was finished by the decode kernel and is left alone.
   int bal_nb, bal_units, bal_ctas;
   int num_sms;          // SMs of the device (caps the grid; 0: one CTA per 8 items)
+  int sparse_splits;    // most split slots of most rows are empty (LSE -inf): load a
+                        // slice only once its weight is known to be non-zero
 };
 // zero_amax: clear *amax first (a memset on the stream); pdl: launch as a
 // programmatic dependent of the preceding kernel on the stream.
