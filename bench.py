@@ -192,6 +192,17 @@ def unique_bytes(s_q: int) -> int:
 LAYERS_OVERRIDE = 0
 
 
+def tail_shape(plan, s_q: int):
+    """(first cut token, splits) when the plan's one-split grid cuts its last wave
+    (r tokens) into min(num_blocks, SMs // r) >= 3 splits; None otherwise."""
+    W = plan.num_sms
+    if plan.tail_ctas <= 0 or plan.num_splits != 1 or s_q <= W:
+        return None
+    r = s_q - (-(-s_q // W) - 1) * W
+    st = min(plan.num_blocks, min(plan.tail_ctas, W) // r)
+    return (s_q - r, st) if st >= 3 else None
+
+
 def layers_for(s_q: int, l2_bytes: int) -> int:
     """How many per-layer caches (and query/index sets) a timed run rotates through so
     that what one call reads has left L2 by the time the same layer comes round again:
@@ -228,6 +239,8 @@ class Case:
         if self.balanced:
             self.P, self.per, self.cut, self.pieces = balanced_schedule(self.s_q, self.plan.num_blocks,
                                                                         self.plan.num_sms)
+        # a one-split grid of more than one wave cuts its last wave's tokens into splits
+        self.tail = tail_shape(self.plan, self.s_q)
         # calls on one stream run one after another, so the layers share one workspace
         self.ws = (torch.empty(self.plan.workspace_bytes, dtype=torch.uint8, device=dev)
                    if self.plan.workspace_bytes else None)
@@ -255,15 +268,20 @@ class Case:
 
     def launches(self) -> int:
         """Kernels one call launches."""
-        return 1 if (self.S == 1 and not self.balanced) else 2
+        return 1 if (self.S == 1 and not self.balanced and self.tail is None) else 2
 
     def schedule(self) -> str:
         if self.balanced:
             return (f"balanced: {self.P} CTAs x <= {self.per} blocks of 64 rows; "
                     f"{self.cut} of {self.s_q} tokens cut into {self.pieces} pieces, folded by the combine")
         D = self.plan.dim_groups
-        return (f"uniform: {self.S} split(s) per token x {D} dim group(s), {self.s_q * self.S * D} CTAs"
-                + (", bf16 partials" if self.plan.partial_bf16 else ""))
+        bf = ", bf16 partials" if self.plan.partial_bf16 else ""
+        if self.tail is not None:
+            first, st = self.tail
+            r = self.s_q - first
+            return (f"uniform: 1 split per token, {first} whole tokens + the last wave's {r} cut into {st} splits "
+                    f"({first + r * st} CTAs), the tail folded by the combine" + bf)
+        return f"uniform: {self.S} split(s) per token x {D} dim group(s), {self.s_q * self.S * D} CTAs" + bf
 
     def _capture(self, fn):
         torch = self.torch

@@ -110,6 +110,10 @@ typedef struct {
                            dim_groups SMs (used when s_q_max * num_splits leaves SMs idle) */
   int32_t partial_bf16; /* 0 (default): O partials in fp32; 1: in bf16 (set with
                            mla_plan_set_partials_bf16; LSE partials stay fp32)     */
+  int32_t tail_ctas;    /* > 0: a call whose one-split grid would leave a last wave
+                           at most a third full cuts that wave's tokens into splits
+                           (see "Tail of the grid" below), in at most this many CTAs;
+                           the workspace holds their partials                      */
   uint64_t o_acc_bytes;     /* num_splits * s_q_max * h_q * d_v * (4, or 2 with bf16
                                partials)                                           */
   uint64_t lse_acc_offset;  /* o_acc_bytes rounded up to 256                       */
@@ -117,6 +121,23 @@ typedef struct {
   uint64_t workspace_bytes; /* what every call on this plan needs; 0 when num_splits == 1
                                and balanced_ctas == 0                              */
 } mla_plan_t;
+
+/* Tail of the grid (plan->tail_ctas > 0; automatic plans with num_splits == 1 and
+ * s_q_max > num_sms). One split per token runs s_q CTAs in ceil(s_q / num_sms)
+ * waves; when the last wave would hold r tokens and S_t = min(num_blocks,
+ * floor(num_sms / r)) >= 3, a call cuts each of those r tokens into S_t splits
+ * (near-equal block ranges, the first num_blocks mod S_t one block longer), run
+ * after the whole tokens, and folds them with the combine over their rows only:
+ * the last wave then walks about num_blocks / S_t blocks instead of num_blocks.
+ * Measured on GB300 (152 SMs, topk 640, 10 blocks; back-to-back calls, e4m3 out):
+ * s_q 153: 59.4 -> 46.1 us, 160: 59.9 -> 49.0, 176: 60.9 -> 49.8, 190: 61.1 ->
+ * 53.2, 200: 61.1 -> 55.7, 320: 89.3 -> 84.1; with two splits (s_q 212, 228) no
+ * gain, hence the bound S_t >= 3. The workspace holds [S_t][r][64][512] O
+ * partials (fp32, or bf16 with mla_plan_set_partials_bf16) and [S_t][r][64] LSE
+ * partials at the next 256-byte boundary, S_t * r <= num_sms. The pages have no
+ * counterpart (their grids are one wave); it reuses their partial / LSE protocol.
+ * The no-allocation entry point never cuts a tail; setting tail_ctas to 0 in a
+ * plan turns it off. */
 
 /* Balanced schedule of the one-shot call (plan->balanced_ctas > 0). FlashMLA PR #25
  * ("Measured") shows the (token, split) grid losing at s_q >= 96, where s_q * S
@@ -434,7 +455,7 @@ MLA_API const char* mla_status_string(int status);
 
 /* ABI version of this header (bumped on any signature or layout change). */
 MLA_API int mla_abi_version(void);
-#define MLA_ABI_VERSION 1
+#define MLA_ABI_VERSION 2
 
 #ifdef __cplusplus
 }

@@ -45,7 +45,7 @@ class MlaPlan(ctypes.Structure):
                 ("d_v", ctypes.c_int32), ("topk", ctypes.c_int32), ("block_rows", ctypes.c_int32),
                 ("num_blocks", ctypes.c_int32), ("num_splits", ctypes.c_int32), ("num_sms", ctypes.c_int32),
                 ("balanced_ctas", ctypes.c_int32), ("dim_groups", ctypes.c_int32),
-                ("partial_bf16", ctypes.c_int32), ("o_acc_bytes", ctypes.c_uint64),
+                ("partial_bf16", ctypes.c_int32), ("tail_ctas", ctypes.c_int32), ("o_acc_bytes", ctypes.c_uint64),
                 ("lse_acc_offset", ctypes.c_uint64), ("lse_acc_bytes", ctypes.c_uint64),
                 ("workspace_bytes", ctypes.c_uint64)]
 

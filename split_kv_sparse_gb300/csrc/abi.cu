@@ -146,6 +146,22 @@ int dim_groups_for(int64_t jobs, int num_sms) {
   return 1;
 }
 
+// The tail of a one-split grid for s_q tokens: when its last wave would hold
+// r <= num_sms / 3 tokens, those are cut into min(num_blocks, num_sms / r) >= 3
+// splits (two splits measured no faster than the uncut wave). Returns false
+// when the plan or the call has no tail.
+bool tail_of(const mla_plan_t* p, int s_q, int* first, int* splits) {
+  if (p->tail_ctas <= 0 || p->num_splits != 1 || s_q <= p->num_sms) return false;
+  const int W = p->num_sms;
+  const int waves = (s_q + W - 1) / W;
+  const int r = s_q - (waves - 1) * W;
+  const int st = std::min(p->num_blocks, std::min(p->tail_ctas, W) / r);
+  if (st < 3) return false;
+  *first = s_q - r;
+  *splits = st;
+  return true;
+}
+
 // The workspace of a plan from its split count, schedule and partial type: the
 // split layout ([S][s_q_max][64][512] O partials of 4 or 2 bytes, then
 // [S][s_q_max][64] fp32 LSE partials at the next 256-byte boundary), large
@@ -159,6 +175,8 @@ void plan_workspace(mla_plan_t* p) {
     p->lse_acc_bytes = static_cast<uint64_t>(p->num_splits) * p->s_q_max * p->h_q * 4ull;
     p->workspace_bytes = round_up(p->lse_acc_offset + p->lse_acc_bytes, 256);
   }
+  if (p->tail_ctas > 0)   // at most tail_ctas (split, tail token) slots
+    p->workspace_bytes = std::max<uint64_t>(p->workspace_bytes, split_workspace_bytes(p->tail_ctas, 1, esz));
   if (p->balanced_ctas > 0)
     p->workspace_bytes = std::max<uint64_t>(
         p->workspace_bytes, split_workspace_bytes(balanced_slots(p->s_q_max, p->num_blocks, p->num_sms), p->s_q_max, esz));
@@ -299,6 +317,8 @@ int mla_decode_plan(int s_q_max, int h_q, int d_qk, int d_v, int topk, int num_s
     const int64_t units = static_cast<int64_t>(s_q_max) * nblk;
     out->balanced_ctas = static_cast<int32_t>(std::min<int64_t>(units, num_sms));
   }
+  // an automatic one-split grid of more than one wave may cut its last wave's tokens
+  if (force_splits == 0 && S == 1 && s_q_max > num_sms && nblk >= 2) out->tail_ctas = num_sms;
   plan_workspace(out);
   return MLA_OK;
 }
@@ -378,6 +398,78 @@ int mla_combine_impl(const mla_plan_t* plan, int s_q, const void* workspace, con
   c.amax = amax_out;
   c.num_sms = dev->num_sms;
   return cuda_status(skv::launch_combine(c, zero_amax, /*pdl=*/true, static_cast<cudaStream_t>(stream)));
+}
+
+// The one-split grid with its tail cut (tail_of): whole tokens 0 .. tail_first-1
+// write their final rows in the decode kernel; the tail tokens' splits write
+// partials ([tail_splits][r][64][512], LSE [tail_splits][r][64]) that the
+// combine, launched as its programmatic dependent, folds into their rows.
+int mla_decode_tail(const mla_plan_t* plan, int s_q, const void* q, const void* kv, int64_t n_kv, const int32_t* idx,
+                    float sm_scale, const float* sink, int out_dtype, float out_inv_scale, void* out, float* lse_out,
+                    float* amax_out, void* workspace, int tail_first, int tail_splits, void* stream) {
+  int st = check_mla_inputs(s_q, plan->topk, q, kv, n_kv, idx, sm_scale);
+  if (st != MLA_OK) return st;
+  if (out == nullptr || !aligned(out, 16) || !valid_out_dtype(out_dtype)) return MLA_ERR_INVALID_ARG;
+  if (out_dtype == MLA_OUT_E4M3 && !std::isfinite(out_inv_scale)) return MLA_ERR_INVALID_ARG;
+  const int esz = plan->partial_bf16 ? 2 : 4;
+  const int r = s_q - tail_first;
+  const uint64_t o_bytes = static_cast<uint64_t>(tail_splits) * r * kMlaHeads * kMlaDv * static_cast<uint64_t>(esz);
+  if (workspace == nullptr || !aligned(workspace, 256) ||
+      plan->workspace_bytes < split_workspace_bytes(tail_splits, r, esz))
+    return MLA_ERR_WORKSPACE;
+  DeviceState* dev = nullptr;
+  if ((st = device_state(&dev)) != MLA_OK) return st;
+  CUtensorMap tq;
+  if ((st = mla_q_tensor_map(s_q, q, &tq)) != MLA_OK) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (amax_out != nullptr) {
+    if ((st = cuda_status(cudaMemsetAsync(amax_out, 0, sizeof(float), cs))) != MLA_OK) return st;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  skv::MlaArgs a{};
+  a.kv = static_cast<const uint8_t*>(kv);
+  a.idx = idx;
+  a.s_q = s_q;
+  a.topk = plan->topk;
+  a.n_kv = static_cast<int>(n_kv);
+  a.num_splits = 1;
+  a.num_blocks = plan->num_blocks;
+  a.dim_groups = 1;
+  a.sched = 0;
+  a.direct_whole = 1;
+  a.tail_first = tail_first;
+  a.tail_splits = tail_splits;
+  a.scale_log2 = sm_scale * 1.4426950408889634f;
+  a.o_acc = reinterpret_cast<float*>(ws);
+  a.lse_acc = reinterpret_cast<float*>(ws + round_up(o_bytes, 256));
+  a.partial_bf16 = plan->partial_bf16;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.inv_scale = out_inv_scale;
+  a.lse_out = lse_out;
+  a.sink = sink;
+  a.amax = amax_out;
+  a.status = dev->status;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.drain_limit_ns = kWaitLimitNs;
+  if ((st = cuda_status(skv::launch_mla_decode(tq, a, cs))) != MLA_OK) return st;
+  const size_t out_esz = out_dtype == MLA_OUT_F32 ? 4 : (out_dtype == MLA_OUT_BF16 ? 2 : 1);
+  skv::CombineArgs c{};
+  c.o_acc = a.o_acc;
+  c.lse_acc = a.lse_acc;
+  c.partial_bf16 = a.partial_bf16;
+  c.num_splits = tail_splits;
+  c.rows = r * kMlaHeads;
+  c.heads = kMlaHeads;
+  c.d = kMlaDv;
+  c.sink = sink;
+  c.out = static_cast<uint8_t*>(out) + static_cast<size_t>(tail_first) * kMlaHeads * kMlaDv * out_esz;
+  c.out_dtype = out_dtype;
+  c.inv_scale = out_inv_scale;
+  c.lse_out = lse_out != nullptr ? lse_out + static_cast<size_t>(tail_first) * kMlaHeads : nullptr;
+  c.amax = amax_out;
+  c.num_sms = dev->num_sms;
+  return cuda_status(skv::launch_combine(c, /*zero_amax=*/false, /*pdl=*/true, cs));
 }
 
 // The one-shot call on the balanced schedule: every SM walks (nearly) the same
@@ -541,6 +633,10 @@ int mla_sparse_decode(const mla_plan_t* plan, int s_q, const void* q, const void
       balanced_per(s_q, plan->num_blocks, plan->num_sms) > 0)
     return mla_decode_balanced(plan, s_q, q, kv, n_kv, idx, sm_scale, sink, out_dtype, out_inv_scale, out, lse_out,
                                amax_out, workspace, stream);
+  int tail_first = 0, tail_splits = 0;
+  if (s_q >= 1 && s_q <= plan->s_q_max && tail_of(plan, s_q, &tail_first, &tail_splits))
+    return mla_decode_tail(plan, s_q, q, kv, n_kv, idx, sm_scale, sink, out_dtype, out_inv_scale, out, lse_out,
+                           amax_out, workspace, tail_first, tail_splits, stream);
   if (plan->num_splits == 1) {
     if (s_q > plan->s_q_max) return MLA_ERR_INVALID_ARG;
     return mla_direct_impl(s_q, plan->topk, q, kv, n_kv, idx, sm_scale, sink, out_dtype, out_inv_scale, out,
@@ -900,6 +996,7 @@ int mla_sparse_decode_noalloc(int s_q, int topk, const void* q, const void* kv, 
   if (st != MLA_OK) return st;
   // the (token, split) jobs: their workspace is num_splits * s_q partial rows
   plan.balanced_ctas = 0;
+  plan.tail_ctas = 0;
   plan.workspace_bytes = plan.num_splits > 1 ? round_up(plan.lse_acc_offset + plan.lse_acc_bytes, 256) : 0;
   if (plan.workspace_bytes > MLA_NOALLOC_SCRATCH_BYTES) return MLA_ERR_WORKSPACE;
   void* scratch = nullptr;

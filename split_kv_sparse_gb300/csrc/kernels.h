@@ -31,6 +31,12 @@ struct MlaArgs {
   int num_ctas;         // balanced schedule: CTAs (<= s_q * num_blocks)
   int direct_whole;     // a job that covers a whole token writes the final output
                         // (sink, cast, LSE, amax) instead of a partial
+  int tail_first;       // uniform schedule with tail_splits > 0: tokens 0 .. tail_first - 1
+  int tail_splits;      // run whole on CTAs 0 .. tail_first - 1; tokens tail_first .. s_q - 1
+                        // are cut into tail_splits splits, CTA tail_first + k running split
+                        // k % tail_splits of tail token k / tail_splits, whose partial goes to
+                        // slot (split, tail token) of the workspace (needs num_splits ==
+                        // dim_groups == 1); 0: no tail
   float scale_log2;     // sm_scale * log2(e)
   // Partial workspace: [slot][s_q][64][512] and [slot][s_q][64]. Uniform: slot =
   // the split. Balanced: slot = a piece's place among the pieces of its token

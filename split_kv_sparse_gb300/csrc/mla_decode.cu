@@ -166,7 +166,23 @@ __device__ __forceinline__ int num_jobs(const MlaArgs& a) {
 template <int kSched>
 __device__ __forceinline__ Job job_at(const MlaArgs& a, int j) {
   Job r;
-  if (kSched == 0) {
+  if (kSched == 0 && a.tail_splits > 0 && static_cast<int>(blockIdx.x) >= a.tail_first) {
+    // a piece of a token of the tail: near-equal block runs as for S splits
+    const int S = a.tail_splits, nt = a.s_q - a.tail_first;
+    const int k = static_cast<int>(blockIdx.x) - a.tail_first;
+    const int tt = k / S, s = k - tt * S;
+    r.nq = 4;
+    r.q0 = 0;
+    const int base = a.num_blocks / S, rem = a.num_blocks - base * S;
+    const int blk0 = s * base + min(s, rem), nblk = base + (s < rem ? 1 : 0);
+    r.t = a.tail_first + tt;
+    r.row0 = min(blk0 * kMlaBlockRows, a.topk);
+    r.row1 = min((blk0 + nblk) * kMlaBlockRows, a.topk);
+    r.nsteps = (r.row1 - r.row0 + kMlaBlockRows - 1) / kMlaBlockRows;
+    r.kind = J_PARTIAL;
+    r.slot = s;
+    r.out_row = (static_cast<size_t>(s) * nt + tt) * kMlaHeads;
+  } else if (kSched == 0) {
     const int S = a.num_splits, D = a.dim_groups;
     const int job = static_cast<int>(blockIdx.x) / D, dg = static_cast<int>(blockIdx.x) - job * D;
     const int t = job / S, s = job - t * S;
@@ -1056,9 +1072,15 @@ cudaError_t prepare_mla_kernels() {
 
 cudaError_t launch_mla_decode(const CUtensorMap& tm_q, const MlaArgs& a, cudaStream_t stream) {
   if (a.sched == 0 && a.dim_groups != 1 && a.dim_groups != 2 && a.dim_groups != 4) return cudaErrorInvalidValue;
-  const dim3 grid(a.sched == 0 ? static_cast<unsigned>(a.s_q) * static_cast<unsigned>(a.num_splits) *
-                                     static_cast<unsigned>(a.dim_groups)
-                               : static_cast<unsigned>(a.num_ctas));
+  if (a.sched == 0 && a.tail_splits > 0 && (a.num_splits != 1 || a.dim_groups != 1 || a.tail_first < 0 ||
+                                            a.tail_first >= a.s_q))
+    return cudaErrorInvalidValue;
+  const dim3 grid(a.sched != 0 ? static_cast<unsigned>(a.num_ctas)
+                  : a.tail_splits > 0
+                      ? static_cast<unsigned>(a.tail_first) +
+                            static_cast<unsigned>(a.s_q - a.tail_first) * static_cast<unsigned>(a.tail_splits)
+                      : static_cast<unsigned>(a.s_q) * static_cast<unsigned>(a.num_splits) *
+                            static_cast<unsigned>(a.dim_groups));
   // launched as a programmatic dependent of the preceding kernel on the stream:
   // its CTAs may become resident and set up while that kernel finishes
   cudaLaunchConfig_t cfg = {};

@@ -121,9 +121,14 @@ def test_plan_is_deterministic_and_follows_rule():
                 assert p1.balanced_ctas == C
                 # CTAs per (token, split) job: 4, 2 or 1, whatever still fits the SMs
                 assert p1.dim_groups == next(d for d in (4, 2, 1) if s_q * S * d <= sms or d == 1)
-                assert p1.workspace_bytes == (max(uni, partials) if enabled else uni)
+                # a one-split grid of more than one wave may cut its last wave's
+                # tokens: up to num_sms (split, token) partial slots
+                tail = sms if (S == 1 and s_q > sms and nblk >= 2) else 0
+                assert p1.tail_ctas == tail
+                tail_ws = ru(ru(tail * 64 * 512 * 4) + tail * 64 * 4) if tail else 0
+                assert p1.workspace_bytes == max(max(uni, partials) if enabled else uni, tail_ws)
                 pf = b.mla_decode_plan(s_q, topk, num_sms=sms, force_splits=S)
-                assert pf.balanced_ctas == 0 and (pf.workspace_bytes == 0) == (S == 1)
+                assert pf.balanced_ctas == 0 and pf.tail_ctas == 0 and (pf.workspace_bytes == 0) == (S == 1)
                 pb = b.mla_decode_plan(s_q, topk, num_sms=sms, force_splits=b.MLA_FORCE_BALANCED)
                 assert pb.num_splits == S
                 assert pb.balanced_ctas == (min(sms, s_q * nblk) if applies else 0)
