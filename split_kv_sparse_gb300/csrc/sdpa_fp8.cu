@@ -49,7 +49,7 @@ constexpr int kCPW = 64 / kKeyWarps;       // O^T columns (query rows) per softm
 constexpr int kConverters = 4;             // the last 4 warps: one key row of the V tile per thread
 constexpr int kFirstConverter = 2 + kSoftmaxWarps;
 constexpr int kThreads = 32 * (kFirstConverter + kConverters);
-static_assert(kKeyWarps == 2 || kKeyWarps == 4, "the TMEM load shapes below");
+static_assert(kKeyWarps == 2, "the TMEM load shapes and the 32-score max below");
 constexpr int kD = 128;
 constexpr int kTile = 128;                 // keys per tile (split unit)
 constexpr int kRows = 64;                  // query rows per job (tokens x group heads)
@@ -461,17 +461,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (w && key0 + kKPT - 1 <= lim_r) {
         if (raw_ok) {
 #pragma unroll
-          for (int i = 0; i < kKPT; ++i) {
-            x[i] = __uint_as_float(raw[i]);
-            mx = fmaxf(mx, x[i]);
-          }
+          for (int i = 0; i < kKPT; ++i) x[i] = __uint_as_float(raw[i]);
         } else {
 #pragma unroll
-          for (int i = 0; i < kKPT; ++i) {
-            x[i] = __uint_as_float(raw[i]) * sc;
-            mx = fmaxf(mx, x[i]);
-          }
+          for (int i = 0; i < kKPT; ++i) x[i] = __uint_as_float(raw[i]) * sc;
         }
+        mx = max32(x);
       } else if (w) {
 #pragma unroll
         for (int i = 0; i < kKPT; ++i) {

@@ -14,6 +14,24 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction (the three-input form of max.f32, sm_100 family).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// The max of 32 values: 17 operations, four deep (a chain of two-input maxima
+// takes 31).
+__device__ __forceinline__ float max32(const float (&x)[32]) {
+  float a[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i) a[i] = fmax3(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
+  a[10] = fmaxf(x[30], x[31]);
+  const float b0 = fmax3(a[0], a[1], a[2]), b1 = fmax3(a[3], a[4], a[5]), b2 = fmax3(a[6], a[7], a[8]);
+  return fmaxf(fmax3(b0, b1, b2), fmaxf(a[9], a[10]));
+}
+
 // Waits without looking at the abort flag (used to drain in-flight copies on abort).
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
