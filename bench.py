@@ -193,14 +193,18 @@ LAYERS_OVERRIDE = 0
 
 
 def tail_shape(plan, s_q: int):
-    """(first cut token, splits) when the plan's one-split grid cuts its last wave
-    (r tokens) into min(num_blocks, SMs // r) >= 3 splits; None otherwise."""
+    """(first tail token, splits, dim groups) when the plan's one-split grid cuts its
+    last wave (r tokens): into min(num_blocks, SMs // r) >= 3 splits (dim groups 0),
+    else, when 2 r <= SMs, into two dim groups per token (splits 0); None otherwise."""
     W = plan.num_sms
     if plan.tail_ctas <= 0 or plan.num_splits != 1 or s_q <= W:
         return None
+    C = min(plan.tail_ctas, W)
     r = s_q - (-(-s_q // W) - 1) * W
-    st = min(plan.num_blocks, min(plan.tail_ctas, W) // r)
-    return (s_q - r, st) if st >= 3 else None
+    st = min(plan.num_blocks, C // r)
+    if st >= 3:
+        return (s_q - r, st, 0)
+    return (s_q - r, 0, 2) if 2 * r <= C else None
 
 
 def layers_for(s_q: int, l2_bytes: int) -> int:
@@ -268,7 +272,8 @@ class Case:
 
     def launches(self) -> int:
         """Kernels one call launches."""
-        return 1 if (self.S == 1 and not self.balanced and self.tail is None) else 2
+        split_tail = self.tail is not None and self.tail[1] > 0
+        return 1 if (self.S == 1 and not self.balanced and not split_tail) else 2
 
     def schedule(self) -> str:
         if self.balanced:
@@ -277,10 +282,13 @@ class Case:
         D = self.plan.dim_groups
         bf = ", bf16 partials" if self.plan.partial_bf16 else ""
         if self.tail is not None:
-            first, st = self.tail
+            first, st, dg = self.tail
             r = self.s_q - first
-            return (f"uniform: 1 split per token, {first} whole tokens + the last wave's {r} cut into {st} splits "
-                    f"({first + r * st} CTAs), the tail folded by the combine" + bf)
+            if st:
+                return (f"uniform: 1 split per token, {first} whole tokens + the last wave's {r} cut into {st} "
+                        f"splits ({first + r * st} CTAs), the tail folded by the combine" + bf)
+            return (f"uniform: 1 split per token, {first} whole tokens + the last wave's {r} on {dg} CTAs each "
+                    f"(a share of the dims each; {first + r * dg} CTAs, no combine)")
         return f"uniform: {self.S} split(s) per token x {D} dim group(s), {self.s_q * self.S * D} CTAs" + bf
 
     def _capture(self, fn):

@@ -111,7 +111,7 @@ typedef struct {
   int32_t partial_bf16; /* 0 (default): O partials in fp32; 1: in bf16 (set with
                            mla_plan_set_partials_bf16; LSE partials stay fp32)     */
   int32_t tail_ctas;    /* > 0: a call whose one-split grid would leave a last wave
-                           at most a third full cuts that wave's tokens into splits
+                           at most half full cuts that wave's tokens into splits or dims
                            (see "Tail of the grid" below), in at most this many CTAs;
                            the workspace holds their partials                      */
   uint64_t o_acc_bytes;     /* num_splits * s_q_max * h_q * d_v * (4, or 2 with bf16
@@ -132,7 +132,11 @@ typedef struct {
  * Measured on GB300 (152 SMs, topk 640, 10 blocks; back-to-back calls, e4m3 out):
  * s_q 153: 59.4 -> 46.1 us, 160: 59.9 -> 49.0, 176: 60.9 -> 49.8, 190: 61.1 ->
  * 53.2, 200: 61.1 -> 55.7, 320: 89.3 -> 84.1; with two splits (s_q 212, 228) no
- * gain, hence the bound S_t >= 3. The workspace holds [S_t][r][64][512] O
+ * gain, hence the bound S_t >= 3. Otherwise, when 2 r <= num_sms, each of the r
+ * tokens runs whole on two CTAs, each with half of the output dims (the full QK
+ * and softmax, half the PV, final rows; no partials, no combine), measured s_q
+ * 212: 61.5 -> 58.4 us, 220: 61.7 -> 57.9, 228: 61.6 -> 59.1 (where two splits
+ * gained nothing). The split form's workspace holds [S_t][r][64][512] O
  * partials (fp32, or bf16 with mla_plan_set_partials_bf16) and [S_t][r][64] LSE
  * partials at the next 256-byte boundary, S_t * r <= num_sms. The pages have no
  * counterpart (their grids are one wave); it reuses their partial / LSE protocol.

@@ -146,19 +146,24 @@ int dim_groups_for(int64_t jobs, int num_sms) {
   return 1;
 }
 
-// The tail of a one-split grid for s_q tokens: when its last wave would hold
-// r <= num_sms / 3 tokens, those are cut into min(num_blocks, num_sms / r) >= 3
-// splits (two splits measured no faster than the uncut wave). Returns false
-// when the plan or the call has no tail.
-bool tail_of(const mla_plan_t* p, int s_q, int* first, int* splits) {
+// The tail of a one-split grid for s_q tokens, whose last wave would hold r
+// tokens: with min(num_blocks, num_sms / r) >= 3 splits those tokens are cut into
+// that many splits (*splits; two splits measured no faster than the uncut
+// wave); else, when 2 r <= num_sms, each runs whole on two CTAs with half of the
+// dims each (*dgroups = 2; full QK, half the PV, final rows, no combine).
+// Returns false when the plan or the call has no tail.
+bool tail_of(const mla_plan_t* p, int s_q, int* first, int* splits, int* dgroups) {
   if (p->tail_ctas <= 0 || p->num_splits != 1 || s_q <= p->num_sms) return false;
-  const int W = p->num_sms;
+  const int W = p->num_sms, C = std::min(p->tail_ctas, W);
   const int waves = (s_q + W - 1) / W;
   const int r = s_q - (waves - 1) * W;
-  const int st = std::min(p->num_blocks, std::min(p->tail_ctas, W) / r);
-  if (st < 3) return false;
+  const int st = std::min(p->num_blocks, C / r);
   *first = s_q - r;
-  *splits = st;
+  *splits = 0;
+  *dgroups = 0;
+  if (st >= 3) *splits = st;
+  else if (2 * r <= C) *dgroups = 2;
+  else return false;
   return true;
 }
 
@@ -578,7 +583,7 @@ namespace {
 // device's SM count).
 int mla_direct_impl(int s_q, int topk, const void* q, const void* kv, int64_t n_kv, const int32_t* idx,
                     float sm_scale, const float* sink, int out_dtype, float out_inv_scale, void* out, float* lse_out,
-                    float* amax_out, int dim_groups, void* stream) {
+                    float* amax_out, int dim_groups, void* stream, int tail_first = 0, int tail_dgroups = 0) {
   int st = check_mla_inputs(s_q, topk, q, kv, n_kv, idx, sm_scale);
   if (st != MLA_OK) return st;
   if (out == nullptr || !aligned(out, 16) || !valid_out_dtype(out_dtype)) return MLA_ERR_INVALID_ARG;
@@ -602,6 +607,8 @@ int mla_direct_impl(int s_q, int topk, const void* q, const void* kv, int64_t n_
   a.dim_groups = dim_groups > 0 ? dim_groups : dim_groups_for(s_q, dev->num_sms);
   a.sched = 0;
   a.direct_whole = 1;
+  a.tail_first = tail_first;
+  a.tail_dgroups = tail_dgroups;
   a.scale_log2 = sm_scale * 1.4426950408889634f;
   a.out = out;
   a.out_dtype = out_dtype;
@@ -633,10 +640,14 @@ int mla_sparse_decode(const mla_plan_t* plan, int s_q, const void* q, const void
       balanced_per(s_q, plan->num_blocks, plan->num_sms) > 0)
     return mla_decode_balanced(plan, s_q, q, kv, n_kv, idx, sm_scale, sink, out_dtype, out_inv_scale, out, lse_out,
                                amax_out, workspace, stream);
-  int tail_first = 0, tail_splits = 0;
-  if (s_q >= 1 && s_q <= plan->s_q_max && tail_of(plan, s_q, &tail_first, &tail_splits))
-    return mla_decode_tail(plan, s_q, q, kv, n_kv, idx, sm_scale, sink, out_dtype, out_inv_scale, out, lse_out,
-                           amax_out, workspace, tail_first, tail_splits, stream);
+  int tail_first = 0, tail_splits = 0, tail_dgroups = 0;
+  if (s_q >= 1 && s_q <= plan->s_q_max && tail_of(plan, s_q, &tail_first, &tail_splits, &tail_dgroups)) {
+    if (tail_splits > 0)
+      return mla_decode_tail(plan, s_q, q, kv, n_kv, idx, sm_scale, sink, out_dtype, out_inv_scale, out, lse_out,
+                             amax_out, workspace, tail_first, tail_splits, stream);
+    return mla_direct_impl(s_q, plan->topk, q, kv, n_kv, idx, sm_scale, sink, out_dtype, out_inv_scale, out,
+                           lse_out, amax_out, 1, stream, tail_first, tail_dgroups);
+  }
   if (plan->num_splits == 1) {
     if (s_q > plan->s_q_max) return MLA_ERR_INVALID_ARG;
     return mla_direct_impl(s_q, plan->topk, q, kv, n_kv, idx, sm_scale, sink, out_dtype, out_inv_scale, out,

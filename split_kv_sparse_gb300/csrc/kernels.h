@@ -37,6 +37,10 @@ struct MlaArgs {
                         // k % tail_splits of tail token k / tail_splits, whose partial goes to
                         // slot (split, tail token) of the workspace (needs num_splits ==
                         // dim_groups == 1); 0: no tail
+  int tail_dgroups;     // uniform schedule, tail_splits == 0: tokens tail_first .. s_q - 1 run
+                        // whole on tail_dgroups (2 or 4) CTAs each, CTA tail_first + k taking
+                        // dim group k % tail_dgroups of tail token k / tail_dgroups and
+                        // writing its final rows (needs num_splits == dim_groups == 1); 0: no
   float scale_log2;     // sm_scale * log2(e)
   // Partial workspace: [slot][s_q][64][512] and [slot][s_q][64]. Uniform: slot =
   // the split. Balanced: slot = a piece's place among the pieces of its token

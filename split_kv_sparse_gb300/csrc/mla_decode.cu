@@ -166,7 +166,21 @@ __device__ __forceinline__ int num_jobs(const MlaArgs& a) {
 template <int kSched>
 __device__ __forceinline__ Job job_at(const MlaArgs& a, int j) {
   Job r;
-  if (kSched == 0 && a.tail_splits > 0 && static_cast<int>(blockIdx.x) >= a.tail_first) {
+  if (kSched == 0 && a.tail_dgroups > 0 && static_cast<int>(blockIdx.x) >= a.tail_first) {
+    // a tail token run whole on tail_dgroups CTAs, each with its share of the dims
+    const int D = a.tail_dgroups;
+    const int k = static_cast<int>(blockIdx.x) - a.tail_first;
+    const int tt = k / D, dg = k - tt * D;
+    r.nq = 4 / D;
+    r.q0 = dg * r.nq;
+    r.t = a.tail_first + tt;
+    r.row0 = 0;
+    r.row1 = a.topk;
+    r.nsteps = a.num_blocks;
+    r.kind = J_FINAL;
+    r.slot = 0;
+    r.out_row = static_cast<size_t>(r.t) * kMlaHeads;
+  } else if (kSched == 0 && a.tail_splits > 0 && static_cast<int>(blockIdx.x) >= a.tail_first) {
     // a piece of a token of the tail: near-equal block runs as for S splits
     const int S = a.tail_splits, nt = a.s_q - a.tail_first;
     const int k = static_cast<int>(blockIdx.x) - a.tail_first;
@@ -1073,12 +1087,17 @@ cudaError_t prepare_mla_kernels() {
 cudaError_t launch_mla_decode(const CUtensorMap& tm_q, const MlaArgs& a, cudaStream_t stream) {
   if (a.sched == 0 && a.dim_groups != 1 && a.dim_groups != 2 && a.dim_groups != 4) return cudaErrorInvalidValue;
   if (a.sched == 0 && a.tail_splits > 0 && (a.num_splits != 1 || a.dim_groups != 1 || a.tail_first < 0 ||
-                                            a.tail_first >= a.s_q))
+                                            a.tail_first >= a.s_q || a.tail_dgroups != 0))
     return cudaErrorInvalidValue;
+  if (a.sched == 0 && a.tail_dgroups != 0 &&
+      ((a.tail_dgroups != 2 && a.tail_dgroups != 4) || a.num_splits != 1 || a.dim_groups != 1 ||
+       a.tail_first < 0 || a.tail_first >= a.s_q || !a.direct_whole))
+    return cudaErrorInvalidValue;
+  const int tail_per = a.tail_splits > 0 ? a.tail_splits : a.tail_dgroups;   // CTAs per tail token
   const dim3 grid(a.sched != 0 ? static_cast<unsigned>(a.num_ctas)
-                  : a.tail_splits > 0
+                  : tail_per > 0
                       ? static_cast<unsigned>(a.tail_first) +
-                            static_cast<unsigned>(a.s_q - a.tail_first) * static_cast<unsigned>(a.tail_splits)
+                            static_cast<unsigned>(a.s_q - a.tail_first) * static_cast<unsigned>(tail_per)
                       : static_cast<unsigned>(a.s_q) * static_cast<unsigned>(a.num_splits) *
                             static_cast<unsigned>(a.dim_groups));
   // launched as a programmatic dependent of the preceding kernel on the stream:

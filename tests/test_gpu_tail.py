@@ -26,13 +26,17 @@ def _gpu():
 
 
 def tail_shape(s_q, nblk, sms):
-    """(first tail token, splits) of the tail rule, or None: restated from the header."""
+    """(first tail token, splits, dim groups) of the tail rule, or None: restated from
+    the header (splits when at least 3 fit, else two dim groups per token when 2 r
+    <= SMs)."""
     if s_q <= sms:
         return None
     waves = -(-s_q // sms)
     r = s_q - (waves - 1) * sms
     st = min(nblk, sms // r)
-    return (s_q - r, st) if st >= 3 else None
+    if st >= 3:
+        return (s_q - r, st, 0)
+    return (s_q - r, 0, 2) if 2 * r <= sms else None
 
 
 @pytest.mark.parametrize("s_q,topk,num_sms", [
@@ -40,8 +44,11 @@ def tail_shape(s_q, nblk, sms):
     (9, 640, 4),      # three waves, 1 tail token in 4 splits
     (13, 200, 6),     # ragged top-k (4 blocks, the last of 8 rows): 1 tail token, 4 one-block splits
     (21, 640, 10),    # 1 tail token in 10 one-block splits
-    (7, 128, 4),      # 2 blocks: 3 tail tokens, 1 split each would not pay -> no tail
-    (14, 640, 8),     # 6 tail tokens: 1 split each -> no tail
+    (7, 128, 4),      # 2 blocks: 3 tail tokens, too many for two CTAs each -> no tail
+    (14, 640, 8),     # 6 tail tokens: 1 split each, 12 CTAs for dims -> no tail
+    (11, 640, 8),     # 3 tail tokens: 2 splits would not pay -> two dim groups each
+    (12, 640, 8),     # 4 tail tokens on two dim groups each (8 CTAs)
+    (9, 200, 6),      # ragged top-k (4 blocks, the last of 8 rows): 3 tail tokens on two dim groups
 ])
 @pytest.mark.parametrize("with_sink", [False, True])
 def test_tail_matches_oracle(s_q, topk, num_sms, with_sink):
@@ -53,18 +60,21 @@ def test_tail_matches_oracle(s_q, topk, num_sms, with_sink):
     assert plan.num_splits == 1 and plan.tail_ctas == num_sms
     shape = tail_shape(s_q, plan.num_blocks, num_sms)
     assert (shape is None) == ((s_q, topk, num_sms) in ((7, 128, 4), (14, 640, 8)))
+    if (s_q, topk, num_sms) in ((11, 640, 8), (12, 640, 8), (9, 200, 6)):
+        assert shape[2] == 2
     assert_o_close(r["out"].numpy(), O)
     assert_lse_close(r["lse"], L)
 
 
+@pytest.mark.parametrize("s_q", [10, 12])
 @pytest.mark.parametrize("out_dtype", ["bf16", "e4m3"])
-def test_tail_casts_and_amax(out_dtype):
-    """Whole tokens are cast by the decode kernel and the tail tokens by the combine;
-    the amax covers both."""
-    inp = wl.mla_inputs(10, 32768, 640, seed=71, v_mean=1.0, with_sink=True)
+def test_tail_casts_and_amax(out_dtype, s_q):
+    """Whole tokens are cast by the decode kernel and the tail tokens by the combine
+    (s_q 10: 4 splits) or by their two dim-group CTAs (s_q 12); the amax covers all."""
+    inp = wl.mla_inputs(s_q, 32768, 640, seed=71, v_mean=1.0, with_sink=True)
     O, L = oracle_mla(inp)
     r = run_mla(inp, 0, out_dtype=out_dtype, inv_scale=64.0, with_amax=True, num_sms=8)
-    assert tail_shape(10, 10, 8) == (8, 4)
+    assert tail_shape(s_q, 10, 8) == ((8, 4, 0) if s_q == 10 else (8, 0, 2))
     assert_cast_close(r["out"], O, out_dtype, 64.0)
     assert_lse_close(r["lse"], L)
     assert abs(r["amax"] - float(np.abs(O).max())) <= 2e-3 * float(np.abs(O).max())
@@ -125,9 +135,8 @@ def test_tail_bf16_partials():
 
 
 def test_tail_fewer_tokens_than_planned():
-    """A plan for 20 tokens on 8 SMs called with 10 (r = 2: 4 splits), 12 (r = 4: 2
-    splits, below the rule: no tail) and 8 (one wave: no tail): the tail follows the
-    call's s_q."""
+    """A plan for 20 tokens on 8 SMs called with 10 (r = 2: 4 splits), 12 (r = 4: two
+    dim groups each) and 8 (one wave: no tail): the tail follows the call's s_q."""
     inp = wl.mla_inputs(12, 32768, 640, seed=89)
     dev = torch.device("cuda")
     plan = b.mla_decode_plan(20, 640, num_sms=8)
@@ -146,11 +155,12 @@ def test_tail_fewer_tokens_than_planned():
         assert_lse_close(lse.cpu().double().numpy(), L, what=f"LSE s_q={s_q}")
 
 
-@pytest.mark.parametrize("s_q", [160, 320])
+@pytest.mark.parametrize("s_q", [160, 228, 320])
 def test_tail_on_device_sms_sampled(s_q):
     """The automatic plan on the device's SMs: 160 tokens on 152 SMs leave 8 in the
-    last wave (cut into one-block splits), 320 leave 16; tokens around the wave edge
-    and the whole tail against the oracle, e4m3 output as the bench runs it."""
+    last wave (cut into one-block splits), 320 leave 16, 228 leave 76 (two dim groups
+    each); tokens around the wave edge and the whole tail against the oracle, e4m3
+    output as the bench runs it."""
     inp = wl.mla_inputs(s_q, 131072, 640, seed=91 + s_q)
     r = run_mla(inp, 0, out_dtype="e4m3", inv_scale=64.0)
     plan = r["plan"]
