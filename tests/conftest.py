@@ -15,5 +15,5 @@ def pytest_configure(config):
 
 def pytest_collection_modifyitems(config, items):
     # GPU tests fail loudly (not skip) when the GPU or the library is missing, so a
-    # `-m gpu` run on a GPU machine cannot pass on a silent fallback.
+    # `-m gpu` run on a machine with a GPU cannot pass on a silent fallback.
     pass
