@@ -67,6 +67,9 @@ extern "C" {
                                        it wrote nothing */
 #define MLA_STATUS_BAD_ALIGN  0x4u  /* the dynamic shared memory base was not 1024-byte aligned;
                                        the sparse kernel wrote nothing */
+#define MLA_STATUS_BAD_INDEX  0x10u /* with index checks on (mla_set_index_checks), a gathered
+                                       index was outside {-1} and [0, n_kv); that row was
+                                       masked, as it always is */
 
 /* Output element types of the final cast (FlashMLA PR #25, "What changes":
  * the FP8 cast moves into the combine; the fp32 pass-through exists for parity). */
@@ -414,6 +417,15 @@ MLA_API int mla_selftest_wait_timeout(uint64_t limit_ns, void* stream);
  * that abort path: a limit far below a step's latency makes real waits run out.
  * The pages have no counterpart (failure handling of this library). */
 MLA_API int mla_set_wait_limit_ns(uint64_t limit_ns);
+
+/* Index checks for the sparse-MLA calls launched after it, process wide (a debug
+ * mode switched at run time; off by default). Every index is masked the same way
+ * with or without it: -1 (padding) and any value outside [0, n_kv) contribute no
+ * row. With enable = 1 a value outside {-1} and [0, n_kv) also sets
+ * MLA_STATUS_BAD_INDEX in the status word (mla_get_status), so a caller can tell
+ * padding from a corrupt index list. enable must be 0 or 1, else
+ * MLA_ERR_INVALID_ARG. No counterpart in the pages (the library's own checking). */
+MLA_API int mla_set_index_checks(int enable);
 
 /* ======================================================================= *
  *  Decode without allocation                                               *

@@ -9,6 +9,7 @@ from .binding import (  # noqa: F401
     mla_abi_version, mla_decode_plan, mla_get_status, mla_selftest_wait_timeout, mla_sparse_decode,
     mla_sparse_decode_host,
     mla_sparse_decode_noalloc, mla_workspace_init, mla_plan_set_partials_bf16, mla_set_wait_limit_ns,
+    mla_set_index_checks,
     mla_sparse_decode_direct, mla_sparse_decode_split, mla_split_combine, sdpa_fp8_decode,
     sdpa_fp8_decode_direct, sdpa_fp8_decode_plan, sdpa_fp8_decode_split, sdpa_split_combine,
 )

@@ -19,6 +19,7 @@ MLA_OK = 0
 MLA_OUT_F32, MLA_OUT_BF16, MLA_OUT_E4M3 = 0, 1, 2
 MLA_STATUS_TIMEOUT = 0x1
 MLA_STATUS_BAD_SHAPE = 0x2
+MLA_STATUS_BAD_INDEX = 0x10
 MLA_STATUS_BAD_ALIGN = 0x4
 MLA_MAX_SPLITS = 64
 MLA_FORCE_BALANCED = -1
@@ -30,7 +31,7 @@ EXPORTS = [
     "mla_sparse_decode", "mla_sparse_decode_host", "sdpa_fp8_decode_plan", "sdpa_fp8_decode_split",
     "sdpa_split_combine", "sdpa_fp8_decode_direct", "sdpa_fp8_decode", "mla_get_status",
     "mla_selftest_wait_timeout", "mla_status_string", "mla_abi_version", "mla_sparse_decode_noalloc",
-    "mla_workspace_init", "mla_set_wait_limit_ns", "mla_plan_set_partials_bf16",
+    "mla_workspace_init", "mla_set_wait_limit_ns", "mla_plan_set_partials_bf16", "mla_set_index_checks",
 ]
 
 
@@ -88,6 +89,7 @@ _SIGS = {
     "mla_sparse_decode_noalloc": [_I, _I, _P, _P, _I64, _P, _F, _P, _I, _I, _F, _P, _P, _P, _P],
     "mla_workspace_init": [ctypes.POINTER(MlaPlan), _P, _P],
     "mla_set_wait_limit_ns": [_U64],
+    "mla_set_index_checks": [_I],
     "mla_plan_set_partials_bf16": [ctypes.POINTER(MlaPlan), _I],
 }
 
@@ -261,6 +263,11 @@ def mla_get_status():
     st, site = ctypes.c_uint32(0), ctypes.c_uint32(0)
     _check(lib().mla_get_status(ctypes.byref(st), ctypes.byref(site)), "mla_get_status")
     return st.value, site.value
+
+
+def mla_set_index_checks(enable: bool = True):
+    """Report gathered indices outside {-1} and [0, n_kv) (status bit MLA_STATUS_BAD_INDEX) in later calls."""
+    _check(lib().mla_set_index_checks(int(enable)), "mla_set_index_checks")
 
 
 def mla_set_wait_limit_ns(limit_ns: int):

@@ -27,6 +27,9 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitim
 // shortens it for tests); an aborting CTA always waits up to kWaitLimitNs for its
 // own copies and MMAs in flight.
 std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
+// 1: the sparse-MLA kernels report indices outside {-1} and [0, n_kv)
+// (mla_set_index_checks); 0 by default.
+std::atomic<int> g_check_idx{0};
 constexpr int kMaxDevices = 64;
 
 struct DeviceState {
@@ -364,6 +367,7 @@ int mla_sparse_decode_split(const mla_plan_t* plan, int s_q, const void* q, cons
   a.lse_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan->lse_acc_offset);
   a.partial_bf16 = plan->partial_bf16;
   a.status = dev->status;
+  a.check_idx = g_check_idx.load();
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.drain_limit_ns = kWaitLimitNs;
   return cuda_status(skv::launch_mla_decode(tq, a, static_cast<cudaStream_t>(stream)));
@@ -455,6 +459,7 @@ int mla_decode_tail(const mla_plan_t* plan, int s_q, const void* q, const void* 
   a.sink = sink;
   a.amax = amax_out;
   a.status = dev->status;
+  a.check_idx = g_check_idx.load();
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.drain_limit_ns = kWaitLimitNs;
   if ((st = cuda_status(skv::launch_mla_decode(tq, a, cs))) != MLA_OK) return st;
@@ -533,6 +538,7 @@ int mla_decode_balanced(const mla_plan_t* plan, int s_q, const void* q, const vo
   a.sink = sink;
   a.amax = amax_out;
   a.status = dev->status;
+  a.check_idx = g_check_idx.load();
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.drain_limit_ns = kWaitLimitNs;
   if ((st = cuda_status(skv::launch_mla_decode(tq, a, cs))) != MLA_OK) return st;
@@ -617,6 +623,7 @@ int mla_direct_impl(int s_q, int topk, const void* q, const void* kv, int64_t n_
   a.sink = sink;
   a.amax = amax_out;
   a.status = dev->status;
+  a.check_idx = g_check_idx.load();
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.drain_limit_ns = kWaitLimitNs;
   return cuda_status(skv::launch_mla_decode(tq, a, cs));
@@ -935,6 +942,12 @@ int mla_set_wait_limit_ns(uint64_t limit_ns) {
   if (limit_ns == 0) limit_ns = kWaitLimitNs;
   if (limit_ns < 100ull || limit_ns > 10000000000ull) return MLA_ERR_INVALID_ARG;
   g_wait_limit_ns.store(limit_ns);
+  return MLA_OK;
+}
+
+int mla_set_index_checks(int enable) {
+  if (enable != 0 && enable != 1) return MLA_ERR_INVALID_ARG;
+  g_check_idx.store(enable);
   return MLA_OK;
 }
 

@@ -37,6 +37,8 @@ struct MlaArgs {
                         // k % tail_splits of tail token k / tail_splits, whose partial goes to
                         // slot (split, tail token) of the workspace (needs num_splits ==
                         // dim_groups == 1); 0: no tail
+  int check_idx;        // 1: a loader that meets an index outside {-1} and [0, n_kv) sets
+                        // status bit 0x10 (the row stays masked either way)
   int tail_dgroups;     // uniform schedule, tail_splits == 0: tokens tail_first .. s_q - 1 run
                         // whole on tail_dgroups (2 or 4) CTAs each, CTA tail_first + k taking
                         // dim group k % tail_dgroups of tail token k / tail_dgroups and

@@ -539,6 +539,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
     for (int g = 0; g < total; ++g) {
       const int h = g & 1;
+      // (index checks on request: -1 is padding, anything else outside [0, n_kv) is reported)
+      if (a.check_idx && ixl != -1 && (ixl < 0 || ixl >= a.n_kv)) atomicOr(&a.status[0], 0x10u);
       if (!copy_group(std::integral_constant<int, 0>{}, g, h) ||
           !copy_group(std::integral_constant<int, 1>{}, g, h))
         break;

@@ -353,3 +353,12 @@ def test_package_reexports_every_entry_point():
         if name == "mla_status_string":
             continue      # wrapped as status_string
         assert hasattr(pkg, name), name
+
+
+def test_index_check_switch_arguments():
+    """mla_set_index_checks takes 0 or 1 only (no GPU needed: it sets a process-wide flag)."""
+    for bad in (2, -1):
+        with pytest.raises(b.SplitKVError) as e:
+            b.mla_set_index_checks(bad)
+        assert e.value.status == 1          # MLA_ERR_INVALID_ARG
+    b.mla_set_index_checks(False)

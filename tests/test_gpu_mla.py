@@ -490,3 +490,48 @@ def test_host_buffer_call(s_q, S):
     O, L = oracle_mla(sub)
     assert_cast_close(out_h[ts], O, "e4m3", 64.0)
     assert_lse_close(lse_h[ts].double().numpy(), L)
+
+
+def _decode_status(inp, S=0):
+    """One decode through mla_sparse_decode; returns (O, LSE, status bits) without asserting the status."""
+    dev = torch.device("cuda")
+    plan = b.mla_decode_plan(inp.s_q, inp.topk, force_splits=S)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev) if plan.workspace_bytes else None
+    out = torch.empty(inp.s_q, 64, 512, dtype=torch.float32, device=dev)
+    lse = torch.empty(inp.s_q, 64, dtype=torch.float32, device=dev)
+    b.mla_sparse_decode(plan, inp.s_q, inp.q.to(dev), inp.kv.to(dev), inp.n_kv, inp.idx.to(dev), inp.sm_scale, None,
+                        "f32", 1.0, out, lse, None, ws)
+    st, _ = b.mla_get_status()
+    return out.cpu().numpy(), lse.cpu().double().numpy(), st
+
+
+@pytest.mark.parametrize("S", [0, 1])
+def test_index_checks_report_corrupt_indices(S):
+    """With index checks on, an index outside {-1} and [0, n_kv) sets MLA_STATUS_BAD_INDEX;
+    -1 padding alone sets nothing; the row is masked either way (the oracle's result);
+    with checks off nothing is reported."""
+    inp = wl.mla_inputs(4, 32768, 640, seed=131)
+    pad = inp.idx.clone()
+    pad[0, 5] = -1
+    pad[1, 600:640] = -1
+    bad = pad.clone()
+    bad[2, 10] = inp.n_kv          # one past the cache
+    bad[3, 300] = -7               # negative, not the padding value
+    pad_in = wl.MlaInputs(q=inp.q, kv=inp.kv, idx=pad, sink=None, sm_scale=inp.sm_scale)
+    bad_in = wl.MlaInputs(q=inp.q, kv=inp.kv, idx=bad, sink=None, sm_scale=inp.sm_scale)
+    O_pad, L_pad = oracle_mla(pad_in)
+    O_bad, L_bad = oracle_mla(bad_in)
+    b.mla_set_index_checks(True)
+    try:
+        o, l, st = _decode_status(pad_in, S)
+        assert st == 0
+        assert_o_close(o, O_pad)
+        o, l, st = _decode_status(bad_in, S)
+        assert st == b.MLA_STATUS_BAD_INDEX
+        assert_o_close(o, O_bad)
+        assert_lse_close(l, L_bad)
+    finally:
+        b.mla_set_index_checks(False)
+    o, l, st = _decode_status(bad_in, S)
+    assert st == 0
+    assert_o_close(o, O_bad)
