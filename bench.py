@@ -675,7 +675,7 @@ def known_traffic(s_q, S):
     except OSError:
         return None
     table = {   # (source hash, s_q, S) -> dram bytes per launch
-        ("395ab653de5fb20d", 96, 1): 55_353_856,
+        ("072ba5384f5884da", 96, 1): 55_474_176,
     }
     return table.get((h, s_q, S))
 
