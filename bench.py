@@ -40,6 +40,10 @@ H_Q, D_QK, D_V = 64, 576, 512
 INV_SCALE = 64.0
 SWEEP_SQ = (1, 6, 16, 96, 384)
 SWEEP_S = (1, 2, 4, 8, 16)
+# more tokens than SMs: the one-split grid with its last wave cut (planner) against
+# the uncut grid (forced one split); 160 leaves 8 tokens in the last wave on 152
+# SMs (cut into splits), 228 leaves 76 (two dim groups each)
+TAIL_SQ = (160, 228)
 BF16_PARTIALS_SQ, BF16_PARTIALS_S = 16, (8, 0)   # sweep points also run with bf16 partials
 FLUSH_BYTES = 256 << 20
 
@@ -464,7 +468,8 @@ def run_gpu(args):
     # inputs: one seeded 131072-row cache, replicated as the per-layer caches of the
     # timed rotation (views of one allocation), and per-layer queries / indices per s_q
     l2_bytes = int(getattr(torch.cuda.get_device_properties(local), "L2_cache_size", 0) or L2_FALLBACK)
-    s_q_list = [args.s_q] + ([] if (args.no_sweep or args.no_mla_sweep) else [s for s in SWEEP_SQ if s != args.s_q])
+    s_q_list = [args.s_q] + ([] if (args.no_sweep or args.no_mla_sweep)
+                             else [s for s in SWEEP_SQ + TAIL_SQ if s != args.s_q])
     global LAYERS_OVERRIDE
     LAYERS_OVERRIDE = args.layers   # a fixed rotation (a small device footprint, e.g. for a profiler capture)
     n_layers_max = max(layers_for(s, l2_bytes) for s in s_q_list)
@@ -578,6 +583,25 @@ def run_gpu(args):
                                   "gb_s": round(cb / (us * 1e-6) / 1e9, 1),
                                   "frac_of_peak": round(cb / (us * 1e-6) / 1e9 / peak, 4)})
                     del c
+            del qs, idxs
+        for s_q in (() if args.no_mla_sweep else TAIL_SQ):
+            qs, idxs = layer_inputs(s_q)
+            for S in (1, 0):
+                c = Case(b, torch, kv_all, qs, idxs, base.sm_scale, S)
+                steps = max(args.sweep_steps, c.layers)
+                us = c.time("call", steps, c.layers)
+                ks = c.time("kernel", steps, c.layers)
+                cb = point_bytes(s_q, c.S, c.balanced, c.plan.num_sms)
+                if c.tail is not None and c.tail[1] > 0:   # the split tail's partials, written and read back
+                    r = s_q - c.tail[0]
+                    cb += 2 * c.tail[1] * r * H_Q * (D_V + 1) * 4
+                sweep.append({"s_q": s_q, "num_splits": "planner" if S == 0 else S, "planner": S == 0,
+                              "partials": "fp32", "layers": c.layers, "steps": steps,
+                              "schedule": c.schedule(), "us_per_call": round(us, 2),
+                              "split_kernel_us": round(ks, 2), "alg_bytes": cb,
+                              "gb_s": round(cb / (us * 1e-6) / 1e9, 1),
+                              "frac_of_peak": round(cb / (us * 1e-6) / 1e9 / peak, 4)})
+                del c
             del qs, idxs
         torch.cuda.synchronize()
         # the dense FP8 GQA variant (same partial / LSE protocol), forced split
