@@ -152,3 +152,28 @@ def test_too_many_rows_is_reported_not_computed():
     st, _ = b.mla_get_status()
     assert st & b.MLA_STATUS_BAD_SHAPE
     assert torch.all(out == 7.0)
+
+
+@pytest.mark.parametrize("S", [0, 1, 3])
+def test_empty_sequences(S):
+    """A batch holding a sequence with no new tokens and no keys, and one with keys but
+    no new tokens: their jobs have no rows (nothing written), the other sequences are
+    the oracle's, with the planner's per-sequence splits, unsplit and forced splits."""
+    import dataclasses
+    base = wl.sdpa_inputs(5, 8, 2, 128, q_per_seq=(1, 3), kv_len=(200, 900), seed=23)
+    cq = base.cu_seqlens_q.tolist()
+    ck = base.cu_seqlens_kv.tolist()
+    # sequence 1: drop its queries and its keys; sequence 3: drop its queries only
+    keep_q = [i for i in range(cq[-1]) if not (cq[1] <= i < cq[2] or cq[3] <= i < cq[4])]
+    keep_k = [i for i in range(ck[-1]) if not (ck[1] <= i < ck[2])]
+    sq = [cq[b + 1] - cq[b] for b in range(5)]
+    sk = [ck[b + 1] - ck[b] for b in range(5)]
+    sq[1] = sq[3] = 0
+    sk[1] = 0
+    new_cq = torch.tensor([0] + list(np.cumsum(sq)), dtype=torch.int32)
+    new_ck = torch.tensor([0] + list(np.cumsum(sk)), dtype=torch.int32)
+    inp = dataclasses.replace(base, q=base.q[keep_q], k=base.k[keep_k], v=base.v[keep_k],
+                              cu_seqlens_q=new_cq, cu_seqlens_kv=new_ck)
+    assert int(new_cq[-1]) == len(keep_q) and int(new_ck[-1]) == len(keep_k)
+    O, L = osd.attention(inp)
+    _check(inp, run_sdpa(inp, S, max_q=3), O, L)
